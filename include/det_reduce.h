@@ -1,0 +1,262 @@
+/*
+ * det_reduce.h -- C ABI of the deterministic multi-writer reduction library
+ * (libdetreduce.so, CUDA for sm_103a).
+ *
+ * The operation.  For destination rows m = 0 .. M-1 of width H:
+ *
+ *     out[m][h] = SUM over { i : idx[i] = m } of  w[i] * x[i][h]
+ *
+ * computed so that the result is the same bits whatever the grid, the SM
+ * count, the batch composition or how the sources are split into shards.
+ * This is the MoE token combine/unpermute (out.index_add_(0, sorted_indices,
+ * permuted_tokens) versus the atomic scatter_add_, "Megatron-LM determinism
+ * developer reference", section 3.1, op catalog), the sparse-attention
+ * backward key-gradient scatter and the MoE backward merge ("DeepSeek-V4
+ * book, Ch 09: Batch invariance and determinism", sections 3.1 and 3.2), and,
+ * without the index, the split-K partial-sum reduce (same chapter, section
+ * 3.3).  Several writers to one address get private slots merged in one fixed
+ * order ("Bit-exact training interview notes", table "where nondeterminism
+ * comes from"), and every shard count goes through the same fp32 tree (same
+ * page, "why pay the overhead", EP-size-invariant expert combine).
+ *
+ * The canonical order (fixed by this library; the pages fix the problem, not
+ * a tree):
+ *   1. the terms of destination m are the sources i with idx[i] = m in
+ *      ascending order key (src_id[i] if given, else the physical row i);
+ *   2. term p = fl32(w[i] * fl32(x[i][h])): one binary32 multiply rounded to
+ *      nearest even, never fused with the add; no multiply when w is NULL;
+ *   3. consecutive chunks of 32 terms are folded left to right, starting from
+ *      the chunk's first term;
+ *   4. chunk sums are combined by a level-wise pairwise tree: at each level
+ *      neighbours (2k, 2k+1) are added and an odd last element is carried up
+ *      unchanged, until one value remains;
+ *   5. an empty destination gives +0.0;
+ *   6. the value is stored as binary32 or rounded to bf16 (nearest even).
+ * Every add is a binary32 add rounded to nearest even; subnormals are kept
+ * (no flush to zero).
+ *
+ * Conventions.
+ *  - Every function returns det_status (0 = DET_OK).  No function throws,
+ *    aborts or prints.
+ *  - "dev" pointers are CUDA device pointers of the current device; "host"
+ *    pointers are ordinary host memory.  All tensor memory (inputs, outputs,
+ *    workspaces) is owned by the caller; the library never allocates device
+ *    memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is enqueued on it and the call returns without waiting,
+ *    except det_reduce_plan, which waits once (see there).
+ *  - Arguments are checked before anything is enqueued (fail closed): an
+ *    option or argument the library cannot honour is an error, never a
+ *    silent fallback.  On error nothing is written to any output.
+ *  - No option in det_opts changes a single output bit.
+ */
+#ifndef DET_REDUCE_H
+#define DET_REDUCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t det_status;
+
+#define DET_OK 0
+#define DET_ERR_ARG 1          /* NULL where data is needed, negative size, bad stride, aliasing, bad alignment */
+#define DET_ERR_DTYPE 2        /* dtype code not supported */
+#define DET_ERR_INDEX_RANGE 3  /* some idx[i] outside [0, M) */
+#define DET_ERR_ORDER_KEY 4    /* two sources of one destination share a src_id: their order is undefined */
+#define DET_ERR_WORKSPACE 5    /* workspace NULL, misaligned or smaller than the size query returned */
+#define DET_ERR_CUDA 6         /* a CUDA call failed; det_last_cuda_error() gives the cudaError_t */
+#define DET_ERR_TIMEOUT 7      /* reserved for bounded device waits (no kernel of this library waits) */
+#define DET_ERR_UNSUPPORTED 8  /* size beyond a documented limit (N, M >= 2^31 - 1, more than DET_MAX_SHARDS shards) */
+
+typedef int32_t det_dtype;
+#define DET_F32 0   /* IEEE binary32 */
+#define DET_BF16 1  /* bfloat16: the high 16 bits of a binary32 pattern */
+
+#define DET_MAX_SHARDS 16
+
+/*
+ * Launch options.  Pass NULL for defaults.  None of them changes output bits;
+ * tests sweep them to prove it.
+ *  grid_ctas        0 = auto; > 0 = exact number of CTAs for the reduce
+ *                   kernels (they loop over their work until done).
+ *  seg_chunks_log2  -1 = auto (3); otherwise 3..10.  A destination with more
+ *                   than 2^g chunks of 32 terms is split into segments of 2^g
+ *                   chunks that run on different warps/CTAs; each segment is
+ *                   one aligned node of the tree, written to a private fp32
+ *                   partial slot, and a second pass applies the rest of the
+ *                   tree in its fixed order.  Plan-time option.
+ *  debug_checks     nonzero: the call waits for its kernels and reports a
+ *                   CUDA error as DET_ERR_CUDA (slower; for tests).
+ */
+typedef struct det_opts {
+    int32_t grid_ctas;
+    int32_t seg_chunks_log2;
+    int32_t debug_checks;
+    int32_t reserved;
+} det_opts;
+
+/* Opaque host handle of a built plan.  Its device arrays live in the
+ * caller's plan workspace, which must stay allocated and unmodified while the
+ * plan is used. */
+typedef struct det_plan_s* det_plan;
+
+/* Read-only description of a built plan (device pointers into the plan
+ * workspace; counts are host values). */
+typedef struct det_plan_desc {
+    int64_t N, M;
+    int32_t seg_chunks_log2;
+    int32_t reserved;
+    const int32_t* row_ptr;   /* dev [M+1]: exclusive prefix sums of destination counts, row_ptr[M] = N */
+    const int32_t* perm;      /* dev [N]: perm[row_ptr[m] + r] = physical row of the r-th term of destination m */
+    int64_t n_units;          /* warp tasks (before H-tiling): whole destinations + hot segments */
+    int64_t n_segments;       /* hot segments = fp32 partial slots needed per H */
+    int64_t n_hot_rows;       /* destinations split into segments */
+    int64_t max_row_len;      /* largest number of terms of one destination */
+} det_plan_desc;
+
+/* Text of a status code (static storage; never NULL). */
+const char* det_status_str(det_status s);
+
+/* The cudaError_t of the last failing CUDA call on this thread (0 if none). */
+int32_t det_last_cuda_error(void);
+
+/* Library ABI version: (major << 16) | minor. */
+int32_t det_version(void);
+
+/*
+ * Bytes of device workspace a plan over N sources and M destinations needs
+ * (with_src_id != 0: the plan will be given order keys).  host out-param.
+ * Errors: DET_ERR_ARG (negative, NULL out), DET_ERR_UNSUPPORTED (N or M >=
+ * 2^31 - 1).
+ */
+det_status det_plan_workspace_size(int64_t N, int64_t M, int32_t with_src_id,
+                                   const det_opts* opts, size_t* bytes);
+
+/*
+ * Build the destination lists (CSR) and the work list of the reduce.
+ *  idx        dev int32 [N]: destination of each physical source row.
+ *  src_id     dev int64 [N] or NULL: order key of each physical row (NULL =
+ *             the physical row number).  Keys must be distinct among the
+ *             sources of one destination; they may be any int64 values
+ *             (e.g. global token ids of a batch subset).  This is the MoE
+ *             backward's stable (expert id, original token id) order, Ch 09
+ *             section 3.2.
+ *  workspace  dev, >= det_plan_workspace_size(N, M, src_id != NULL) bytes,
+ *             256-byte aligned; holds the plan's device arrays afterwards.
+ *  out_plan   host out-param; release with det_plan_destroy.
+ * Steps on the device: destination histogram, exclusive scan, stable LSD
+ * radix sort of source rows by destination (after a sort by src_id when
+ * given), all integer and exact; then the work list (whole destinations and
+ * hot segments).  The call waits once for the stream to read the error flags
+ * and the work counts; it is therefore not capturable in a CUDA graph.  The
+ * plan is reusable for any x, w, H, dtype and shard split over the same idx.
+ * Errors: DET_ERR_ARG, DET_ERR_WORKSPACE, DET_ERR_UNSUPPORTED,
+ * DET_ERR_INDEX_RANGE (an idx outside [0, M)), DET_ERR_ORDER_KEY,
+ * DET_ERR_CUDA.  On error *out_plan is NULL.
+ */
+det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N, int64_t M,
+                           void* workspace, size_t ws_bytes, const det_opts* opts,
+                           void* stream, det_plan* out_plan);
+
+/* Release the host handle (the workspace stays the caller's).  NULL is OK. */
+det_status det_plan_destroy(det_plan plan);
+
+/* Fill *desc (host) from a built plan. */
+det_status det_plan_describe(det_plan plan, det_plan_desc* desc);
+
+/*
+ * Bytes of device workspace det_scatter_reduce needs for the hot-segment
+ * partial slots at row width H (0 when the plan has no hot destination).
+ */
+det_status det_scatter_workspace_size(det_plan plan, int64_t H, size_t* bytes);
+
+/*
+ * out[m][0..H) = canonical sum over the terms of destination m (see top).
+ *  x_shards    host array [P] of dev pointers; shard q holds the physical
+ *              rows [R_q, R_q + shard_rows[q]), R_q = sum of earlier
+ *              shard_rows, row r at x_shards[q] + (r - R_q) * ldx elements.
+ *              Shards say only where bytes live; the order key is global, so
+ *              P = 1, 2, 4, 8 give identical bits (simulated expert-parallel
+ *              shards on one GPU).
+ *  shard_rows  host int64 [P], summing to the plan's N.  1 <= P <=
+ *              DET_MAX_SHARDS.
+ *  x_dtype     DET_F32 or DET_BF16; ldx >= H elements.
+ *  w           dev float [N] or NULL (no multiply).
+ *  out         dev [M][ldo] of out_dtype, ldo >= H; overwritten, never
+ *              accumulated into (elements h >= H of a row are not touched);
+ *              must not overlap x, w, the plan workspace or `workspace`.
+ *  workspace   dev, >= det_scatter_workspace_size(plan, H) bytes, 256-byte
+ *              aligned (may be NULL when that size is 0).
+ * Rows are read with 16-byte vector loads when every shard pointer is
+ * 16-byte aligned and ldx, H are multiples of 16 bytes' worth of elements;
+ * otherwise with scalar loads.  Both give the same bits.
+ * Errors: DET_ERR_ARG, DET_ERR_DTYPE, DET_ERR_WORKSPACE, DET_ERR_UNSUPPORTED,
+ * DET_ERR_CUDA.
+ */
+det_status det_scatter_reduce(det_plan plan,
+                              const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                              det_dtype x_dtype, int64_t ldx, int64_t H,
+                              const float* w, void* out, int64_t ldo, det_dtype out_dtype,
+                              void* workspace, size_t ws_bytes,
+                              const det_opts* opts, void* stream);
+
+/*
+ * Split-K reduce: out[e] = canonical sum over s = 0 .. S-1 (split-id order)
+ * of partials[s * ldp + e], e = 0 .. count-1, no multiply (Ch 09, section
+ * 3.3: each K-split writes its own buffer; a reduce kernel sums them in
+ * split-id order).
+ *  partials  dev float [S][ldp], ldp >= count.
+ *  out       dev [count] of out_dtype; must not overlap partials.
+ * Errors: DET_ERR_ARG, DET_ERR_DTYPE, DET_ERR_UNSUPPORTED, DET_ERR_CUDA.
+ */
+det_status det_splitk_reduce(const float* partials, int32_t S, int64_t count, int64_t ldp,
+                             void* out, det_dtype out_dtype, const det_opts* opts, void* stream);
+
+/*
+ * u64 fingerprint of nbytes bytes at dev pointer p, written to dev *out.
+ * The repeatability gate compares per-tensor fingerprints byte for byte
+ * instead of a printed loss ("Bit-exact training interview notes", "how to
+ * verify: three gates").  Definition (this library's, not torch.hash_tensor):
+ *   h = mix(nbytes ^ 0x6A09E667F3BCC909)
+ *       + sum_j mix(word_j ^ (j * 0x9E3779B97F4A7C15))   mod 2^64,
+ * word_j = bytes [8j, 8j+8) read little-endian, zero-padded past nbytes, and
+ * mix = the SplitMix64 finalizer.  Integer sums commute, so the value does
+ * not depend on the grid.  p may have any alignment.  *out is overwritten.
+ * Errors: DET_ERR_ARG (p NULL with nbytes > 0, out NULL or not 8-byte
+ * aligned), DET_ERR_CUDA.
+ */
+det_status det_hash(const void* p, uint64_t nbytes, uint64_t* out, void* stream);
+
+/*
+ * Bytes of workspace det_atomic_scatter_reduce needs: 256 bytes of flags, plus
+ * an fp32 [M][H] accumulator when out_dtype is DET_BF16.
+ */
+det_status det_atomic_workspace_size(int64_t M, int64_t H, det_dtype out_dtype, size_t* bytes);
+
+/*
+ * NOT DETERMINISTIC -- benchmark baseline only.  The atomic twin of
+ * det_scatter_reduce (scatter_add_ in the op catalog): out is zeroed, then
+ * each term w[i] * x[i][h] (binary32 multiply) is added to out[idx[i]][h]
+ * with atomic adds whose order the scheduler picks.  bf16 output: the adds
+ * go to the fp32 accumulator in the workspace, which is then rounded to bf16
+ * (nearest even).  Sources whose idx is outside [0, M) are skipped and
+ * counted in the workspace flags; with opts->debug_checks the call waits and
+ * returns DET_ERR_INDEX_RANGE if any were seen.
+ * Arguments as det_scatter_reduce, with idx (dev int32 [N]) instead of a plan.
+ */
+det_status det_atomic_scatter_reduce(const int32_t* idx, int64_t N, int64_t M,
+                                     const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                                     det_dtype x_dtype, int64_t ldx, int64_t H,
+                                     const float* w, void* out, int64_t ldo, det_dtype out_dtype,
+                                     void* workspace, size_t ws_bytes,
+                                     const det_opts* opts, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DET_REDUCE_H */

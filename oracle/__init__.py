@@ -1,0 +1,187 @@
+"""CPU oracle for the deterministic multi-writer reduction (ctypes over oracle.c).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
+CPU-baseline leg use it.  The GPU library never imports, links or calls it and
+it shares no code with the GPU library.
+
+Every function takes and returns numpy arrays.  bf16 data travels as
+``np.uint16`` bit patterns.  The arithmetic itself lives in ``oracle.c``,
+which documents the canonical order it implements.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+F32 = 0
+BF16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so beside it (gcc, no fused multiply-add)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB)
+        i32, i64, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+        vp, fp = ctypes.c_void_p, ctypes.c_float
+        lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f32.restype = fp
+        lib.oracle_f32_to_bf16.argtypes = [fp]
+        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_f32_to_bf16_array.argtypes = [vp, vp, i64]
+        lib.oracle_f32_to_bf16_array.restype = None
+        lib.oracle_bf16_to_f32_array.argtypes = [vp, vp, i64]
+        lib.oracle_bf16_to_f32_array.restype = None
+        lib.oracle_canonical_sum.argtypes = [vp, i64, ctypes.POINTER(i32)]
+        lib.oracle_canonical_sum.restype = fp
+        lib.oracle_build_lists.argtypes = [vp, vp, i64, i64, vp, vp]
+        lib.oracle_build_lists.restype = ctypes.c_int
+        lib.oracle_scatter_reduce.argtypes = [vp, vp, i64, i64, vp, vp, i32, i32, i64, i64, vp, vp, i64, i32]
+        lib.oracle_scatter_reduce.restype = ctypes.c_int
+        lib.oracle_splitk_reduce.argtypes = [vp, i32, i64, i64, vp, i32]
+        lib.oracle_splitk_reduce.restype = ctypes.c_int
+        lib.oracle_mix64.argtypes = [u64]
+        lib.oracle_mix64.restype = u64
+        lib.oracle_hash.argtypes = [vp, u64]
+        lib.oracle_hash.restype = u64
+        _lib = lib
+        return lib
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        names = {-1: "bad argument", -2: "index out of range", -3: "duplicate order key", -4: "out of memory"}
+        super().__init__(f"oracle {what}: {names.get(code, code)}")
+        self.code = code
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"x must be float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def f32_to_bf16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint16)
+    _load().oracle_f32_to_bf16_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def bf16_to_f32(a) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    out = np.empty(a.shape, dtype=np.float32)
+    _load().oracle_bf16_to_f32_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def canonical_sum(terms) -> np.float32:
+    """Canonical fold of a 1-D sequence of binary32 terms."""
+    t = np.ascontiguousarray(terms, dtype=np.float32).reshape(-1)
+    ok = ctypes.c_int32(0)
+    r = _load().oracle_canonical_sum(_ptr(t), t.size, ctypes.byref(ok))
+    if not ok.value:
+        raise MemoryError("oracle canonical_sum")
+    return np.float32(r)
+
+
+def build_lists(idx, M: int, src_id=None):
+    """(row_ptr[M+1] int64, perm[N] int64): sources of each destination in order-key order."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32).reshape(-1)
+    sid = None if src_id is None else np.ascontiguousarray(src_id, dtype=np.int64).reshape(-1)
+    N = idx.size
+    row_ptr = np.empty(M + 1, dtype=np.int64)
+    perm = np.empty(max(N, 1), dtype=np.int64)
+    rc = _load().oracle_build_lists(_ptr(idx), _ptr(sid), N, M, _ptr(row_ptr), _ptr(perm))
+    if rc != 0:
+        raise OracleError(rc, "build_lists")
+    return row_ptr, perm[:N]
+
+
+def scatter_reduce(idx, x_shards, M: int, w=None, out_dtype: int = F32, src_id=None, H: int | None = None):
+    """out[m] = canonical sum over {i : idx[i] = m} of w[i] * x[i] (rows in order-key order).
+
+    ``x_shards`` is one 2-D array or a list of 2-D arrays (rows of consecutive
+    global source ranges), all float32 or all uint16 (bf16 bits), rows
+    possibly padded (the row stride is taken from the array).  Returns float32
+    [M, H] or uint16 [M, H] (bf16 bits).
+    """
+    if isinstance(x_shards, np.ndarray):
+        x_shards = [x_shards]
+    shards = [np.ascontiguousarray(s) for s in x_shards]
+    code = _dtype_code(shards[0])
+    if any(_dtype_code(s) != code for s in shards):
+        raise TypeError("all shards must share one dtype")
+    ldx = shards[0].shape[1]
+    if any(s.ndim != 2 or s.shape[1] != ldx for s in shards):
+        raise ValueError("shards must be 2-D with equal row length")
+    H = ldx if H is None else H
+    idx = np.ascontiguousarray(idx, dtype=np.int32).reshape(-1)
+    N = idx.size
+    rows = np.array([s.shape[0] for s in shards], dtype=np.int64)
+    ptrs = (ctypes.c_void_p * len(shards))(*[s.ctypes.data for s in shards])
+    wv = None if w is None else np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+    sid = None if src_id is None else np.ascontiguousarray(src_id, dtype=np.int64).reshape(-1)
+    out = np.empty((M, H), dtype=np.float32 if out_dtype == F32 else np.uint16)
+    rc = _load().oracle_scatter_reduce(_ptr(idx), _ptr(sid), N, M, ctypes.cast(ptrs, ctypes.c_void_p),
+                                       _ptr(rows), len(shards), code, ldx, H, _ptr(wv), _ptr(out), H,
+                                       out_dtype)
+    if rc != 0:
+        raise OracleError(rc, "scatter_reduce")
+    return out
+
+
+def splitk_reduce(partials, out_dtype: int = F32):
+    """out[e] = canonical sum over s of partials[s, e] (partials float32 [S, count])."""
+    p = np.ascontiguousarray(partials, dtype=np.float32)
+    S, count = p.shape
+    out = np.empty(count, dtype=np.float32 if out_dtype == F32 else np.uint16)
+    rc = _load().oracle_splitk_reduce(_ptr(p), S, count, count, _ptr(out), out_dtype)
+    if rc != 0:
+        raise OracleError(rc, "splitk_reduce")
+    return out
+
+
+def mix64(z: int) -> int:
+    return int(_load().oracle_mix64(z & 0xFFFFFFFFFFFFFFFF))
+
+
+def hash_bytes(buf) -> int:
+    """u64 fingerprint of a byte buffer (numpy array of any dtype, or bytes)."""
+    if isinstance(buf, (bytes, bytearray)):
+        a = np.frombuffer(bytes(buf), dtype=np.uint8)
+    else:
+        a = np.ascontiguousarray(buf).view(np.uint8).reshape(-1)
+    if a.size == 0:
+        a = np.zeros(1, dtype=np.uint8)
+        return int(_load().oracle_hash(_ptr(a), 0))
+    return int(_load().oracle_hash(_ptr(a), a.size))
