@@ -1,0 +1,559 @@
+#!/usr/bin/env python3
+"""Benchmark of the deterministic multi-writer reduction on one node.
+
+Metric: deterministic scatter-reduce HBM GB/s (compulsory bytes: sources read
+once, outputs written once, indices and weights read once), its fraction of
+the measured HBM peak, and the overhead against the in-repo atomicAdd kernel.
+
+One step = the whole hot path over one batch of the workload: the plan
+(destination histogram, scan, stable sort of sources, work list) followed by
+the gather-reduce (and the hot-destination second pass when the workload has
+hot destinations).  Inputs are resident in HBM when the timed region starts;
+L2 is flushed (a 256 MiB write) before every timed step, outside the step's
+CUDA events.  Every step is timed with CUDA events on the launching stream.
+
+Default workload: the MoE combine/unpermute, T=4096 tokens, E=128 experts,
+top-8, H=4096, bf16 expert outputs with fp32 routing weights, bf16 out.  The
+sparse-attention key scatter and the split-K reduce are measured alongside
+and reported under "also" (same timing rules).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (single thread, the machine's host cores)
+on a bounded sample of the same workload and prints the same JSON line with
+"impl": "reference".  With N > 1 (torchrun) every rank runs an independent
+replica of the workload on its own GPU (the path has no exchange step on one
+node): value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "deterministic scatter-reduce HBM GB/s (% of peak) and overhead vs atomicAdd"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+WORKLOADS = {
+    "moe_combine": "moe_combine T=4096 E=128 top-k=8 H=4096 bf16 x, fp32 w -> bf16 out",
+    "sparse_key_scatter": "sparse_key_scatter Q=16384 K=512 S=65536 zipf=1.1 H=128 bf16 x -> fp32 out",
+    "ep_invariance": "ep_invariance T=16384 E=256 top-k=8 H=7168 bf16 x, fp32 w -> bf16 out",
+    "splitk": "splitk S=56 R=16384 C=24 fp32 -> fp32",
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["moe_combine", "sparse_key_scatter", "ep_invariance"],
+                    default="moe_combine")
+    ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    a = ap.parse_args(argv)
+    a.warmup = max(3, a.warmup)
+    a.steps = max(1, a.steps)
+    return a
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def read_traffic(kernel_file: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    import hashlib
+    src = os.path.join(ROOT, "invariant_gradient_reduction_gb300", "csrc", kernel_file)
+    summ = os.path.join(ROOT, "profiles", f"{os.path.splitext(kernel_file)[0]}_{workload}.md")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        fields = {}
+        for line in open(summ):
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+        if fields.get("source_sha256_16") != digest:
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.windows = []
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+        rows = []
+        import datetime
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        inwin = [r for r in rows if t0 - 0.02 <= r[0] <= t1 + 0.02]
+        window = "timed"
+        if len(inwin) < 3:
+            inwin = [r for r in rows if r[0] <= t1 + 0.02]
+            window = "warmup+timed (timed region shorter than the sampling interval)"
+        if not inwin:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in inwin for k, v in enumerate(r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inwin), "sm_max_mhz": max(r[2] for r in inwin),
+                "reasons": reasons, "samples": len(inwin), "window": window}
+
+
+# --------------------------------------------------------------------------
+# timing helpers
+# --------------------------------------------------------------------------
+
+class Timer:
+    """Per-step CUDA events on the current stream; an L2 flush before each step, outside the events."""
+
+    def __init__(self, torch, device):
+        self.torch = torch
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def flush(self):
+        self.flush_buf.zero_()
+
+    def run(self, fn, steps: int, warmup: int, flush: bool = True):
+        torch = self.torch
+        for _ in range(warmup):
+            if flush:
+                self.flush()
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        from invariant_gradient_reduction_gb300 import detreduce as dr
+        l0 = dr.det_kernel_launches()
+        for s, e in ev:
+            if flush:
+                self.flush()
+            s.record()
+            fn()
+            e.record()
+        torch.cuda.synchronize()
+        launches = dr.det_kernel_launches() - l0
+        return [s.elapsed_time(e) for s, e in ev], launches
+
+
+def gbs(nbytes: float, ms: float) -> float:
+    return nbytes / (ms * 1e-3) / 1e9
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def make_case(name, device):
+    from invariant_gradient_reduction_gb300 import workloads as wl
+    return wl.make(name, "full", device=device)
+
+
+def scatter_step_fns(case, torch):
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    dev = case.x.device
+    ws_plan = torch.empty(dr.det_plan_workspace_size(case.N, case.M) + 256, dtype=torch.uint8, device=dev)
+    out = torch.empty(case.M, case.H, dtype=case.out_dtype, device=dev)
+    state = {}
+
+    def plan_and_reduce():
+        p = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan)
+        dr.det_scatter_reduce(p, case.x, out, w=case.w, workspace=state.get("ws_red"))
+        state["plan"] = p
+
+    plan0 = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan)
+    need = dr.det_scatter_workspace_size(plan0, case.H)
+    state["ws_red"] = torch.empty(need + 256, dtype=torch.uint8, device=dev) if need else None
+    ws_plan_fixed = torch.empty_like(ws_plan)
+    plan_fixed = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan_fixed)
+
+    def reduce_only():
+        dr.det_scatter_reduce(plan_fixed, case.x, out, w=case.w, workspace=state.get("ws_red"))
+
+    ws_atomic = torch.empty(dr.det_atomic_workspace_size(case.M, case.H, case.out_dtype) + 256, dtype=torch.uint8,
+                            device=dev)
+    out_atomic = torch.empty_like(out)
+
+    def atomic():
+        dr.det_atomic_scatter_reduce(case.idx, case.M, case.x, out_atomic, w=case.w, workspace=ws_atomic)
+
+    return plan_and_reduce, reduce_only, atomic, out, plan_fixed
+
+
+def measure_scatter(case, timer, steps, warmup, torch, with_e2e=True):
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    cb = case.compulsory_bytes()
+    full, red, atom, out, plan = scatter_step_fns(case, torch)
+    t_full, l_full = timer.run(full, steps, warmup)
+    t_red, _ = timer.run(red, steps, warmup)
+    t_atom, _ = timer.run(atom, steps, warmup)
+    ms_full, ms_red, ms_atom = statistics.mean(t_full), statistics.mean(t_red), statistics.mean(t_atom)
+    res = {
+        "compulsory_bytes": cb,
+        "plan_reduce": {"ms": ms_full, "gbs": gbs(cb, ms_full), "ms_median": statistics.median(t_full)},
+        "reduce_only": {"ms": ms_red, "gbs": gbs(cb, ms_red), "ms_median": statistics.median(t_red)},
+        "atomic": {"ms": ms_atom, "gbs": gbs(cb, ms_atom)},
+        "overhead_vs_atomic": {"reduce_only": ms_red / ms_atom - 1.0, "plan_reduce": ms_full / ms_atom - 1.0},
+        "launches_per_step": l_full / max(1, steps),
+        "plan": {k: v for k, v in plan.describe().items() if k not in ("row_ptr", "perm")},
+        "times_full": t_full,
+        "launches_total": l_full,
+    }
+    h = dr.det_hash(out).item() & (2 ** 64 - 1)
+    res["out_fingerprint"] = f"{h:016x}"
+    if with_e2e:
+        res["e2e"] = measure_e2e(case, timer, max(3, min(steps, 20)), warmup, torch)
+    return res
+
+
+def measure_e2e(case, timer, steps, warmup, torch):
+    """Same step through the public API from pinned HOST buffers: H2D of x, idx, w, the
+    plan and reduce, and the D2H of out, all inside each step's events."""
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    dev = case.x.device
+    x_h = case.x.cpu().pin_memory()
+    idx_h = case.idx.cpu().pin_memory()
+    w_h = None if case.w is None else case.w.cpu().pin_memory()
+    x_d, idx_d = torch.empty_like(case.x), torch.empty_like(case.idx)
+    w_d = None if case.w is None else torch.empty_like(case.w)
+    out_d = torch.empty(case.M, case.H, dtype=case.out_dtype, device=dev)
+    out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+    ws_plan = torch.empty(dr.det_plan_workspace_size(case.N, case.M) + 256, dtype=torch.uint8, device=dev)
+    p0 = dr.det_reduce_plan(case.idx, case.M)
+    need = dr.det_scatter_workspace_size(p0, case.H)
+    ws_red = torch.empty(need + 256, dtype=torch.uint8, device=dev) if need else None
+
+    def step():
+        x_d.copy_(x_h, non_blocking=True)
+        idx_d.copy_(idx_h, non_blocking=True)
+        if w_h is not None:
+            w_d.copy_(w_h, non_blocking=True)
+        p = dr.det_reduce_plan(idx_d, case.M, workspace=ws_plan)
+        dr.det_scatter_reduce(p, x_d, out_d, w=w_d, workspace=ws_red)
+        out_h.copy_(out_d, non_blocking=True)
+
+    t, _ = timer.run(step, steps, warmup)
+    ms = statistics.mean(t)
+    bi = x_h.numel() * x_h.element_size() + idx_h.numel() * 4 + (0 if w_h is None else w_h.numel() * 4)
+    bo = out_h.numel() * out_h.element_size()
+    return {"value": gbs(case.compulsory_bytes(), ms), "unit": UNIT, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "ms_per_step": ms, "steps": steps}
+
+
+def measure_splitk(timer, steps, warmup, torch, device):
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    from invariant_gradient_reduction_gb300 import workloads as wl
+    P = wl.make("splitk", "full", device=device)
+    res = {}
+    for name, odt in (("f32_out", torch.float32), ("bf16_out", torch.bfloat16)):
+        out = torch.empty(P.shape[1], dtype=odt, device=device)
+        t, l = timer.run(lambda: dr.det_splitk_reduce(P, out), steps, warmup)
+        cb = P.numel() * 4 + out.numel() * out.element_size()
+        ms = statistics.mean(t)
+        res[name] = {"ms": ms, "gbs": gbs(cb, ms), "compulsory_bytes": cb, "launches_per_step": l / steps}
+    return res
+
+
+def oracle_sample_seconds(case, max_rows: int):
+    """Run the CPU oracle once on the first max_rows destinations and all their sources.
+    Returns (seconds, compulsory bytes of the sample, description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    idx = case.idx.cpu().numpy().astype(np.int32)
+    rows = min(case.M, max_rows)
+    keep = idx < rows
+    xs = case.x.cpu()[torch.from_numpy(keep)]
+    x_np = xs.view(torch.int16).numpy().view(np.uint16) if xs.dtype == torch.bfloat16 else xs.numpy()
+    w_np = None if case.w is None else case.w.cpu().numpy()[keep]
+    od = oracle.F32 if case.out_dtype == torch.float32 else oracle.BF16
+    sub_idx = idx[keep]
+    t0 = time.perf_counter()
+    oracle.scatter_reduce(sub_idx, x_np, rows, w=w_np, out_dtype=od)
+    dt = time.perf_counter() - t0
+    n = int(keep.sum())
+    cb = n * case.H * case.x.element_size() + n * 4 + (0 if case.w is None else n * 4) + \
+        rows * case.H * (4 if case.out_dtype == torch.float32 else 2)
+    return dt, cb, f"first {rows} of {case.M} destinations and their {n} sources ({cb} compulsory bytes)"
+
+
+def cpu_baseline(case, budget_s: float = 20.0):
+    import oracle
+    oracle.build()
+    rows = min(case.M, 256)
+    dt, cb, desc = oracle_sample_seconds(case, rows)
+    # grow the sample towards ~1/3 of the budget per run, then take the median of 3 runs
+    if dt < budget_s / 9 and rows < case.M:
+        rows = min(case.M, int(rows * max(1.0, (budget_s / 9) / max(dt, 1e-3))))
+    runs = []
+    for _ in range(3):
+        dt, cb, desc = oracle_sample_seconds(case, rows)
+        runs.append(dt)
+        if sum(runs) > budget_s:
+            break
+    s = statistics.median(runs)
+    return {"value": gbs(cb, s * 1e3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{desc}; median of {len(runs)} run(s), single thread", "seconds": s}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as tdist
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        tdist.init_process_group(backend="nccl", init_method="env://")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+
+    from invariant_gradient_reduction_gb300 import build as libbuild
+    libbuild.build()
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    dr.lib()
+
+    peaks = read_peaks()
+    timer = Timer(torch, device)
+    case = make_case(args.workload, device)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank).start()
+    time.sleep(0.1)
+    # warm-up, then exactly K timed steps bracketed by barrier + synchronize
+    full, red, atom, out, plan = scatter_step_fns(case, torch)
+    for _ in range(args.warmup):
+        timer.flush()
+        full()
+    if world > 1:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    l0 = dr.det_kernel_launches()
+    for s, e in ev:
+        timer.flush()
+        s.record()
+        full()
+        e.record()
+    torch.cuda.synchronize()
+    launches = dr.det_kernel_launches() - l0
+    if world > 1:
+        tdist.barrier()
+    t_wall1 = time.time()
+    times = [s.elapsed_time(e) for s, e in ev]
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    ms_step = sum(times) / len(times)
+
+    # reduce-only (the dominant kernel, for the roofline) and the atomic baseline
+    t_red, _ = timer.run(red, args.steps, args.warmup)
+    t_atom, _ = timer.run(atom, args.steps, args.warmup)
+    ms_red, ms_atom = statistics.mean(t_red), statistics.mean(t_atom)
+    cb = case.compulsory_bytes()
+    fingerprint = dr.det_hash(out).item() & (2 ** 64 - 1)
+
+    local = {"ms_step": ms_step, "ms_red": ms_red, "ms_atom": ms_atom, "launches": launches,
+             "wall_ms_per_step": (t_wall1 - t_wall0) * 1e3 / args.steps, "fingerprint": fingerprint}
+    if world > 1:
+        gathered = [None] * world
+        tdist.all_gather_object(gathered, local)
+    else:
+        gathered = [local]
+    agg = combine_ranks(gathered)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(case, timer, max(3, min(args.steps, 20)), args.warmup, torch)
+        if world > 1:
+            ge = [None] * world
+            tdist.all_gather_object(ge, e2e["ms_per_step"])
+            e2e["ms_per_step"] = max(ge)
+            e2e["value"] = world * gbs(cb, e2e["ms_per_step"])
+
+    also = {}
+    if not args.no_also and rank == 0:
+        for name in ("sparse_key_scatter",):
+            if name == args.workload:
+                continue
+            c2 = make_case(name, device)
+            r2 = measure_scatter(c2, timer, max(5, min(args.steps, 30)), args.warmup, torch, with_e2e=False)
+            r2.pop("times_full", None)
+            r2["frac_reduce_only"] = r2["reduce_only"]["gbs"] / peaks["hbm_gbs"]
+            r2["workload"] = WORKLOADS[name]
+            also[name] = r2
+            del c2
+            torch.cuda.empty_cache()
+        also["splitk"] = measure_splitk(timer, max(10, min(args.steps, 50)), args.warmup, torch, device)
+        also["splitk"]["workload"] = WORKLOADS["splitk"]
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = cpu_baseline(case)
+
+    if rank == 0:
+        red_gbs = gbs(cb, agg["ms_red"])
+        traffic = read_traffic("gather.cu", args.workload)
+        line = {
+            "metric": METRIC,
+            "value": world * gbs(cb, agg["ms_step"]),
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": agg["ms_step"],
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.workload],
+                       "step": "plan (histogram+scan+stable sort+work list) + gather-reduce",
+                       "l2": "flushed (256 MiB write) before every timed step, outside the step events",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "compulsory_bytes_per_step": cb},
+            "roofline": {"kernel": "gather_reduce_kernel", "bound": "hbm",
+                         "achieved": red_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": red_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                         "peak_source": peaks["source"] + " copy bandwidth (burst)",
+                         "algorithmic_bytes_per_launch": cb, "launch_ms": agg["ms_red"]},
+            "reduce_only": {"value": world * red_gbs, "ms": agg["ms_red"]},
+            "atomic": {"ms": agg["ms_atom"], "value": world * gbs(cb, agg["ms_atom"]),
+                       "overhead_reduce_only": agg["ms_red"] / agg["ms_atom"] - 1.0,
+                       "overhead_plan_reduce": agg["ms_step"] / agg["ms_atom"] - 1.0},
+            "e2e": e2e,
+            "gpu_launches": agg["launches"],
+            "clocks": clocks,
+            "wall_ms_per_step": agg["wall_ms_per_step"],
+            "out_fingerprint": f"{agg['fingerprint']:016x}",
+            "cpu_baseline": cpu,
+            "also": also or None,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        tdist.barrier()
+        tdist.destroy_process_group()
+
+
+def combine_ranks(per_rank):
+    """Max over ranks of the timed quantities; launches summed; fingerprints must agree."""
+    fps = {r["fingerprint"] for r in per_rank}
+    if len(fps) != 1:
+        raise RuntimeError(f"replicas disagree on the output fingerprint: {sorted(fps)}")
+    return {"ms_step": max(r["ms_step"] for r in per_rank), "ms_red": max(r["ms_red"] for r in per_rank),
+            "ms_atom": max(r["ms_atom"] for r in per_rank), "launches": sum(r["launches"] for r in per_rank),
+            "wall_ms_per_step": max(r["wall_ms_per_step"] for r in per_rank), "fingerprint": fps.pop()}
+
+
+# --------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    from invariant_gradient_reduction_gb300 import workloads as wl
+    case = wl.make(args.workload, "full", device="cpu")
+    # each step: the oracle on a bounded sample (a prefix of the destinations and their sources)
+    rows = 128
+    dt, cb, desc = oracle_sample_seconds(case, rows)
+    target = 2.0  # seconds per step
+    rows = max(1, min(case.M, int(rows * target / max(dt, 1e-3))))
+    for _ in range(args.warmup):
+        dt, cb, desc = oracle_sample_seconds(case, rows)
+    times = []
+    for _ in range(args.steps):
+        dt, cb, desc = oracle_sample_seconds(case, rows)
+        times.append(dt)
+    ms = statistics.mean(times) * 1e3
+    v = gbs(cb, ms)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload], "step": "CPU oracle (lists + canonical fold) on a sample",
+                   "parallelism": "single thread"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

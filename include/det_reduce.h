@@ -83,7 +83,7 @@ typedef int32_t det_dtype;
  * tests sweep them to prove it.
  *  grid_ctas        0 = auto; > 0 = exact number of CTAs for the reduce
  *                   kernels (they loop over their work until done).
- *  seg_chunks_log2  -1 = auto (3); otherwise 3..10.  A destination with more
+ *  seg_chunks_log2  -1 = auto (3); otherwise 3..6.  A destination with more
  *                   than 2^g chunks of 32 terms is split into segments of 2^g
  *                   chunks that run on different warps/CTAs; each segment is
  *                   one aligned node of the tree, written to a private fp32
@@ -126,6 +126,10 @@ int32_t det_last_cuda_error(void);
 
 /* Library ABI version: (major << 16) | minor. */
 int32_t det_version(void);
+
+/* Number of kernels this library has launched in this process (all threads,
+ * all devices), for counting launches inside a timed region. */
+int64_t det_kernel_launches(void);
 
 /*
  * Bytes of device workspace a plan over N sources and M destinations needs

@@ -1,0 +1,519 @@
+// gather.cu -- the deterministic gather-reduce (destination-major) and the
+// second pass for hot destinations.
+//
+// One warp task = one unit of the plan (a whole destination, or one hot
+// segment of 2^g chunks) x a group of H-tiles.  Inside a warp, lanes are
+// (slot, vector): T lanes cover one H-tile of a source row with 16-byte
+// loads, and 32/T slots fold different chunks of 32 terms at the same time.
+// Each lane folds its chunk left to right in registers; the slots of one
+// round are combined by a level-wise tree over xor shuffles, in which an
+// absent right neighbour leaves its left neighbour unchanged (the odd carry);
+// the round nodes, which are aligned tree nodes, go into a binary counter
+// whose merge order is exactly the level-wise pairwise tree.  None of these
+// choices changes a bit: each output element is the canonical sum of its
+// terms.
+//
+// The problem and its constraints: the MoE token combine index_add_ versus
+// scatter_add_ ("Megatron-LM determinism developer reference", section 3.1);
+// the sparse-attention backward scatter onto hot keys ("DeepSeek-V4 book, Ch
+// 09", section 3.1); private slots merged in a fixed order instead of writers
+// racing on one address ("Bit-exact training interview notes", table "where
+// nondeterminism comes from").
+#include <algorithm>
+
+#include "common.cuh"
+#include "plan_internal.cuh"
+
+namespace detr {
+
+constexpr int kGatherThreads = 256;
+constexpr int kGatherWarps = kGatherThreads / 32;
+constexpr int kBatch = 8;
+constexpr int kStagePad = 33;
+constexpr int kFinishThreads = 256;
+constexpr int kFinishLevels = 24;  // segments of one row < 2^23
+
+struct GatherArgs {
+    const int4* units;
+    long long n_tasks;
+    int tile_groups;      // task groups per unit
+    int tiles_per_group;
+    int ntiles;           // H-tiles per row
+    int H;
+    int T_log2;           // lanes per H-tile (row vector count)
+    int S_log2;           // chunk slots per warp = 32 >> T_log2
+    int g;                // a segment covers 2^g chunks
+    int out_vec;          // vector stores to out allowed
+    const int* row_ptr;
+    const int* perm;
+    const float* w;
+    long long ldx_bytes;
+    void* out;
+    long long ldo;
+    float* part;
+    long long ldpart;
+};
+
+template <typename XT, bool VECTOR>
+struct Loader;
+
+template <>
+struct Loader<float, true> {
+    static constexpr int VEC = 4;
+    using Raw = uint4;
+    static __device__ __forceinline__ Raw load(const unsigned char* p) { return ld_stream_v4(p); }
+    static __device__ __forceinline__ void expand(const Raw& r, float* f)
+    {
+        f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+        f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+    }
+};
+
+template <>
+struct Loader<uint16_t, true> {
+    static constexpr int VEC = 8;
+    using Raw = uint4;
+    static __device__ __forceinline__ Raw load(const unsigned char* p) { return ld_stream_v4(p); }
+    static __device__ __forceinline__ void expand(const Raw& r, float* f)
+    {
+        f[0] = bf16lo(r.x); f[1] = bf16hi(r.x); f[2] = bf16lo(r.y); f[3] = bf16hi(r.y);
+        f[4] = bf16lo(r.z); f[5] = bf16hi(r.z); f[6] = bf16lo(r.w); f[7] = bf16hi(r.w);
+    }
+};
+
+template <>
+struct Loader<float, false> {
+    static constexpr int VEC = 1;
+    using Raw = float;
+    static __device__ __forceinline__ Raw load(const unsigned char* p) { return __ldg(reinterpret_cast<const float*>(p)); }
+    static __device__ __forceinline__ void expand(const Raw& r, float* f) { f[0] = r; }
+};
+
+template <>
+struct Loader<uint16_t, false> {
+    static constexpr int VEC = 1;
+    using Raw = unsigned short;
+    static __device__ __forceinline__ Raw load(const unsigned char* p)
+    {
+        return __ldg(reinterpret_cast<const unsigned short*>(p));
+    }
+    static __device__ __forceinline__ void expand(const Raw& r, float* f)
+    {
+        f[0] = __uint_as_float(static_cast<uint32_t>(r) << 16);
+    }
+};
+
+// Store VEC fp32 values as OT (binary32, or bf16 rounded to nearest even).
+template <typename OT, int VEC>
+__device__ __forceinline__ void store_out(void* base, long long off, const float* v, bool vec)
+{
+    if (sizeof(OT) == 4) {
+        float* o = static_cast<float*>(base) + off;
+        if (vec && VEC % 4 == 0) {
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4)
+                *reinterpret_cast<float4*>(o + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = v[e];
+        }
+    } else {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(base) + off;
+        if (vec && VEC == 8) {
+            uint4 pk;
+            __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]);
+            __nv_bfloat162 t1 = __floats2bfloat162_rn(v[2], v[3]);
+            __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]);
+            __nv_bfloat162 t3 = __floats2bfloat162_rn(v[6], v[7]);
+            pk.x = *reinterpret_cast<uint32_t*>(&t0);
+            pk.y = *reinterpret_cast<uint32_t*>(&t1);
+            pk.z = *reinterpret_cast<uint32_t*>(&t2);
+            pk.w = *reinterpret_cast<uint32_t*>(&t3);
+            *reinterpret_cast<uint4*>(o) = pk;
+        } else if (vec && VEC == 4) {
+            uint2 pk;
+            __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]);
+            __nv_bfloat162 t1 = __floats2bfloat162_rn(v[2], v[3]);
+            pk.x = *reinterpret_cast<uint32_t*>(&t0);
+            pk.y = *reinterpret_cast<uint32_t*>(&t1);
+            *reinterpret_cast<uint2*>(o) = pk;
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = __float2bfloat16_rn(v[e]);
+        }
+    }
+}
+
+// Binary counter over aligned tree nodes: pushing node number `cnt` merges it
+// with its completed left neighbours, exactly as the level-wise tree pairs them.
+template <int DR, int VEC>
+__device__ __forceinline__ void counter_push(float (&stk)[DR][VEC], unsigned int cnt, float* node)
+{
+    unsigned int c = cnt;
+    bool placed = false;
+#pragma unroll
+    for (int L = 0; L < DR; ++L) {
+        if (!placed) {
+            if (c & 1u) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) node[e] = __fadd_rn(stk[L][e], node[e]);
+                c >>= 1;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) stk[L][e] = node[e];
+                placed = true;
+            }
+        }
+    }
+}
+
+// After the last push: the partial nodes at the right edge are carried up,
+// so the remaining levels combine from the lowest (rightmost) upward.
+template <int DR, int VEC>
+__device__ __forceinline__ void counter_collapse(const float (&stk)[DR][VEC], unsigned int cnt, float* res)
+{
+    bool have = false;
+#pragma unroll
+    for (int L = 0; L < DR; ++L) {
+        if ((cnt >> L) & 1u) {
+            if (!have) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) res[e] = stk[L][e];
+                have = true;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) res[e] = __fadd_rn(stk[L][e], res[e]);
+            }
+        }
+    }
+}
+
+template <typename XT, typename OT, bool VECTOR, int DR>
+__global__ void __launch_bounds__(kGatherThreads)
+gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant__ ShardTable tbl)
+{
+    using LD = Loader<XT, VECTOR>;
+    constexpr int VEC = LD::VEC;
+    extern __shared__ __align__(16) unsigned char smem[];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int S = 1 << a.S_log2;
+    const int T = 1 << a.T_log2;
+    const int lane_t = lane & (T - 1);
+    const int slot = lane >> a.T_log2;
+    const unsigned char** sptr =
+        reinterpret_cast<const unsigned char**>(smem) + static_cast<size_t>(warp) * S * kStagePad;
+    float* swt = reinterpret_cast<float*>(reinterpret_cast<const unsigned char**>(smem) +
+                                          static_cast<size_t>(kGatherWarps) * S * kStagePad) +
+                 static_cast<size_t>(warp) * S * kStagePad;
+    const bool has_w = a.w != nullptr;
+    const long long seg_terms = static_cast<long long>(kChunk) << a.g;
+
+    const long long nwarps = static_cast<long long>(gridDim.x) * kGatherWarps;
+    for (long long task = static_cast<long long>(blockIdx.x) * kGatherWarps + warp; task < a.n_tasks;
+         task += nwarps) {
+        const long long u = task / a.tile_groups;
+        const int tg = static_cast<int>(task - u * a.tile_groups);
+        const int4 ud = a.units[u];
+        const int m = ud.x, seg = ud.y;
+        const int lo = a.row_ptr[m], hi = a.row_ptr[m + 1];
+        int beg = lo, end = hi;
+        if (seg >= 0) {
+            beg = lo + static_cast<int>(seg * seg_terms);
+            end = static_cast<int>(min(static_cast<long long>(beg) + seg_terms, static_cast<long long>(hi)));
+        }
+        const int n = end - beg;
+        const int nch = (n + kChunk - 1) / kChunk;
+        const int nrounds = (nch + S - 1) >> a.S_log2;
+        const int t0 = tg * a.tiles_per_group;
+        const int t1 = min(t0 + a.tiles_per_group, a.ntiles);
+        bool staged = false;
+
+        for (int tile = t0; tile < t1; ++tile) {
+            const int v = tile * T + lane_t;
+            const int e0 = v * VEC;
+            const bool active = e0 < a.H;
+            float stk[DR][VEC];
+            unsigned int cnt = 0;
+            for (int r = 0; r < nrounds; ++r) {
+                if (nrounds > 1 || !staged) {
+                    __syncwarp();
+                    for (int s2 = 0; s2 < S; ++s2) {
+                        const int c2 = r * S + s2;
+                        const int j = beg + c2 * kChunk + lane;
+                        const unsigned char* p = nullptr;
+                        float wv = 1.0f;
+                        if (c2 < nch && j < end) {
+                            const int i = a.perm[j];
+                            p = shard_row(tbl, i, a.ldx_bytes);
+                            if (has_w) wv = a.w[i];
+                        }
+                        sptr[s2 * kStagePad + lane] = p;
+                        swt[s2 * kStagePad + lane] = wv;
+                    }
+                    __syncwarp();
+                    staged = true;
+                }
+                // fold this lane's chunk, left to right from its first term
+                const int c = r * S + slot;
+                float acc[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+                if (c < nch) {
+                    const int cnt_c = min(kChunk, n - c * kChunk);
+                    const unsigned char** myp = sptr + slot * kStagePad;
+                    const float* myw = swt + slot * kStagePad;
+                    const long long eoff = static_cast<long long>(e0) * sizeof(XT);
+                    for (int jb = 0; jb < cnt_c; jb += kBatch) {
+                        typename LD::Raw raw[kBatch];
+#pragma unroll
+                        for (int q = 0; q < kBatch; ++q)
+                            if (jb + q < cnt_c && active) raw[q] = LD::load(myp[jb + q] + eoff);
+#pragma unroll
+                        for (int q = 0; q < kBatch; ++q) {
+                            if (jb + q < cnt_c) {
+                                float xf[VEC];
+                                if (active) LD::expand(raw[q], xf);
+                                else {
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e) xf[e] = 0.0f;
+                                }
+                                if (has_w) {
+                                    const float wv = myw[jb + q];
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e) xf[e] = __fmul_rn(wv, xf[e]);
+                                }
+                                if (jb + q == 0) {
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e) acc[e] = xf[e];
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(acc[e], xf[e]);
+                                }
+                            }
+                        }
+                    }
+                }
+                // level-wise tree over the slots of this round (xor partners)
+                for (int lvl = 0; lvl < a.S_log2; ++lvl) {
+                    const int off = 1 << (a.T_log2 + lvl);
+                    float pv[VEC];
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) pv[e] = __shfl_xor_sync(0xffffffffu, acc[e], off);
+                    const int mine = r * S + ((slot >> lvl) << lvl);
+                    const int theirs = r * S + (((slot ^ (1 << lvl)) >> lvl) << lvl);
+                    if (mine < nch && theirs < nch) {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(acc[e], pv[e]);
+                    } else if (mine >= nch) {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc[e] = pv[e];
+                    }
+                }
+                counter_push<DR, VEC>(stk, cnt, acc);
+                ++cnt;
+            }
+            float res[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) res[e] = 0.0f;  // empty destination: +0.0
+            counter_collapse<DR, VEC>(stk, cnt, res);
+            if (slot == 0 && active) {
+                if (seg < 0) {
+                    store_out<OT, VEC>(a.out, static_cast<long long>(m) * a.ldo + e0, res, a.out_vec != 0);
+                } else {
+                    float* o = a.part + static_cast<long long>(ud.z) * a.ldpart + e0;
+                    if (VEC % 4 == 0) {
+#pragma unroll
+                        for (int e = 0; e < VEC; e += 4)
+                            *reinterpret_cast<float4*>(o + e) = make_float4(res[e], res[e + 1], res[e + 2], res[e + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) o[e] = res[e];
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Second pass for hot destinations: the level-wise tree over the row's
+// segment nodes (aligned nodes of 2^g chunks), in segment order.
+template <typename OT>
+__global__ void __launch_bounds__(kFinishThreads)
+finish_kernel(const int4* finish, long long n_items, int H, const float* part, long long ldpart, void* out,
+              long long ldo)
+{
+    const long long t = static_cast<long long>(blockIdx.x) * kFinishThreads + threadIdx.x;
+    if (t >= n_items) return;
+    const long long row_task = t / H;
+    const int h = static_cast<int>(t - row_task * H);
+    const int4 ft = finish[row_task];
+    const int m = ft.x, s0 = ft.y, ns = ft.z;
+    float stk[kFinishLevels][1];
+    unsigned int cnt = 0;
+    for (int s = 0; s < ns; s += kBatch) {
+        float v[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q)
+            if (s + q < ns) v[q] = __ldcs(part + static_cast<long long>(s0 + s + q) * ldpart + h);
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            if (s + q < ns) {
+                float node[1] = {v[q]};
+                counter_push<kFinishLevels, 1>(stk, cnt, node);
+                ++cnt;
+            }
+        }
+    }
+    float res[1] = {0.0f};
+    counter_collapse<kFinishLevels, 1>(stk, cnt, res);
+    store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
+}
+
+template <typename XT, typename OT, bool VECTOR, int DR>
+static det_status launch_gather(const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
+{
+    const size_t smem = static_cast<size_t>(kGatherWarps) * (1 << a.S_log2) * kStagePad * (sizeof(void*) + sizeof(float));
+    gather_reduce_kernel<XT, OT, VECTOR, DR><<<grid, kGatherThreads, smem, st>>>(a, t);
+    DETR_LAUNCHED();
+    return DET_OK;
+}
+
+template <typename XT, typename OT, bool VECTOR>
+static det_status launch_gather_dr(int DR, const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
+{
+    if (DR <= 1) return launch_gather<XT, OT, VECTOR, 1>(a, t, grid, st);
+    if (DR <= 4) return launch_gather<XT, OT, VECTOR, 4>(a, t, grid, st);
+    return launch_gather<XT, OT, VECTOR, 7>(a, t, grid, st);
+}
+
+template <typename XT, typename OT>
+static det_status launch_gather_vec(bool vec, int DR, const GatherArgs& a, const ShardTable& t, int grid,
+                                    cudaStream_t st)
+{
+    return vec ? launch_gather_dr<XT, OT, true>(DR, a, t, grid, st)
+               : launch_gather_dr<XT, OT, false>(DR, a, t, grid, st);
+}
+
+static int log2_floor(int64_t v)
+{
+    int r = 0;
+    while ((int64_t(1) << (r + 1)) <= v) ++r;
+    return r;
+}
+
+}  // namespace detr
+
+using namespace detr;
+
+extern "C" {
+
+det_status det_scatter_workspace_size(det_plan plan, int64_t H, size_t* bytes)
+{
+    if (!plan || !bytes || H < 0) return DET_ERR_ARG;
+    if (H > kMaxRows) return DET_ERR_UNSUPPORTED;
+    const int64_t ldpart = (H + 7) / 8 * 8;
+    *bytes = static_cast<size_t>(plan->n_segments) * static_cast<size_t>(ldpart) * sizeof(float);
+    return DET_OK;
+}
+
+det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                              det_dtype x_dtype, int64_t ldx, int64_t H, const float* w, void* out, int64_t ldo,
+                              det_dtype out_dtype, void* workspace, size_t ws_bytes, const det_opts* opts,
+                              void* stream)
+{
+    if (!plan) return DET_ERR_ARG;
+    if (!dtype_ok(x_dtype) || !dtype_ok(out_dtype)) return DET_ERR_DTYPE;
+    if (H < 0 || ldo < H) return DET_ERR_ARG;
+    if (H > kMaxRows) return DET_ERR_UNSUPPORTED;
+    ShardTable tbl;
+    size_t xbytes[DET_MAX_SHARDS] = {};
+    det_status s = make_shard_table(x_shards, shard_rows, P, plan->N, ldx, H, x_dtype, &tbl, xbytes);
+    if (s) return s;
+    const int64_t M = plan->M;
+    const int osz = dtype_size(out_dtype);
+    if (M > 0 && H > 0 && !out) return DET_ERR_ARG;
+    if (!aligned(out, static_cast<size_t>(osz)) || !aligned(w, 4)) return DET_ERR_ARG;
+    if (ldo > (int64_t(1) << 40)) return DET_ERR_ARG;
+    const size_t out_bytes = M > 0 && H > 0 ? static_cast<size_t>((M - 1) * ldo + H) * osz : 0;
+    size_t need = 0;
+    det_scatter_workspace_size(plan, H, &need);
+    if (need > 0 && (!workspace || !aligned(workspace, 256) || ws_bytes < need)) return DET_ERR_WORKSPACE;
+    for (int q = 0; q < P; ++q)
+        if (overlaps(out, out_bytes, x_shards[q], xbytes[q])) return DET_ERR_ARG;
+    if (overlaps(out, out_bytes, w, w ? static_cast<size_t>(plan->N) * 4 : 0) ||
+        overlaps(out, out_bytes, plan->ws, plan->ws_bytes) || overlaps(out, out_bytes, workspace, ws_bytes))
+        return DET_ERR_ARG;
+    if (need > 0 && overlaps(workspace, need, plan->ws, plan->ws_bytes)) return DET_ERR_ARG;
+    if (M == 0 || H == 0) return DET_OK;
+
+    const int xsz = dtype_size(x_dtype);
+    const int VEC = 16 / xsz;
+    bool vec = (H % VEC == 0) && ((ldx * xsz) % 16 == 0);
+    for (int q = 0; q < P; ++q)
+        if (shard_rows[q] > 0 && !aligned(x_shards[q], 16)) vec = false;
+    const int64_t V = vec ? H / VEC : H;
+
+    GatherArgs a{};
+    int T_log2 = V >= 32 ? 5 : std::max(2, log2_floor(V) + ((V & (V - 1)) ? 1 : 0));
+    a.T_log2 = T_log2;
+    a.S_log2 = 5 - T_log2;
+    a.ntiles = static_cast<int>(cdiv(V, int64_t(1) << T_log2));
+    a.H = static_cast<int>(H);
+    a.g = plan->g;
+    a.units = plan->units;
+    a.row_ptr = plan->row_ptr;
+    a.perm = plan->perm;
+    a.w = w;
+    a.ldx_bytes = ldx * xsz;
+    a.out = out;
+    a.ldo = ldo;
+    a.out_vec = aligned(out, 16) && (ldo * osz) % 16 == 0;
+    a.part = static_cast<float*>(workspace);
+    a.ldpart = (H + 7) / 8 * 8;
+
+    int sms = 0;
+    s = current_sm_count(&sms);
+    if (s) return s;
+    // Split the H-tiles of a unit into groups until there are enough warp
+    // tasks to fill the GPU several times over (the split changes no bit).
+    const int64_t target = static_cast<int64_t>(sms) * 64 * 4;
+    int tpg = a.ntiles;
+    while (tpg > 1 && plan->n_units * cdiv(a.ntiles, tpg) < target) tpg = static_cast<int>(cdiv(tpg, 2));
+    a.tiles_per_group = tpg;
+    a.tile_groups = static_cast<int>(cdiv(a.ntiles, tpg));
+    a.n_tasks = plan->n_units * a.tile_groups;
+
+    // Register stack depth: enough levels for the longest unit's rounds.
+    const int64_t G = int64_t(1) << plan->g;
+    const int64_t max_chunks = std::min(cdiv(plan->max_row_len, kChunk), G);
+    const int64_t max_rounds = cdiv(max_chunks, int64_t(1) << a.S_log2);
+    const int DR = max_rounds <= 1 ? 1 : (max_rounds <= 15 ? 4 : 7);
+
+    int64_t grid64 = opts && opts->grid_ctas > 0 ? opts->grid_ctas : cdiv(a.n_tasks, kGatherWarps);
+    grid64 = std::max<int64_t>(1, std::min<int64_t>(grid64, 2147483647));
+    const int grid = static_cast<int>(grid64);
+    cudaStream_t st = as_stream(stream);
+
+    if (a.n_tasks > 0) {
+        if (x_dtype == DET_BF16 && out_dtype == DET_BF16) s = launch_gather_vec<uint16_t, __nv_bfloat16>(vec, DR, a, tbl, grid, st);
+        else if (x_dtype == DET_BF16) s = launch_gather_vec<uint16_t, float>(vec, DR, a, tbl, grid, st);
+        else if (out_dtype == DET_BF16) s = launch_gather_vec<float, __nv_bfloat16>(vec, DR, a, tbl, grid, st);
+        else s = launch_gather_vec<float, float>(vec, DR, a, tbl, grid, st);
+        if (s) return s;
+    }
+    if (plan->n_hot_rows > 0) {
+        const long long items = plan->n_hot_rows * H;
+        const unsigned int fgrid = static_cast<unsigned int>(cdiv(items, kFinishThreads));
+        if (out_dtype == DET_BF16)
+            finish_kernel<__nv_bfloat16><<<fgrid, kFinishThreads, 0, st>>>(plan->finish, items, a.H, a.part, a.ldpart, out, ldo);
+        else
+            finish_kernel<float><<<fgrid, kFinishThreads, 0, st>>>(plan->finish, items, a.H, a.part, a.ldpart, out, ldo);
+        DETR_LAUNCHED();
+    }
+    if (opts && opts->debug_checks) DETR_CUDA(cudaStreamSynchronize(st));
+    return DET_OK;
+}
+
+}  // extern "C"

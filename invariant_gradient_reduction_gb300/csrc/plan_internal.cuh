@@ -1,0 +1,37 @@
+// plan_internal.cuh -- the plan handle and the device counter block, shared by
+// plan.cu (which builds a plan) and gather.cu (which runs it).
+#pragma once
+
+#include <stdint.h>
+#include <vector_types.h>
+
+namespace detr {
+
+// int32 counter block at the start of the plan workspace.
+enum {
+    kCtrErrIndex = 0,  // some idx outside [0, M)
+    kCtrErrDup = 1,    // two sources of one destination share an order key
+    kCtrSegs = 2,      // hot segments (units that write partial slots)
+    kCtrNormal = 3,    // whole-destination units
+    kCtrHot = 4,       // destinations split into segments (finish tasks)
+    kCtrMaxLen = 5,    // longest destination list
+    kCtrCount = 16
+};
+
+}  // namespace detr
+
+// Host handle.  Device arrays live in the caller's plan workspace.
+//   units[u]  = {row m, segment s (-1 = whole row), partial slot, 0}; hot
+//               segments first, then whole rows in row order.
+//   finish[k] = {row m, first partial slot, number of segments, 0}.
+struct det_plan_s {
+    int64_t N = 0, M = 0;
+    int g = 3;                       // a hot segment covers 2^g chunks of 32 terms
+    unsigned char* ws = nullptr;
+    size_t ws_bytes = 0;
+    int* row_ptr = nullptr;          // [M+1]
+    int* perm = nullptr;             // [N]
+    int4* units = nullptr;
+    int4* finish = nullptr;
+    int64_t n_units = 0, n_segments = 0, n_hot_rows = 0, max_row_len = 0;
+};

@@ -1,0 +1,232 @@
+// splitk.cu -- split-id-ordered split-K reduce.
+//
+// The mHC backward cannot avoid split-K (output width 24, K = 7168): every
+// K-split writes its own buffer and a deterministic reduce kernel sums them
+// in split-id order ("DeepSeek-V4 book, Ch 09: Batch invariance and
+// determinism", section 3.3).  Here the sum over s is the same canonical fold
+// as the scatter-reduce: chunks of 32 splits folded left to right, then the
+// level-wise pairwise tree with the odd chunk carried up.  A thread owns four
+// consecutive outputs (16-byte loads) and one chunk slot; neighbouring lanes
+// fold neighbouring chunks and meet through xor shuffles.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace detr {
+
+constexpr int kSplitThreads = 256;
+constexpr int kSplitBatch = 8;
+constexpr int kMaxSplitSlotsLog2 = 3;
+constexpr int kMaxSplitRounds = 127;
+
+struct SplitArgs {
+    const float* P;
+    long long ldp;
+    long long nvec;     // output vectors (VEC outputs each)
+    long long items;    // nvec << slots_log2
+    void* out;
+    int S;
+    int slots_log2;
+    int out_vec;
+};
+
+template <int DR, int VEC>
+__device__ __forceinline__ void sk_push(float (&stk)[DR][VEC], unsigned int cnt, float* node)
+{
+    unsigned int c = cnt;
+    bool placed = false;
+#pragma unroll
+    for (int L = 0; L < DR; ++L) {
+        if (!placed) {
+            if (c & 1u) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) node[e] = __fadd_rn(stk[L][e], node[e]);
+                c >>= 1;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) stk[L][e] = node[e];
+                placed = true;
+            }
+        }
+    }
+}
+
+template <typename OT, bool VECTOR, int DR>
+__global__ void __launch_bounds__(kSplitThreads) splitk_kernel(const __grid_constant__ SplitArgs a)
+{
+    constexpr int VEC = VECTOR ? 4 : 1;
+    const int lane = threadIdx.x & 31;
+    const int slots = 1 << a.slots_log2;
+    const int nch = (a.S + kChunk - 1) / kChunk;
+    const int nrounds = (nch + slots - 1) >> a.slots_log2;
+    const long long gwarp = (static_cast<long long>(blockIdx.x) * kSplitThreads + threadIdx.x) >> 5;
+    const long long nwarps = (static_cast<long long>(gridDim.x) * kSplitThreads) >> 5;
+    for (long long base = gwarp * 32; base < a.items; base += nwarps * 32) {
+        const long long item = base + lane;
+        const bool valid = item < a.items;
+        const long long v = item >> a.slots_log2;
+        const int slot = static_cast<int>(item & (slots - 1));
+        const long long e0 = v * VEC;
+        float stk[DR][VEC];
+        unsigned int cnt = 0;
+        for (int r = 0; r < nrounds; ++r) {
+            const int c = r * slots + slot;
+            float acc[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+            if (valid && c < nch) {
+                const int s_lo = c * kChunk;
+                const int cnt_c = min(kChunk, a.S - s_lo);
+                const float* col = a.P + static_cast<long long>(s_lo) * a.ldp + e0;
+                for (int jb = 0; jb < cnt_c; jb += kSplitBatch) {
+                    float vals[kSplitBatch][VEC];
+#pragma unroll
+                    for (int q = 0; q < kSplitBatch; ++q) {
+                        if (jb + q < cnt_c) {
+                            const float* src = col + static_cast<long long>(jb + q) * a.ldp;
+                            if (VECTOR) {
+                                const uint4 u = ld_stream_v4(src);
+                                vals[q][0] = __uint_as_float(u.x);
+                                if (VEC > 1) {
+                                    vals[q][VEC > 1 ? 1 : 0] = __uint_as_float(u.y);
+                                    vals[q][VEC > 2 ? 2 : 0] = __uint_as_float(u.z);
+                                    vals[q][VEC > 3 ? 3 : 0] = __uint_as_float(u.w);
+                                }
+                            } else {
+                                vals[q][0] = __ldcs(src);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < kSplitBatch; ++q) {
+                        if (jb + q < cnt_c) {
+                            if (jb + q == 0) {
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e) acc[e] = vals[q][e];
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(acc[e], vals[q][e]);
+                            }
+                        }
+                    }
+                }
+            }
+            for (int lvl = 0; lvl < a.slots_log2; ++lvl) {
+                float pv[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) pv[e] = __shfl_xor_sync(0xffffffffu, acc[e], 1 << lvl);
+                const int mine = r * slots + ((slot >> lvl) << lvl);
+                const int theirs = r * slots + (((slot ^ (1 << lvl)) >> lvl) << lvl);
+                if (mine < nch && theirs < nch) {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(acc[e], pv[e]);
+                } else if (mine >= nch) {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[e] = pv[e];
+                }
+            }
+            sk_push<DR, VEC>(stk, cnt, acc);
+            ++cnt;
+        }
+        float res[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) res[e] = 0.0f;
+        bool have = false;
+#pragma unroll
+        for (int L = 0; L < DR; ++L) {
+            if ((cnt >> L) & 1u) {
+                if (!have) {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) res[e] = stk[L][e];
+                    have = true;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) res[e] = __fadd_rn(stk[L][e], res[e]);
+                }
+            }
+        }
+        if (valid && slot == 0) {
+            if (sizeof(OT) == 4) {
+                float* o = static_cast<float*>(a.out) + e0;
+                if (VECTOR && a.out_vec) *reinterpret_cast<float4*>(o) = make_float4(res[0], res[VEC > 1 ? 1 : 0], res[VEC > 2 ? 2 : 0], res[VEC > 3 ? 3 : 0]);
+                else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) o[e] = res[e];
+                }
+            } else {
+                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + e0;
+                if (VECTOR && a.out_vec) {
+                    __nv_bfloat162 t0 = __floats2bfloat162_rn(res[0], res[VEC > 1 ? 1 : 0]);
+                    __nv_bfloat162 t1 = __floats2bfloat162_rn(res[VEC > 2 ? 2 : 0], res[VEC > 3 ? 3 : 0]);
+                    uint2 pk;
+                    pk.x = *reinterpret_cast<uint32_t*>(&t0);
+                    pk.y = *reinterpret_cast<uint32_t*>(&t1);
+                    *reinterpret_cast<uint2*>(o) = pk;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) o[e] = __float2bfloat16_rn(res[e]);
+                }
+            }
+        }
+    }
+}
+
+template <typename OT, bool VECTOR>
+static void launch_splitk(int DR, const SplitArgs& a, int grid, cudaStream_t st)
+{
+    if (DR <= 1) splitk_kernel<OT, VECTOR, 1><<<grid, kSplitThreads, 0, st>>>(a);
+    else if (DR <= 4) splitk_kernel<OT, VECTOR, 4><<<grid, kSplitThreads, 0, st>>>(a);
+    else splitk_kernel<OT, VECTOR, 7><<<grid, kSplitThreads, 0, st>>>(a);
+}
+
+}  // namespace detr
+
+using namespace detr;
+
+extern "C" det_status det_splitk_reduce(const float* partials, int32_t S, int64_t count, int64_t ldp, void* out,
+                                        det_dtype out_dtype, const det_opts* opts, void* stream)
+{
+    if (!dtype_ok(out_dtype)) return DET_ERR_DTYPE;
+    if (S < 0 || count < 0 || ldp < count) return DET_ERR_ARG;
+    if (count == 0) return DET_OK;
+    if (!out || (S > 0 && !partials)) return DET_ERR_ARG;
+    if (!aligned(partials, 4) || !aligned(out, static_cast<size_t>(dtype_size(out_dtype)))) return DET_ERR_ARG;
+    if (ldp > (int64_t(1) << 40) || count > (int64_t(1) << 40)) return DET_ERR_UNSUPPORTED;
+    const size_t pbytes = S > 0 ? static_cast<size_t>((S - 1) * ldp + count) * 4 : 0;
+    if (overlaps(out, static_cast<size_t>(count) * dtype_size(out_dtype), partials, pbytes)) return DET_ERR_ARG;
+    const int nch = (S + kChunk - 1) / kChunk;
+    int slots_log2 = 0;
+    while ((1 << slots_log2) < nch && slots_log2 < kMaxSplitSlotsLog2) ++slots_log2;
+    const int rounds = (nch + (1 << slots_log2) - 1) >> slots_log2;
+    if (rounds > kMaxSplitRounds) return DET_ERR_UNSUPPORTED;
+    const int DR = rounds <= 1 ? 1 : (rounds <= 15 ? 4 : 7);
+    const bool vec = aligned(partials, 16) && ldp % 4 == 0 && count % 4 == 0;
+    SplitArgs a{};
+    a.P = partials;
+    a.ldp = ldp;
+    a.nvec = vec ? count / 4 : count;
+    a.slots_log2 = slots_log2;
+    a.items = a.nvec << slots_log2;
+    a.out = out;
+    a.S = S;
+    a.out_vec = aligned(out, 16);
+    int64_t grid64 = opts && opts->grid_ctas > 0 ? opts->grid_ctas : cdiv(a.items, kSplitThreads);
+    grid64 = std::max<int64_t>(1, std::min<int64_t>(grid64, 2147483647));
+    cudaStream_t st = as_stream(stream);
+    if (S == 0) {
+        // no terms: every output is +0.0
+        DETR_CUDA(cudaMemsetAsync(out, 0, static_cast<size_t>(count) * dtype_size(out_dtype), st));
+        return DET_OK;
+    }
+    const int grid = static_cast<int>(grid64);
+    if (out_dtype == DET_BF16) {
+        if (vec) launch_splitk<__nv_bfloat16, true>(DR, a, grid, st);
+        else launch_splitk<__nv_bfloat16, false>(DR, a, grid, st);
+    } else {
+        if (vec) launch_splitk<float, true>(DR, a, grid, st);
+        else launch_splitk<float, false>(DR, a, grid, st);
+    }
+    DETR_LAUNCHED();
+    if (opts && opts->debug_checks) DETR_CUDA(cudaStreamSynchronize(st));
+    return DET_OK;
+}

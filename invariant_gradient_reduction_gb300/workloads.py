@@ -176,7 +176,7 @@ SMALL = {
                         out_dtype=torch.bfloat16, seed=12),
     "ep_invariance": dict(kind="moe", T=512, E=64, k=8, H=712, x_dtype=torch.bfloat16,
                           out_dtype=torch.bfloat16, seed=13),
-    "sparse_key_scatter": dict(kind="sparse", Q=256, K=128, S=4096, H=128, zipf_s=1.1, sigma=0.02, seed=14),
+    "sparse_key_scatter": dict(kind="sparse", Q=640, K=128, S=4096, H=128, zipf_s=1.1, sigma=0.02, seed=14),
     "splitk": dict(kind="splitk", S=56, R=1000, C=24, seed=15),
 }
 

@@ -1,0 +1,442 @@
+"""GPU path vs the CPU oracle, byte for byte, through the C ABI.
+
+Tolerance: 0 ULP everywhere (bytes compared); the canonical order fixes every
+bit, so any difference is a bug.  Covers the five workloads (small sizes in
+full, full sizes on sampled destinations), the grid / segment-size / replay /
+shard invariances, and the edge cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_bytes_equal, gpu_scatter, np_bits, oracle_scatter
+from invariant_gradient_reduction_gb300 import detreduce as dr
+from invariant_gradient_reduction_gb300 import workloads as wl
+from invariant_gradient_reduction_gb300.workloads import ScatterCase
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from invariant_gradient_reduction_gb300 import build
+    build.build()
+    dr.lib()
+    oracle.build()
+
+
+def sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def small_case(name):
+    return wl.make(name, "small", device=DEV)
+
+
+SCATTER_SMALL = ["tiny_moe", "moe_combine", "ep_invariance", "sparse_key_scatter"]
+
+
+# --------------------------------------------------------------------------
+# plan: destination lists are integer-exact
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,M,src", [(0, 7, False), (1, 1, False), (1000, 1, False), (5000, 37, False),
+                                     (70000, 300, False), (20000, 70000, False), (9000, 600, True),
+                                     (100000, 65536, False), (40000, 5, True)])
+def test_plan_lists_match_oracle(N, M, src):
+    g = torch.Generator().manual_seed(N * 31 + M)
+    idx = torch.randint(0, M, (N,), generator=g, dtype=torch.int32)
+    sid = None
+    if src:
+        sid = (torch.randperm(N, generator=g) * 5 - 100).to(torch.int64)
+    plan = dr.det_reduce_plan(idx.to(DEV), M, src_id=None if sid is None else sid.to(DEV))
+    rp, perm = dr.plan_lists(plan)
+    want_rp, want_perm = oracle.build_lists(idx.numpy(), M, src_id=None if sid is None else sid.numpy())
+    assert np.array_equal(rp.cpu().numpy().astype(np.int64), want_rp)
+    assert np.array_equal(perm.cpu().numpy().astype(np.int64), want_perm)
+    d = plan.describe()
+    counts = np.diff(want_rp)
+    assert d["max_row_len"] == (counts.max() if M else 0)
+
+
+def test_plan_zipf_hot_rows_and_work_list():
+    case = small_case("sparse_key_scatter")
+    plan = dr.det_reduce_plan(case.idx, case.M)
+    rp, perm = dr.plan_lists(plan)
+    want_rp, want_perm = oracle.build_lists(case.idx.cpu().numpy(), case.M)
+    assert np.array_equal(rp.cpu().numpy(), want_rp)
+    assert np.array_equal(perm.cpu().numpy(), want_perm)
+    d = plan.describe()
+    counts = np.diff(want_rp)
+    nch = (counts + 31) // 32
+    G = 1 << d["seg_chunks_log2"]
+    hot = nch > G
+    assert d["n_hot_rows"] == int(hot.sum())
+    assert d["n_segments"] == int(((nch[hot] + G - 1) // G).sum())
+    assert d["n_units"] == d["n_segments"] + int((~hot).sum())
+    assert d["n_hot_rows"] > 0
+
+
+def test_plan_errors():
+    idx = torch.tensor([0, 1, 5, 2], dtype=torch.int32, device=DEV)
+    with pytest.raises(dr.DetError) as e:
+        dr.det_reduce_plan(idx, 5)
+    assert e.value.code == dr.DET_ERR_INDEX_RANGE
+    with pytest.raises(dr.DetError) as e:
+        dr.det_reduce_plan(torch.tensor([0, -1], dtype=torch.int32, device=DEV), 5)
+    assert e.value.code == dr.DET_ERR_INDEX_RANGE
+    with pytest.raises(dr.DetError) as e:
+        dr.det_reduce_plan(torch.tensor([1, 1, 0], dtype=torch.int32, device=DEV), 3,
+                           src_id=torch.tensor([7, 7, 7], dtype=torch.int64, device=DEV))
+    assert e.value.code == dr.DET_ERR_ORDER_KEY
+    # equal keys in different destinations are fine
+    dr.det_reduce_plan(torch.tensor([1, 2, 0], dtype=torch.int32, device=DEV), 3,
+                       src_id=torch.tensor([7, 7, 7], dtype=torch.int64, device=DEV))
+    with pytest.raises(dr.DetError) as e:
+        dr.det_reduce_plan(idx[:2], 5, workspace=torch.empty(64, dtype=torch.uint8, device=DEV))
+    assert e.value.code == dr.DET_ERR_WORKSPACE
+
+
+# --------------------------------------------------------------------------
+# scatter-reduce parity
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", SCATTER_SMALL)
+def test_scatter_small_matches_oracle(name):
+    case = small_case(name)
+    out, plan = gpu_scatter(case)
+    assert_bytes_equal(np_bits(out), oracle_scatter(case), name)
+
+
+@pytest.mark.parametrize("name", ["moe_combine", "sparse_key_scatter"])
+@pytest.mark.parametrize("seg", [3, 4, 5, 6])
+def test_segment_size_changes_no_bit(name, seg):
+    case = small_case(name)
+    base, _ = gpu_scatter(case)
+    out, plan = gpu_scatter(case, opts={"seg_chunks_log2": seg})
+    assert_bytes_equal(np_bits(out), np_bits(base), f"{name} g={seg}")
+
+
+@pytest.mark.parametrize("name", ["moe_combine", "sparse_key_scatter", "tiny_moe"])
+def test_grid_size_changes_no_bit(name):
+    case = small_case(name)
+    base, plan = gpu_scatter(case)
+    want = np_bits(base)
+    for grid in (1, 3, sms() - 1, sms(), 4 * sms(), 0):
+        out = torch.empty_like(base)
+        dr.det_scatter_reduce(plan, case.x, out, w=case.w, opts={"grid_ctas": grid})
+        assert_bytes_equal(np_bits(out), want, f"{name} grid={grid}")
+
+
+def test_replays_identical_under_contention():
+    """R replays give identical bytes and identical fingerprints, also while a side
+    stream runs matmuls (the pages' contention replay)."""
+    case = small_case("sparse_key_scatter")
+    base, plan = gpu_scatter(case)
+    want = np_bits(base)
+    h0 = dr.det_hash(base).item()
+    side = torch.cuda.Stream()
+    a = torch.randn(2048, 2048, device=DEV)
+    for r in range(6):
+        with torch.cuda.stream(side):
+            for _ in range(4):
+                a = a @ a.T * 1e-3
+        out = torch.empty_like(base)
+        dr.det_scatter_reduce(plan, case.x, out, w=case.w)
+        torch.cuda.synchronize()
+        assert dr.det_hash(out).item() == h0
+        assert_bytes_equal(np_bits(out), want, f"replay {r}")
+
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8])
+def test_ep_shards_identical(P):
+    """Sources split into P separate expert-shard buffers give identical bytes."""
+    case = small_case("ep_invariance")
+    base, plan = gpu_scatter(case)
+    rows = wl.ep_shard_rows(case, P)
+    shards = wl.split_rows(case.x, rows)
+    out, _ = gpu_scatter(case, shards=shards, plan=plan)
+    assert_bytes_equal(np_bits(out), np_bits(base), f"P={P}")
+    assert_bytes_equal(np_bits(out), oracle_scatter(case), f"P={P} vs oracle")
+
+
+def test_physical_row_permutation_with_src_id():
+    case = small_case("moe_combine")
+    base, _ = gpu_scatter(case)
+    g = torch.Generator().manual_seed(5)
+    pr = torch.randperm(case.N, generator=g)
+    prd = pr.to(DEV)
+    perm_case = ScatterCase(name="permuted", idx=case.idx[prd].contiguous(), x=case.x[prd].contiguous(),
+                            w=case.w[prd].contiguous(), M=case.M, out_dtype=case.out_dtype,
+                            src_id=prd.to(torch.int64))
+    out, _ = gpu_scatter(perm_case)
+    assert_bytes_equal(np_bits(out), np_bits(base), "permuted rows with src_id")
+
+
+def test_batch_invariance():
+    """One token's 8 rows combined alone and inside batches of other sizes, at other
+    positions: identical output row (property A of the DeepSeek-V4 chapter)."""
+    H = 4096
+    g = torch.Generator(device=DEV).manual_seed(3)
+    tok = torch.randn(8, H, generator=g, device=DEV).to(torch.bfloat16)
+    tw = torch.rand(8, generator=g, device=DEV)
+    alone = ScatterCase("alone", torch.zeros(8, dtype=torch.int32, device=DEV), tok, tw, 1, torch.bfloat16)
+    want = np_bits(gpu_scatter(alone)[0])[0]
+    for T in (3, 64, 1000):
+        big = wl.moe_combine(T, 16, 8, H, seed=T, device=DEV)
+        pos = T // 2
+        keep = big.idx != pos
+        others_idx, others_x, others_w = big.idx[keep], big.x[keep], big.w[keep]
+        n = others_idx.numel()
+        slots = torch.sort(torch.randperm(n + 8, generator=torch.Generator().manual_seed(T))[:8]).values.to(DEV)
+        mask = torch.zeros(n + 8, dtype=torch.bool, device=DEV)
+        mask[slots] = True
+        idx = torch.empty(n + 8, dtype=torch.int32, device=DEV)
+        x = torch.empty(n + 8, H, dtype=torch.bfloat16, device=DEV)
+        w = torch.empty(n + 8, device=DEV)
+        idx[mask], x[mask], w[mask] = pos, tok, tw
+        idx[~mask], x[~mask], w[~mask] = others_idx, others_x, others_w
+        out, _ = gpu_scatter(ScatterCase("batch", idx, x, w, T, torch.bfloat16))
+        assert np_bits(out)[pos].tobytes() == want.tobytes()
+
+
+# --------------------------------------------------------------------------
+# full-size workloads (sampled destinations checked against the oracle)
+# --------------------------------------------------------------------------
+
+def _sample_rows(case, k, rng):
+    counts = torch.bincount(case.idx.long(), minlength=case.M).cpu().numpy()
+    hot = np.argsort(-counts, kind="stable")[:8]
+    rows = set(hot.tolist()) | set(rng.choice(case.M, size=k, replace=False).tolist()) | {0, case.M - 1}
+    return sorted(rows)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["tiny_moe", "moe_combine", "ep_invariance", "sparse_key_scatter"])
+def test_full_size_sampled_parity(name):
+    case = wl.make(name, "full", device=DEV)
+    out, plan = gpu_scatter(case)
+    rng = np.random.default_rng(2024)
+    rows = _sample_rows(case, 64 if name != "tiny_moe" else case.M - 2, rng)
+    want = oracle_scatter(case, rows)
+    got = np_bits(out)[np.array(rows)]
+    assert_bytes_equal(got, want, name)
+    if name == "ep_invariance":
+        for P in (2, 4, 8):
+            shards = wl.split_rows(case.x, wl.ep_shard_rows(case, P))
+            o2, _ = gpu_scatter(case, shards=shards, plan=plan)
+            assert torch.equal(o2.view(torch.int16), out.view(torch.int16)), P
+            del shards, o2
+    if name == "sparse_key_scatter":
+        for grid in (sms(), 3 * sms() + 1):
+            o3 = torch.empty_like(out)
+            dr.det_scatter_reduce(plan, case.x, o3, w=case.w, opts={"grid_ctas": grid})
+            assert torch.equal(o3.view(torch.int32), out.view(torch.int32)), grid
+
+
+# --------------------------------------------------------------------------
+# edge cases
+# --------------------------------------------------------------------------
+
+def _case(idx, x, M, w=None, out_dtype=torch.float32, src_id=None):
+    return ScatterCase("edge", torch.as_tensor(idx, dtype=torch.int32).to(DEV), x.to(DEV),
+                       None if w is None else w.to(DEV), M, out_dtype,
+                       None if src_id is None else src_id.to(DEV))
+
+
+@pytest.mark.parametrize("n", [1, 2, 31, 32, 33, 63, 64, 65, 255, 256, 257, 1000, 4097, 16384, 20001])
+@pytest.mark.parametrize("H,xdt", [(128, torch.bfloat16), (24, torch.float32), (13, torch.bfloat16)])
+def test_row_lengths(n, H, xdt):
+    g = torch.Generator().manual_seed(n + H)
+    M = 3
+    idx = torch.full((n,), 1, dtype=torch.int32)
+    idx[::7] = 0
+    x = (torch.randn(n, H, generator=g) * torch.exp2(torch.randint(-12, 12, (n, 1), generator=g).float())).to(xdt)
+    w = torch.rand(n, generator=g)
+    for od in (torch.float32, torch.bfloat16):
+        case = _case(idx, x, M, w, od)
+        out, _ = gpu_scatter(case)
+        assert_bytes_equal(np_bits(out), oracle_scatter(case), f"n={n} H={H} {xdt} -> {od}")
+
+
+def test_empty_inputs():
+    x = torch.zeros(0, 16, dtype=torch.bfloat16)
+    case = _case([], x, 5)
+    out = torch.full((5, 16), 7.0, device=DEV)
+    gpu_scatter(case, out=out)
+    assert torch.equal(out, torch.zeros_like(out)) and not torch.signbit(out).any()
+    # M = 0, N = 0
+    case0 = _case([], x, 0)
+    gpu_scatter(case0)
+    # H = 0
+    casen = _case([0, 1], torch.zeros(2, 0), 3)
+    gpu_scatter(casen)
+
+
+def test_negative_zero_and_specials():
+    """All -0.0 terms give -0.0; empty rows give +0.0; inf, subnormals and NaN propagate."""
+    n = 70
+    H = 8
+    x = torch.full((n, H), -0.0)
+    x[:, 1] = torch.tensor(float("inf"))
+    x[5, 2] = float("-inf")
+    x[7, 2] = float("inf")  # inf - inf: NaN
+    x[:, 3] = 1e-40  # subnormal
+    x[:, 4] = -1e-45
+    x[3, 5] = float("nan")
+    x[:, 6] = 3.4e38
+    idx = torch.zeros(n, dtype=torch.int32)
+    case = _case(idx, x, 2)
+    out = np_bits(gpu_scatter(case)[0])
+    want = oracle_scatter(case)
+    assert out[0, 0].view(np.uint32) == 0x80000000
+    assert out[1].view(np.uint32).tolist() == [0] * H
+    assert np.isnan(out[0, 2]) and np.isnan(out[0, 5])
+    fin = [0, 1, 3, 4, 6, 7]
+    assert_bytes_equal(out[:, fin], want[:, fin], "specials")
+    assert np.isinf(out[0, 6])  # overflow to +inf
+
+
+def test_padded_and_unaligned_rows():
+    """Row strides that are not a multiple of 16 bytes take the scalar path: same bits."""
+    g = torch.Generator().manual_seed(9)
+    N, M, H = 3000, 40, 96
+    idx = torch.randint(0, M, (N,), generator=g, dtype=torch.int32)
+    base = torch.randn(N, H + 3, generator=g).to(torch.bfloat16)
+    w = torch.rand(N, generator=g)
+    padded = _case(idx, base[:, :H], M, w, torch.bfloat16)  # ldx = 99 elements: scalar loads
+    dense = _case(idx, base[:, :H].contiguous(), M, w, torch.bfloat16)
+    a = np_bits(gpu_scatter(padded)[0])
+    b = np_bits(gpu_scatter(dense)[0])
+    assert_bytes_equal(a, b, "padded vs dense")
+    assert_bytes_equal(a, oracle_scatter(dense), "vs oracle")
+    # padded output rows: columns beyond H untouched
+    out = torch.full((M, H + 5), 3.0, dtype=torch.bfloat16, device=DEV)[:, :H]
+    gpu_scatter(dense, out=out)
+    full = out.as_strided((M, H + 5), (H + 5, 1))
+    assert torch.all(full[:, H:] == 3.0)
+    assert_bytes_equal(np_bits(out), b, "padded out")
+
+
+def test_no_fused_multiply_add_on_gpu():
+    """Same construction as the oracle pin: a fused multiply-add would give 2^-24."""
+    xs = torch.tensor([[1.0 + 2.0 ** -7] * 8, [-(1.0 + 2.0 ** -7)] * 8]).to(torch.bfloat16)
+    w = torch.tensor([1.0 + 2.0 ** -17] * 2)
+    case = _case([0, 0], xs, 1, w, src_id=torch.tensor([1, 0], dtype=torch.int64))
+    out = np_bits(gpu_scatter(case)[0])
+    assert np.all(out.view(np.uint32) == 0)
+
+
+def test_scatter_argument_errors():
+    case = small_case("tiny_moe")
+    plan = dr.det_reduce_plan(case.idx, case.M)
+    out = torch.empty(case.M, case.H, device=DEV)
+    with pytest.raises(dr.DetError) as e:  # out aliases x
+        dr.det_scatter_reduce(plan, case.x, case.x[:case.M], w=case.w)
+    assert e.value.code == dr.DET_ERR_ARG
+    with pytest.raises(dr.DetError) as e:  # shards do not add up to N
+        dr.det_scatter_reduce(plan, [case.x[:10]], out, w=case.w)
+    assert e.value.code == dr.DET_ERR_ARG
+
+
+# --------------------------------------------------------------------------
+# split-K
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("size", ["small", "full"])
+@pytest.mark.parametrize("odt", [torch.float32, torch.bfloat16])
+def test_splitk_matches_oracle(size, odt):
+    P = wl.make("splitk", size, device=DEV)
+    out = torch.empty(P.shape[1], dtype=odt, device=DEV)
+    dr.det_splitk_reduce(P, out)
+    want = oracle.splitk_reduce(P.cpu().numpy(), out_dtype=oracle.F32 if odt == torch.float32 else oracle.BF16)
+    assert_bytes_equal(np_bits(out), want, f"splitk {size} {odt}")
+    for grid in (1, 7, sms(), 5 * sms()):
+        o2 = torch.empty_like(out)
+        dr.det_splitk_reduce(P, o2, opts={"grid_ctas": grid})
+        assert_bytes_equal(np_bits(o2), want, f"grid {grid}")
+
+
+@pytest.mark.parametrize("S", [0, 1, 2, 31, 32, 33, 56, 64, 65, 100, 257, 1000, 4000])
+def test_splitk_split_counts(S):
+    g = torch.Generator().manual_seed(S)
+    count = 4 * 37
+    P = (torch.randn(S, count, generator=g) * torch.exp2(torch.rand(S, count, generator=g) * 16 - 8))
+    want = oracle.splitk_reduce(P.numpy()) if S > 0 else np.zeros(count, np.float32)
+    out = torch.empty(count, device=DEV)
+    dr.det_splitk_reduce(P.to(DEV), out)
+    assert_bytes_equal(np_bits(out), want, f"S={S}")
+    # unaligned count / stride: scalar path
+    P2 = P[:, :count - 1].to(DEV)
+    o2 = torch.empty(count - 1, device=DEV)
+    dr.det_splitk_reduce(P2, o2)
+    assert_bytes_equal(np_bits(o2), want[:count - 1], f"S={S} scalar")
+
+
+# --------------------------------------------------------------------------
+# fingerprint
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("nbytes", [0, 1, 7, 8, 9, 15, 16, 17, 31, 33, 1000, 4096, 65537, 10_000_019])
+def test_hash_matches_oracle(nbytes):
+    g = torch.Generator().manual_seed(nbytes)
+    buf = torch.randint(0, 256, (nbytes + 16,), generator=g, dtype=torch.uint8)
+    dbuf = buf.to(DEV)
+    for off in (0, 1, 3, 8, 12):
+        got = dr.det_hash(dbuf, nbytes=nbytes, byte_offset=off).item() & (2 ** 64 - 1)
+        want = oracle.hash_bytes(buf[off:off + nbytes].numpy())
+        assert got == want, (nbytes, off)
+
+
+# --------------------------------------------------------------------------
+# the atomic baseline: close to the exact sum, and (on hot keys) not repeatable
+# --------------------------------------------------------------------------
+
+def test_atomic_baseline_close_to_oracle():
+    case = small_case("sparse_key_scatter")
+    out = torch.empty(case.M, case.H, device=DEV)
+    dr.det_atomic_scatter_reduce(case.idx, case.M, case.x, out, w=case.w, opts={"debug_checks": 1})
+    want = oracle_scatter(case).astype(np.float64)
+    counts = np.bincount(case.idx.cpu().numpy(), minlength=case.M)[:, None]
+    xs = np.abs(np_bits(case.x.float()).astype(np.float64))
+    absum = np.zeros((case.M, case.H))
+    np.add.at(absum, case.idx.cpu().numpy(), xs)
+    bound = 2 * (counts + 1) * 2.0 ** -24 * absum + 1e-30
+    assert np.all(np.abs(np_bits(out).astype(np.float64) - want) <= bound)
+
+
+def test_atomic_baseline_bf16_and_index_errors():
+    case = small_case("moe_combine")
+    out = torch.empty(case.M, case.H, dtype=torch.bfloat16, device=DEV)
+    dr.det_atomic_scatter_reduce(case.idx, case.M, case.x, out, w=case.w)
+    want = oracle.bf16_to_f32(oracle_scatter(case)).astype(np.float64)
+    got = np_bits(out.float()).astype(np.float64)
+    assert np.all(np.abs(got - want) <= 2.0 ** -7 * np.abs(want) + 1e-6)
+    bad = case.idx.clone()
+    bad[3] = case.M + 5
+    with pytest.raises(dr.DetError) as e:
+        dr.det_atomic_scatter_reduce(bad, case.M, case.x, out, w=case.w, opts={"debug_checks": 1})
+    assert e.value.code == dr.DET_ERR_INDEX_RANGE
+
+
+def test_atomic_negative_control_differs_across_replays():
+    """The pages' negative control: the atomic path on hot keys is not byte-repeatable,
+    which shows the replay check is sensitive.  The deterministic path on the same
+    input is (see the replay test)."""
+    case = wl.sparse_key_scatter(2048, 512, 8192, 128, device=DEV, seed=77)
+    ref = None
+    differing = 0
+    for r in range(6):
+        out = torch.empty(case.M, case.H, device=DEV)
+        dr.det_atomic_scatter_reduce(case.idx, case.M, case.x, out)
+        b = out.view(torch.int32).clone()
+        if ref is None:
+            ref = b
+        elif not torch.equal(b, ref):
+            differing += 1
+    assert differing > 0
