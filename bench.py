@@ -59,6 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["moe_combine", "sparse_key_scatter", "ep_invariance"],
                     default="moe_combine")
+    ap.add_argument("--size", choices=["full", "medium"], default="full",
+                    help="medium: a quarter-size case of the same shape (for profiler captures only)")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -210,9 +212,9 @@ def gbs(nbytes: float, ms: float) -> float:
 # our arm
 # --------------------------------------------------------------------------
 
-def make_case(name, device):
+def make_case(name, device, size="full"):
     from invariant_gradient_reduction_gb300 import workloads as wl
-    return wl.make(name, "full", device=device)
+    return wl.make(name, size, device=device)
 
 
 def scatter_step_fns(case, torch):
@@ -380,7 +382,7 @@ def run_ours(args):
 
     peaks = read_peaks()
     timer = Timer(torch, device)
-    case = make_case(args.workload, device)
+    case = make_case(args.workload, device, args.size)
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local_rank).start()
@@ -472,7 +474,7 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOADS[args.workload],
+            "config": {"workload": WORKLOADS[args.workload] + ("" if args.size == "full" else f" [{args.size}]"),
                        "step": "plan (histogram+scan+stable sort+work list) + gather-reduce",
                        "l2": "flushed (256 MiB write) before every timed step, outside the step events",
                        "parallelism": "replicas" if world > 1 else "single GPU",

@@ -22,6 +22,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "gather_internal.cuh"
 #include "plan_internal.cuh"
 
 namespace detr {
@@ -396,6 +397,15 @@ static det_status launch_gather_vec(bool vec, int DR, const GatherArgs& a, const
                : launch_gather_dr<XT, OT, false>(DR, a, t, grid, st);
 }
 
+// Wait for the stream and report a CUDA error or an expired device wait.
+static det_status debug_sync_status(det_plan plan, cudaStream_t st)
+{
+    DETR_CUDA(cudaStreamSynchronize(st));
+    int h = 0;
+    DETR_CUDA(cudaMemcpy(&h, plan->counters + kCtrErrTimeout, sizeof(int), cudaMemcpyDeviceToHost));
+    return h ? DET_ERR_TIMEOUT : DET_OK;
+}
+
 static int log2_floor(int64_t v)
 {
     int r = 0;
@@ -496,6 +506,32 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     const int grid = static_cast<int>(grid64);
     cudaStream_t st = as_stream(stream);
 
+    // Wide rows with at most 32 terms per destination (the MoE combine): TMA-staged kernel.
+    int tile_elems = 0, tile_stride = 0, bulk_tiles = 0;
+    if (vec && plan->max_row_len <= 32 && H * xsz >= 1024 && plan->n_units > 0 &&
+        bulk_plan_tiles(H, xsz, plan->max_row_len, &tile_elems, &tile_stride, &bulk_tiles)) {
+        BulkArgs b{};
+        b.units = plan->units;
+        b.n_items = plan->n_units * bulk_tiles;
+        b.ntiles = bulk_tiles;
+        b.tile_elems = tile_elems;
+        b.tile_stride = tile_stride;
+        b.H = a.H;
+        b.out_vec = a.out_vec;
+        b.row_ptr = plan->row_ptr;
+        b.perm = plan->perm;
+        b.w = w;
+        b.ldx_bytes = a.ldx_bytes;
+        b.out = out;
+        b.ldo = ldo;
+        b.status = plan->counters;
+        int64_t bgrid = opts && opts->grid_ctas > 0 ? opts->grid_ctas : std::min<int64_t>(b.n_items, sms);
+        bgrid = std::max<int64_t>(1, std::min<int64_t>(bgrid, 2147483647));
+        s = launch_gather_bulk(x_dtype, out_dtype, b, tbl, static_cast<int>(bgrid), st);
+        if (s) return s;
+        if (opts && opts->debug_checks) return debug_sync_status(plan, st);
+        return DET_OK;
+    }
     if (a.n_tasks > 0) {
         if (x_dtype == DET_BF16 && out_dtype == DET_BF16) s = launch_gather_vec<uint16_t, __nv_bfloat16>(vec, DR, a, tbl, grid, st);
         else if (x_dtype == DET_BF16) s = launch_gather_vec<uint16_t, float>(vec, DR, a, tbl, grid, st);
@@ -512,7 +548,7 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
             finish_kernel<float><<<fgrid, kFinishThreads, 0, st>>>(plan->finish, items, a.H, a.part, a.ldpart, out, ldo);
         DETR_LAUNCHED();
     }
-    if (opts && opts->debug_checks) DETR_CUDA(cudaStreamSynchronize(st));
+    if (opts && opts->debug_checks) return debug_sync_status(plan, st);
     return DET_OK;
 }
 

@@ -1,0 +1,307 @@
+// gather_bulk.cu -- gather-reduce for wide rows with few terms (the MoE
+// combine: top-k <= 32 rows of several KB per destination), staged by TMA.
+//
+// A persistent CTA = one producer warp + eight consumer warps.  The producer
+// walks the CTA's work items (destination, H-tile) in order; for each it
+// reads the destination's source list, writes the weights to shared memory
+// and issues one cp.async.bulk per source row tile into a ring of shared
+// memory stages, completing on the stage's mbarrier.  Consumers wait for the
+// stage, fold the (at most 32) terms of every 16-byte column left to right --
+// the whole canonical fold when a destination has a single chunk -- round to
+// the output type and store, then release the stage.  The bulk copies keep
+// ~100 KB per SM in flight without registers, which is what the
+// register-staged gather could not reach.
+//
+// Every mbarrier wait is bounded; on expiry the CTA records kCtrErrTimeout in
+// the plan's counter block, drains the copies it issued (also bounded) and
+// returns.
+#include "common.cuh"
+#include "gather_internal.cuh"
+#include "plan_internal.cuh"
+
+namespace detr {
+
+constexpr int kBulkConsumerWarps = 8;
+constexpr int kBulkConsumers = kBulkConsumerWarps * 32;
+constexpr int kBulkThreads = kBulkConsumers + 32;
+constexpr int kBulkStages = 3;
+constexpr int kBulkStageBytes = 64 * 1024;
+constexpr int kBulkMaxTerms = 32;
+constexpr int kBulkVecPerThread = 2;  // tile <= 8 KB = 512 16-byte vectors
+constexpr unsigned long long kWaitLimit = 1ull << 22;
+
+struct BulkStageMeta {
+    int m;      // destination
+    int n;      // terms
+    int col0;   // first element of the tile
+    int bytes;  // bytes per term in this tile
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false if the barrier did not complete within the limit.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity)
+{
+    for (unsigned long long it = 0; it < kWaitLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+template <typename XT>
+struct BulkVec;
+template <>
+struct BulkVec<uint16_t> {
+    static constexpr int VEC = 8;
+    static __device__ __forceinline__ void expand(const uint4& r, float* f)
+    {
+        f[0] = bf16lo(r.x); f[1] = bf16hi(r.x); f[2] = bf16lo(r.y); f[3] = bf16hi(r.y);
+        f[4] = bf16lo(r.z); f[5] = bf16hi(r.z); f[6] = bf16lo(r.w); f[7] = bf16hi(r.w);
+    }
+};
+template <>
+struct BulkVec<float> {
+    static constexpr int VEC = 4;
+    static __device__ __forceinline__ void expand(const uint4& r, float* f)
+    {
+        f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+        f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+    }
+};
+
+template <typename OT, int VEC>
+__device__ __forceinline__ void bulk_store(void* base, long long off, const float* v, bool vec)
+{
+    if (sizeof(OT) == 4) {
+        float* o = static_cast<float*>(base) + off;
+        if (vec) {
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4)
+                *reinterpret_cast<float4*>(o + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = v[e];
+        }
+    } else {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(base) + off;
+        if (vec) {
+            uint32_t pk[VEC / 2];
+#pragma unroll
+            for (int e = 0; e < VEC; e += 2) {
+                __nv_bfloat162 t = __floats2bfloat162_rn(v[e], v[e + 1]);
+                pk[e / 2] = *reinterpret_cast<uint32_t*>(&t);
+            }
+            if (VEC == 8) *reinterpret_cast<uint4*>(o) = make_uint4(pk[0], pk[1 % (VEC / 2)], pk[2 % (VEC / 2)], pk[3 % (VEC / 2)]);
+            else *reinterpret_cast<uint2*>(o) = make_uint2(pk[0], pk[1 % (VEC / 2)]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = __float2bfloat16_rn(v[e]);
+        }
+    }
+}
+
+template <typename XT, typename OT>
+__global__ void __launch_bounds__(kBulkThreads, 1)
+gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ ShardTable tbl)
+{
+    using BV = BulkVec<XT>;
+    constexpr int VEC = BV::VEC;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* stage_buf = smem;  // kBulkStages x kBulkStageBytes
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBulkStages * kBulkStageBytes);
+    uint64_t* empty = full + kBulkStages;
+    float* swt = reinterpret_cast<float*>(empty + kBulkStages);            // [kBulkStages][32]
+    BulkStageMeta* meta = reinterpret_cast<BulkStageMeta*>(swt + kBulkStages * kBulkMaxTerms);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + kBulkStages);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBulkStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kBulkConsumerWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const long long n_items = a.n_items;
+    if (warp == kBulkConsumerWarps) {
+        // ---------------- producer warp ----------------
+        long long k = 0;
+        for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
+            const int s = static_cast<int>(k % kBulkStages);
+            const uint32_t ph = static_cast<uint32_t>((k / kBulkStages) & 1);
+            bool ok = true;
+            if (k >= kBulkStages) ok = mbar_wait_bounded(&empty[s], ph ^ 1u);
+            if (!__all_sync(0xffffffffu, ok) || *abort_flag) {
+                if (lane == 0) { *abort_flag = 1; atomicOr(a.status + kCtrErrTimeout, 1); }
+                break;
+            }
+            const long long u = item / a.ntiles;
+            const int t = static_cast<int>(item - u * a.ntiles);
+            const int m = a.units[u].x;
+            const int lo = a.row_ptr[m];
+            const int n = a.row_ptr[m + 1] - lo;
+            const int col0 = t * a.tile_elems;
+            const int bytes = min(a.tile_elems, a.H - col0) * static_cast<int>(sizeof(XT));
+            const unsigned char* src = nullptr;
+            if (lane < n) {
+                const int i = a.perm[lo + lane];
+                src = shard_row(tbl, i, a.ldx_bytes) + static_cast<long long>(col0) * sizeof(XT);
+                swt[s * kBulkMaxTerms + lane] = a.w ? a.w[i] : 1.0f;
+            }
+            if (lane == 0) meta[s] = BulkStageMeta{m, n, col0, bytes};
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(n * bytes));
+            __syncwarp();
+            if (lane < n)
+                bulk_g2s(stage_buf + static_cast<size_t>(s) * kBulkStageBytes + static_cast<size_t>(lane) * a.tile_stride,
+                         src, static_cast<uint32_t>(bytes), &full[s]);
+        }
+        return;
+    }
+
+    // ---------------- consumer warps ----------------
+    const int ctid = threadIdx.x;  // 0 .. kBulkConsumers-1
+    long long k = 0;
+    long long item = blockIdx.x;
+    for (; item < n_items; item += gridDim.x, ++k) {
+        const int s = static_cast<int>(k % kBulkStages);
+        const uint32_t ph = static_cast<uint32_t>((k / kBulkStages) & 1);
+        const bool ok = mbar_wait_bounded(&full[s], ph);
+        if (!ok || *abort_flag) {
+            *abort_flag = 1;
+            atomicOr(a.status + kCtrErrTimeout, 1);
+            break;
+        }
+        const BulkStageMeta md = meta[s];
+        const unsigned char* buf = stage_buf + static_cast<size_t>(s) * kBulkStageBytes;
+        const float* wts = swt + s * kBulkMaxTerms;
+        const int nvec = md.bytes / 16;
+#pragma unroll
+        for (int r = 0; r < kBulkVecPerThread; ++r) {
+            const int v = ctid + r * kBulkConsumers;
+            if (v < nvec) {
+                float acc[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;  // empty destination: +0.0
+                for (int j = 0; j < md.n; ++j) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(buf + static_cast<size_t>(j) * a.tile_stride + v * 16);
+                    float xf[VEC];
+                    BV::expand(raw, xf);
+                    if (a.w) {
+                        const float wv = wts[j];
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) xf[e] = __fmul_rn(wv, xf[e]);
+                    }
+                    if (j == 0) {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc[e] = xf[e];
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(acc[e], xf[e]);
+                    }
+                }
+                bulk_store<OT, VEC>(a.out, static_cast<long long>(md.m) * a.ldo + md.col0 + v * VEC, acc,
+                                    a.out_vec != 0);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (item < n_items) {
+        // aborted: drain the copies this CTA may still have in flight (bounded)
+        for (int s = 0; s < kBulkStages; ++s) {
+            const long long kk = k + s;
+            const uint32_t ph = static_cast<uint32_t>((kk / kBulkStages) & 1);
+            mbar_wait_bounded(&full[kk % kBulkStages], ph);
+        }
+    }
+}
+
+template <typename XT, typename OT>
+static det_status launch_bulk_t(const BulkArgs& a, const ShardTable& t, int grid, cudaStream_t st)
+{
+    const size_t smem = bulk_smem_bytes();
+    DETR_CUDA(cudaFuncSetAttribute(gather_bulk_kernel<XT, OT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(smem)));
+    gather_bulk_kernel<XT, OT><<<grid, kBulkThreads, smem, st>>>(a, t);
+    DETR_LAUNCHED();
+    return DET_OK;
+}
+
+size_t bulk_smem_bytes()
+{
+    return static_cast<size_t>(kBulkStages) * kBulkStageBytes + 2 * kBulkStages * sizeof(uint64_t) +
+           kBulkStages * kBulkMaxTerms * sizeof(float) + kBulkStages * sizeof(BulkStageMeta) + 16;
+}
+
+bool bulk_plan_tiles(int64_t H, int xsz, int64_t max_terms, int* tile_elems, int* tile_stride, int* ntiles)
+{
+    if (max_terms > kBulkMaxTerms) return false;
+    const int64_t row_bytes = H * xsz;
+    const int64_t terms = std::max<int64_t>(1, max_terms);
+    for (int64_t k = 1; k <= 64; ++k) {
+        const int64_t tb = (cdiv(row_bytes, k) + 15) / 16 * 16;  // 16-byte multiple
+        if (tb > 16 * kBulkConsumers * kBulkVecPerThread) continue;
+        const int64_t stride = (tb + 127) / 128 * 128;
+        if (stride * terms > kBulkStageBytes) continue;
+        *tile_elems = static_cast<int>(tb / xsz);
+        *tile_stride = static_cast<int>(stride);
+        *ntiles = static_cast<int>(cdiv(H, tb / xsz));
+        return true;
+    }
+    return false;
+}
+
+det_status launch_gather_bulk(det_dtype x_dtype, det_dtype out_dtype, const BulkArgs& a, const ShardTable& t, int grid,
+                              cudaStream_t st)
+{
+    if (x_dtype == DET_BF16 && out_dtype == DET_BF16) return launch_bulk_t<uint16_t, __nv_bfloat16>(a, t, grid, st);
+    if (x_dtype == DET_BF16) return launch_bulk_t<uint16_t, float>(a, t, grid, st);
+    if (out_dtype == DET_BF16) return launch_bulk_t<float, __nv_bfloat16>(a, t, grid, st);
+    return launch_bulk_t<float, float>(a, t, grid, st);
+}
+
+}  // namespace detr

@@ -578,6 +578,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     p->g = g;
     p->ws = ws;
     p->ws_bytes = ws_bytes;
+    p->counters = counters;
     p->row_ptr = row_ptr;
     p->perm = perm;
     p->units = units;

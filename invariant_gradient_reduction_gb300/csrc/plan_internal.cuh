@@ -15,6 +15,7 @@ enum {
     kCtrNormal = 3,    // whole-destination units
     kCtrHot = 4,       // destinations split into segments (finish tasks)
     kCtrMaxLen = 5,    // longest destination list
+    kCtrErrTimeout = 6,  // a bounded wait inside a reduce kernel expired
     kCtrCount = 16
 };
 
@@ -29,6 +30,7 @@ struct det_plan_s {
     int g = 3;                       // a hot segment covers 2^g chunks of 32 terms
     unsigned char* ws = nullptr;
     size_t ws_bytes = 0;
+    int* counters = nullptr;         // [kCtrCount]
     int* row_ptr = nullptr;          // [M+1]
     int* perm = nullptr;             // [N]
     int4* units = nullptr;

@@ -181,9 +181,21 @@ SMALL = {
 }
 
 
+MEDIUM = {
+    # same shapes with a quarter of the queries / tokens: sources still far larger than L2,
+    # small enough for multi-pass profiler captures
+    "sparse_key_scatter": dict(kind="sparse", Q=4096, K=512, S=65536, H=128, zipf_s=1.1, sigma=0.02, seed=24),
+    "moe_combine": FULL["moe_combine"],
+    "ep_invariance": dict(kind="moe", T=4096, E=256, k=8, H=7168, x_dtype=torch.bfloat16,
+                          out_dtype=torch.bfloat16, seed=23),
+    "tiny_moe": FULL["tiny_moe"],
+    "splitk": FULL["splitk"],
+}
+
+
 def make(name: str, size: str = "full", device="cpu"):
-    """Build a named workload ('full' or 'small').  Returns a ScatterCase or a split-K tensor."""
-    spec = dict((FULL if size == "full" else SMALL)[name])
+    """Build a named workload ('full', 'medium' or 'small').  Returns a ScatterCase or a split-K tensor."""
+    spec = dict({"full": FULL, "medium": MEDIUM, "small": SMALL}[size][name])
     kind = spec.pop("kind")
     if kind == "moe":
         return moe_combine(device=device, name=f"{name}[{size}]", **spec)
@@ -220,4 +232,4 @@ def cdiv(a: int, b: int) -> int:
 
 
 __all__ = ["ScatterCase", "moe_routing", "moe_combine", "zipf_key_lists", "sparse_key_scatter",
-           "splitk_partials", "FULL", "SMALL", "make", "ep_shard_rows", "split_rows", "round_up", "cdiv"]
+           "splitk_partials", "FULL", "MEDIUM", "SMALL", "make", "ep_shard_rows", "split_rows", "round_up", "cdiv"]
