@@ -209,6 +209,33 @@ det_status det_scatter_reduce(det_plan plan,
                               const det_opts* opts, void* stream);
 
 /*
+ * det_scatter_reduce without a caller workspace.  The pages describe no such
+ * call; it exists for callers that cannot allocate device memory when they
+ * call in: code inside a larger runtime whose allocator owns all device
+ * memory, a path that must not allocate after start-up, or a fixed interface
+ * with no way to pass a scratch buffer.  The scratch that det_scatter_reduce
+ * takes from `workspace` (fp32 partial slots for hot destinations) comes here
+ * from a fixed 16 MiB array in the library's device image, which the module
+ * loader reserves on every GPU that loads the library until the process exits.
+ *  - Same arguments and results as det_scatter_reduce, minus the workspace.
+ *  - Limit: det_scatter_workspace_size(plan, H) must be <= 16 MiB (16777216
+ *    bytes), else DET_ERR_UNSUPPORTED and nothing is launched.
+ *  - The first call on each device looks up the array's device address (once
+ *    per device, with that device current) and keeps it; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Nothing in it needs clearing (each slot is written before it is read),
+ *    but calls whose work overlaps on the GPU (other streams, other threads)
+ *    race on it: order them.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+det_status det_scatter_reduce_noalloc(det_plan plan,
+                                      const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                                      det_dtype x_dtype, int64_t ldx, int64_t H,
+                                      const float* w, void* out, int64_t ldo, det_dtype out_dtype,
+                                      const det_opts* opts, void* stream);
+
+/*
  * Split-K reduce: out[e] = canonical sum over s = 0 .. S-1 (split-id order)
  * of partials[s * ldp + e], e = 0 .. count-1, no multiply (Ch 09, section
  * 3.3: each K-split writes its own buffer; a reduce kernel sums them in

@@ -327,3 +327,21 @@ def det_atomic_scatter_reduce(idx: torch.Tensor, M: int, x, out: torch.Tensor, w
 
 __all__ = [n for n in dir() if n.startswith("det_") or n.startswith("DET_")] + ["Plan", "DetError", "lib",
                                                                                    "plan_lists", "LIB_PATH"]
+
+
+def det_scatter_reduce_noalloc(plan: Plan, x, out: torch.Tensor, w: Optional[torch.Tensor] = None,
+                               opts: Optional[dict] = None, stream=None):
+    """det_scatter_reduce for callers that cannot allocate: its scratch is the
+    library's fixed 16 MiB device array (see the C header for the limits)."""
+    f = lib().det_scatter_reduce_noalloc
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    f.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(i64), i32, i32, i64, i64, vp, vp, i64, i32,
+                  ctypes.POINTER(det_opts), vp]
+    f.restype = i32
+    ptrs, rows, P, xdt, ldx, H = _shards(x)
+    ldo, Ho = _rows(out)
+    if Ho != H or out.shape[0] != plan.M or out.dtype not in _TORCH_TO_DET:
+        raise ValueError("out must be a float32/bfloat16 [M, H] tensor")
+    _check(f(plan.handle, ptrs, rows, P, xdt, ldx, H, _ptr(w), _ptr(out), ldo, _TORCH_TO_DET[out.dtype], _opts(opts),
+             _stream(stream)), "det_scatter_reduce_noalloc")
+    return out
