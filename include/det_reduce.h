@@ -69,7 +69,7 @@ typedef int32_t det_status;
 #define DET_ERR_ORDER_KEY 4    /* two sources of one destination share a src_id: their order is undefined */
 #define DET_ERR_WORKSPACE 5    /* workspace NULL, misaligned or smaller than the size query returned */
 #define DET_ERR_CUDA 6         /* a CUDA call failed; det_last_cuda_error() gives the cudaError_t */
-#define DET_ERR_TIMEOUT 7      /* reserved for bounded device waits (no kernel of this library waits) */
+#define DET_ERR_TIMEOUT 7      /* a bounded device wait expired (reported when debug_checks is set) */
 #define DET_ERR_UNSUPPORTED 8  /* size beyond a documented limit (N, M >= 2^31 - 1, more than DET_MAX_SHARDS shards) */
 
 typedef int32_t det_dtype;
@@ -90,13 +90,20 @@ typedef int32_t det_dtype;
  *                   partial slot, and a second pass applies the rest of the
  *                   tree in its fixed order.  Plan-time option.
  *  debug_checks     nonzero: the call waits for its kernels and reports a
- *                   CUDA error as DET_ERR_CUDA (slower; for tests).
+ *                   CUDA error, or an expired bounded wait, as DET_ERR_CUDA /
+ *                   DET_ERR_TIMEOUT (slower; for tests).
+ *  gather_path      0 = auto.  1 = register-staged warp kernel, 2 = warp
+ *                   kernel with cp.async copies into shared memory, 3 = TMA
+ *                   bulk-staged kernel (only when every destination has at
+ *                   most 32 terms and rows are at least 1 KB; otherwise the
+ *                   call fails with DET_ERR_UNSUPPORTED).  For comparing the
+ *                   kernels; every path gives the same bits.
  */
 typedef struct det_opts {
     int32_t grid_ctas;
     int32_t seg_chunks_log2;
     int32_t debug_checks;
-    int32_t reserved;
+    int32_t gather_path;
 } det_opts;
 
 /* Opaque host handle of a built plan.  Its device arrays live in the

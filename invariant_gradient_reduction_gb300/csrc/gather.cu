@@ -24,6 +24,7 @@
 #include "common.cuh"
 #include "gather_internal.cuh"
 #include "plan_internal.cuh"
+#include "reduce_common.cuh"
 
 namespace detr {
 
@@ -34,163 +35,9 @@ constexpr int kStagePad = 33;
 constexpr int kFinishThreads = 256;
 constexpr int kFinishLevels = 24;  // segments of one row < 2^23
 
-struct GatherArgs {
-    const int4* units;
-    long long n_tasks;
-    int tile_groups;      // task groups per unit
-    int tiles_per_group;
-    int ntiles;           // H-tiles per row
-    int H;
-    int T_log2;           // lanes per H-tile (row vector count)
-    int S_log2;           // chunk slots per warp = 32 >> T_log2
-    int g;                // a segment covers 2^g chunks
-    int out_vec;          // vector stores to out allowed
-    const int* row_ptr;
-    const int* perm;
-    const float* w;
-    long long ldx_bytes;
-    void* out;
-    long long ldo;
-    float* part;
-    long long ldpart;
-};
 
-template <typename XT, bool VECTOR>
-struct Loader;
-
-template <>
-struct Loader<float, true> {
-    static constexpr int VEC = 4;
-    using Raw = uint4;
-    static __device__ __forceinline__ Raw load(const unsigned char* p) { return ld_stream_v4(p); }
-    static __device__ __forceinline__ void expand(const Raw& r, float* f)
-    {
-        f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
-        f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
-    }
-};
-
-template <>
-struct Loader<uint16_t, true> {
-    static constexpr int VEC = 8;
-    using Raw = uint4;
-    static __device__ __forceinline__ Raw load(const unsigned char* p) { return ld_stream_v4(p); }
-    static __device__ __forceinline__ void expand(const Raw& r, float* f)
-    {
-        f[0] = bf16lo(r.x); f[1] = bf16hi(r.x); f[2] = bf16lo(r.y); f[3] = bf16hi(r.y);
-        f[4] = bf16lo(r.z); f[5] = bf16hi(r.z); f[6] = bf16lo(r.w); f[7] = bf16hi(r.w);
-    }
-};
-
-template <>
-struct Loader<float, false> {
-    static constexpr int VEC = 1;
-    using Raw = float;
-    static __device__ __forceinline__ Raw load(const unsigned char* p) { return __ldg(reinterpret_cast<const float*>(p)); }
-    static __device__ __forceinline__ void expand(const Raw& r, float* f) { f[0] = r; }
-};
-
-template <>
-struct Loader<uint16_t, false> {
-    static constexpr int VEC = 1;
-    using Raw = unsigned short;
-    static __device__ __forceinline__ Raw load(const unsigned char* p)
-    {
-        return __ldg(reinterpret_cast<const unsigned short*>(p));
-    }
-    static __device__ __forceinline__ void expand(const Raw& r, float* f)
-    {
-        f[0] = __uint_as_float(static_cast<uint32_t>(r) << 16);
-    }
-};
-
-// Store VEC fp32 values as OT (binary32, or bf16 rounded to nearest even).
-template <typename OT, int VEC>
-__device__ __forceinline__ void store_out(void* base, long long off, const float* v, bool vec)
-{
-    if (sizeof(OT) == 4) {
-        float* o = static_cast<float*>(base) + off;
-        if (vec && VEC % 4 == 0) {
-#pragma unroll
-            for (int e = 0; e < VEC; e += 4)
-                *reinterpret_cast<float4*>(o + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) o[e] = v[e];
-        }
-    } else {
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(base) + off;
-        if (vec && VEC == 8) {
-            uint4 pk;
-            __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]);
-            __nv_bfloat162 t1 = __floats2bfloat162_rn(v[2], v[3]);
-            __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]);
-            __nv_bfloat162 t3 = __floats2bfloat162_rn(v[6], v[7]);
-            pk.x = *reinterpret_cast<uint32_t*>(&t0);
-            pk.y = *reinterpret_cast<uint32_t*>(&t1);
-            pk.z = *reinterpret_cast<uint32_t*>(&t2);
-            pk.w = *reinterpret_cast<uint32_t*>(&t3);
-            *reinterpret_cast<uint4*>(o) = pk;
-        } else if (vec && VEC == 4) {
-            uint2 pk;
-            __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]);
-            __nv_bfloat162 t1 = __floats2bfloat162_rn(v[2], v[3]);
-            pk.x = *reinterpret_cast<uint32_t*>(&t0);
-            pk.y = *reinterpret_cast<uint32_t*>(&t1);
-            *reinterpret_cast<uint2*>(o) = pk;
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) o[e] = __float2bfloat16_rn(v[e]);
-        }
-    }
-}
-
-// Binary counter over aligned tree nodes: pushing node number `cnt` merges it
-// with its completed left neighbours, exactly as the level-wise tree pairs them.
-template <int DR, int VEC>
-__device__ __forceinline__ void counter_push(float (&stk)[DR][VEC], unsigned int cnt, float* node)
-{
-    unsigned int c = cnt;
-    bool placed = false;
-#pragma unroll
-    for (int L = 0; L < DR; ++L) {
-        if (!placed) {
-            if (c & 1u) {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) node[e] = __fadd_rn(stk[L][e], node[e]);
-                c >>= 1;
-            } else {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) stk[L][e] = node[e];
-                placed = true;
-            }
-        }
-    }
-}
-
-// After the last push: the partial nodes at the right edge are carried up,
-// so the remaining levels combine from the lowest (rightmost) upward.
-template <int DR, int VEC>
-__device__ __forceinline__ void counter_collapse(const float (&stk)[DR][VEC], unsigned int cnt, float* res)
-{
-    bool have = false;
-#pragma unroll
-    for (int L = 0; L < DR; ++L) {
-        if ((cnt >> L) & 1u) {
-            if (!have) {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) res[e] = stk[L][e];
-                have = true;
-            } else {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) res[e] = __fadd_rn(stk[L][e], res[e]);
-            }
-        }
-    }
-}
-
-template <typename XT, typename OT, bool VECTOR, int DR>
-__global__ void __launch_bounds__(kGatherThreads)
+template <typename XT, typename OT, bool VECTOR>
+__global__ void __launch_bounds__(kGatherThreads, 3)
 gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant__ ShardTable tbl)
 {
     using LD = Loader<XT, VECTOR>;
@@ -208,6 +55,10 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
     float* swt = reinterpret_cast<float*>(reinterpret_cast<const unsigned char**>(smem) +
                                           static_cast<size_t>(kGatherWarps) * S * kStagePad) +
                  static_cast<size_t>(warp) * S * kStagePad;
+    float* stk = reinterpret_cast<float*>(reinterpret_cast<const unsigned char**>(smem) +
+                                          static_cast<size_t>(kGatherWarps) * S * kStagePad) +
+                 static_cast<size_t>(kGatherWarps) * S * kStagePad +
+                 static_cast<size_t>(warp) * a.levels * VEC * 32;
     const bool has_w = a.w != nullptr;
     const long long seg_terms = static_cast<long long>(kChunk) << a.g;
 
@@ -235,7 +86,6 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
             const int v = tile * T + lane_t;
             const int e0 = v * VEC;
             const bool active = e0 < a.H;
-            float stk[DR][VEC];
             unsigned int cnt = 0;
             for (int r = 0; r < nrounds; ++r) {
                 if (nrounds > 1 || !staged) {
@@ -312,13 +162,13 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
                         for (int e = 0; e < VEC; ++e) acc[e] = pv[e];
                     }
                 }
-                counter_push<DR, VEC>(stk, cnt, acc);
+                scounter_push<VEC>(stk, lane, cnt, acc);
                 ++cnt;
             }
             float res[VEC];
 #pragma unroll
             for (int e = 0; e < VEC; ++e) res[e] = 0.0f;  // empty destination: +0.0
-            counter_collapse<DR, VEC>(stk, cnt, res);
+            scounter_collapse<VEC>(stk, lane, cnt, res);
             if (slot == 0 && active) {
                 if (seg < 0) {
                     store_out<OT, VEC>(a.out, static_cast<long long>(m) * a.ldo + e0, res, a.out_vec != 0);
@@ -372,29 +222,24 @@ finish_kernel(const int4* finish, long long n_items, int H, const float* part, l
     store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
 }
 
-template <typename XT, typename OT, bool VECTOR, int DR>
+template <typename XT, typename OT, bool VECTOR>
 static det_status launch_gather(const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
 {
-    const size_t smem = static_cast<size_t>(kGatherWarps) * (1 << a.S_log2) * kStagePad * (sizeof(void*) + sizeof(float));
-    gather_reduce_kernel<XT, OT, VECTOR, DR><<<grid, kGatherThreads, smem, st>>>(a, t);
+    constexpr int VEC = Loader<XT, VECTOR>::VEC;
+    const size_t smem = static_cast<size_t>(kGatherWarps) *
+                        ((1 << a.S_log2) * kStagePad * (sizeof(void*) + sizeof(float)) +
+                         static_cast<size_t>(a.levels) * VEC * 32 * sizeof(float));
+    DETR_CUDA(cudaFuncSetAttribute(gather_reduce_kernel<XT, OT, VECTOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(smem)));
+    gather_reduce_kernel<XT, OT, VECTOR><<<grid, kGatherThreads, smem, st>>>(a, t);
     DETR_LAUNCHED();
     return DET_OK;
 }
 
-template <typename XT, typename OT, bool VECTOR>
-static det_status launch_gather_dr(int DR, const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
-{
-    if (DR <= 1) return launch_gather<XT, OT, VECTOR, 1>(a, t, grid, st);
-    if (DR <= 4) return launch_gather<XT, OT, VECTOR, 4>(a, t, grid, st);
-    return launch_gather<XT, OT, VECTOR, 7>(a, t, grid, st);
-}
-
 template <typename XT, typename OT>
-static det_status launch_gather_vec(bool vec, int DR, const GatherArgs& a, const ShardTable& t, int grid,
-                                    cudaStream_t st)
+static det_status launch_gather_vec(bool vec, const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
 {
-    return vec ? launch_gather_dr<XT, OT, true>(DR, a, t, grid, st)
-               : launch_gather_dr<XT, OT, false>(DR, a, t, grid, st);
+    return vec ? launch_gather<XT, OT, true>(a, t, grid, st) : launch_gather<XT, OT, false>(a, t, grid, st);
 }
 
 // Wait for the stream and report a CUDA error or an expired device wait.
@@ -495,21 +340,26 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     a.tile_groups = static_cast<int>(cdiv(a.ntiles, tpg));
     a.n_tasks = plan->n_units * a.tile_groups;
 
-    // Register stack depth: enough levels for the longest unit's rounds.
+    // Binary-counter depth: enough levels for the longest unit's rounds.
     const int64_t G = int64_t(1) << plan->g;
     const int64_t max_chunks = std::min(cdiv(plan->max_row_len, kChunk), G);
-    const int64_t max_rounds = cdiv(max_chunks, int64_t(1) << a.S_log2);
-    const int DR = max_rounds <= 1 ? 1 : (max_rounds <= 15 ? 4 : 7);
+    const int64_t max_rounds = std::max<int64_t>(1, cdiv(max_chunks, int64_t(1) << a.S_log2));
+    a.levels = log2_floor(max_rounds) + 1;
 
     int64_t grid64 = opts && opts->grid_ctas > 0 ? opts->grid_ctas : cdiv(a.n_tasks, kGatherWarps);
     grid64 = std::max<int64_t>(1, std::min<int64_t>(grid64, 2147483647));
     const int grid = static_cast<int>(grid64);
     cudaStream_t st = as_stream(stream);
 
+    const int path = opts ? opts->gather_path : 0;
+    if (path < 0 || path > 3) return DET_ERR_ARG;
     // Wide rows with at most 32 terms per destination (the MoE combine): TMA-staged kernel.
     int tile_elems = 0, tile_stride = 0, bulk_tiles = 0;
-    if (vec && plan->max_row_len <= 32 && H * xsz >= 1024 && plan->n_units > 0 &&
-        bulk_plan_tiles(H, xsz, plan->max_row_len, &tile_elems, &tile_stride, &bulk_tiles)) {
+    const bool bulk_ok = vec && plan->max_row_len <= 32 && H * xsz >= 1024 && plan->n_units > 0 &&
+                         bulk_plan_tiles(H, xsz, plan->max_row_len, &tile_elems, &tile_stride, &bulk_tiles);
+    if (path == 3 && !bulk_ok) return DET_ERR_UNSUPPORTED;
+    if (path == 2 && !vec) return DET_ERR_UNSUPPORTED;
+    if (bulk_ok && (path == 0 || path == 3)) {
         BulkArgs b{};
         b.units = plan->units;
         b.n_items = plan->n_units * bulk_tiles;
@@ -532,11 +382,17 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
         if (opts && opts->debug_checks) return debug_sync_status(plan, st);
         return DET_OK;
     }
-    if (a.n_tasks > 0) {
-        if (x_dtype == DET_BF16 && out_dtype == DET_BF16) s = launch_gather_vec<uint16_t, __nv_bfloat16>(vec, DR, a, tbl, grid, st);
-        else if (x_dtype == DET_BF16) s = launch_gather_vec<uint16_t, float>(vec, DR, a, tbl, grid, st);
-        else if (out_dtype == DET_BF16) s = launch_gather_vec<float, __nv_bfloat16>(vec, DR, a, tbl, grid, st);
-        else s = launch_gather_vec<float, float>(vec, DR, a, tbl, grid, st);
+    if (a.n_tasks > 0 && vec && path == 2) {
+        // 16-byte rows: asynchronous copies into a shared-memory ring
+        int64_t agrid = opts && opts->grid_ctas > 0 ? opts->grid_ctas : cdiv(a.n_tasks, kAsyncWarps);
+        agrid = std::max<int64_t>(1, std::min<int64_t>(agrid, 2147483647));
+        s = launch_gather_async(x_dtype, out_dtype, a, tbl, static_cast<int>(agrid), st);
+        if (s) return s;
+    } else if (a.n_tasks > 0) {
+        if (x_dtype == DET_BF16 && out_dtype == DET_BF16) s = launch_gather_vec<uint16_t, __nv_bfloat16>(vec, a, tbl, grid, st);
+        else if (x_dtype == DET_BF16) s = launch_gather_vec<uint16_t, float>(vec, a, tbl, grid, st);
+        else if (out_dtype == DET_BF16) s = launch_gather_vec<float, __nv_bfloat16>(vec, a, tbl, grid, st);
+        else s = launch_gather_vec<float, float>(vec, a, tbl, grid, st);
         if (s) return s;
     }
     if (plan->n_hot_rows > 0) {

@@ -1,7 +1,7 @@
 // gather_bulk.cu -- gather-reduce for wide rows with few terms (the MoE
 // combine: top-k <= 32 rows of several KB per destination), staged by TMA.
 //
-// A persistent CTA = one producer warp + eight consumer warps.  The producer
+// A persistent CTA = one producer warp + sixteen consumer warps.  The producer
 // walks the CTA's work items (destination, H-tile) in order; for each it
 // reads the destination's source list, writes the weights to shared memory
 // and issues one cp.async.bulk per source row tile into a ring of shared
@@ -21,13 +21,13 @@
 
 namespace detr {
 
-constexpr int kBulkConsumerWarps = 8;
+constexpr int kBulkConsumerWarps = 16;
 constexpr int kBulkConsumers = kBulkConsumerWarps * 32;
 constexpr int kBulkThreads = kBulkConsumers + 32;
 constexpr int kBulkStages = 3;
 constexpr int kBulkStageBytes = 64 * 1024;
 constexpr int kBulkMaxTerms = 32;
-constexpr int kBulkVecPerThread = 2;  // tile <= 8 KB = 512 16-byte vectors
+constexpr int kBulkVecPerThread = 1;  // tile <= 8 KB = 512 16-byte vectors
 constexpr unsigned long long kWaitLimit = 1ull << 22;
 
 struct BulkStageMeta {
@@ -168,8 +168,42 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
     const long long n_items = a.n_items;
     if (warp == kBulkConsumerWarps) {
         // ---------------- producer warp ----------------
-        long long k = 0;
-        for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
+        // Item k of this CTA is blockIdx.x + k * gridDim.x.  The list lookups
+        // run 32 items ahead (lane l holds item kb + l of the current and of
+        // the next batch), and the next item's source rows and weights are
+        // read while the producer waits for a free stage, so copies are issued
+        // as soon as a stage is released.
+        const long long g = gridDim.x;
+        int bm = 0, blo = 0, bn = -1, nm = 0, nlo = 0, nn = -1;
+        auto fetch_meta = [&](long long kb, int& fm, int& flo, int& fn) {
+            const long long it = blockIdx.x + (kb + lane) * g;
+            fn = -1;
+            if (it < n_items) {
+                fm = a.units[it / a.ntiles].x;
+                flo = a.row_ptr[fm];
+                fn = a.row_ptr[fm + 1] - flo;
+            }
+        };
+        auto load_src = [&](long long k, int lo, int n, const unsigned char*& src, float& wv) {
+            src = nullptr;
+            wv = 1.0f;
+            if (lane < n) {
+                const long long it = blockIdx.x + k * g;
+                const int t = static_cast<int>(it % a.ntiles);
+                const int i = a.perm[lo + lane];
+                src = shard_row(tbl, i, a.ldx_bytes) + static_cast<long long>(t) * a.tile_elems * sizeof(XT);
+                if (a.w) wv = a.w[i];
+            }
+        };
+        fetch_meta(0, bm, blo, bn);
+        fetch_meta(32, nm, nlo, nn);
+        int cm = __shfl_sync(0xffffffffu, bm, 0);
+        int clo = __shfl_sync(0xffffffffu, blo, 0);
+        int cn = __shfl_sync(0xffffffffu, bn, 0);
+        const unsigned char* csrc = nullptr;
+        float cw = 1.0f;
+        if (blockIdx.x < n_items) load_src(0, clo, cn, csrc, cw);
+        for (long long k = 0; blockIdx.x + k * g < n_items; ++k) {
             const int s = static_cast<int>(k % kBulkStages);
             const uint32_t ph = static_cast<uint32_t>((k / kBulkStages) & 1);
             bool ok = true;
@@ -178,26 +212,28 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
                 if (lane == 0) { *abort_flag = 1; atomicOr(a.status + kCtrErrTimeout, 1); }
                 break;
             }
-            const long long u = item / a.ntiles;
-            const int t = static_cast<int>(item - u * a.ntiles);
-            const int m = a.units[u].x;
-            const int lo = a.row_ptr[m];
-            const int n = a.row_ptr[m + 1] - lo;
+            const long long it = blockIdx.x + k * g;
+            const int t = static_cast<int>(it % a.ntiles);
             const int col0 = t * a.tile_elems;
             const int bytes = min(a.tile_elems, a.H - col0) * static_cast<int>(sizeof(XT));
-            const unsigned char* src = nullptr;
-            if (lane < n) {
-                const int i = a.perm[lo + lane];
-                src = shard_row(tbl, i, a.ldx_bytes) + static_cast<long long>(col0) * sizeof(XT);
-                swt[s * kBulkMaxTerms + lane] = a.w ? a.w[i] : 1.0f;
-            }
-            if (lane == 0) meta[s] = BulkStageMeta{m, n, col0, bytes};
+            if (lane < cn) swt[s * kBulkMaxTerms + lane] = cw;
+            if (lane == 0) meta[s] = BulkStageMeta{cm, cn, col0, bytes};
             __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(n * bytes));
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cn * bytes));
             __syncwarp();
-            if (lane < n)
+            if (lane < cn)
                 bulk_g2s(stage_buf + static_cast<size_t>(s) * kBulkStageBytes + static_cast<size_t>(lane) * a.tile_stride,
-                         src, static_cast<uint32_t>(bytes), &full[s]);
+                         csrc, static_cast<uint32_t>(bytes), &full[s]);
+            // advance to item k+1
+            const int j = static_cast<int>((k + 1) & 31);
+            if (j == 0) {
+                bm = nm; blo = nlo; bn = nn;
+                fetch_meta(k + 1 + 32, nm, nlo, nn);
+            }
+            cm = __shfl_sync(0xffffffffu, bm, j);
+            clo = __shfl_sync(0xffffffffu, blo, j);
+            cn = __shfl_sync(0xffffffffu, bn, j);
+            if (blockIdx.x + (k + 1) * g < n_items) load_src(k + 1, clo, cn, csrc, cw);
         }
         return;
     }

@@ -8,6 +8,35 @@
 
 namespace detr {
 
+// Arguments of the warp-task gather-reduce kernels (gather.cu, gather_async.cu).
+struct GatherArgs {
+    const int4* units;
+    long long n_tasks;
+    int tile_groups;      // task groups per unit
+    int tiles_per_group;
+    int ntiles;           // H-tiles per row
+    int H;
+    int T_log2;           // lanes per H-tile (row vector count)
+    int S_log2;           // chunk slots per warp = 32 >> T_log2
+    int g;                // a segment covers 2^g chunks
+    int out_vec;          // vector stores to out allowed
+    int levels;           // binary-counter levels a unit can need (floor(log2(rounds)) + 1)
+    const int* row_ptr;
+    const int* perm;
+    const float* w;
+    long long ldx_bytes;
+    void* out;
+    long long ldo;
+    float* part;
+    long long ldpart;
+};
+
+// Vector-path gather with per-lane asynchronous copies into a shared-memory ring.
+size_t async_smem_bytes(int S_log2, int levels, int vec);
+det_status launch_gather_async(det_dtype x_dtype, det_dtype out_dtype, const GatherArgs& a,
+                               const ShardTable& t, int grid, cudaStream_t st);
+constexpr int kAsyncWarps = 4;
+
 struct BulkArgs {
     const int4* units;     // whole-destination units (every list has <= 32 terms)
     long long n_items;     // units x tiles

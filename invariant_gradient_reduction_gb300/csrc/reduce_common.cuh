@@ -1,0 +1,186 @@
+// reduce_common.cuh -- device helpers shared by the gather-reduce kernels:
+// row loaders, output stores and the binary counter that applies the
+// level-wise pairwise tree over aligned tree nodes.
+#pragma once
+
+#include "common.cuh"
+
+namespace detr {
+
+template <typename XT, bool VECTOR>
+struct Loader;
+
+template <>
+struct Loader<float, true> {
+    static constexpr int VEC = 4;
+    using Raw = uint4;
+    static __device__ __forceinline__ Raw load(const unsigned char* p) { return ld_stream_v4(p); }
+    static __device__ __forceinline__ void expand(const Raw& r, float* f)
+    {
+        f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+        f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+    }
+};
+
+template <>
+struct Loader<uint16_t, true> {
+    static constexpr int VEC = 8;
+    using Raw = uint4;
+    static __device__ __forceinline__ Raw load(const unsigned char* p) { return ld_stream_v4(p); }
+    static __device__ __forceinline__ void expand(const Raw& r, float* f)
+    {
+        f[0] = bf16lo(r.x); f[1] = bf16hi(r.x); f[2] = bf16lo(r.y); f[3] = bf16hi(r.y);
+        f[4] = bf16lo(r.z); f[5] = bf16hi(r.z); f[6] = bf16lo(r.w); f[7] = bf16hi(r.w);
+    }
+};
+
+template <>
+struct Loader<float, false> {
+    static constexpr int VEC = 1;
+    using Raw = float;
+    static __device__ __forceinline__ Raw load(const unsigned char* p) { return __ldg(reinterpret_cast<const float*>(p)); }
+    static __device__ __forceinline__ void expand(const Raw& r, float* f) { f[0] = r; }
+};
+
+template <>
+struct Loader<uint16_t, false> {
+    static constexpr int VEC = 1;
+    using Raw = unsigned short;
+    static __device__ __forceinline__ Raw load(const unsigned char* p)
+    {
+        return __ldg(reinterpret_cast<const unsigned short*>(p));
+    }
+    static __device__ __forceinline__ void expand(const Raw& r, float* f)
+    {
+        f[0] = __uint_as_float(static_cast<uint32_t>(r) << 16);
+    }
+};
+
+// Store VEC fp32 values as OT (binary32, or bf16 rounded to nearest even).
+template <typename OT, int VEC>
+__device__ __forceinline__ void store_out(void* base, long long off, const float* v, bool vec)
+{
+    if (sizeof(OT) == 4) {
+        float* o = static_cast<float*>(base) + off;
+        if (vec && VEC % 4 == 0) {
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4)
+                *reinterpret_cast<float4*>(o + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = v[e];
+        }
+    } else {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(base) + off;
+        if (vec && VEC == 8) {
+            uint4 pk;
+            __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]);
+            __nv_bfloat162 t1 = __floats2bfloat162_rn(v[2], v[3]);
+            __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]);
+            __nv_bfloat162 t3 = __floats2bfloat162_rn(v[6], v[7]);
+            pk.x = *reinterpret_cast<uint32_t*>(&t0);
+            pk.y = *reinterpret_cast<uint32_t*>(&t1);
+            pk.z = *reinterpret_cast<uint32_t*>(&t2);
+            pk.w = *reinterpret_cast<uint32_t*>(&t3);
+            *reinterpret_cast<uint4*>(o) = pk;
+        } else if (vec && VEC == 4) {
+            uint2 pk;
+            __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]);
+            __nv_bfloat162 t1 = __floats2bfloat162_rn(v[2], v[3]);
+            pk.x = *reinterpret_cast<uint32_t*>(&t0);
+            pk.y = *reinterpret_cast<uint32_t*>(&t1);
+            *reinterpret_cast<uint2*>(o) = pk;
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[e] = __float2bfloat16_rn(v[e]);
+        }
+    }
+}
+
+// Binary counter over aligned tree nodes: pushing node number `cnt` merges it
+// with its completed left neighbours, exactly as the level-wise tree pairs them.
+template <int DR, int VEC>
+__device__ __forceinline__ void counter_push(float (&stk)[DR][VEC], unsigned int cnt, float* node)
+{
+    unsigned int c = cnt;
+    bool placed = false;
+#pragma unroll
+    for (int L = 0; L < DR; ++L) {
+        if (!placed) {
+            if (c & 1u) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) node[e] = __fadd_rn(stk[L][e], node[e]);
+                c >>= 1;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) stk[L][e] = node[e];
+                placed = true;
+            }
+        }
+    }
+}
+
+// After the last push: the partial nodes at the right edge are carried up,
+// so the remaining levels combine from the lowest (rightmost) upward.
+template <int DR, int VEC>
+__device__ __forceinline__ void counter_collapse(const float (&stk)[DR][VEC], unsigned int cnt, float* res)
+{
+    bool have = false;
+#pragma unroll
+    for (int L = 0; L < DR; ++L) {
+        if ((cnt >> L) & 1u) {
+            if (!have) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) res[e] = stk[L][e];
+                have = true;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) res[e] = __fadd_rn(stk[L][e], res[e]);
+            }
+        }
+    }
+}
+
+// The same binary counter with its stack in shared memory: lane-private
+// columns laid out [level][element][lane], so the accesses of a warp are
+// conflict-free.  Used by the warp-task kernels, which push one node per round.
+__device__ __forceinline__ float* scounter_slot(float* st, int L, int e, int VEC, int lane)
+{
+    return st + (static_cast<size_t>(L) * VEC + e) * 32 + lane;
+}
+
+template <int VEC>
+__device__ __forceinline__ void scounter_push(float* st, int lane, unsigned int cnt, float* node)
+{
+    unsigned int c = cnt;
+    int L = 0;
+    while (c & 1u) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) node[e] = __fadd_rn(*scounter_slot(st, L, e, VEC, lane), node[e]);
+        c >>= 1;
+        ++L;
+    }
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) *scounter_slot(st, L, e, VEC, lane) = node[e];
+}
+
+template <int VEC>
+__device__ __forceinline__ void scounter_collapse(const float* st, int lane, unsigned int cnt, float* res)
+{
+    bool have = false;
+    for (int L = 0; (cnt >> L) != 0u; ++L) {
+        if ((cnt >> L) & 1u) {
+            const float* col = st + static_cast<size_t>(L) * VEC * 32 + lane;
+            if (!have) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) res[e] = col[e * 32];
+                have = true;
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) res[e] = __fadd_rn(col[e * 32], res[e]);
+            }
+        }
+    }
+}
+
+}  // namespace detr

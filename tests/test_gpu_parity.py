@@ -133,6 +133,22 @@ def test_grid_size_changes_no_bit(name):
         assert_bytes_equal(np_bits(out), want, f"{name} grid={grid}")
 
 
+@pytest.mark.parametrize("name", ["moe_combine", "sparse_key_scatter", "tiny_moe", "ep_invariance"])
+def test_gather_path_changes_no_bit(name):
+    """Every gather kernel (register-staged, cp.async ring, TMA bulk ring) gives the same bytes."""
+    case = small_case(name)
+    base, plan = gpu_scatter(case)
+    want = np_bits(base)
+    for path in (1, 2, 3):
+        out = torch.empty_like(base)
+        try:
+            dr.det_scatter_reduce(plan, case.x, out, w=case.w, opts={"gather_path": path})
+        except dr.DetError as e:
+            assert path == 3 and e.code == dr.DET_ERR_UNSUPPORTED
+            continue
+        assert_bytes_equal(np_bits(out), want, f"{name} path={path}")
+
+
 def test_replays_identical_under_contention():
     """R replays give identical bytes and identical fingerprints, also while a side
     stream runs matmuls (the pages' contention replay)."""
