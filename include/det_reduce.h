@@ -98,12 +98,17 @@ typedef int32_t det_dtype;
  *                   most 32 terms and rows are at least 1 KB; otherwise the
  *                   call fails with DET_ERR_UNSUPPORTED).  For comparing the
  *                   kernels; every path gives the same bits.
+ *  tiles_per_task   0 = auto; > 0 = H-tiles one warp task of the warp kernels
+ *                   covers (the work split changes no bit).
+ *  reserved         must be zero.
  */
 typedef struct det_opts {
     int32_t grid_ctas;
     int32_t seg_chunks_log2;
     int32_t debug_checks;
     int32_t gather_path;
+    int32_t tiles_per_task;
+    int32_t reserved[3];
 } det_opts;
 
 /* Opaque host handle of a built plan.  Its device arrays live in the

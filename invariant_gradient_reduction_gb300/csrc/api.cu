@@ -1,5 +1,7 @@
 // api.cu -- status codes, version, argument helpers shared by the entry points.
 #include <atomic>
+#include <mutex>
+#include <unordered_map>
 
 #include "common.cuh"
 
@@ -12,12 +14,44 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 void set_last_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
 
+constexpr int kMaxDevices = 64;
+static std::atomic<int> g_sm_count[kMaxDevices];
+
 det_status current_sm_count(int* sms)
 {
     int dev = 0;
     DETR_CUDA(cudaGetDevice(&dev));
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int c = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (c > 0) { *sms = c; return DET_OK; }
+    }
     DETR_CUDA(cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev));
     if (*sms <= 0) *sms = 1;
+    if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(*sms, std::memory_order_relaxed);
+    return DET_OK;
+}
+
+// Largest dynamic shared memory already allowed per (kernel, device).
+static std::mutex g_attr_mu;
+static std::unordered_map<const void*, size_t> g_attr_set[kMaxDevices];
+
+det_status allow_dynamic_smem(const void* func, size_t bytes)
+{
+    if (bytes <= 48 * 1024) return DET_OK;
+    int dev = 0;
+    DETR_CUDA(cudaGetDevice(&dev));
+    const bool cacheable = dev >= 0 && dev < kMaxDevices;
+    if (cacheable) {
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        auto it = g_attr_set[dev].find(func);
+        if (it != g_attr_set[dev].end() && it->second >= bytes) return DET_OK;
+    }
+    DETR_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)));
+    if (cacheable) {
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        size_t& v = g_attr_set[dev][func];
+        v = std::max(v, bytes);
+    }
     return DET_OK;
 }
 

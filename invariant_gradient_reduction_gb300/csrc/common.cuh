@@ -44,9 +44,12 @@ inline size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// SM count of the current device (queried per call: cheap, and correct when
-// the caller switches devices).
+// SM count of the current device (cached per device).
 det_status current_sm_count(int* sms);
+
+// Allow `bytes` of dynamic shared memory for `func` on the current device
+// (cudaFuncSetAttribute, called once per kernel, device and larger size).
+det_status allow_dynamic_smem(const void* func, size_t bytes);
 
 // Half-open byte ranges [a, a+na) and [b, b+nb) overlap?
 inline bool overlaps(const void* a, size_t na, const void* b, size_t nb)

@@ -33,11 +33,14 @@ constexpr int kGatherWarps = kGatherThreads / 32;
 constexpr int kBatch = 8;
 constexpr int kStagePad = 33;
 constexpr int kFinishThreads = 256;
-constexpr int kFinishLevels = 24;  // segments of one row < 2^23
 
+
+#ifndef DETR_GATHER_MIN_BLOCKS
+#define DETR_GATHER_MIN_BLOCKS 3
+#endif
 
 template <typename XT, typename OT, bool VECTOR>
-__global__ void __launch_bounds__(kGatherThreads, 3)
+__global__ void __launch_bounds__(kGatherThreads, DETR_GATHER_MIN_BLOCKS)
 gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant__ ShardTable tbl)
 {
     using LD = Loader<XT, VECTOR>;
@@ -67,7 +70,7 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
          task += nwarps) {
         const long long u = task / a.tile_groups;
         const int tg = static_cast<int>(task - u * a.tile_groups);
-        const int4 ud = a.units[u];
+        const int4 ud = unit_at(a, u);
         const int m = ud.x, seg = ud.y;
         const int lo = a.row_ptr[m], hi = a.row_ptr[m + 1];
         int beg = lo, end = hi;
@@ -162,13 +165,13 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
                         for (int e = 0; e < VEC; ++e) acc[e] = pv[e];
                     }
                 }
-                scounter_push<VEC>(stk, lane, cnt, acc);
+                scounter_push<VEC>(stk, 32, lane, cnt, acc);
                 ++cnt;
             }
             float res[VEC];
 #pragma unroll
             for (int e = 0; e < VEC; ++e) res[e] = 0.0f;  // empty destination: +0.0
-            scounter_collapse<VEC>(stk, lane, cnt, res);
+            scounter_collapse<VEC>(stk, 32, lane, cnt, res);
             if (slot == 0 && active) {
                 if (seg < 0) {
                     store_out<OT, VEC>(a.out, static_cast<long long>(m) * a.ldo + e0, res, a.out_vec != 0);
@@ -189,19 +192,20 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
 }
 
 // Second pass for hot destinations: the level-wise tree over the row's
-// segment nodes (aligned nodes of 2^g chunks), in segment order.
+// segment nodes (aligned nodes of 2^g chunks), in segment order, through the
+// binary counter (stack in shared memory, one column per thread).
 template <typename OT>
 __global__ void __launch_bounds__(kFinishThreads)
 finish_kernel(const int4* finish, long long n_items, int H, const float* part, long long ldpart, void* out,
               long long ldo)
 {
+    extern __shared__ float fstk[];  // [levels][kFinishThreads]
     const long long t = static_cast<long long>(blockIdx.x) * kFinishThreads + threadIdx.x;
     if (t >= n_items) return;
     const long long row_task = t / H;
     const int h = static_cast<int>(t - row_task * H);
     const int4 ft = finish[row_task];
     const int m = ft.x, s0 = ft.y, ns = ft.z;
-    float stk[kFinishLevels][1];
     unsigned int cnt = 0;
     for (int s = 0; s < ns; s += kBatch) {
         float v[kBatch];
@@ -212,13 +216,13 @@ finish_kernel(const int4* finish, long long n_items, int H, const float* part, l
         for (int q = 0; q < kBatch; ++q) {
             if (s + q < ns) {
                 float node[1] = {v[q]};
-                counter_push<kFinishLevels, 1>(stk, cnt, node);
+                scounter_push<1>(fstk, kFinishThreads, threadIdx.x, cnt, node);
                 ++cnt;
             }
         }
     }
     float res[1] = {0.0f};
-    counter_collapse<kFinishLevels, 1>(stk, cnt, res);
+    scounter_collapse<1>(fstk, kFinishThreads, threadIdx.x, cnt, res);
     store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
 }
 
@@ -229,8 +233,20 @@ static det_status launch_gather(const GatherArgs& a, const ShardTable& t, int gr
     const size_t smem = static_cast<size_t>(kGatherWarps) *
                         ((1 << a.S_log2) * kStagePad * (sizeof(void*) + sizeof(float)) +
                          static_cast<size_t>(a.levels) * VEC * 32 * sizeof(float));
-    DETR_CUDA(cudaFuncSetAttribute(gather_reduce_kernel<XT, OT, VECTOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(smem)));
+    {
+        const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR>), smem);
+        if (a_) return a_;
+    }
+    if (grid <= 0) {
+        // persistent: as many CTAs as fit at once; warps take tasks round-robin
+        int per_sm = 1, sms = 1;
+        DETR_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_reduce_kernel<XT, OT, VECTOR>,
+                                                                kGatherThreads, smem));
+        det_status s = current_sm_count(&sms);
+        if (s) return s;
+        grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(a.n_tasks, kGatherWarps),
+                                                                        int64_t(std::max(per_sm, 1)) * sms)));
+    }
     gather_reduce_kernel<XT, OT, VECTOR><<<grid, kGatherThreads, smem, st>>>(a, t);
     DETR_LAUNCHED();
     return DET_OK;
@@ -317,7 +333,9 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     a.ntiles = static_cast<int>(cdiv(V, int64_t(1) << T_log2));
     a.H = static_cast<int>(H);
     a.g = plan->g;
-    a.units = plan->units;
+    a.seg_units = plan->seg_units;
+    a.row_units = plan->row_units;
+    a.n_seg = plan->n_segments;
     a.row_ptr = plan->row_ptr;
     a.perm = plan->perm;
     a.w = w;
@@ -331,11 +349,16 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     int sms = 0;
     s = current_sm_count(&sms);
     if (s) return s;
-    // Split the H-tiles of a unit into groups until there are enough warp
-    // tasks to fill the GPU several times over (the split changes no bit).
-    const int64_t target = static_cast<int64_t>(sms) * 64 * 4;
-    int tpg = a.ntiles;
-    while (tpg > 1 && plan->n_units * cdiv(a.ntiles, tpg) < target) tpg = static_cast<int>(cdiv(tpg, 2));
+    // Tiles per warp task: about 16 KB of source data per task amortises the
+    // task's list lookups, while keeping at least two tasks per resident warp
+    // (measured best on the MoE combine and EP-invariance shapes; the split
+    // changes no bit).
+    const int64_t avg_terms = std::max<int64_t>(1, plan->N / std::max<int64_t>(1, plan->n_units));
+    const int64_t tile_bytes = (int64_t(1) << T_log2) * (vec ? 16 : xsz);
+    int tpg = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, 16384 / (avg_terms * tile_bytes))));
+    const int64_t min_tasks = static_cast<int64_t>(sms) * 24 * 2;
+    while (tpg > 1 && plan->n_units * cdiv(a.ntiles, tpg) < min_tasks) tpg = static_cast<int>(cdiv(tpg, 2));
+    if (opts && opts->tiles_per_task > 0) tpg = std::min(opts->tiles_per_task, a.ntiles);
     a.tiles_per_group = tpg;
     a.tile_groups = static_cast<int>(cdiv(a.ntiles, tpg));
     a.n_tasks = plan->n_units * a.tile_groups;
@@ -346,22 +369,25 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     const int64_t max_rounds = std::max<int64_t>(1, cdiv(max_chunks, int64_t(1) << a.S_log2));
     a.levels = log2_floor(max_rounds) + 1;
 
-    int64_t grid64 = opts && opts->grid_ctas > 0 ? opts->grid_ctas : cdiv(a.n_tasks, kGatherWarps);
-    grid64 = std::max<int64_t>(1, std::min<int64_t>(grid64, 2147483647));
-    const int grid = static_cast<int>(grid64);
+    // 0 = persistent grid sized by occupancy in the launcher
+    const int grid = opts && opts->grid_ctas > 0 ? opts->grid_ctas : 0;
     cudaStream_t st = as_stream(stream);
 
     const int path = opts ? opts->gather_path : 0;
-    if (path < 0 || path > 3) return DET_ERR_ARG;
+    if (path < 0 || path > 3 || (opts && (opts->tiles_per_task < 0 || opts->reserved[0] || opts->reserved[1] ||
+                                          opts->reserved[2])))
+        return DET_ERR_ARG;
     // Wide rows with at most 32 terms per destination (the MoE combine): TMA-staged kernel.
     int tile_elems = 0, tile_stride = 0, bulk_tiles = 0;
     const bool bulk_ok = vec && plan->max_row_len <= 32 && H * xsz >= 1024 && plan->n_units > 0 &&
                          bulk_plan_tiles(H, xsz, plan->max_row_len, &tile_elems, &tile_stride, &bulk_tiles);
     if (path == 3 && !bulk_ok) return DET_ERR_UNSUPPORTED;
     if (path == 2 && !vec) return DET_ERR_UNSUPPORTED;
-    if (bulk_ok && (path == 0 || path == 3)) {
+    // The register-staged kernel is the default (measured faster on every
+    // workload shape); the bulk kernel runs on request.
+    if (bulk_ok && path == 3) {
         BulkArgs b{};
-        b.units = plan->units;
+        b.units = plan->row_units;
         b.n_items = plan->n_units * bulk_tiles;
         b.ntiles = bulk_tiles;
         b.tile_elems = tile_elems;
@@ -384,9 +410,7 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     }
     if (a.n_tasks > 0 && vec && path == 2) {
         // 16-byte rows: asynchronous copies into a shared-memory ring
-        int64_t agrid = opts && opts->grid_ctas > 0 ? opts->grid_ctas : cdiv(a.n_tasks, kAsyncWarps);
-        agrid = std::max<int64_t>(1, std::min<int64_t>(agrid, 2147483647));
-        s = launch_gather_async(x_dtype, out_dtype, a, tbl, static_cast<int>(agrid), st);
+        s = launch_gather_async(x_dtype, out_dtype, a, tbl, grid, st);
         if (s) return s;
     } else if (a.n_tasks > 0) {
         if (x_dtype == DET_BF16 && out_dtype == DET_BF16) s = launch_gather_vec<uint16_t, __nv_bfloat16>(vec, a, tbl, grid, st);
@@ -398,10 +422,15 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     if (plan->n_hot_rows > 0) {
         const long long items = plan->n_hot_rows * H;
         const unsigned int fgrid = static_cast<unsigned int>(cdiv(items, kFinishThreads));
+        const int64_t max_segs = cdiv(cdiv(plan->max_row_len, kChunk), G);
+        const size_t fsmem = static_cast<size_t>(log2_floor(std::max<int64_t>(1, max_segs)) + 1) * kFinishThreads *
+                             sizeof(float);
         if (out_dtype == DET_BF16)
-            finish_kernel<__nv_bfloat16><<<fgrid, kFinishThreads, 0, st>>>(plan->finish, items, a.H, a.part, a.ldpart, out, ldo);
+            finish_kernel<__nv_bfloat16><<<fgrid, kFinishThreads, fsmem, st>>>(plan->finish, items, a.H, a.part,
+                                                                               a.ldpart, out, ldo);
         else
-            finish_kernel<float><<<fgrid, kFinishThreads, 0, st>>>(plan->finish, items, a.H, a.part, a.ldpart, out, ldo);
+            finish_kernel<float><<<fgrid, kFinishThreads, fsmem, st>>>(plan->finish, items, a.H, a.part, a.ldpart,
+                                                                       out, ldo);
         DETR_LAUNCHED();
     }
     if (opts && opts->debug_checks) return debug_sync_status(plan, st);

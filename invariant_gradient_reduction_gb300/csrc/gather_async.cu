@@ -83,7 +83,7 @@ gather_async_kernel(const __grid_constant__ GatherArgs a, const __grid_constant_
          task += nwarps) {
         const long long u = task / a.tile_groups;
         const int tg = static_cast<int>(task - u * a.tile_groups);
-        const int4 ud = a.units[u];
+        const int4 ud = unit_at(a, u);
         const int m = ud.x, seg = ud.y;
         const int lo = a.row_ptr[m], hi = a.row_ptr[m + 1];
         int beg = lo, end = hi;
@@ -241,7 +241,7 @@ gather_async_kernel(const __grid_constant__ GatherArgs a, const __grid_constant_
                                 for (int e = 0; e < VEC; ++e) acc[e] = pv[e];
                             }
                         }
-                        scounter_push<VEC>(stk, lane, cnt, acc);
+                        scounter_push<VEC>(stk, 32, lane, cnt, acc);
                         ++cnt;
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
@@ -251,7 +251,7 @@ gather_async_kernel(const __grid_constant__ GatherArgs a, const __grid_constant_
             float res[VEC];
 #pragma unroll
             for (int e = 0; e < VEC; ++e) res[e] = 0.0f;  // empty destination: +0.0
-            scounter_collapse<VEC>(stk, lane, cnt, res);
+            scounter_collapse<VEC>(stk, 32, lane, cnt, res);
             if (slot == 0 && active) {
                 if (seg < 0) {
                     store_out<OT, VEC>(a.out, static_cast<long long>(m) * a.ldo + e0, res, a.out_vec != 0);
@@ -275,8 +275,19 @@ template <typename XT, typename OT>
 static det_status launch_async_t(const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
 {
     const size_t smem = async_smem_bytes(a.S_log2, a.levels, Loader<XT, true>::VEC);
-    DETR_CUDA(cudaFuncSetAttribute(gather_async_kernel<XT, OT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(smem)));
+    {
+        const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(gather_async_kernel<XT, OT>), smem);
+        if (a_) return a_;
+    }
+    if (grid <= 0) {
+        int per_sm = 1, sms = 1;
+        DETR_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_async_kernel<XT, OT>, kAsyncThreads,
+                                                                smem));
+        det_status s = current_sm_count(&sms);
+        if (s) return s;
+        grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(a.n_tasks, kAsyncWarps),
+                                                                        int64_t(std::max(per_sm, 1)) * sms)));
+    }
     gather_async_kernel<XT, OT><<<grid, kAsyncThreads, smem, st>>>(a, t);
     DETR_LAUNCHED();
     return DET_OK;

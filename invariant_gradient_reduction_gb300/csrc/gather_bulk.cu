@@ -300,8 +300,10 @@ template <typename XT, typename OT>
 static det_status launch_bulk_t(const BulkArgs& a, const ShardTable& t, int grid, cudaStream_t st)
 {
     const size_t smem = bulk_smem_bytes();
-    DETR_CUDA(cudaFuncSetAttribute(gather_bulk_kernel<XT, OT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(smem)));
+    {
+        const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(gather_bulk_kernel<XT, OT>), smem);
+        if (a_) return a_;
+    }
     gather_bulk_kernel<XT, OT><<<grid, kBulkThreads, smem, st>>>(a, t);
     DETR_LAUNCHED();
     return DET_OK;

@@ -10,7 +10,9 @@ namespace detr {
 
 // Arguments of the warp-task gather-reduce kernels (gather.cu, gather_async.cu).
 struct GatherArgs {
-    const int4* units;
+    const int4* seg_units;
+    const int4* row_units;
+    long long n_seg;      // units below n_seg are hot segments
     long long n_tasks;
     int tile_groups;      // task groups per unit
     int tiles_per_group;
@@ -38,7 +40,7 @@ det_status launch_gather_async(det_dtype x_dtype, det_dtype out_dtype, const Gat
 constexpr int kAsyncWarps = 4;
 
 struct BulkArgs {
-    const int4* units;     // whole-destination units (every list has <= 32 terms)
+    const int4* units;     // whole-destination units (every list has <= 32 terms, so no segments)
     long long n_items;     // units x tiles
     int ntiles;            // H-tiles per row
     int tile_elems;        // elements per H-tile (the last tile may be shorter)
@@ -53,6 +55,11 @@ struct BulkArgs {
     long long ldo;
     int* status;           // counter block; kCtrErrTimeout is set if a bounded wait expires
 };
+
+__device__ __forceinline__ int4 unit_at(const GatherArgs& a, long long u)
+{
+    return u < a.n_seg ? a.seg_units[u] : a.row_units[u - a.n_seg];
+}
 
 size_t bulk_smem_bytes();
 // Tile a row of H elements so that max_terms staged tiles fit one stage; false if not possible.

@@ -4,10 +4,24 @@
 // order key (src_id[i], default i): the stable (expert id, original token id)
 // order the MoE backward sorts by ("DeepSeek-V4 book, Ch 09: Batch invariance
 // and determinism", section 3.2).  Everything here is integer work and exact,
-// so any correct method gives the same bytes; this one is a stable LSD radix
-// sort in 8-bit digits (order keys first when given, then the destination),
-// followed by a boundary pass that writes row_ptr and a three-phase scan that
-// writes the work list.  No kernel waits on another CTA.
+// so any correct method gives the same bytes.  This one:
+//
+//   1. plan_hist_kernel     one read of idx (and src_id): range check and the
+//                           256-bin digit histograms of every radix pass;
+//   2. radix_pass_kernel    one kernel per 8-bit digit (order keys first when
+//                           given, then the destination): a stable LSD radix
+//                           pass.  Each tile ranks its keys (match_any in
+//                           element order), finds the number of equal digits in
+//                           earlier tiles by decoupled look-back, and writes
+//                           its keys to their final places;
+//   3. units_kernel         row_ptr (binary search of each destination in the
+//                           sorted destinations) and the work list, with
+//                           decoupled look-back over row tiles.
+//
+// Look-back: tiles take their index from an atomic ticket when they start, so a
+// tile only ever waits for tiles that started before it.  Every wait is bounded;
+// on expiry the kernel sets kCtrErrTimeout, writes nothing out of range and the
+// plan reports DET_ERR_TIMEOUT.
 #include <algorithm>
 #include <new>
 
@@ -16,19 +30,24 @@
 
 namespace detr {
 
-constexpr int kSortThreads = 512;
-constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kItems = 16;
-constexpr int kTile = kSortThreads * kItems;  // keys per sort tile
+// Sort tiles: large problems use 4096-key tiles (256 threads x 16 keys, two
+// CTAs per SM), small ones 1024-key tiles (256 x 4) so that more CTAs share
+// the work.
+constexpr int kBigThreads = 256, kBigItems = 16;
+constexpr int kSmallThreads = 256, kSmallItems = 4;
+constexpr int64_t kSmallSortMaxN = 1 << 20;
 constexpr int kRadix = 256;
-constexpr int kUnitThreads = 256;
-constexpr int kUnitRowsPerThread = 16;
-constexpr int kUnitTile = kUnitThreads * kUnitRowsPerThread;
+constexpr int kHistThreads = 256;
+constexpr int kMaxPasses = 12;  // 8 order-key passes + up to 4 destination passes
+constexpr int kUnitThreads = 256;  // one row per thread
+constexpr unsigned long long kLookbackLimit = 1ull << 22;
+constexpr unsigned long long kFlagAggregate = 1ull << 32;
+constexpr unsigned long long kFlagPrefix = 2ull << 32;
 
 enum KeyMode { KM_DIRECT = 0, KM_CARRY = 1, KM_GATHER = 2 };
 
 // ------------------------------------------------------------------------
-// block scans
+// block scans and look-back
 // ------------------------------------------------------------------------
 
 // Exclusive scan of one int per thread over a block of NT threads; *total gets
@@ -63,8 +82,80 @@ __device__ __forceinline__ int block_excl_scan(int v, int* ws, int* total)
     return r;
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Decoupled look-back for one value of a tile.  status is [tiles][stride]
+// words (flag << 32 | count), zero before the kernel.  Publishes this tile's
+// aggregate, adds the earlier tiles' values (stopping at the first inclusive
+// prefix), publishes this tile's inclusive prefix and returns the exclusive
+// one.  Predecessors are read eight at a time (nearest first), so the walk
+// back over tiles that are still running costs few round trips.  Waits only
+// on tiles with smaller tickets; bounded.
+constexpr int kLookbackBatch = 8;
+
+__device__ __forceinline__ void publish_aggregate(unsigned long long* status, int tile, int stride, int k,
+                                                  unsigned int aggregate)
+{
+    st_release(&status[static_cast<long long>(tile) * stride + k], kFlagAggregate | aggregate);
+}
+
+// The walk back, once this tile's aggregate is published.
+__device__ __forceinline__ unsigned int lookback_walk(unsigned long long* status, int tile, int stride, int k,
+                                                      unsigned int aggregate, int* counters)
+{
+    unsigned long long excl = 0;
+    unsigned long long spins = 0;
+    int t = tile - 1;
+    while (t >= 0) {
+        unsigned long long v[kLookbackBatch];
+#pragma unroll
+        for (int q = 0; q < kLookbackBatch; ++q)
+            v[q] = t - q >= 0 ? ld_acquire(&status[static_cast<long long>(t - q) * stride + k]) : 0ull;
+        int used = 0;
+        bool done = false, stalled = false;
+#pragma unroll
+        for (int q = 0; q < kLookbackBatch; ++q) {
+            if (done || stalled || t - q < 0) continue;
+            const unsigned long long flag = v[q] >> 32;
+            if (flag == 0) {
+                stalled = true;
+                continue;
+            }
+            excl += v[q] & 0xffffffffull;
+            ++used;
+            if (flag == (kFlagPrefix >> 32)) done = true;
+        }
+        if (done) break;
+        t -= used;
+        if (stalled && ++spins > kLookbackLimit) {
+            atomicOr(&counters[kCtrErrTimeout], 1);
+            break;
+        }
+    }
+    st_release(&status[static_cast<long long>(tile) * stride + k],
+               kFlagPrefix | ((excl + aggregate) & 0xffffffffull));
+    return static_cast<unsigned int>(excl);
+}
+
+__device__ __forceinline__ unsigned int lookback(unsigned long long* status, int tile, int stride, int k,
+                                                 unsigned int aggregate, int* counters)
+{
+    publish_aggregate(status, tile, stride, k, aggregate);
+    return lookback_walk(status, tile, stride, k, aggregate, counters);
+}
+
 // ------------------------------------------------------------------------
-// radix sort passes
+// keys
 // ------------------------------------------------------------------------
 
 template <typename K>
@@ -103,93 +194,101 @@ __device__ __forceinline__ int digit_of(K key, int shift)
     return static_cast<int>((key >> shift) & static_cast<K>(kRadix - 1));
 }
 
-// Per-tile digit histogram; the first destination pass also range-checks idx.
-template <typename K, int MODE, bool CHECK>
-__global__ void __launch_bounds__(kSortThreads)
-radix_count_kernel(const void* kin, const int* vin, const int* gather, int* counts, long long N, int ntiles,
-                   int shift, unsigned int M, int* counters)
+// ------------------------------------------------------------------------
+// 1. histograms
+// ------------------------------------------------------------------------
+
+// ghist is [passes][256] in execution order: the 8 order-key byte passes
+// first when src_id is given, then the np32 destination digit passes.
+__global__ void __launch_bounds__(kHistThreads)
+plan_hist_kernel(const int* idx, const long long* src_id, long long N, unsigned int M, int np32, int* ghist,
+                 int* counters)
 {
-    __shared__ int hist[kRadix];
-    for (int d = threadIdx.x; d < kRadix; d += kSortThreads) hist[d] = 0;
+    __shared__ int hist[kMaxPasses * kRadix];
+    const int npass = np32 + (src_id ? 8 : 0);
+    const int dbase = src_id ? 8 : 0;
+    for (int i = threadIdx.x; i < npass * kRadix; i += kHistThreads) hist[i] = 0;
     __syncthreads();
-    const long long base = static_cast<long long>(blockIdx.x) * kTile;
     bool bad = false;
-    for (int i = threadIdx.x; i < kTile; i += kSortThreads) {
-        const long long p = base + i;
-        if (p >= N) break;
-        K key;
-        int val;
-        load_kv<K, MODE>(kin, vin, gather, p, key, val);
-        if (CHECK && static_cast<unsigned long long>(key) >= M) bad = true;
-        atomicAdd(&hist[digit_of<K>(key, shift)], 1);
-    }
-    if (CHECK && __syncthreads_or(bad) && threadIdx.x == 0) atomicOr(&counters[kCtrErrIndex], 1);
-    __syncthreads();
-    for (int d = threadIdx.x; d < kRadix; d += kSortThreads)
-        counts[static_cast<long long>(d) * ntiles + blockIdx.x] = hist[d];
-}
-
-// One CTA per digit: exclusive scan of that digit's per-tile counts, in place.
-__global__ void __launch_bounds__(256) radix_colscan_kernel(int* counts, int* col_total, int ntiles)
-{
-    __shared__ int ws[256 / 32 + 1];
-    int* row = counts + static_cast<long long>(blockIdx.x) * ntiles;
-    int carry = 0;
-    for (int base = 0; base < ntiles; base += 256 * 4) {
-        const int i0 = base + threadIdx.x * 4;
-        int v[4], s = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            v[k] = i0 + k < ntiles ? row[i0 + k] : 0;
-            s += v[k];
+    const long long stride = static_cast<long long>(gridDim.x) * kHistThreads;
+    for (long long p = static_cast<long long>(blockIdx.x) * kHistThreads + threadIdx.x; p < N; p += stride) {
+        const unsigned int key = static_cast<unsigned int>(idx[p]);
+        if (key >= M) {
+            bad = true;
+        } else {
+            for (int j = 0; j < np32; ++j) atomicAdd(&hist[(dbase + j) * kRadix + ((key >> (8 * j)) & 255u)], 1);
         }
-        int total;
-        int run = carry + block_excl_scan<256>(s, ws, &total);
+        if (src_id) {
+            const unsigned long long k64 = static_cast<unsigned long long>(src_id[p]) ^ 0x8000000000000000ull;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (i0 + k < ntiles) { row[i0 + k] = run; run += v[k]; }
-        carry += total;
+            for (int j = 0; j < 8; ++j) atomicAdd(&hist[j * kRadix + static_cast<int>((k64 >> (8 * j)) & 255u)], 1);
+        }
     }
-    if (threadIdx.x == 0) col_total[blockIdx.x] = carry;
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(&counters[kCtrErrIndex], 1);
+    for (int i = threadIdx.x; i < npass * kRadix; i += kHistThreads)
+        if (hist[i]) atomicAdd(&ghist[i], hist[i]);
 }
 
-// Stable scatter of one tile: ranks inside a warp come from match_any in
-// element order, warps are offset per digit in warp order, the tile is staged
-// in shared memory in sorted order and written out coalesced.
-template <typename K, int MODE>
-__global__ void __launch_bounds__(kSortThreads)
-radix_scatter_kernel(const void* kin, const int* vin, const int* gather, K* kout, int* vout,
-                     const int* counts, const int* col_total, long long N, int ntiles, int shift)
+// ------------------------------------------------------------------------
+// 2. one stable radix pass
+// ------------------------------------------------------------------------
+
+// Warp w owns elements [w*32*ITEMS, (w+1)*32*ITEMS) of the tile, item k of
+// lane l being element w*32*ITEMS + k*32 + l.  Ranks inside a warp come from
+// match_any in element order, warps are offset per digit in warp order, tiles
+// per digit by look-back; the tile is staged in shared memory in sorted order
+// and written out coalesced.
+template <typename K, int MODE, int NT, int ITEMS, bool WRITE_KEYS>
+__global__ void __launch_bounds__(NT)
+radix_pass_kernel(const void* kin, const int* vin, const int* gather, K* kout, int* vout, const int* ghist_p,
+                  unsigned long long* status_p, int* ticket_p, long long N, int shift, int* counters)
 {
+    constexpr int W = NT / 32;
+    constexpr int TILE = NT * ITEMS;
     extern __shared__ __align__(16) unsigned char smem[];
     K* skeys = reinterpret_cast<K*>(smem);
-    int* svals = reinterpret_cast<int*>(skeys + kTile);
-    int* whist = svals + kTile;               // [kSortWarps][kRadix]
-    int* tstart = whist + kSortWarps * kRadix;
+    int* svals = reinterpret_cast<int*>(skeys + TILE);
+    int* whist = svals + TILE;                // [W][kRadix]
+    int* tstart = whist + W * kRadix;
     int* gbase = tstart + kRadix;
-    int* ws = gbase + kRadix;                 // scan scratch
+    int* ws = gbase + kRadix;                 // scan scratch (NT/32 + 1)
+    int* s_tile = ws + NT / 32 + 1;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < kSortWarps * kRadix; i += kSortThreads) whist[i] = 0;
+    if (threadIdx.x == 0) *s_tile = atomicAdd(ticket_p, 1);
+    for (int i = threadIdx.x; i < W * kRadix; i += NT) whist[i] = 0;
+    for (int i = threadIdx.x; i < kRadix; i += NT) tstart[i] = 0;  // tile histogram first
     __syncthreads();
-
-    const long long base = static_cast<long long>(blockIdx.x) * kTile;
+    const int tile = *s_tile;
+    const long long base = static_cast<long long>(tile) * TILE;
     unsigned int lt;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
 
-    K key[kItems];
-    int val[kItems];
-    int rank[kItems];
-    int dig[kItems];
+    K key[ITEMS];
+    int val[ITEMS];
+    int rank[ITEMS];
+    int dig[ITEMS];
 #pragma unroll
-    for (int k = 0; k < kItems; ++k) {
-        const long long p = base + static_cast<long long>(warp) * 32 * kItems + k * 32 + lane;
-        const bool valid = p < N;
-        int d = kRadix;  // sentinel: invalid lanes only match each other
-        if (valid) {
+    for (int k = 0; k < ITEMS; ++k) {  // all loads first
+        const long long p = base + static_cast<long long>(warp) * 32 * ITEMS + k * 32 + lane;
+        dig[k] = -1;
+        if (p < N) {
             load_kv<K, MODE>(kin, vin, gather, p, key[k], val[k]);
-            d = digit_of<K>(key[k], shift);
+            dig[k] = 0;
         }
+    }
+    // this tile's digit counts, published before the ranking so that later
+    // tiles rarely wait for them
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k)
+        if (dig[k] >= 0) atomicAdd(&tstart[digit_of<K>(key[k], shift)], 1);
+    __syncthreads();
+    if (threadIdx.x < kRadix)
+        publish_aggregate(status_p, tile, kRadix, threadIdx.x, static_cast<unsigned int>(tstart[threadIdx.x]));
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) {
+        const bool valid = dig[k] >= 0;
+        const int d = valid ? digit_of<K>(key[k], shift) : kRadix;  // invalid lanes only match each other
         const unsigned int peers = __match_any_sync(0xffffffffu, d);
         const int leader = __ffs(peers) - 1;
         int old = 0;
@@ -209,7 +308,7 @@ radix_scatter_kernel(const void* kin, const int* vin, const int* gather, K* kout
     if (threadIdx.x < kRadix) {
         const int d = threadIdx.x;
         int run = 0;
-        for (int w = 0; w < kSortWarps; ++w) {
+        for (int w = 0; w < W; ++w) {
             const int c = whist[w * kRadix + d];
             whist[w * kRadix + d] = run;
             run += c;
@@ -217,18 +316,19 @@ radix_scatter_kernel(const void* kin, const int* vin, const int* gather, K* kout
         tot = run;
     }
     int total_unused;
-    const int excl = block_excl_scan<kSortThreads>(tot, ws, &total_unused);
-    const int ctot = threadIdx.x < kRadix ? col_total[threadIdx.x] : 0;
-    const int dstart = block_excl_scan<kSortThreads>(ctot, ws, &total_unused);
+    const int excl = block_excl_scan<NT>(tot, ws, &total_unused);
+    const int gh = threadIdx.x < kRadix ? ghist_p[threadIdx.x] : 0;
+    const int dstart = block_excl_scan<NT>(gh, ws, &total_unused);
     if (threadIdx.x < kRadix) {
         const int d = threadIdx.x;
+        const unsigned int before = lookback_walk(status_p, tile, kRadix, d, static_cast<unsigned int>(tot), counters);
         tstart[d] = excl;
-        gbase[d] = dstart + counts[static_cast<long long>(d) * ntiles + blockIdx.x] - excl;
+        gbase[d] = dstart + static_cast<int>(before) - excl;
     }
     __syncthreads();
 
 #pragma unroll
-    for (int k = 0; k < kItems; ++k) {
+    for (int k = 0; k < ITEMS; ++k) {
         if (dig[k] >= 0) {
             const int pos = tstart[dig[k]] + whist[warp * kRadix + dig[k]] + rank[k];
             skeys[pos] = key[k];
@@ -238,143 +338,112 @@ radix_scatter_kernel(const void* kin, const int* vin, const int* gather, K* kout
     __syncthreads();
 
     const long long rem = N - base;
-    const int nvalid = rem < kTile ? static_cast<int>(rem) : kTile;
-    for (int i = threadIdx.x; i < nvalid; i += kSortThreads) {
+    const int nvalid = rem < TILE ? static_cast<int>(rem) : TILE;
+    for (int i = threadIdx.x; i < nvalid; i += NT) {
         const K kk = skeys[i];
         const long long g = static_cast<long long>(gbase[digit_of<K>(kk, shift)]) + i;
-        kout[g] = kk;
-        vout[g] = svals[i];
+        if (g >= 0 && g < N) {  // only false after an expired look-back
+            if (WRITE_KEYS) kout[g] = kk;
+            vout[g] = svals[i];
+        }
     }
 }
 
-template <typename K>
-static size_t scatter_smem_bytes()
+template <typename K, int NT, int ITEMS>
+static size_t pass_smem_bytes()
 {
-    return static_cast<size_t>(kTile) * (sizeof(K) + sizeof(int)) +
-           static_cast<size_t>(kSortWarps * kRadix + 2 * kRadix + kSortThreads / 32 + 1) * sizeof(int);
+    return static_cast<size_t>(NT * ITEMS) * (sizeof(K) + sizeof(int)) +
+           static_cast<size_t>((NT / 32) * kRadix + 2 * kRadix + NT / 32 + 2) * sizeof(int);
+}
+
+// Sources of one destination must carry distinct order keys.
+__global__ void dup_key_kernel(const int* skeys, const int* perm, const long long* src_id, long long N, int* counters)
+{
+    const long long p = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x + 1;
+    if (p >= N) return;
+    if (skeys[p] == skeys[p - 1] && src_id[perm[p]] == src_id[perm[p - 1]]) atomicOr(&counters[kCtrErrDup], 1);
 }
 
 // ------------------------------------------------------------------------
-// row_ptr from the sorted destinations; order-key uniqueness
+// 3. row_ptr and the work list
 // ------------------------------------------------------------------------
 
-__global__ void row_ptr_kernel(const int* skeys, long long N, long long M, int* row_ptr,
-                               const long long* src_id, const int* perm, int* counters)
+// First position p in the sorted destinations with skeys[p] >= m.
+__device__ __forceinline__ int lower_bound(const int* skeys, int n, int m)
 {
-    if (counters[kCtrErrIndex]) return;
-    const long long p = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (p > N) return;
-    if (p < N) {
-        const long long k = skeys[p];
-        const long long prev = p == 0 ? -1 : skeys[p - 1];
-        for (long long m = prev + 1; m <= k; ++m) row_ptr[m] = static_cast<int>(p);
-        if (src_id && p > 0 && prev == k && src_id[perm[p]] == src_id[perm[p - 1]])
-            atomicOr(&counters[kCtrErrDup], 1);
-    } else {
-        const long long last = N == 0 ? -1 : skeys[N - 1];
-        for (long long m = last + 1; m <= M; ++m) row_ptr[m] = static_cast<int>(N);
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(skeys + mid) < m) lo = mid + 1;
+        else hi = mid;
     }
+    return lo;
 }
 
-// ------------------------------------------------------------------------
-// work list: whole destinations, and hot destinations split into segments
-// ------------------------------------------------------------------------
-
-struct RowWork {
-    int seg;     // hot segments of this row (0 if not hot)
-    int normal;  // 1 if the row is one whole unit
-    int hot;     // 1 if the row needs a finish task
-};
-
-__device__ __forceinline__ RowWork row_work(const int* row_ptr, long long m, int g, int* len)
+// One row per thread: hot rows (more than 2^g chunks) give `seg` segment
+// units and one finish task; the others one whole-row unit.  row_ptr[m] is a
+// binary search of the sorted destinations (the row's end comes from the
+// next lane).  Emits the segment units [A], the row units [B], the finish
+// tasks [C], and the totals A, B, C and the longest list into the counter
+// block.
+__global__ void __launch_bounds__(kUnitThreads)
+units_kernel(const int* skeys, long long N, long long M, int g, int* row_ptr, int4* seg_units, int4* row_units,
+             int4* finish, unsigned long long* ustatus, int* uticket, int nut, int* counters)
 {
-    const int n = row_ptr[m + 1] - row_ptr[m];
-    *len = n;
-    const int nch = (n + kChunk - 1) / kChunk;
+    __shared__ int ws[kUnitThreads / 32 + 1];
+    __shared__ int s_tile;
+    __shared__ int s_excl[4];
+    if (threadIdx.x == 0) s_tile = atomicAdd(uticket, 1);
+    __syncthreads();
+    const int tile = s_tile;
+    if (counters[kCtrErrIndex] || counters[kCtrErrTimeout]) {
+        // keep the look-back chain alive for later tiles, emit nothing
+        if (threadIdx.x < 3) lookback(ustatus, tile, 4, threadIdx.x, 0u, counters);
+        return;
+    }
+    const int lane = threadIdx.x & 31;
     const int G = 1 << g;
-    RowWork r;
-    if (nch > G) { r.seg = (nch + G - 1) >> g; r.normal = 0; r.hot = 1; }
-    else { r.seg = 0; r.normal = 1; r.hot = 0; }
-    return r;
-}
-
-__global__ void __launch_bounds__(kUnitThreads)
-units_count_kernel(const int* row_ptr, long long M, int g, int* upart, int nut, int* counters)
-{
-    __shared__ int ws[kUnitThreads / 32 + 1];
-    if (counters[kCtrErrIndex]) return;
-    const long long m0 = static_cast<long long>(blockIdx.x) * kUnitTile + threadIdx.x * kUnitRowsPerThread;
-    int a = 0, b = 0, c = 0, mx = 0;
-    for (int k = 0; k < kUnitRowsPerThread; ++k) {
-        const long long m = m0 + k;
-        if (m >= M) break;
-        int len;
-        const RowWork r = row_work(row_ptr, m, g, &len);
-        a += r.seg; b += r.normal; c += r.hot;
-        mx = max(mx, len);
-    }
-    int ta, tb, tc;
-    block_excl_scan<kUnitThreads>(a, ws, &ta);
-    block_excl_scan<kUnitThreads>(b, ws, &tb);
-    block_excl_scan<kUnitThreads>(c, ws, &tc);
-    if (threadIdx.x == 0) {
-        upart[blockIdx.x] = ta;
-        upart[nut + blockIdx.x] = tb;
-        upart[2 * nut + blockIdx.x] = tc;
-    }
-    if (mx > 0) atomicMax(&counters[kCtrMaxLen], mx);
-}
-
-__global__ void __launch_bounds__(1024) units_scan_kernel(int* upart, int nut, int* counters)
-{
-    __shared__ int ws[1024 / 32 + 1];
-    if (counters[kCtrErrIndex]) return;
-    for (int arr = 0; arr < 3; ++arr) {
-        int* v = upart + arr * nut;
-        int carry = 0;
-        for (int base = 0; base < nut; base += 1024) {
-            const int i = base + threadIdx.x;
-            const int x = i < nut ? v[i] : 0;
-            int total;
-            const int e = block_excl_scan<1024>(x, ws, &total);
-            if (i < nut) v[i] = carry + e;
-            carry += total;
-        }
-        if (threadIdx.x == 0) counters[kCtrSegs + arr] = carry;
-    }
-}
-
-__global__ void __launch_bounds__(kUnitThreads)
-units_emit_kernel(const int* row_ptr, long long M, int g, const int* upart, int nut, const int* counters,
-                  int4* units, int4* finish)
-{
-    __shared__ int ws[kUnitThreads / 32 + 1];
-    if (counters[kCtrErrIndex]) return;
-    const long long m0 = static_cast<long long>(blockIdx.x) * kUnitTile + threadIdx.x * kUnitRowsPerThread;
+    const long long m = static_cast<long long>(tile) * kUnitThreads + threadIdx.x;
+    const int n = static_cast<int>(N);
+    const int start = m < M ? lower_bound(skeys, n, static_cast<int>(m)) : n;
+    int next = __shfl_down_sync(0xffffffffu, start, 1);
+    if (lane == 31) next = m + 1 < M ? lower_bound(skeys, n, static_cast<int>(m + 1)) : n;
+    if (m + 1 >= M) next = n;
+    const int len = m < M ? next - start : 0;
+    const int nch = (len + kChunk - 1) / kChunk;
     int a = 0, b = 0, c = 0;
-    for (int k = 0; k < kUnitRowsPerThread; ++k) {
-        const long long m = m0 + k;
-        if (m >= M) break;
-        int len;
-        const RowWork r = row_work(row_ptr, m, g, &len);
-        a += r.seg; b += r.normal; c += r.hot;
+    if (m < M) {
+        if (nch > G) { a = (nch + G - 1) >> g; c = 1; }
+        else b = 1;
     }
-    int t;
-    int ao = block_excl_scan<kUnitThreads>(a, ws, &t) + upart[blockIdx.x];
-    int bo = block_excl_scan<kUnitThreads>(b, ws, &t) + upart[nut + blockIdx.x] + counters[kCtrSegs];
-    int co = block_excl_scan<kUnitThreads>(c, ws, &t) + upart[2 * nut + blockIdx.x];
-    for (int k = 0; k < kUnitRowsPerThread; ++k) {
-        const long long m = m0 + k;
-        if (m >= M) break;
-        int len;
-        const RowWork r = row_work(row_ptr, m, g, &len);
-        if (r.hot) {
-            finish[co++] = make_int4(static_cast<int>(m), ao, r.seg, 0);
-            for (int s = 0; s < r.seg; ++s) units[ao + s] = make_int4(static_cast<int>(m), s, ao + s, 0);
-            ao += r.seg;
+    int tA, tB, tC;
+    int eA = block_excl_scan<kUnitThreads>(a, ws, &tA);
+    int eB = block_excl_scan<kUnitThreads>(b, ws, &tB);
+    int eC = block_excl_scan<kUnitThreads>(c, ws, &tC);
+    if (threadIdx.x < 3) {
+        const int tot = threadIdx.x == 0 ? tA : (threadIdx.x == 1 ? tB : tC);
+        s_excl[threadIdx.x] =
+            static_cast<int>(lookback(ustatus, tile, 4, threadIdx.x, static_cast<unsigned int>(tot), counters));
+    }
+    __syncthreads();
+    eA += s_excl[0];
+    eB += s_excl[1];
+    eC += s_excl[2];
+    if (m < M) {
+        row_ptr[m] = start;
+        if (nch > G) {
+            finish[eC] = make_int4(static_cast<int>(m), eA, a, 0);
+            for (int s = 0; s < a; ++s) seg_units[eA + s] = make_int4(static_cast<int>(m), s, eA + s, 0);
         } else {
-            units[bo++] = make_int4(static_cast<int>(m), -1, 0, 0);
+            row_units[eB] = make_int4(static_cast<int>(m), -1, 0, 0);
         }
+        if (len > 0) atomicMax(&counters[kCtrMaxLen], len);
+    }
+    if (tile == nut - 1 && threadIdx.x == 0) {
+        row_ptr[M] = n;
+        counters[kCtrSegs] = s_excl[0] + tA;
+        counters[kCtrNormal] = s_excl[1] + tB;
+        counters[kCtrHot] = s_excl[2] + tC;
     }
 }
 
@@ -383,11 +452,27 @@ units_emit_kernel(const int* row_ptr, long long M, int g, const int* upart, int 
 // ------------------------------------------------------------------------
 
 struct PlanLayout {
-    size_t row_ptr, perm, skeys, k32_tmp, v_tmp, k64_a, k64_b, va, vb, counts, col_total, units, finish,
-        upart, counters, total;
-    int ntiles, nut;
-    int64_t max_units, max_finish;
+    // zeroed at the start of every plan: counters, tickets, histograms,
+    // per-destination counts, row_ptr and the look-back status words
+    size_t counters, tickets, ghist, row_ptr, status, ustatus, zero_end;
+    size_t perm, skeys, k32_tmp, v_tmp, k64_a, k64_b, va, vb, seg_units, row_units, finish, total;
+    int ntiles, nut, npass;
+    int64_t max_segs, max_rows, max_finish;
 };
+
+static int sort_tile(int64_t N)
+{
+    return N <= kSmallSortMaxN ? kSmallThreads * kSmallItems : kBigThreads * kBigItems;
+}
+
+static int bit_length(int64_t v)
+{
+    int b = 0;
+    while (v > 0) { ++b; v >>= 1; }
+    return b;
+}
+
+static int dest_passes(int64_t M) { return (std::max(1, bit_length(M - 1)) + 7) / 8; }
 
 static PlanLayout plan_layout(int64_t N, int64_t M, bool with_src, int g)
 {
@@ -398,13 +483,20 @@ static PlanLayout plan_layout(int64_t N, int64_t M, bool with_src, int g)
         off = align_up(off + (bytes ? bytes : 1), 256);
         return at;
     };
-    L.ntiles = static_cast<int>(std::max<int64_t>(1, cdiv(N, kTile)));
-    L.nut = static_cast<int>(std::max<int64_t>(1, cdiv(M, kUnitTile)));
+    L.ntiles = static_cast<int>(std::max<int64_t>(1, cdiv(N, sort_tile(N))));
+    L.nut = static_cast<int>(std::max<int64_t>(1, cdiv(M, kUnitThreads)));
+    L.npass = dest_passes(M) + (with_src ? 8 : 0);
     const int64_t seg_terms = static_cast<int64_t>(kChunk) << g;
     L.max_finish = cdiv(N, seg_terms) + 1;
-    L.max_units = M + 2 * cdiv(N, seg_terms) + 1;
+    L.max_segs = 2 * cdiv(N, seg_terms) + 1;
+    L.max_rows = M + 1;
     L.counters = take(kCtrCount * sizeof(int));
+    L.tickets = take(static_cast<size_t>(kMaxPasses + 1) * sizeof(int));
+    L.ghist = take(static_cast<size_t>(L.npass) * kRadix * sizeof(int));
     L.row_ptr = take(static_cast<size_t>(M + 1) * sizeof(int));
+    L.status = take(static_cast<size_t>(L.npass) * L.ntiles * kRadix * sizeof(unsigned long long));
+    L.ustatus = take(static_cast<size_t>(L.nut) * 4 * sizeof(unsigned long long));
+    L.zero_end = off;
     L.perm = take(static_cast<size_t>(N) * sizeof(int));
     L.skeys = take(static_cast<size_t>(N) * sizeof(int));
     L.k32_tmp = take(static_cast<size_t>(N) * sizeof(int));
@@ -415,11 +507,9 @@ static PlanLayout plan_layout(int64_t N, int64_t M, bool with_src, int g)
         L.va = take(static_cast<size_t>(N) * sizeof(int));
         L.vb = take(static_cast<size_t>(N) * sizeof(int));
     }
-    L.counts = take(static_cast<size_t>(kRadix) * L.ntiles * sizeof(int));
-    L.col_total = take(kRadix * sizeof(int));
-    L.units = take(static_cast<size_t>(L.max_units) * sizeof(int4));
+    L.seg_units = take(static_cast<size_t>(L.max_segs) * sizeof(int4));
+    L.row_units = take(static_cast<size_t>(L.max_rows) * sizeof(int4));
     L.finish = take(static_cast<size_t>(L.max_finish) * sizeof(int4));
-    L.upart = take(static_cast<size_t>(3) * L.nut * sizeof(int));
     L.total = off;
     return L;
 }
@@ -434,30 +524,30 @@ static det_status resolve_seg_log2(const det_opts* o, int* g)
     return DET_OK;
 }
 
-static int bit_length(int64_t v)
+template <typename K, int MODE, int NT, int ITEMS, bool WRITE_KEYS>
+static det_status radix_pass_t(const void* kin, const int* vin, const int* gather, K* kout, int* vout,
+                               const int* ghist_p, unsigned long long* status_p, int* ticket_p, int64_t N, int ntiles,
+                               int shift, int* counters, cudaStream_t st)
 {
-    int b = 0;
-    while (v > 0) { ++b; v >>= 1; }
-    return b;
-}
-
-template <typename K, int MODE, bool CHECK>
-static det_status radix_pass(const void* kin, const int* vin, const int* gather, K* kout, int* vout,
-                             int* counts, int* col_total, int64_t N, int ntiles, int shift, int64_t M,
-                             int* counters, cudaStream_t st)
-{
-    radix_count_kernel<K, MODE, CHECK><<<ntiles, kSortThreads, 0, st>>>(
-        kin, vin, gather, counts, N, ntiles, shift, static_cast<unsigned int>(M), counters);
-    DETR_LAUNCHED();
-    radix_colscan_kernel<<<kRadix, 256, 0, st>>>(counts, col_total, ntiles);
-    DETR_LAUNCHED();
-    const size_t smem = scatter_smem_bytes<K>();
-    DETR_CUDA(cudaFuncSetAttribute(radix_scatter_kernel<K, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(smem)));
-    radix_scatter_kernel<K, MODE><<<ntiles, kSortThreads, smem, st>>>(kin, vin, gather, kout, vout, counts,
-                                                                    col_total, N, ntiles, shift);
+    const size_t smem = pass_smem_bytes<K, NT, ITEMS>();
+    auto kern = radix_pass_kernel<K, MODE, NT, ITEMS, WRITE_KEYS>;
+    { const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(kern), smem); if (a_) return a_; }
+    kern<<<ntiles, NT, smem, st>>>(kin, vin, gather, kout, vout, ghist_p, status_p, ticket_p, N, shift, counters);
     DETR_LAUNCHED();
     return DET_OK;
+}
+
+template <typename K, int MODE, bool WRITE_KEYS>
+static det_status radix_pass(bool small, const void* kin, const int* vin, const int* gather, K* kout, int* vout,
+                             const int* ghist_p, unsigned long long* status_p, int* ticket_p, int64_t N, int ntiles,
+                             int shift, int* counters, cudaStream_t st)
+{
+    if (small)
+        return radix_pass_t<K, MODE, kSmallThreads, kSmallItems, WRITE_KEYS>(kin, vin, gather, kout, vout, ghist_p,
+                                                                             status_p, ticket_p, N, ntiles, shift,
+                                                                             counters, st);
+    return radix_pass_t<K, MODE, kBigThreads, kBigItems, WRITE_KEYS>(kin, vin, gather, kout, vout, ghist_p, status_p,
+                                                                     ticket_p, N, ntiles, shift, counters, st);
 }
 
 }  // namespace detr
@@ -501,74 +591,102 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     cudaStream_t st = as_stream(stream);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     int* counters = reinterpret_cast<int*>(ws + L.counters);
+    int* tickets = reinterpret_cast<int*>(ws + L.tickets);
+    int* ghist = reinterpret_cast<int*>(ws + L.ghist);
     int* row_ptr = reinterpret_cast<int*>(ws + L.row_ptr);
+    unsigned long long* status = reinterpret_cast<unsigned long long*>(ws + L.status);
+    unsigned long long* ustatus = reinterpret_cast<unsigned long long*>(ws + L.ustatus);
     int* perm = reinterpret_cast<int*>(ws + L.perm);
     int* skeys = reinterpret_cast<int*>(ws + L.skeys);
     int* k32_tmp = reinterpret_cast<int*>(ws + L.k32_tmp);
     int* v_tmp = reinterpret_cast<int*>(ws + L.v_tmp);
-    int* counts = reinterpret_cast<int*>(ws + L.counts);
-    int* col_total = reinterpret_cast<int*>(ws + L.col_total);
-    int4* units = reinterpret_cast<int4*>(ws + L.units);
+    int4* seg_units = reinterpret_cast<int4*>(ws + L.seg_units);
+    int4* row_units = reinterpret_cast<int4*>(ws + L.row_units);
     int4* finish = reinterpret_cast<int4*>(ws + L.finish);
-    int* upart = reinterpret_cast<int*>(ws + L.upart);
 
-    DETR_CUDA(cudaMemsetAsync(counters, 0, kCtrCount * sizeof(int), st));
+    const int np32 = dest_passes(M);
+    DETR_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, st));
+    int sms = 0;
+    s = current_sm_count(&sms);
+    if (s) return s;
 
     if (N > 0) {
+        const int hgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(N, kHistThreads * 16),
+                                                                                  int64_t(sms) * 8)));
+        plan_hist_kernel<<<hgrid, kHistThreads, 0, st>>>(idx, with_src ? reinterpret_cast<const long long*>(src_id)
+                                                                       : nullptr,
+                                                         N, static_cast<unsigned int>(M), np32, ghist, counters);
+        DETR_LAUNCHED();
         const int ntiles = L.ntiles;
+        const bool small = N <= kSmallSortMaxN;
+        const size_t sstride = static_cast<size_t>(ntiles) * kRadix;
+        int pass = 0;
         const int* vals_in = nullptr;
         if (with_src) {
             unsigned long long* k64[2] = {reinterpret_cast<unsigned long long*>(ws + L.k64_a),
                                           reinterpret_cast<unsigned long long*>(ws + L.k64_b)};
             int* v64[2] = {reinterpret_cast<int*>(ws + L.va), reinterpret_cast<int*>(ws + L.vb)};
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 8; ++j, ++pass) {
                 const int o = j & 1;
                 if (j == 0)
-                    s = radix_pass<unsigned long long, KM_DIRECT, false>(src_id, nullptr, nullptr, k64[o], v64[o],
-                                                                         counts, col_total, N, ntiles, 0, M,
-                                                                         counters, st);
+                    s = radix_pass<unsigned long long, KM_DIRECT, true>(small, src_id, nullptr, nullptr, k64[o], v64[o],
+                                                                        ghist + pass * kRadix, status + pass * sstride,
+                                                                        tickets + pass, N, ntiles, 0, counters, st);
                 else
-                    s = radix_pass<unsigned long long, KM_CARRY, false>(k64[o ^ 1], v64[o ^ 1], nullptr, k64[o],
-                                                                        v64[o], counts, col_total, N, ntiles,
-                                                                        8 * j, M, counters, st);
+                    s = radix_pass<unsigned long long, KM_CARRY, true>(small, k64[o ^ 1], v64[o ^ 1], nullptr, k64[o],
+                                                                       v64[o], ghist + pass * kRadix,
+                                                                       status + pass * sstride, tickets + pass, N,
+                                                                       ntiles, 8 * j, counters, st);
                 if (s) return s;
             }
             vals_in = v64[1];
         }
-        const int np32 = (std::max(1, bit_length(M - 1)) + 7) / 8;
-        for (int j = 0; j < np32; ++j) {
+        for (int j = 0; j < np32; ++j, ++pass) {
+            const bool last = j == np32 - 1;
             const bool to_final = ((np32 - 1 - j) % 2) == 0;
             unsigned int* ko = reinterpret_cast<unsigned int*>(to_final ? skeys : k32_tmp);
             int* vo = to_final ? perm : v_tmp;
             const unsigned int* ki = reinterpret_cast<const unsigned int*>(to_final ? k32_tmp : skeys);
             const int* vi = to_final ? v_tmp : perm;
+            const int* gh = ghist + pass * kRadix;
+            unsigned long long* stp = status + pass * sstride;
+            // the last pass writes the sorted destinations too: the work list
+            // finds row_ptr in them
+            const bool wk = true;
+            (void)last;
             if (j == 0 && with_src)
-                s = radix_pass<unsigned int, KM_GATHER, true>(nullptr, vals_in, idx, ko, vo, counts, col_total, N,
-                                                              ntiles, 0, M, counters, st);
+                s = wk ? radix_pass<unsigned int, KM_GATHER, true>(small, nullptr, vals_in, idx, ko, vo, gh, stp,
+                                                                   tickets + pass, N, ntiles, 0, counters, st)
+                       : radix_pass<unsigned int, KM_GATHER, false>(small, nullptr, vals_in, idx, ko, vo, gh, stp,
+                                                                    tickets + pass, N, ntiles, 0, counters, st);
             else if (j == 0)
-                s = radix_pass<unsigned int, KM_DIRECT, true>(idx, nullptr, nullptr, ko, vo, counts, col_total, N,
-                                                              ntiles, 0, M, counters, st);
+                s = wk ? radix_pass<unsigned int, KM_DIRECT, true>(small, idx, nullptr, nullptr, ko, vo, gh, stp,
+                                                                   tickets + pass, N, ntiles, 0, counters, st)
+                       : radix_pass<unsigned int, KM_DIRECT, false>(small, idx, nullptr, nullptr, ko, vo, gh, stp,
+                                                                    tickets + pass, N, ntiles, 0, counters, st);
             else
-                s = radix_pass<unsigned int, KM_CARRY, false>(ki, vi, nullptr, ko, vo, counts, col_total, N, ntiles,
-                                                              8 * j, M, counters, st);
+                s = wk ? radix_pass<unsigned int, KM_CARRY, true>(small, ki, vi, nullptr, ko, vo, gh, stp,
+                                                                  tickets + pass, N, ntiles, 8 * j, counters, st)
+                       : radix_pass<unsigned int, KM_CARRY, false>(small, ki, vi, nullptr, ko, vo, gh, stp,
+                                                                   tickets + pass, N, ntiles, 8 * j, counters, st);
             if (s) return s;
         }
+        if (with_src && N > 1) {
+            dup_key_kernel<<<static_cast<unsigned int>(cdiv(N - 1, 256)), 256, 0, st>>>(
+                skeys, perm, reinterpret_cast<const long long*>(src_id), N, counters);
+            DETR_LAUNCHED();
+        }
     }
-    row_ptr_kernel<<<static_cast<unsigned int>(cdiv(N + 1, 256)), 256, 0, st>>>(
-        skeys, N, M, row_ptr, with_src ? reinterpret_cast<const long long*>(src_id) : nullptr, perm, counters);
-    DETR_LAUNCHED();
     if (M > 0) {
-        units_count_kernel<<<L.nut, kUnitThreads, 0, st>>>(row_ptr, M, g, upart, L.nut, counters);
-        DETR_LAUNCHED();
-        units_scan_kernel<<<1, 1024, 0, st>>>(upart, L.nut, counters);
-        DETR_LAUNCHED();
-        units_emit_kernel<<<L.nut, kUnitThreads, 0, st>>>(row_ptr, M, g, upart, L.nut, counters, units, finish);
+        units_kernel<<<L.nut, kUnitThreads, 0, st>>>(skeys, N, M, g, row_ptr, seg_units, row_units, finish, ustatus,
+                                                     tickets + kMaxPasses, L.nut, counters);
         DETR_LAUNCHED();
     }
     int h[kCtrCount];
     DETR_CUDA(cudaMemcpyAsync(h, counters, sizeof(h), cudaMemcpyDeviceToHost, st));
     DETR_CUDA(cudaStreamSynchronize(st));
     if (h[kCtrErrIndex]) return DET_ERR_INDEX_RANGE;
+    if (h[kCtrErrTimeout]) return DET_ERR_TIMEOUT;
     if (h[kCtrErrDup]) return DET_ERR_ORDER_KEY;
 
     det_plan_s* p = new (std::nothrow) det_plan_s();
@@ -581,7 +699,8 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     p->counters = counters;
     p->row_ptr = row_ptr;
     p->perm = perm;
-    p->units = units;
+    p->seg_units = seg_units;
+    p->row_units = row_units;
     p->finish = finish;
     p->n_segments = h[kCtrSegs];
     p->n_units = static_cast<int64_t>(h[kCtrSegs]) + h[kCtrNormal];

@@ -22,9 +22,11 @@ enum {
 }  // namespace detr
 
 // Host handle.  Device arrays live in the caller's plan workspace.
-//   units[u]  = {row m, segment s (-1 = whole row), partial slot, 0}; hot
-//               segments first, then whole rows in row order.
-//   finish[k] = {row m, first partial slot, number of segments, 0}.
+//   seg_units[u] = {row m, segment s, partial slot, 0} for the hot segments;
+//   row_units[u] = {row m, -1, 0, 0} for the whole-row units, in row order;
+//   finish[k]    = {row m, first partial slot, number of segments, 0}.
+// Work unit u of the reduce is seg_units[u] for u < n_segments, else
+// row_units[u - n_segments] (hot segments first: they are the longest).
 struct det_plan_s {
     int64_t N = 0, M = 0;
     int g = 3;                       // a hot segment covers 2^g chunks of 32 terms
@@ -33,7 +35,8 @@ struct det_plan_s {
     int* counters = nullptr;         // [kCtrCount]
     int* row_ptr = nullptr;          // [M+1]
     int* perm = nullptr;             // [N]
-    int4* units = nullptr;
+    int4* seg_units = nullptr;
+    int4* row_units = nullptr;
     int4* finish = nullptr;
     int64_t n_units = 0, n_segments = 0, n_hot_rows = 0, max_row_len = 0;
 };

@@ -141,43 +141,43 @@ __device__ __forceinline__ void counter_collapse(const float (&stk)[DR][VEC], un
     }
 }
 
-// The same binary counter with its stack in shared memory: lane-private
-// columns laid out [level][element][lane], so the accesses of a warp are
-// conflict-free.  Used by the warp-task kernels, which push one node per round.
-__device__ __forceinline__ float* scounter_slot(float* st, int L, int e, int VEC, int lane)
+// The same binary counter with its stack in shared memory: each thread owns
+// a column (`col` of `ncol`), laid out [level][element][column] so that the
+// accesses of a warp are conflict-free.  Pushes happen once per round, so a
+// short dynamic loop costs little.
+__device__ __forceinline__ float* scounter_slot(float* st, int L, int e, int VEC, int ncol, int col)
 {
-    return st + (static_cast<size_t>(L) * VEC + e) * 32 + lane;
+    return st + (static_cast<size_t>(L) * VEC + e) * ncol + col;
 }
 
 template <int VEC>
-__device__ __forceinline__ void scounter_push(float* st, int lane, unsigned int cnt, float* node)
+__device__ __forceinline__ void scounter_push(float* st, int ncol, int col, unsigned int cnt, float* node)
 {
     unsigned int c = cnt;
     int L = 0;
     while (c & 1u) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) node[e] = __fadd_rn(*scounter_slot(st, L, e, VEC, lane), node[e]);
+        for (int e = 0; e < VEC; ++e) node[e] = __fadd_rn(*scounter_slot(st, L, e, VEC, ncol, col), node[e]);
         c >>= 1;
         ++L;
     }
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) *scounter_slot(st, L, e, VEC, lane) = node[e];
+    for (int e = 0; e < VEC; ++e) *scounter_slot(st, L, e, VEC, ncol, col) = node[e];
 }
 
 template <int VEC>
-__device__ __forceinline__ void scounter_collapse(const float* st, int lane, unsigned int cnt, float* res)
+__device__ __forceinline__ void scounter_collapse(float* st, int ncol, int col, unsigned int cnt, float* res)
 {
     bool have = false;
     for (int L = 0; (cnt >> L) != 0u; ++L) {
         if ((cnt >> L) & 1u) {
-            const float* col = st + static_cast<size_t>(L) * VEC * 32 + lane;
             if (!have) {
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) res[e] = col[e * 32];
+                for (int e = 0; e < VEC; ++e) res[e] = *scounter_slot(st, L, e, VEC, ncol, col);
                 have = true;
             } else {
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) res[e] = __fadd_rn(col[e * 32], res[e]);
+                for (int e = 0; e < VEC; ++e) res[e] = __fadd_rn(*scounter_slot(st, L, e, VEC, ncol, col), res[e]);
             }
         }
     }
