@@ -95,9 +95,9 @@ typedef int32_t det_dtype;
  *  gather_path      0 = auto.  1 = register-staged warp kernel, 2 = warp
  *                   kernel with cp.async copies into shared memory, 3 = TMA
  *                   bulk-staged kernel (only when every destination has at
- *                   most 32 terms and rows are at least 1 KB; otherwise the
- *                   call fails with DET_ERR_UNSUPPORTED).  For comparing the
- *                   kernels; every path gives the same bits.
+ *                   most 32 terms and rows are at least 1 KB).  A path that
+ *                   does not apply fails with DET_ERR_UNSUPPORTED.  For
+ *                   comparing the kernels; every path gives the same bits.
  *  tiles_per_task   0 = auto; > 0 = H-tiles one warp task of the warp kernels
  *                   covers (the work split changes no bit).
  *  reserved         must be zero.

@@ -133,18 +133,7 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
 #pragma unroll
                                     for (int e = 0; e < VEC; ++e) xf[e] = 0.0f;
                                 }
-                                if (has_w) {
-                                    const float wv = myw[jb + q];
-#pragma unroll
-                                    for (int e = 0; e < VEC; ++e) xf[e] = __fmul_rn(wv, xf[e]);
-                                }
-                                if (jb + q == 0) {
-#pragma unroll
-                                    for (int e = 0; e < VEC; ++e) acc[e] = xf[e];
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(acc[e], xf[e]);
-                                }
+                                fold_term<VEC>(acc, xf, has_w, has_w ? myw[jb + q] : 1.0f, jb + q == 0);
                             }
                         }
                     }

@@ -209,18 +209,7 @@ gather_async_kernel(const __grid_constant__ GatherArgs a, const __grid_constant_
 #pragma unroll
                                     for (int e = 0; e < VEC; ++e) xf[e] = 0.0f;
                                 }
-                                if (has_w) {
-                                    const float wv = myw[j];
-#pragma unroll
-                                    for (int e = 0; e < VEC; ++e) xf[e] = __fmul_rn(wv, xf[e]);
-                                }
-                                if (j == 0) {
-#pragma unroll
-                                    for (int e = 0; e < VEC; ++e) acc[e] = xf[e];
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(acc[e], xf[e]);
-                                }
+                                fold_term<VEC>(acc, xf, has_w, has_w ? myw[j] : 1.0f, j == 0);
                             }
                         }
                     }

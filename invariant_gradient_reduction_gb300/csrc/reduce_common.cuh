@@ -97,6 +97,54 @@ __device__ __forceinline__ void store_out(void* base, long long off, const float
     }
 }
 
+// Packed FP32 add (sm_100 and later): one instruction performs two IEEE
+// binary32 adds, each rounded to nearest even on its own, so the bits equal
+// those of two __fadd_rn.  Measured on this GPU over 2^21 random pairs: equal
+// bits.  The weight multiply stays scalar (__fmul_rn): a packed multiply
+// feeding a packed add was measured to be contracted into a fused
+// multiply-add by the assembler, which would change the bits.
+__device__ __forceinline__ unsigned long long pack2(float a, float b)
+{
+    unsigned long long d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ void unpack2(unsigned long long v, float& a, float& b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+
+__device__ __forceinline__ unsigned long long add2_rn(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// One term of the left-to-right fold on VEC elements: p = fl32(w * x) (no
+// multiply without weights), then acc = p for the chunk's first term, else
+// acc = fl32(acc + p).
+template <int VEC>
+__device__ __forceinline__ void fold_term(float* acc, const float* xf, bool has_w, float wv, bool first)
+{
+    float p[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) p[e] = has_w ? __fmul_rn(wv, xf[e]) : xf[e];
+    if (first) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = p[e];
+    } else if (VEC % 2 == 0) {
+#pragma unroll
+        for (int e = 0; e < VEC; e += 2)
+            unpack2(add2_rn(pack2(acc[e], acc[(e + 1) % VEC]), pack2(p[e], p[(e + 1) % VEC])), acc[e],
+                    acc[(e + 1) % VEC]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(acc[e], p[e]);
+    }
+}
+
 // Binary counter over aligned tree nodes: pushing node number `cnt` merges it
 // with its completed left neighbours, exactly as the level-wise tree pairs them.
 template <int DR, int VEC>
