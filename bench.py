@@ -41,6 +41,7 @@ if ROOT not in sys.path:
 
 METRIC = "deterministic scatter-reduce HBM GB/s (% of peak) and overhead vs atomicAdd"
 UNIT = "GB/s"
+ASYNC = {"async_plan": 1}  # plans enqueue without a host wait
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 WORKLOADS = {
@@ -224,13 +225,15 @@ def scatter_step_fns(case, torch):
     out = torch.empty(case.M, case.H, dtype=case.out_dtype, device=dev)
     state = {}
 
+    # The step's plan does not wait for its counts (they stay on the device);
+    # its error status is read once after the timed region (check_last_plan).
     def plan_and_reduce():
-        p = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan)
-        dr.det_scatter_reduce(p, case.x, out, w=case.w, workspace=state.get("ws_red"))
+        p = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan, opts=ASYNC)
+        dr.det_scatter_reduce(p, case.x, out, w=case.w, workspace=state.get("ws_red"), opts=ASYNC)
         state["plan"] = p
 
-    plan0 = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan)
-    need = dr.det_scatter_workspace_size(plan0, case.H)
+    plan0 = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan, opts=ASYNC)
+    need = dr.det_scatter_workspace_size(plan0, case.H)  # the bound for an unwaited plan covers a waited one
     state["ws_red"] = torch.empty(need + 256, dtype=torch.uint8, device=dev) if need else None
     ws_plan_fixed = torch.empty_like(ws_plan)
     plan_fixed = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan_fixed)
@@ -245,14 +248,18 @@ def scatter_step_fns(case, torch):
     def atomic():
         dr.det_atomic_scatter_reduce(case.idx, case.M, case.x, out_atomic, w=case.w, workspace=ws_atomic)
 
-    return plan_and_reduce, reduce_only, atomic, out, plan_fixed
+    def check_last_plan():
+        dr.det_plan_status(state.get("plan", plan0))
+
+    return plan_and_reduce, reduce_only, atomic, out, plan_fixed, check_last_plan
 
 
 def measure_scatter(case, timer, steps, warmup, torch, with_e2e=True):
     from invariant_gradient_reduction_gb300 import detreduce as dr
     cb = case.compulsory_bytes()
-    full, red, atom, out, plan = scatter_step_fns(case, torch)
+    full, red, atom, out, plan, check_last_plan = scatter_step_fns(case, torch)
     t_full, l_full = timer.run(full, steps, warmup)
+    check_last_plan()
     t_red, _ = timer.run(red, steps, warmup)
     t_atom, _ = timer.run(atom, steps, warmup)
     ms_full, ms_red, ms_atom = statistics.mean(t_full), statistics.mean(t_red), statistics.mean(t_atom)
@@ -287,20 +294,23 @@ def measure_e2e(case, timer, steps, warmup, torch):
     out_d = torch.empty(case.M, case.H, dtype=case.out_dtype, device=dev)
     out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
     ws_plan = torch.empty(dr.det_plan_workspace_size(case.N, case.M) + 256, dtype=torch.uint8, device=dev)
-    p0 = dr.det_reduce_plan(case.idx, case.M)
+    p0 = dr.det_reduce_plan(case.idx, case.M, opts=ASYNC)
     need = dr.det_scatter_workspace_size(p0, case.H)
     ws_red = torch.empty(need + 256, dtype=torch.uint8, device=dev) if need else None
+    last = {"plan": p0}
 
     def step():
         x_d.copy_(x_h, non_blocking=True)
         idx_d.copy_(idx_h, non_blocking=True)
         if w_h is not None:
             w_d.copy_(w_h, non_blocking=True)
-        p = dr.det_reduce_plan(idx_d, case.M, workspace=ws_plan)
-        dr.det_scatter_reduce(p, x_d, out_d, w=w_d, workspace=ws_red)
+        p = dr.det_reduce_plan(idx_d, case.M, workspace=ws_plan, opts=ASYNC)
+        dr.det_scatter_reduce(p, x_d, out_d, w=w_d, workspace=ws_red, opts=ASYNC)
         out_h.copy_(out_d, non_blocking=True)
+        last["plan"] = p
 
     t, _ = timer.run(step, steps, warmup)
+    dr.det_plan_status(last["plan"])
     ms = statistics.mean(t)
     bi = x_h.numel() * x_h.element_size() + idx_h.numel() * 4 + (0 if w_h is None else w_h.numel() * 4)
     bo = out_h.numel() * out_h.element_size()
@@ -388,7 +398,7 @@ def run_ours(args):
     sampler = ClockSampler(local_rank).start()
     time.sleep(0.1)
     # warm-up, then exactly K timed steps bracketed by barrier + synchronize
-    full, red, atom, out, plan = scatter_step_fns(case, torch)
+    full, red, atom, out, plan, check_last_plan = scatter_step_fns(case, torch)
     for _ in range(args.warmup):
         timer.flush()
         full()
@@ -405,6 +415,7 @@ def run_ours(args):
         e.record()
     torch.cuda.synchronize()
     launches = dr.det_kernel_launches() - l0
+    check_last_plan()
     if world > 1:
         tdist.barrier()
     t_wall1 = time.time()

@@ -100,6 +100,14 @@ typedef int32_t det_dtype;
  *                   comparing the kernels; every path gives the same bits.
  *  tiles_per_task   0 = auto; > 0 = H-tiles one warp task of the warp kernels
  *                   covers (the work split changes no bit).
+ *  async_plan       plan-time option.  0 (default): det_reduce_plan waits once
+ *                   and reports index and order-key errors itself.  Nonzero:
+ *                   det_reduce_plan only enqueues its kernels and returns; the
+ *                   work counts stay on the device, where det_scatter_reduce
+ *                   reads them, and errors are reported by det_plan_status.
+ *                   If the plan recorded an error, det_scatter_reduce writes
+ *                   nothing.  Lets plan and reduce run back to back (and be
+ *                   captured in a CUDA graph).
  *  reserved         must be zero.
  */
 typedef struct det_opts {
@@ -108,7 +116,8 @@ typedef struct det_opts {
     int32_t debug_checks;
     int32_t gather_path;
     int32_t tiles_per_task;
-    int32_t reserved[3];
+    int32_t async_plan;
+    int32_t reserved[2];
 } det_opts;
 
 /* Opaque host handle of a built plan.  Its device arrays live in the
@@ -128,6 +137,7 @@ typedef struct det_plan_desc {
     int64_t n_segments;       /* hot segments = fp32 partial slots needed per H */
     int64_t n_hot_rows;       /* destinations split into segments */
     int64_t max_row_len;      /* largest number of terms of one destination */
+    /* (the four counts are -1 for an async plan until det_plan_status) */
 } det_plan_desc;
 
 /* Text of a status code (static storage; never NULL). */
@@ -181,12 +191,22 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
 /* Release the host handle (the workspace stays the caller's).  NULL is OK. */
 det_status det_plan_destroy(det_plan plan);
 
+/*
+ * Wait for the plan's kernels on `stream` and report what they found:
+ * DET_OK, DET_ERR_INDEX_RANGE, DET_ERR_ORDER_KEY or DET_ERR_TIMEOUT.  For a
+ * plan built with async_plan this is where errors surface; afterwards the
+ * work counts are known on the host (det_plan_describe).  For a synchronous
+ * plan it returns DET_OK.
+ */
+det_status det_plan_status(det_plan plan, void* stream);
+
 /* Fill *desc (host) from a built plan. */
 det_status det_plan_describe(det_plan plan, det_plan_desc* desc);
 
 /*
  * Bytes of device workspace det_scatter_reduce needs for the hot-segment
- * partial slots at row width H (0 when the plan has no hot destination).
+ * partial slots at row width H (0 when the plan has no hot destination; for
+ * an async plan whose counts are still on the device, an upper bound).
  */
 det_status det_scatter_workspace_size(det_plan plan, int64_t H, size_t* bytes);
 

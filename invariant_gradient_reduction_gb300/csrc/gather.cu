@@ -66,11 +66,13 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
     const long long seg_terms = static_cast<long long>(kChunk) << a.g;
 
     const long long nwarps = static_cast<long long>(gridDim.x) * kGatherWarps;
-    for (long long task = static_cast<long long>(blockIdx.x) * kGatherWarps + warp; task < a.n_tasks;
+    long long n_tasks, n_seg;
+    if (!task_counts(a, &n_tasks, &n_seg)) return;
+    for (long long task = static_cast<long long>(blockIdx.x) * kGatherWarps + warp; task < n_tasks;
          task += nwarps) {
         const long long u = task / a.tile_groups;
         const int tg = static_cast<int>(task - u * a.tile_groups);
-        const int4 ud = unit_at(a, u);
+        const int4 ud = unit_at(a, u, n_seg);
         const int m = ud.x, seg = ud.y;
         const int lo = a.row_ptr[m], hi = a.row_ptr[m + 1];
         int beg = lo, end = hi;
@@ -186,11 +188,15 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
 template <typename OT>
 __global__ void __launch_bounds__(kFinishThreads)
 finish_kernel(const int4* finish, long long n_items, int H, const float* part, long long ldpart, void* out,
-              long long ldo)
+              long long ldo, const int* dev_counters)
 {
     extern __shared__ float fstk[];  // [levels][kFinishThreads]
-    const long long t = static_cast<long long>(blockIdx.x) * kFinishThreads + threadIdx.x;
-    if (t >= n_items) return;
+    if (dev_counters) {
+        if (dev_counters[kCtrErrIndex] | dev_counters[kCtrErrDup] | dev_counters[kCtrErrTimeout]) return;
+        n_items = static_cast<long long>(dev_counters[kCtrHot]) * H;
+    }
+    for (long long t = static_cast<long long>(blockIdx.x) * kFinishThreads + threadIdx.x; t < n_items;
+         t += static_cast<long long>(gridDim.x) * kFinishThreads) {
     const long long row_task = t / H;
     const int h = static_cast<int>(t - row_task * H);
     const int4 ft = finish[row_task];
@@ -213,6 +219,7 @@ finish_kernel(const int4* finish, long long n_items, int H, const float* part, l
     float res[1] = {0.0f};
     scounter_collapse<1>(fstk, kFinishThreads, threadIdx.x, cnt, res);
     store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
+    }
 }
 
 template <typename XT, typename OT, bool VECTOR>
@@ -274,7 +281,9 @@ det_status det_scatter_workspace_size(det_plan plan, int64_t H, size_t* bytes)
     if (!plan || !bytes || H < 0) return DET_ERR_ARG;
     if (H > kMaxRows) return DET_ERR_UNSUPPORTED;
     const int64_t ldpart = (H + 7) / 8 * 8;
-    *bytes = static_cast<size_t>(plan->n_segments) * static_cast<size_t>(ldpart) * sizeof(float);
+    const int64_t segs = plan->counts_on_host ? plan->n_segments
+                                              : 2 * cdiv(plan->N, static_cast<int64_t>(kChunk) << plan->g) + 1;
+    *bytes = static_cast<size_t>(segs) * static_cast<size_t>(ldpart) * sizeof(float);
     return DET_OK;
 }
 
@@ -322,9 +331,12 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     a.ntiles = static_cast<int>(cdiv(V, int64_t(1) << T_log2));
     a.H = static_cast<int>(H);
     a.g = plan->g;
+    const bool dev_counts = !plan->counts_on_host;  // async plan: counts stay on the device
     a.seg_units = plan->seg_units;
     a.row_units = plan->row_units;
-    a.n_seg = plan->n_segments;
+    a.n_seg = dev_counts ? 0 : plan->n_segments;
+    a.dev_counters = dev_counts ? plan->counters : nullptr;
+    const int64_t n_units = dev_counts ? std::max<int64_t>(1, M) : plan->n_units;  // estimate when unknown
     a.row_ptr = plan->row_ptr;
     a.perm = plan->perm;
     a.w = w;
@@ -342,19 +354,20 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     // task's list lookups, while keeping at least two tasks per resident warp
     // (measured best on the MoE combine and EP-invariance shapes; the split
     // changes no bit).
-    const int64_t avg_terms = std::max<int64_t>(1, plan->N / std::max<int64_t>(1, plan->n_units));
+    const int64_t avg_terms = std::max<int64_t>(1, plan->N / std::max<int64_t>(1, n_units));
     const int64_t tile_bytes = (int64_t(1) << T_log2) * (vec ? 16 : xsz);
     int tpg = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, 16384 / (avg_terms * tile_bytes))));
     const int64_t min_tasks = static_cast<int64_t>(sms) * 24 * 2;
-    while (tpg > 1 && plan->n_units * cdiv(a.ntiles, tpg) < min_tasks) tpg = static_cast<int>(cdiv(tpg, 2));
+    while (tpg > 1 && n_units * cdiv(a.ntiles, tpg) < min_tasks) tpg = static_cast<int>(cdiv(tpg, 2));
     if (opts && opts->tiles_per_task > 0) tpg = std::min(opts->tiles_per_task, a.ntiles);
     a.tiles_per_group = tpg;
     a.tile_groups = static_cast<int>(cdiv(a.ntiles, tpg));
-    a.n_tasks = plan->n_units * a.tile_groups;
+    a.n_tasks = dev_counts ? (plan->M + 2 * cdiv(plan->N, int64_t(kChunk) << plan->g) + 1) * a.tile_groups
+                           : plan->n_units * a.tile_groups;  // an upper bound when the counts are on the device
 
     // Binary-counter depth: enough levels for the longest unit's rounds.
     const int64_t G = int64_t(1) << plan->g;
-    const int64_t max_chunks = std::min(cdiv(plan->max_row_len, kChunk), G);
+    const int64_t max_chunks = dev_counts ? G : std::min(cdiv(plan->max_row_len, kChunk), G);
     const int64_t max_rounds = std::max<int64_t>(1, cdiv(max_chunks, int64_t(1) << a.S_log2));
     a.levels = log2_floor(max_rounds) + 1;
 
@@ -363,12 +376,11 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     cudaStream_t st = as_stream(stream);
 
     const int path = opts ? opts->gather_path : 0;
-    if (path < 0 || path > 3 || (opts && (opts->tiles_per_task < 0 || opts->reserved[0] || opts->reserved[1] ||
-                                          opts->reserved[2])))
+    if (path < 0 || path > 3 || (opts && (opts->tiles_per_task < 0 || opts->reserved[0] || opts->reserved[1])))
         return DET_ERR_ARG;
     // Wide rows with at most 32 terms per destination (the MoE combine): TMA-staged kernel.
     int tile_elems = 0, tile_stride = 0, bulk_tiles = 0;
-    const bool bulk_ok = vec && plan->max_row_len <= 32 && H * xsz >= 1024 && plan->n_units > 0 &&
+    const bool bulk_ok = vec && !dev_counts && plan->max_row_len <= 32 && H * xsz >= 1024 && plan->n_units > 0 &&
                          bulk_plan_tiles(H, xsz, plan->max_row_len, &tile_elems, &tile_stride, &bulk_tiles);
     if (path == 3 && !bulk_ok) return DET_ERR_UNSUPPORTED;
     if (path == 2 && !vec) return DET_ERR_UNSUPPORTED;
@@ -408,18 +420,26 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
         else s = launch_gather_vec<float, float>(vec, a, tbl, grid, st);
         if (s) return s;
     }
-    if (plan->n_hot_rows > 0) {
-        const long long items = plan->n_hot_rows * H;
-        const unsigned int fgrid = static_cast<unsigned int>(cdiv(items, kFinishThreads));
-        const int64_t max_segs = cdiv(cdiv(plan->max_row_len, kChunk), G);
+    // Hot destinations: a second pass.  With device-side counts it runs
+    // whenever a hot destination is possible, on a grid-stride launch.
+    const bool maybe_hot = dev_counts ? plan->N > (int64_t(kChunk) << plan->g) : plan->n_hot_rows > 0;
+    if (maybe_hot) {
+        const int64_t max_row = dev_counts ? plan->N : plan->max_row_len;
+        const long long items = dev_counts ? (cdiv(plan->N, (int64_t(kChunk) << plan->g) + 1) + 1) * H
+                                           : plan->n_hot_rows * H;
+        const int64_t fgrid64 = dev_counts ? std::min<int64_t>(cdiv(items, kFinishThreads), int64_t(sms) * 16)
+                                           : cdiv(items, kFinishThreads);
+        const unsigned int fgrid = static_cast<unsigned int>(std::max<int64_t>(1, fgrid64));
+        const int64_t max_segs = cdiv(cdiv(max_row, kChunk), G);
         const size_t fsmem = static_cast<size_t>(log2_floor(std::max<int64_t>(1, max_segs)) + 1) * kFinishThreads *
                              sizeof(float);
+        const int* dc = dev_counts ? plan->counters : nullptr;
         if (out_dtype == DET_BF16)
             finish_kernel<__nv_bfloat16><<<fgrid, kFinishThreads, fsmem, st>>>(plan->finish, items, a.H, a.part,
-                                                                               a.ldpart, out, ldo);
+                                                                               a.ldpart, out, ldo, dc);
         else
             finish_kernel<float><<<fgrid, kFinishThreads, fsmem, st>>>(plan->finish, items, a.H, a.part, a.ldpart,
-                                                                       out, ldo);
+                                                                       out, ldo, dc);
         DETR_LAUNCHED();
     }
     if (opts && opts->debug_checks) return debug_sync_status(plan, st);

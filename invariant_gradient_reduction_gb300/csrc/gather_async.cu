@@ -79,11 +79,13 @@ gather_async_kernel(const __grid_constant__ GatherArgs a, const __grid_constant_
     const long long seg_terms = static_cast<long long>(kChunk) << a.g;
 
     const long long nwarps = static_cast<long long>(gridDim.x) * kAsyncWarps;
-    for (long long task = static_cast<long long>(blockIdx.x) * kAsyncWarps + warp; task < a.n_tasks;
+    long long n_tasks, n_seg;
+    if (!task_counts(a, &n_tasks, &n_seg)) return;
+    for (long long task = static_cast<long long>(blockIdx.x) * kAsyncWarps + warp; task < n_tasks;
          task += nwarps) {
         const long long u = task / a.tile_groups;
         const int tg = static_cast<int>(task - u * a.tile_groups);
-        const int4 ud = unit_at(a, u);
+        const int4 ud = unit_at(a, u, n_seg);
         const int m = ud.x, seg = ud.y;
         const int lo = a.row_ptr[m], hi = a.row_ptr[m + 1];
         int beg = lo, end = hi;

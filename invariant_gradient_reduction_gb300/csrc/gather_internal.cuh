@@ -5,6 +5,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "plan_internal.cuh"
 
 namespace detr {
 
@@ -31,7 +32,24 @@ struct GatherArgs {
     long long ldo;
     float* part;
     long long ldpart;
+    const int* dev_counters;  // non-null: read the work counts (and plan errors) from the device
 };
+
+// Work counts of a launch: from the host, or from the plan's counter block
+// when the plan did not wait.  Returns false if the plan recorded an error
+// (the kernel then writes nothing).
+__device__ __forceinline__ bool task_counts(const GatherArgs& a, long long* n_tasks, long long* n_seg)
+{
+    *n_tasks = a.n_tasks;
+    *n_seg = a.n_seg;
+    if (a.dev_counters) {
+        const int* c = a.dev_counters;
+        if (c[kCtrErrIndex] | c[kCtrErrDup] | c[kCtrErrTimeout]) return false;
+        *n_seg = c[kCtrSegs];
+        *n_tasks = (static_cast<long long>(c[kCtrSegs]) + c[kCtrNormal]) * a.tile_groups;
+    }
+    return true;
+}
 
 // Vector-path gather with per-lane asynchronous copies into a shared-memory ring.
 size_t async_smem_bytes(int S_log2, int levels, int vec);
@@ -56,9 +74,9 @@ struct BulkArgs {
     int* status;           // counter block; kCtrErrTimeout is set if a bounded wait expires
 };
 
-__device__ __forceinline__ int4 unit_at(const GatherArgs& a, long long u)
+__device__ __forceinline__ int4 unit_at(const GatherArgs& a, long long u, long long n_seg)
 {
-    return u < a.n_seg ? a.seg_units[u] : a.row_units[u - a.n_seg];
+    return u < n_seg ? a.seg_units[u] : a.row_units[u - n_seg];
 }
 
 size_t bulk_smem_bytes();

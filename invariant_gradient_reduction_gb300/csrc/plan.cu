@@ -514,6 +514,22 @@ static PlanLayout plan_layout(int64_t N, int64_t M, bool with_src, int g)
     return L;
 }
 
+static det_status counter_status(const int* h)
+{
+    if (h[kCtrErrIndex]) return DET_ERR_INDEX_RANGE;
+    if (h[kCtrErrTimeout]) return DET_ERR_TIMEOUT;
+    if (h[kCtrErrDup]) return DET_ERR_ORDER_KEY;
+    return DET_OK;
+}
+
+static void set_counts(det_plan_s* p, const int* h)
+{
+    p->n_segments = h[kCtrSegs];
+    p->n_units = static_cast<int64_t>(h[kCtrSegs]) + h[kCtrNormal];
+    p->n_hot_rows = h[kCtrHot];
+    p->max_row_len = h[kCtrMaxLen];
+}
+
 static det_status resolve_seg_log2(const det_opts* o, int* g)
 {
     *g = kDefaultSegLog2;
@@ -682,12 +698,14 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
                                                      tickets + kMaxPasses, L.nut, counters);
         DETR_LAUNCHED();
     }
-    int h[kCtrCount];
-    DETR_CUDA(cudaMemcpyAsync(h, counters, sizeof(h), cudaMemcpyDeviceToHost, st));
-    DETR_CUDA(cudaStreamSynchronize(st));
-    if (h[kCtrErrIndex]) return DET_ERR_INDEX_RANGE;
-    if (h[kCtrErrTimeout]) return DET_ERR_TIMEOUT;
-    if (h[kCtrErrDup]) return DET_ERR_ORDER_KEY;
+    const bool async = opts && opts->async_plan;
+    int h[kCtrCount] = {};
+    if (!async) {
+        DETR_CUDA(cudaMemcpyAsync(h, counters, sizeof(h), cudaMemcpyDeviceToHost, st));
+        DETR_CUDA(cudaStreamSynchronize(st));
+        const det_status e = counter_status(h);
+        if (e) return e;
+    }
 
     det_plan_s* p = new (std::nothrow) det_plan_s();
     if (!p) return DET_ERR_ARG;
@@ -702,11 +720,28 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     p->seg_units = seg_units;
     p->row_units = row_units;
     p->finish = finish;
-    p->n_segments = h[kCtrSegs];
-    p->n_units = static_cast<int64_t>(h[kCtrSegs]) + h[kCtrNormal];
-    p->n_hot_rows = h[kCtrHot];
-    p->max_row_len = h[kCtrMaxLen];
+    if (async) {
+        p->counts_on_host = false;
+        p->n_segments = p->n_units = p->n_hot_rows = p->max_row_len = -1;
+    } else {
+        set_counts(p, h);
+    }
     *out_plan = p;
+    return DET_OK;
+}
+
+det_status det_plan_status(det_plan plan, void* stream)
+{
+    if (!plan) return DET_ERR_ARG;
+    if (plan->counts_on_host) return DET_OK;
+    int h[kCtrCount];
+    cudaStream_t st = as_stream(stream);
+    DETR_CUDA(cudaMemcpyAsync(h, plan->counters, sizeof(h), cudaMemcpyDeviceToHost, st));
+    DETR_CUDA(cudaStreamSynchronize(st));
+    const det_status e = counter_status(h);
+    if (e) return e;
+    set_counts(plan, h);
+    plan->counts_on_host = true;
     return DET_OK;
 }
 

@@ -39,4 +39,5 @@ struct det_plan_s {
     int4* row_units = nullptr;
     int4* finish = nullptr;
     int64_t n_units = 0, n_segments = 0, n_hot_rows = 0, max_row_len = 0;
+    bool counts_on_host = true;      // false for an async plan until det_plan_status
 };

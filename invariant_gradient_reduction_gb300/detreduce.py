@@ -48,7 +48,7 @@ class DetError(RuntimeError):
 class det_opts(ctypes.Structure):
     _fields_ = [("grid_ctas", ctypes.c_int32), ("seg_chunks_log2", ctypes.c_int32),
                 ("debug_checks", ctypes.c_int32), ("gather_path", ctypes.c_int32),
-                ("tiles_per_task", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("tiles_per_task", ctypes.c_int32), ("async_plan", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
 
 
 class det_plan_desc(ctypes.Structure):
@@ -74,6 +74,7 @@ def _declare(lib):
         "det_reduce_plan": ([vp, vp, i64, i64, vp, sz, P(det_opts), vp, P(vp)], i32),
         "det_plan_destroy": ([vp], i32),
         "det_plan_describe": ([vp, P(det_plan_desc)], i32),
+        "det_plan_status": ([vp, vp], i32),
         "det_scatter_workspace_size": ([vp, i64, P(sz)], i32),
         "det_scatter_reduce": ([vp, P(vp), P(i64), i32, i32, i64, i64, vp, vp, i64, i32, vp, sz,
                                 P(det_opts), vp], i32),
@@ -116,7 +117,7 @@ def _opts(opts: Optional[dict]):
         return None
     o = det_opts(grid_ctas=int(opts.get("grid_ctas", 0)), seg_chunks_log2=int(opts.get("seg_chunks_log2", -1)),
                  debug_checks=int(opts.get("debug_checks", 0)), gather_path=int(opts.get("gather_path", 0)),
-                 tiles_per_task=int(opts.get("tiles_per_task", 0)))
+                 tiles_per_task=int(opts.get("tiles_per_task", 0)), async_plan=int(opts.get("async_plan", 0)))
     return ctypes.byref(o)
 
 
@@ -216,6 +217,11 @@ def det_reduce_plan(idx: torch.Tensor, M: int, src_id: Optional[torch.Tensor] = 
     _check(lib().det_reduce_plan(_ptr(idx), _ptr(src_id), N, M, _aligned_ptr(ws), _aligned_bytes(ws), _opts(opts),
                                  _stream(stream), ctypes.byref(h)), "det_reduce_plan")
     return Plan(h, ws, N, M)
+
+
+def det_plan_status(plan: Plan, stream=None) -> None:
+    """Wait for the plan's kernels and raise DetError if they found an error (async plans)."""
+    _check(lib().det_plan_status(plan.handle, _stream(stream)), "det_plan_status")
 
 
 def det_plan_describe(plan: Plan) -> dict:

@@ -456,3 +456,59 @@ def test_atomic_negative_control_differs_across_replays():
         elif not torch.equal(b, ref):
             differing += 1
     assert differing > 0
+
+
+# --------------------------------------------------------------------------
+# plan without a host wait: counts read on the device
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", SCATTER_SMALL)
+def test_async_plan_same_bytes(name):
+    """A plan that does not wait gives the same bytes, on every gather kernel that accepts it."""
+    case = small_case(name)
+    want = oracle_scatter(case)
+    out, plan = gpu_scatter(case, opts={"async_plan": 1})
+    assert_bytes_equal(np_bits(out), want, f"{name} async")
+    assert plan.describe()["n_units"] == -1
+    for path, grid in ((1, 0), (1, 3), (2, 0), (0, sms())):
+        out2 = torch.full_like(out, 7.0)
+        dr.det_scatter_reduce(plan, case.x, out2, w=case.w, opts={"async_plan": 1, "gather_path": path,
+                                                                   "grid_ctas": grid})
+        assert_bytes_equal(np_bits(out2), want, f"{name} async path={path} grid={grid}")
+    dr.det_plan_status(plan)
+    d = plan.describe()
+    want_rp, _ = oracle.build_lists(case.idx.cpu().numpy(), case.M)
+    assert d["max_row_len"] == int(np.diff(want_rp).max())
+    # once the counts are on the host the plan behaves like a waited one
+    out3, _ = gpu_scatter(case, plan=plan)
+    assert_bytes_equal(np_bits(out3), want, f"{name} after status")
+
+
+def test_async_plan_full_size_sampled():
+    case = wl.make("sparse_key_scatter", "full", device=DEV)
+    out, plan = gpu_scatter(case, opts={"async_plan": 1})
+    dr.det_plan_status(plan)
+    rng = np.random.default_rng(5)
+    rows = _sample_rows(case, 48, rng)
+    got = np_bits(out)[rows]
+    assert_bytes_equal(got, oracle_scatter(case, rows), "sparse_key_scatter full async")
+
+
+def test_async_plan_errors_reported_and_nothing_written():
+    M, H = 6, 64
+    x = torch.randn(4, H, device=DEV)
+    for idx, sid, code in (([0, 1, 6, 2], None, dr.DET_ERR_INDEX_RANGE),
+                           ([0, -3, 1, 1], None, dr.DET_ERR_INDEX_RANGE),
+                           ([1, 1, 0, 2], [4, 4, 1, 2], dr.DET_ERR_ORDER_KEY)):
+        it = torch.tensor(idx, dtype=torch.int32, device=DEV)
+        st = None if sid is None else torch.tensor(sid, dtype=torch.int64, device=DEV)
+        plan = dr.det_reduce_plan(it, M, src_id=st, opts={"async_plan": 1})
+        out = torch.full((M, H), 3.5, device=DEV)
+        dr.det_scatter_reduce(plan, x, out, opts={"async_plan": 1})
+        with pytest.raises(dr.DetError) as e:
+            dr.det_plan_status(plan)
+        assert e.value.code == code
+        assert bool((out == 3.5).all()), "a failed plan must leave the output untouched"
+    # a waited plan reports OK from det_plan_status
+    plan = dr.det_reduce_plan(torch.tensor([0, 1], dtype=torch.int32, device=DEV), 2)
+    dr.det_plan_status(plan)
