@@ -108,6 +108,14 @@ typedef int32_t det_dtype;
  *                   If the plan recorded an error, det_scatter_reduce writes
  *                   nothing.  Lets plan and reduce run back to back (and be
  *                   captured in a CUDA graph).
+ *  plan_path        plan-time option.  0 = auto.  1 = multi-kernel plan
+ *                   (histogram, one radix pass per digit, work list).  2 =
+ *                   single-cluster plan: one kernel on a thread-block cluster
+ *                   of up to 16 CTAs holding the sources in distributed shared
+ *                   memory; only without src_id, for N <= 131072 and
+ *                   M <= 8192 x (cluster CTAs), and only where the device can
+ *                   schedule the cluster (else DET_ERR_UNSUPPORTED).  Auto
+ *                   takes path 2 where it applies.  Both build the same lists.
  *  reserved         must be zero.
  */
 typedef struct det_opts {
@@ -117,7 +125,8 @@ typedef struct det_opts {
     int32_t gather_path;
     int32_t tiles_per_task;
     int32_t async_plan;
-    int32_t reserved[2];
+    int32_t plan_path;
+    int32_t reserved[1];
 } det_opts;
 
 /* Opaque host handle of a built plan.  Its device arrays live in the

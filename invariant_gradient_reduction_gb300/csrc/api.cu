@@ -14,7 +14,6 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 void set_last_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
 
-constexpr int kMaxDevices = 64;
 static std::atomic<int> g_sm_count[kMaxDevices];
 
 det_status current_sm_count(int* sms)

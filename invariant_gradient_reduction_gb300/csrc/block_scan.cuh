@@ -1,0 +1,38 @@
+// block_scan.cuh -- exclusive scan of one int per thread over a thread block.
+#pragma once
+
+namespace detr {
+
+// Exclusive scan of one int per thread over a block of NT threads; *total gets
+// the block sum.  `ws` is shared scratch of NT/32 + 1 ints.  Ends synchronised.
+template <int NT>
+__device__ __forceinline__ int block_excl_scan(int v, int* ws, int* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) ws[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int s = lane < NT / 32 ? ws[lane] : 0;
+        int si = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int t = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) si += t;
+        }
+        if (lane < NT / 32) ws[lane] = si - s;
+        if (lane == 31) ws[NT / 32] = si;
+    }
+    __syncthreads();
+    int r = incl - v + ws[warp];
+    *total = ws[NT / 32];
+    __syncthreads();
+    return r;
+}
+
+}  // namespace detr

@@ -12,6 +12,7 @@ namespace detr {
 
 // Limits: sizes and offsets of the destination lists are int32 on the device.
 constexpr int64_t kMaxRows = 2147483646;  // N, M <= 2^31 - 2
+constexpr int kMaxDevices = 64;            // per-device caches
 
 // Canonical fold: consecutive chunks of this many terms are folded left to right.
 constexpr int kChunk = 32;

@@ -376,7 +376,7 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     cudaStream_t st = as_stream(stream);
 
     const int path = opts ? opts->gather_path : 0;
-    if (path < 0 || path > 3 || (opts && (opts->tiles_per_task < 0 || opts->reserved[0] || opts->reserved[1])))
+    if (path < 0 || path > 3 || (opts && (opts->tiles_per_task < 0 || opts->reserved[0])))
         return DET_ERR_ARG;
     // Wide rows with at most 32 terms per destination (the MoE combine): TMA-staged kernel.
     int tile_elems = 0, tile_stride = 0, bulk_tiles = 0;

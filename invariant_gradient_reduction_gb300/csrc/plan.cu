@@ -25,6 +25,7 @@
 #include <algorithm>
 #include <new>
 
+#include "block_scan.cuh"
 #include "common.cuh"
 #include "plan_internal.cuh"
 
@@ -49,38 +50,6 @@ enum KeyMode { KM_DIRECT = 0, KM_CARRY = 1, KM_GATHER = 2 };
 // ------------------------------------------------------------------------
 // block scans and look-back
 // ------------------------------------------------------------------------
-
-// Exclusive scan of one int per thread over a block of NT threads; *total gets
-// the block sum.  `ws` is shared scratch of NT/32 + 1 ints.  Ends synchronised.
-template <int NT>
-__device__ __forceinline__ int block_excl_scan(int v, int* ws, int* total)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    if (lane == 31) ws[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int s = lane < NT / 32 ? ws[lane] : 0;
-        int si = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int t = __shfl_up_sync(0xffffffffu, si, o);
-            if (lane >= o) si += t;
-        }
-        if (lane < NT / 32) ws[lane] = si - s;
-        if (lane == 31) ws[NT / 32] = si;
-    }
-    __syncthreads();
-    int r = incl - v + ws[warp];
-    *total = ws[NT / 32];
-    __syncthreads();
-    return r;
-}
 
 __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p)
 {
@@ -596,6 +565,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     int g;
     det_status s = resolve_seg_log2(opts, &g);
     if (s) return s;
+    if (opts && (opts->plan_path < 0 || opts->plan_path > 2 || opts->reserved[0])) return DET_ERR_ARG;
     const bool with_src = src_id != nullptr && N > 0;
     const PlanLayout L = plan_layout(N, M, with_src, g);
     if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return DET_ERR_WORKSPACE;
@@ -621,13 +591,22 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     int4* finish = reinterpret_cast<int4*>(ws + L.finish);
 
     const int np32 = dest_passes(M);
+    const int plan_path = opts ? opts->plan_path : 0;
+    bool one_cluster = false;
+    if (plan_path != 1 && !with_src && N > 0) {
+        s = launch_plan_cluster(idx, N, M, g, np32, row_ptr, perm, seg_units, row_units, finish, counters, st,
+                                &one_cluster);
+        if (s) return s;
+    }
+    if (plan_path == 2 && !one_cluster) return DET_ERR_UNSUPPORTED;
+    if (!one_cluster) {
     DETR_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, st));
     int sms = 0;
     s = current_sm_count(&sms);
     if (s) return s;
 
     if (N > 0) {
-        const int hgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(N, kHistThreads * 16),
+        const int hgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(N, kHistThreads * 2),
                                                                                   int64_t(sms) * 8)));
         plan_hist_kernel<<<hgrid, kHistThreads, 0, st>>>(idx, with_src ? reinterpret_cast<const long long*>(src_id)
                                                                        : nullptr,
@@ -698,6 +677,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
                                                      tickets + kMaxPasses, L.nut, counters);
         DETR_LAUNCHED();
     }
+    }  // multi-kernel plan
     const bool async = opts && opts->async_plan;
     int h[kCtrCount] = {};
     if (!async) {

@@ -1,0 +1,430 @@
+// plan_cluster.cu -- the whole plan in one kernel on one thread-block cluster,
+// for small problems ordered by source position (no src_id).
+//
+// The lists are the same as the multi-kernel plan's: the terms of destination
+// m are the sources with idx[i] = m in ascending i ("DeepSeek-V4 book, Ch 09:
+// Batch invariance and determinism", section 3.2), and the work list splits
+// destinations with more than 2^g chunks into aligned segments.  All of it is
+// integer work, so both methods give the same arrays.
+//
+// A small plan built from separate kernels is latency-bound: every kernel pays
+// its launch and a few dependent round trips to L2.  Here one cluster of C CTAs
+// (one per SM, C <= 16) keeps the sources in distributed shared memory, each
+// CTA a slice of E consecutive positions, and runs every step between cluster
+// barriers:
+//   1. each CTA loads its slice of idx and checks the range;
+//   2. per 8-bit digit of the destination, a stable LSD radix pass: the CTA
+//      ranks its slice (match_any in element order, warps in order), publishes
+//      its 256 digit counts, reads those of every CTA of the cluster (the
+//      earlier CTAs give its offsets, all of them the digit starts) and writes
+//      each key to its place in the owning CTA's slice;
+//   3. perm from the sorted slices; row_ptr[m] by a binary search for m in the
+//      sorted keys (the owning slice from the CTAs' last keys, then inside it);
+//   4. the work list: rows classified as whole-row units or hot rows, offsets
+//      by scans inside the CTA and across the cluster; CTA 0 writes the counter
+//      block.
+// Cluster barriers are hardware barriers: no thread waits on a flag.
+#include <cooperative_groups.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "block_scan.cuh"
+#include "common.cuh"
+#include "plan_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace detr {
+
+constexpr int kCluThreads = 1024;
+constexpr int kCluWarps = kCluThreads / 32;
+constexpr int kCluItems = 8;
+constexpr int kCluRadix = 256;
+static_assert(kCluThreads * kCluItems == kCluMaxSlice, "one slice is one item per thread per kCluItems");
+static_assert(kCluMaxCtas < 32, "the cluster-level scan runs on one warp");
+
+__device__ __forceinline__ long long min_ll(long long a, long long b) { return a < b ? a : b; }
+
+struct CluShared {
+    unsigned int keys[kCluMaxSlice];  // this CTA's slice of the current order
+    int vals[kCluMaxSlice];           // source position of each key
+    int whist[kCluWarps * kCluRadix];  // per warp digit counts, then warp offsets
+    int chist[kCluRadix];             // this CTA's digit counts (read by the cluster)
+    int gbase[kCluRadix];             // first position of this CTA's keys of each digit
+    int ws[3 * (kCluWarps + 1)];      // scan scratch
+    unsigned int lastk[kCluMaxCtas];  // last key of every CTA's sorted slice
+    int tot[4];                       // seg units, row units, finish tasks, longest row (read by the cluster)
+    int base[3];                      // this CTA's offsets into the three unit arrays
+    int grand[4];                     // cluster totals
+    int bad;                          // this CTA saw an index outside [0, M) (read by the cluster)
+    int any_bad;
+};
+
+// Exclusive scans of three ints per thread over 1024 threads at once; tot gets
+// the three block sums.  Ends synchronised.
+__device__ __forceinline__ void block_excl_scan3(int v[3], int* ws, int tot[3])
+{
+    constexpr int W = kCluWarps;  // 32: one lane per warp in the second level
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        incl[j] = v[j];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl[j], o);
+            if (lane >= o) incl[j] += t;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) ws[j * (W + 1) + warp] = incl[j];
+    }
+    __syncthreads();
+    if (warp < 3) {
+        const int s = ws[warp * (W + 1) + lane];
+        int si = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) si += t;
+        }
+        ws[warp * (W + 1) + lane] = si - s;
+        if (lane == 31) ws[warp * (W + 1) + W] = si;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        tot[j] = ws[j * (W + 1) + W];
+        v[j] = incl[j] - v[j] + ws[j * (W + 1) + warp];
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ int slice_len(long long N, int E, int r)
+{
+    const long long rem = N - static_cast<long long>(r) * E;
+    return rem <= 0 ? 0 : (rem < E ? static_cast<int>(rem) : E);
+}
+
+// Number of sorted keys below m (the first position of destination m).
+__device__ __forceinline__ int cluster_lower_bound(cg::cluster_group& cl, CluShared& S, int C, long long N, int E,
+                                                   unsigned int m)
+{
+    int r = 0;
+    while (r < C && (slice_len(N, E, r) == 0 || S.lastk[r] < m)) ++r;
+    if (r == C) return static_cast<int>(N);
+    const unsigned int* kk = cl.map_shared_rank(S.keys, r);
+    int lo = 0, hi = slice_len(N, E, r);
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (kk[mid] < m) lo = mid + 1;
+        else hi = mid;
+    }
+    return r * E + lo;
+}
+
+__global__ void __launch_bounds__(kCluThreads, 1)
+plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E, int np32, int g,
+                    int* __restrict__ row_ptr, int* __restrict__ perm, int4* __restrict__ seg_units,
+                    int4* __restrict__ row_units, int4* __restrict__ finish, int* __restrict__ counters)
+{
+    cg::cluster_group cl = cg::this_cluster();
+    extern __shared__ __align__(16) unsigned char clu_smem[];
+    CluShared& S = *reinterpret_cast<CluShared*>(clu_smem);
+    const int C = static_cast<int>(cl.num_blocks());
+    const int c = static_cast<int>(cl.block_rank());
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cnt = slice_len(N, E, c);
+    const long long c0 = static_cast<long long>(c) * E;
+    unsigned int lt;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+    if (tid == 0) S.tot[3] = 0;
+
+    // 1. the slice, in position order: item k of lane l of warp w is element
+    //    w*32*kCluItems + k*32 + l
+    unsigned int key[kCluItems];
+    int val[kCluItems];
+    int rank[kCluItems];
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < kCluItems; ++k) {
+        const int p = warp * 32 * kCluItems + k * 32 + lane;
+        key[k] = 0u;
+        val[k] = 0;
+        if (p < cnt) {
+            key[k] = static_cast<unsigned int>(__ldg(idx + c0 + p));
+            val[k] = static_cast<int>(c0 + p);
+            bad |= static_cast<long long>(key[k]) >= M;
+        }
+    }
+    const int cta_bad = __syncthreads_or(bad);
+    if (tid == 0) S.bad = cta_bad;
+
+    // 2. stable radix passes over the destination digits
+    for (int pass = 0; pass < np32; ++pass) {
+        const int shift = 8 * pass;
+        if (pass > 0) {
+#pragma unroll
+            for (int k = 0; k < kCluItems; ++k) {
+                const int p = warp * 32 * kCluItems + k * 32 + lane;
+                if (p < cnt) {
+                    key[k] = S.keys[p];
+                    val[k] = S.vals[p];
+                }
+            }
+        }
+        for (int i = tid; i < kCluWarps * kCluRadix; i += kCluThreads) S.whist[i] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kCluItems; ++k) {
+            const bool valid = warp * 32 * kCluItems + k * 32 + lane < cnt;
+            const int d = valid ? static_cast<int>((key[k] >> shift) & 255u) : kCluRadix;
+            const unsigned int peers = __match_any_sync(0xffffffffu, d);
+            const int leader = __ffs(peers) - 1;
+            int old = 0;
+            if (valid && lane == leader) {
+                old = S.whist[warp * kCluRadix + d];
+                S.whist[warp * kCluRadix + d] = old + __popc(peers);
+            }
+            old = __shfl_sync(0xffffffffu, old, leader);
+            rank[k] = old + __popc(peers & lt);
+            __syncwarp();
+        }
+        __syncthreads();
+        if (tid < kCluRadix) {
+            int run = 0;
+            for (int w = 0; w < kCluWarps; ++w) {
+                const int x = S.whist[w * kCluRadix + tid];
+                S.whist[w * kCluRadix + tid] = run;
+                run += x;
+            }
+            S.chist[tid] = run;
+        }
+        cl.sync();  // every CTA's digit counts are visible
+        int excl = 0, tot = 0;
+        if (tid < kCluRadix) {
+            for (int r = 0; r < C; ++r) {
+                const int v = *cl.map_shared_rank(&S.chist[tid], r);
+                excl += r < c ? v : 0;
+                tot += v;
+            }
+        }
+        int sum_unused;
+        const int dstart = block_excl_scan<kCluThreads>(tid < kCluRadix ? tot : 0, S.ws, &sum_unused);
+        if (tid < kCluRadix) S.gbase[tid] = dstart + excl;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kCluItems; ++k) {
+            if (warp * 32 * kCluItems + k * 32 + lane < cnt) {
+                const int d = static_cast<int>((key[k] >> shift) & 255u);
+                const int gpos = S.gbase[d] + S.whist[warp * kCluRadix + d] + rank[k];  // in [0, N)
+                const int owner = gpos / E;
+                const int li = gpos - owner * E;
+                *cl.map_shared_rank(&S.keys[li], owner) = key[k];
+                *cl.map_shared_rank(&S.vals[li], owner) = val[k];
+            }
+        }
+        cl.sync();  // the pass's output is in place
+    }
+
+    // 3. perm, the CTAs' last keys, the cluster's error flag
+    for (int i = tid; i < cnt; i += kCluThreads) perm[c0 + i] = S.vals[i];
+    if (tid < C) {
+        const int n_r = slice_len(N, E, tid);
+        S.lastk[tid] = n_r > 0 ? *cl.map_shared_rank(&S.keys[n_r - 1], tid) : 0u;
+    }
+    if (tid == 0) {
+        int b = 0;
+        for (int r = 0; r < C; ++r) b |= *cl.map_shared_rank(&S.bad, r);
+        S.any_bad = b;
+    }
+    __syncthreads();
+    const bool any_bad = S.any_bad != 0;
+
+    // rows [r_lo, r_hi) belong to this CTA, q consecutive rows per thread
+    const long long R = (M + C - 1) / C;
+    const long long r_lo = min_ll(M, static_cast<long long>(c) * R);
+    const long long r_hi = min_ll(M, r_lo + R);
+    const int q = static_cast<int>((R + kCluThreads - 1) / kCluThreads);  // <= kCluRowsPerThread
+    const long long t_lo = min_ll(r_hi, r_lo + static_cast<long long>(tid) * q);
+    const long long t_hi = min_ll(r_hi, t_lo + q);
+    const int nrows = any_bad ? 0 : static_cast<int>(t_hi - t_lo);
+    int lb[kCluRowsPerThread + 1];
+#pragma unroll
+    for (int j = 0; j <= kCluRowsPerThread; ++j) {
+        lb[j] = 0;
+        if (nrows > 0 && j <= nrows) lb[j] = cluster_lower_bound(cl, S, C, N, E, static_cast<unsigned int>(t_lo + j));
+    }
+
+    // 4. the work list
+    const int G = 1 << g;
+    int v3[3] = {0, 0, 0};
+    int mx = 0;
+#pragma unroll
+    for (int j = 0; j < kCluRowsPerThread; ++j) {
+        if (j < nrows) {
+            const int len = lb[j + 1] - lb[j];
+            const int nch = (len + 31) >> 5;
+            if (nch > G) {
+                v3[0] += (nch + G - 1) >> g;
+                v3[2] += 1;
+            } else {
+                v3[1] += 1;
+            }
+            mx = max(mx, len);
+        }
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0 && mx > 0) atomicMax(&S.tot[3], mx);
+    int t3[3];
+    block_excl_scan3(v3, S.ws, t3);
+    if (tid == 0) {
+        S.tot[0] = t3[0];
+        S.tot[1] = t3[1];
+        S.tot[2] = t3[2];
+    }
+    cl.sync();  // every CTA's totals are visible
+    if (warp == 0) {
+        int a = 0, b = 0, h = 0, m = 0;
+        if (lane < C) {
+            const int* rt = cl.map_shared_rank(S.tot, lane);
+            a = rt[0];
+            b = rt[1];
+            h = rt[2];
+            m = rt[3];
+        }
+        int ia = a, ib = b, ih = h;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ta = __shfl_up_sync(0xffffffffu, ia, o);
+            const int tb = __shfl_up_sync(0xffffffffu, ib, o);
+            const int th = __shfl_up_sync(0xffffffffu, ih, o);
+            if (lane >= o) {
+                ia += ta;
+                ib += tb;
+                ih += th;
+            }
+        }
+        const int gm = __reduce_max_sync(0xffffffffu, m);
+        if (lane == c) {
+            S.base[0] = ia - a;
+            S.base[1] = ib - b;
+            S.base[2] = ih - h;
+        }
+        if (lane == 31) {
+            S.grand[0] = ia;
+            S.grand[1] = ib;
+            S.grand[2] = ih;
+            S.grand[3] = gm;
+        }
+    }
+    __syncthreads();
+    if (!any_bad) {
+        int eA = v3[0] + S.base[0], eB = v3[1] + S.base[1], eC = v3[2] + S.base[2];
+#pragma unroll
+        for (int j = 0; j < kCluRowsPerThread; ++j) {
+            if (j < nrows) {
+                const int m = static_cast<int>(t_lo + j);
+                const int len = lb[j + 1] - lb[j];
+                const int nch = (len + 31) >> 5;
+                row_ptr[m] = lb[j];
+                if (nch > G) {
+                    const int a = (nch + G - 1) >> g;
+                    finish[eC++] = make_int4(m, eA, a, 0);
+                    for (int s = 0; s < a; ++s) seg_units[eA + s] = make_int4(m, s, eA + s, 0);
+                    eA += a;
+                } else {
+                    row_units[eB++] = make_int4(m, -1, 0, 0);
+                }
+            }
+        }
+        if (c == 0 && tid == 0) row_ptr[M] = static_cast<int>(N);
+    }
+    if (c == 0 && tid < kCtrCount) {
+        int v = 0;
+        if (tid == kCtrErrIndex) v = any_bad ? 1 : 0;
+        else if (!any_bad && tid == kCtrSegs) v = S.grand[0];
+        else if (!any_bad && tid == kCtrNormal) v = S.grand[1];
+        else if (!any_bad && tid == kCtrHot) v = S.grand[2];
+        else if (!any_bad && tid == kCtrMaxLen) v = S.grand[3];
+        counters[tid] = v;
+    }
+    cl.sync();  // no CTA leaves while another may still read its shared memory
+}
+
+// ------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------
+
+namespace {
+std::mutex g_clu_mu;
+signed char g_clu_ok[kMaxDevices][kCluMaxCtas + 1];  // 0 unknown, 1 schedulable, -1 not
+bool g_clu_attr[kMaxDevices];
+}  // namespace
+
+int plan_cluster_ctas(int64_t N, int64_t M)
+{
+    if (N <= 0 || N > static_cast<int64_t>(kCluMaxCtas) * kCluMaxSlice) return 0;
+    const int C = static_cast<int>(std::min<int64_t>(kCluMaxCtas, std::max<int64_t>(1, cdiv(N, kCluTargetSlice))));
+    if (cdiv(N, C) > kCluMaxSlice) return 0;
+    if (cdiv(cdiv(M, C), kCluThreads) > kCluRowsPerThread) return 0;
+    return C;
+}
+
+det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, int np32, int* row_ptr, int* perm,
+                               int4* seg_units, int4* row_units, int4* finish, int* counters, cudaStream_t st,
+                               bool* launched)
+{
+    *launched = false;
+    const int C = plan_cluster_ctas(N, M);
+    if (C == 0) return DET_OK;
+    int dev = 0;
+    DETR_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return DET_OK;
+    const size_t smem = sizeof(CluShared);
+    auto kern = plan_cluster_kernel;
+    {
+        std::lock_guard<std::mutex> lock(g_clu_mu);
+        if (!g_clu_attr[dev]) {
+            DETR_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+            DETR_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+            g_clu_attr[dev] = true;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned int>(C), 1, 1);
+    cfg.blockDim = dim3(kCluThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned int>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    signed char ok;
+    {
+        std::lock_guard<std::mutex> lock(g_clu_mu);
+        ok = g_clu_ok[dev][C];
+    }
+    if (ok == 0) {
+        int n = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) (void)cudaGetLastError();
+        ok = (e == cudaSuccess && n >= 1) ? 1 : -1;
+        std::lock_guard<std::mutex> lock(g_clu_mu);
+        g_clu_ok[dev][C] = ok;
+    }
+    if (ok < 0) return DET_OK;
+    const long long E = static_cast<long long>(cdiv(N, C));
+    DETR_CUDA(cudaLaunchKernelEx(&cfg, kern, idx, static_cast<long long>(N), static_cast<long long>(M),
+                                 static_cast<int>(E), np32, g, row_ptr, perm, seg_units, row_units, finish, counters));
+    DETR_LAUNCHED();
+    *launched = true;
+    return DET_OK;
+}
+
+}  // namespace detr

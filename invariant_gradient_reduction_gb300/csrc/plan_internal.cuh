@@ -2,8 +2,11 @@
 // plan.cu (which builds a plan) and gather.cu (which runs it).
 #pragma once
 
+#include <cuda_runtime.h>
 #include <stdint.h>
 #include <vector_types.h>
+
+#include "det_reduce.h"
 
 namespace detr {
 
@@ -18,6 +21,25 @@ enum {
     kCtrErrTimeout = 6,  // a bounded wait inside a reduce kernel expired
     kCtrCount = 16
 };
+
+// Single-cluster plan (plan_cluster.cu): up to kCluMaxCtas CTAs of 1024
+// threads, each holding a slice of at most kCluMaxSlice sources (about
+// kCluTargetSlice when there are enough sources) and at most
+// kCluRowsPerThread destinations per thread.
+constexpr int kCluMaxCtas = 16;
+constexpr int kCluMaxSlice = 8192;
+constexpr int kCluTargetSlice = 4096;
+constexpr int kCluRowsPerThread = 8;
+
+// CTAs the single-cluster plan would use for (N, M); 0 where it does not apply.
+int plan_cluster_ctas(int64_t N, int64_t M);
+
+// Enqueues the single-cluster plan when it applies and the device can
+// schedule the cluster (*launched = true); otherwise does nothing.  Writes
+// row_ptr, perm, the three unit arrays and the whole counter block.
+det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, int np32, int* row_ptr, int* perm,
+                               int4* seg_units, int4* row_units, int4* finish, int* counters, cudaStream_t st,
+                               bool* launched);
 
 }  // namespace detr
 

@@ -48,7 +48,8 @@ class DetError(RuntimeError):
 class det_opts(ctypes.Structure):
     _fields_ = [("grid_ctas", ctypes.c_int32), ("seg_chunks_log2", ctypes.c_int32),
                 ("debug_checks", ctypes.c_int32), ("gather_path", ctypes.c_int32),
-                ("tiles_per_task", ctypes.c_int32), ("async_plan", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
+                ("tiles_per_task", ctypes.c_int32), ("async_plan", ctypes.c_int32),
+                ("plan_path", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 class det_plan_desc(ctypes.Structure):
@@ -117,7 +118,8 @@ def _opts(opts: Optional[dict]):
         return None
     o = det_opts(grid_ctas=int(opts.get("grid_ctas", 0)), seg_chunks_log2=int(opts.get("seg_chunks_log2", -1)),
                  debug_checks=int(opts.get("debug_checks", 0)), gather_path=int(opts.get("gather_path", 0)),
-                 tiles_per_task=int(opts.get("tiles_per_task", 0)), async_plan=int(opts.get("async_plan", 0)))
+                 tiles_per_task=int(opts.get("tiles_per_task", 0)), async_plan=int(opts.get("async_plan", 0)),
+                 plan_path=int(opts.get("plan_path", 0)))
     return ctypes.byref(o)
 
 

@@ -45,16 +45,33 @@ SCATTER_SMALL = ["tiny_moe", "moe_combine", "ep_invariance", "sparse_key_scatter
 # plan: destination lists are integer-exact
 # --------------------------------------------------------------------------
 
+def cluster_plan_applies(N, M, src):
+    """Mirror of the single-cluster plan's size rule (1024 threads, slices of ~4096, <= 16 CTAs)."""
+    if src or N <= 0 or N > 16 * 8192:
+        return False
+    C = min(16, max(1, -(-N // 4096)))
+    return -(-(-(-M // C)) // 1024) <= 8
+
+
+@pytest.mark.parametrize("plan_path", [0, 1, 2])
 @pytest.mark.parametrize("N,M,src", [(0, 7, False), (1, 1, False), (1000, 1, False), (5000, 37, False),
                                      (70000, 300, False), (20000, 70000, False), (9000, 600, True),
-                                     (100000, 65536, False), (40000, 5, True)])
-def test_plan_lists_match_oracle(N, M, src):
+                                     (100000, 65536, False), (40000, 5, True), (31, 3, False),
+                                     (4097, 4096, False), (131072, 16384, False), (131072, 131072, False),
+                                     (65536 + 17, 2, False)])
+def test_plan_lists_match_oracle(N, M, src, plan_path):
     g = torch.Generator().manual_seed(N * 31 + M)
     idx = torch.randint(0, M, (N,), generator=g, dtype=torch.int32)
     sid = None
     if src:
         sid = (torch.randperm(N, generator=g) * 5 - 100).to(torch.int64)
-    plan = dr.det_reduce_plan(idx.to(DEV), M, src_id=None if sid is None else sid.to(DEV))
+    opts = {"plan_path": plan_path}
+    if plan_path == 2 and not cluster_plan_applies(N, M, src):
+        with pytest.raises(dr.DetError) as e:
+            dr.det_reduce_plan(idx.to(DEV), M, src_id=None if sid is None else sid.to(DEV), opts=opts)
+        assert e.value.code == dr.DET_ERR_UNSUPPORTED
+        return
+    plan = dr.det_reduce_plan(idx.to(DEV), M, src_id=None if sid is None else sid.to(DEV), opts=opts)
     rp, perm = dr.plan_lists(plan)
     want_rp, want_perm = oracle.build_lists(idx.numpy(), M, src_id=None if sid is None else sid.numpy())
     assert np.array_equal(rp.cpu().numpy().astype(np.int64), want_rp)
@@ -82,14 +99,25 @@ def test_plan_zipf_hot_rows_and_work_list():
     assert d["n_hot_rows"] > 0
 
 
-def test_plan_errors():
+@pytest.mark.parametrize("plan_path", [0, 1])
+def test_plan_errors(plan_path):
+    o = {"plan_path": plan_path}
     idx = torch.tensor([0, 1, 5, 2], dtype=torch.int32, device=DEV)
     with pytest.raises(dr.DetError) as e:
-        dr.det_reduce_plan(idx, 5)
+        dr.det_reduce_plan(idx, 5, opts=o)
     assert e.value.code == dr.DET_ERR_INDEX_RANGE
     with pytest.raises(dr.DetError) as e:
-        dr.det_reduce_plan(torch.tensor([0, -1], dtype=torch.int32, device=DEV), 5)
+        dr.det_reduce_plan(torch.tensor([0, -1], dtype=torch.int32, device=DEV), 5, opts=o)
     assert e.value.code == dr.DET_ERR_INDEX_RANGE
+    # an out-of-range index in a later CTA of the cluster
+    big = torch.zeros(50000, dtype=torch.int32, device=DEV)
+    big[-1] = 9
+    with pytest.raises(dr.DetError) as e:
+        dr.det_reduce_plan(big, 9, opts=o)
+    assert e.value.code == dr.DET_ERR_INDEX_RANGE
+    with pytest.raises(dr.DetError) as e:
+        dr.det_reduce_plan(idx, 5, opts={"plan_path": 7})
+    assert e.value.code == dr.DET_ERR_ARG
     with pytest.raises(dr.DetError) as e:
         dr.det_reduce_plan(torch.tensor([1, 1, 0], dtype=torch.int32, device=DEV), 3,
                            src_id=torch.tensor([7, 7, 7], dtype=torch.int64, device=DEV))
@@ -111,6 +139,36 @@ def test_scatter_small_matches_oracle(name):
     case = small_case(name)
     out, plan = gpu_scatter(case)
     assert_bytes_equal(np_bits(out), oracle_scatter(case), name)
+
+
+@pytest.mark.parametrize("name", SCATTER_SMALL)
+def test_plan_paths_give_same_bytes(name):
+    """The multi-kernel plan and the single-cluster plan feed the reduce the same lists."""
+    case = small_case(name)
+    want = oracle_scatter(case)
+    for path in (1, 2):
+        if path == 2 and not cluster_plan_applies(case.N, case.M, case.src_id is not None):
+            continue
+        for seg in (3, 5):
+            out, plan = gpu_scatter(case, opts={"plan_path": path, "seg_chunks_log2": seg})
+            assert_bytes_equal(np_bits(out), want, f"{name} plan_path={path} g={seg}")
+
+
+def test_cluster_plan_hot_rows():
+    """Zipf-like destinations with rows far longer than a segment, through the single-cluster plan."""
+    g = torch.Generator().manual_seed(77)
+    N, M, H = 60000, 300, 40
+    r = torch.rand(N, generator=g, dtype=torch.float64)
+    idx = torch.minimum((M * r ** 4).floor(), torch.tensor(M - 1.0)).to(torch.int32)
+    x = torch.randn(N, H, generator=g)
+    w = torch.rand(N, generator=g)
+    case = _case(idx, x, M, w=w)
+    want = oracle_scatter(case)
+    for path in (1, 2):
+        out, plan = gpu_scatter(case, opts={"plan_path": path})
+        d = plan.describe()
+        assert d["n_hot_rows"] > 0 and d["n_segments"] > d["n_hot_rows"]
+        assert_bytes_equal(np_bits(out), want, f"hot rows plan_path={path}")
 
 
 @pytest.mark.parametrize("name", ["moe_combine", "sparse_key_scatter"])
