@@ -14,19 +14,25 @@
 // barriers:
 //   1. each CTA loads its slice of idx and checks the range;
 //   2. per 8-bit digit of the destination, a stable LSD radix pass: the CTA
-//      ranks its slice (match_any in element order, warps in order), publishes
-//      its 256 digit counts, reads those of every CTA of the cluster (the
-//      earlier CTAs give its offsets, all of them the digit starts) and writes
-//      each key to its place in the owning CTA's slice;
-//   3. perm from the sorted slices; row_ptr[m] by a binary search for m in the
-//      sorted keys (the owning slice from the CTAs' last keys, then inside it);
+//      ranks its slice (peers of a digit from ballots, in element order, warps
+//      in order), publishes its 256 digit counts and reads those of every CTA
+//      of the cluster (the earlier CTAs give its offsets, all of them the digit
+//      starts), stages its pairs in (digit, position) order in its own shared
+//      memory and copies them out in runs, so that a warp's stores go to
+//      consecutive words of one owner;
+//   3. row_ptr: the first position of every key present is stored into the
+//      shared memory of the CTA that owns the key's row range; each CTA then
+//      takes suffix minima over its rows (an empty row starts where the next
+//      present one does), bounded by the first position past its range, which
+//      is the sum over the slices of their keys below the range end;
 //   4. the work list: rows classified as whole-row units or hot rows, offsets
-//      by scans inside the CTA and across the cluster; CTA 0 writes the counter
-//      block.
+//      by scans inside the CTA and across the cluster; then perm, row_ptr, the
+//      unit arrays and (CTA 0) the counter block go out to global memory.
 // Cluster barriers are hardware barriers: no thread waits on a flag.
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "block_scan.cuh"
@@ -41,24 +47,28 @@ constexpr int kCluThreads = 1024;
 constexpr int kCluWarps = kCluThreads / 32;
 constexpr int kCluItems = 8;
 constexpr int kCluRadix = 256;
-static_assert(kCluThreads * kCluItems == kCluMaxSlice, "one slice is one item per thread per kCluItems");
+constexpr int kCluMaxRowsPerCta = kCluRowsPerThread * kCluThreads;
+static_assert(kCluThreads * kCluItems == kCluMaxSlice, "a slice is at most kCluItems per thread");
 static_assert(kCluMaxCtas < 32, "the cluster-level scan runs on one warp");
 
 __device__ __forceinline__ long long min_ll(long long a, long long b) { return a < b ? a : b; }
 
 struct CluShared {
-    unsigned int keys[kCluMaxSlice];  // this CTA's slice of the current order
-    int vals[kCluMaxSlice];           // source position of each key
+    uint2 kv[kCluMaxSlice];          // this CTA's slice of the current order: {key, source position}
+    uint2 stage[kCluMaxSlice];       // the same pairs in (digit, position) order, before they go out
+    int rstart[kCluMaxRowsPerCta];   // first sorted position of each destination of this CTA, or INT_MAX
     int whist[kCluWarps * kCluRadix];  // per warp digit counts, then warp offsets
-    int chist[kCluRadix];             // this CTA's digit counts (read by the cluster)
-    int gbase[kCluRadix];             // first position of this CTA's keys of each digit
-    int ws[3 * (kCluWarps + 1)];      // scan scratch
-    unsigned int lastk[kCluMaxCtas];  // last key of every CTA's sorted slice
-    int tot[4];                       // seg units, row units, finish tasks, longest row (read by the cluster)
-    int base[3];                      // this CTA's offsets into the three unit arrays
-    int grand[4];                     // cluster totals
-    int bad;                          // this CTA saw an index outside [0, M) (read by the cluster)
+    int chist[kCluRadix];            // this CTA's digit counts (read by the cluster)
+    int tstart[kCluRadix];           // first staged position of each digit
+    int gbase[kCluRadix];            // first global position of this CTA's keys of each digit
+    int cnt_lt[kCluMaxCtas];         // keys of this slice below the end of CTA r's rows (read by the cluster)
+    int ws[3 * (kCluWarps + 1)];     // scan scratch
+    int tot[4];                      // seg units, row units, finish tasks, longest row (read by the cluster)
+    int base[3];                     // this CTA's offsets into the three unit arrays
+    int grand[4];                    // cluster totals
+    int bad;                         // this CTA saw an index outside [0, M) (read by the cluster)
     int any_bad;
+    int next_start;                  // first sorted position past this CTA's rows
 };
 
 // Exclusive scans of three ints per thread over 1024 threads at once; tot gets
@@ -102,27 +112,68 @@ __device__ __forceinline__ void block_excl_scan3(int v[3], int* ws, int tot[3])
     __syncthreads();
 }
 
+// Minimum of v over the threads with a larger index (INT_MAX for the last
+// thread), over 1024 threads.  Ends synchronised.
+__device__ __forceinline__ int block_suffix_min_excl(int v, int* ws)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;  // min over lanes >= lane
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl = min(incl, t);
+    }
+    if (lane == 0) ws[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int si = ws[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_down_sync(0xffffffffu, si, o);
+            if (lane + o < 32) si = min(si, t);
+        }
+        ws[lane] = si;  // min over warps >= lane
+    }
+    __syncthreads();
+    int next = __shfl_down_sync(0xffffffffu, incl, 1);
+    if (lane == 31) next = INT_MAX;
+    const int after = warp + 1 < kCluWarps ? ws[warp + 1] : INT_MAX;
+    __syncthreads();
+    return min(next, after);
+}
+
+// Lanes of the warp holding the same 8-bit digit as this lane (valid lanes
+// only match valid lanes), from nine ballots: one per digit bit and one for
+// validity.
+__device__ __forceinline__ unsigned int digit_peers(int d, bool valid)
+{
+    unsigned int peers = __ballot_sync(0xffffffffu, valid);
+    if (!valid) peers = ~peers;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const unsigned int set = __ballot_sync(0xffffffffu, (d >> b) & 1);
+        peers &= ((d >> b) & 1) ? set : ~set;
+    }
+    return peers;
+}
+
+// Cluster barrier whose arrival does not wait for this thread's earlier
+// memory operations: for a CTA that only has to stay resident while other
+// CTAs read its shared memory.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ int slice_len(long long N, int E, int r)
 {
     const long long rem = N - static_cast<long long>(r) * E;
     return rem <= 0 ? 0 : (rem < E ? static_cast<int>(rem) : E);
-}
-
-// Number of sorted keys below m (the first position of destination m).
-__device__ __forceinline__ int cluster_lower_bound(cg::cluster_group& cl, CluShared& S, int C, long long N, int E,
-                                                   unsigned int m)
-{
-    int r = 0;
-    while (r < C && (slice_len(N, E, r) == 0 || S.lastk[r] < m)) ++r;
-    if (r == C) return static_cast<int>(N);
-    const unsigned int* kk = cl.map_shared_rank(S.keys, r);
-    int lo = 0, hi = slice_len(N, E, r);
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (kk[mid] < m) lo = mid + 1;
-        else hi = mid;
-    }
-    return r * E + lo;
 }
 
 __global__ void __launch_bounds__(kCluThreads, 1)
@@ -138,22 +189,30 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cnt = slice_len(N, E, c);
     const long long c0 = static_cast<long long>(c) * E;
+    // warp w owns the elements [w*ipw, (w+1)*ipw) of the slice, nk per lane
+    const int ipw = (((cnt + kCluWarps - 1) / kCluWarps) + 31) & ~31;
+    const int nk = ipw >> 5;  // <= kCluItems
+    // rows [r_lo, r_hi) belong to this CTA
+    const long long R = (M + C - 1) / C;
+    const long long r_lo = min_ll(M, static_cast<long long>(c) * R);
+    const long long r_hi = min_ll(M, r_lo + R);
     unsigned int lt;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
     if (tid == 0) S.tot[3] = 0;
+    for (int i = tid; i < r_hi - r_lo; i += kCluThreads) S.rstart[i] = INT_MAX;
 
     // 1. the slice, in position order: item k of lane l of warp w is element
-    //    w*32*kCluItems + k*32 + l
+    //    w*ipw + k*32 + l
     unsigned int key[kCluItems];
     int val[kCluItems];
     int rank[kCluItems];
     bool bad = false;
 #pragma unroll
     for (int k = 0; k < kCluItems; ++k) {
-        const int p = warp * 32 * kCluItems + k * 32 + lane;
+        const int p = warp * ipw + k * 32 + lane;
         key[k] = 0u;
         val[k] = 0;
-        if (p < cnt) {
+        if (k < nk && p < cnt) {
             key[k] = static_cast<unsigned int>(__ldg(idx + c0 + p));
             val[k] = static_cast<int>(c0 + p);
             bad |= static_cast<long long>(key[k]) >= M;
@@ -168,10 +227,11 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
         if (pass > 0) {
 #pragma unroll
             for (int k = 0; k < kCluItems; ++k) {
-                const int p = warp * 32 * kCluItems + k * 32 + lane;
-                if (p < cnt) {
-                    key[k] = S.keys[p];
-                    val[k] = S.vals[p];
+                const int p = warp * ipw + k * 32 + lane;
+                if (k < nk && p < cnt) {
+                    const uint2 e = S.kv[p];
+                    key[k] = e.x;
+                    val[k] = static_cast<int>(e.y);
                 }
             }
         }
@@ -179,9 +239,9 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < kCluItems; ++k) {
-            const bool valid = warp * 32 * kCluItems + k * 32 + lane < cnt;
-            const int d = valid ? static_cast<int>((key[k] >> shift) & 255u) : kCluRadix;
-            const unsigned int peers = __match_any_sync(0xffffffffu, d);
+            const bool valid = k < nk && warp * ipw + k * 32 + lane < cnt;
+            const int d = static_cast<int>((key[k] >> shift) & 255u);
+            const unsigned int peers = digit_peers(d, valid);
             const int leader = __ffs(peers) - 1;
             int old = 0;
             if (valid && lane == leader) {
@@ -193,16 +253,21 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
             __syncwarp();
         }
         __syncthreads();
+        int mine = 0;
         if (tid < kCluRadix) {
-            int run = 0;
             for (int w = 0; w < kCluWarps; ++w) {
                 const int x = S.whist[w * kCluRadix + tid];
-                S.whist[w * kCluRadix + tid] = run;
-                run += x;
+                S.whist[w * kCluRadix + tid] = mine;
+                mine += x;
             }
-            S.chist[tid] = run;
+            S.chist[tid] = mine;
         }
         cl.sync();  // every CTA's digit counts are visible
+        if (pass == 0 && tid == 0) {
+            int b = 0;
+            for (int r = 0; r < C; ++r) b |= *cl.map_shared_rank(&S.bad, r);
+            S.any_bad = b;
+        }
         int excl = 0, tot = 0;
         if (tid < kCluRadix) {
             for (int r = 0; r < C; ++r) {
@@ -211,52 +276,85 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
                 tot += v;
             }
         }
-        int sum_unused;
-        const int dstart = block_excl_scan<kCluThreads>(tid < kCluRadix ? tot : 0, S.ws, &sum_unused);
-        if (tid < kCluRadix) S.gbase[tid] = dstart + excl;
+        int sc[3] = {mine, tot, 0}, sums[3];
+        block_excl_scan3(sc, S.ws, sums);  // sc = {local digit start, global digit start, 0}
+        if (tid < kCluRadix) {
+            S.tstart[tid] = sc[0];
+            S.gbase[tid] = sc[1] + excl;
+        }
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < kCluItems; ++k) {
-            if (warp * 32 * kCluItems + k * 32 + lane < cnt) {
+            if (k < nk && warp * ipw + k * 32 + lane < cnt) {
                 const int d = static_cast<int>((key[k] >> shift) & 255u);
-                const int gpos = S.gbase[d] + S.whist[warp * kCluRadix + d] + rank[k];  // in [0, N)
-                const int owner = gpos / E;
-                const int li = gpos - owner * E;
-                *cl.map_shared_rank(&S.keys[li], owner) = key[k];
-                *cl.map_shared_rank(&S.vals[li], owner) = val[k];
+                const int lpos = S.tstart[d] + S.whist[warp * kCluRadix + d] + rank[k];  // in [0, cnt)
+                S.stage[lpos] = make_uint2(key[k], static_cast<unsigned int>(val[k]));
             }
+        }
+        __syncthreads();
+        for (int i = tid; i < cnt; i += kCluThreads) {
+            const uint2 e = S.stage[i];
+            const int d = static_cast<int>((e.x >> shift) & 255u);
+            const int gpos = S.gbase[d] + (i - S.tstart[d]);  // in [0, N)
+            const int owner = gpos / E;
+            *cl.map_shared_rank(&S.kv[gpos - owner * E], owner) = e;
         }
         cl.sync();  // the pass's output is in place
     }
 
-    // 3. perm, the CTAs' last keys, the cluster's error flag
-    for (int i = tid; i < cnt; i += kCluThreads) perm[c0 + i] = S.vals[i];
-    if (tid < C) {
-        const int n_r = slice_len(N, E, tid);
-        S.lastk[tid] = n_r > 0 ? *cl.map_shared_rank(&S.keys[n_r - 1], tid) : 0u;
+    // 3. the first position of every key present, stored with the key's row
+    //    owner; this slice's keys below the end of every CTA's rows
+    const bool any_bad = S.any_bad != 0;
+    if (!any_bad) {
+        for (int i = tid; i < cnt; i += kCluThreads) {
+            const unsigned int k = S.kv[i].x;
+            bool first;
+            if (i > 0) first = S.kv[i - 1].x != k;
+            else first = c == 0 || cl.map_shared_rank(S.kv, c - 1)[E - 1].x != k;
+            if (first) {
+                const int owner = static_cast<int>(k / static_cast<unsigned long long>(R));
+                *cl.map_shared_rank(&S.rstart[k - static_cast<long long>(owner) * R], owner) =
+                    static_cast<int>(c0 + i);
+            }
+        }
+        if (tid < C) {
+            const unsigned long long X = static_cast<unsigned long long>(min_ll(M, (tid + 1) * R));
+            int lo = 0, hi = cnt;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (S.kv[mid].x < X) lo = mid + 1;
+                else hi = mid;
+            }
+            S.cnt_lt[tid] = lo;
+        }
     }
+    cl.sync();  // row starts and counts are visible
     if (tid == 0) {
-        int b = 0;
-        for (int r = 0; r < C; ++r) b |= *cl.map_shared_rank(&S.bad, r);
-        S.any_bad = b;
+        int sum = 0;
+        if (!any_bad)
+            for (int r = 0; r < C; ++r) sum += *cl.map_shared_rank(&S.cnt_lt[c], r);
+        S.next_start = sum;
     }
     __syncthreads();
-    const bool any_bad = S.any_bad != 0;
 
-    // rows [r_lo, r_hi) belong to this CTA, q consecutive rows per thread
-    const long long R = (M + C - 1) / C;
-    const long long r_lo = min_ll(M, static_cast<long long>(c) * R);
-    const long long r_hi = min_ll(M, r_lo + R);
+    // row_ptr over this CTA's rows: q consecutive rows per thread
     const int q = static_cast<int>((R + kCluThreads - 1) / kCluThreads);  // <= kCluRowsPerThread
     const long long t_lo = min_ll(r_hi, r_lo + static_cast<long long>(tid) * q);
     const long long t_hi = min_ll(r_hi, t_lo + q);
     const int nrows = any_bad ? 0 : static_cast<int>(t_hi - t_lo);
-    int lb[kCluRowsPerThread + 1];
+    int rp[kCluRowsPerThread];
+    int run = INT_MAX;
 #pragma unroll
-    for (int j = 0; j <= kCluRowsPerThread; ++j) {
-        lb[j] = 0;
-        if (nrows > 0 && j <= nrows) lb[j] = cluster_lower_bound(cl, S, C, N, E, static_cast<unsigned int>(t_lo + j));
+    for (int j = kCluRowsPerThread - 1; j >= 0; --j) {
+        rp[j] = INT_MAX;
+        if (j < nrows) {
+            run = min(run, S.rstart[t_lo - r_lo + j]);
+            rp[j] = run;
+        }
     }
+    const int after = min(block_suffix_min_excl(run, S.ws), S.next_start);
+#pragma unroll
+    for (int j = 0; j < kCluRowsPerThread; ++j) rp[j] = min(rp[j], after);
 
     // 4. the work list
     const int G = 1 << g;
@@ -265,7 +363,7 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
 #pragma unroll
     for (int j = 0; j < kCluRowsPerThread; ++j) {
         if (j < nrows) {
-            const int len = lb[j + 1] - lb[j];
+            const int len = (j + 1 < nrows ? rp[j + 1] : after) - rp[j];
             const int nch = (len + 31) >> 5;
             if (nch > G) {
                 v3[0] += (nch + G - 1) >> g;
@@ -285,7 +383,7 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
         S.tot[1] = t3[1];
         S.tot[2] = t3[2];
     }
-    cl.sync();  // every CTA's totals are visible
+    cl.sync();  // every CTA's totals are visible (no global store is pending here)
     if (warp == 0) {
         int a = 0, b = 0, h = 0, m = 0;
         if (lane < C) {
@@ -321,15 +419,19 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
         }
     }
     __syncthreads();
+    // the last reads of other CTAs' shared memory are done: arrive now, write
+    // the results, wait before leaving
+    cluster_arrive_relaxed();
+    for (int i = tid; i < cnt; i += kCluThreads) perm[c0 + i] = static_cast<int>(S.kv[i].y);
     if (!any_bad) {
         int eA = v3[0] + S.base[0], eB = v3[1] + S.base[1], eC = v3[2] + S.base[2];
 #pragma unroll
         for (int j = 0; j < kCluRowsPerThread; ++j) {
             if (j < nrows) {
                 const int m = static_cast<int>(t_lo + j);
-                const int len = lb[j + 1] - lb[j];
+                const int len = (j + 1 < nrows ? rp[j + 1] : after) - rp[j];
                 const int nch = (len + 31) >> 5;
-                row_ptr[m] = lb[j];
+                row_ptr[m] = rp[j];
                 if (nch > G) {
                     const int a = (nch + G - 1) >> g;
                     finish[eC++] = make_int4(m, eA, a, 0);
@@ -351,7 +453,7 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
         else if (!any_bad && tid == kCtrMaxLen) v = S.grand[3];
         counters[tid] = v;
     }
-    cl.sync();  // no CTA leaves while another may still read its shared memory
+    cluster_wait();  // no CTA leaves while another may still read its shared memory
 }
 
 // ------------------------------------------------------------------------
