@@ -50,6 +50,7 @@ constexpr int kCluRadix = 256;
 constexpr int kCluMaxRowsPerCta = kCluRowsPerThread * kCluThreads;
 static_assert(kCluThreads * kCluItems == kCluMaxSlice, "a slice is at most kCluItems per thread");
 static_assert(kCluMaxCtas < 32, "the cluster-level scan runs on one warp");
+static_assert(kCluThreads == 4 * kCluRadix && kCluMaxCtas % 4 == 0, "four readers per digit");
 
 __device__ __forceinline__ long long min_ll(long long a, long long b) { return a < b ? a : b; }
 
@@ -142,13 +143,13 @@ __device__ __forceinline__ int block_suffix_min_excl(int v, int* ws)
     return min(next, after);
 }
 
-// Lanes of the warp holding the same 8-bit digit as this lane (valid lanes
-// only match valid lanes), from nine ballots: one per digit bit and one for
-// validity.
-__device__ __forceinline__ unsigned int digit_peers(int d, bool valid)
+// Lanes among `live` holding the same 8-bit digit as this lane, from one
+// ballot per digit bit.  Warp votes are the ranking's main cost (measured: about
+// a dozen cycles each per SM sub-partition), so there is no separate vote for
+// validity and callers skip items that no lane holds.
+__device__ __forceinline__ unsigned int digit_peers(int d, unsigned int live)
 {
-    unsigned int peers = __ballot_sync(0xffffffffu, valid);
-    if (!valid) peers = ~peers;
+    unsigned int peers = live;
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
         const unsigned int set = __ballot_sync(0xffffffffu, (d >> b) & 1);
@@ -201,55 +202,45 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
     if (tid == 0) S.tot[3] = 0;
     for (int i = tid; i < r_hi - r_lo; i += kCluThreads) S.rstart[i] = INT_MAX;
 
-    // 1. the slice, in position order: item k of lane l of warp w is element
-    //    w*ipw + k*32 + l
-    unsigned int key[kCluItems];
-    int val[kCluItems];
-    int rank[kCluItems];
+    // 1. the slice, in position order, into kv; in the passes item k of lane
+    //    l of warp w is element w*ipw + k*32 + l
     bool bad = false;
-#pragma unroll
-    for (int k = 0; k < kCluItems; ++k) {
-        const int p = warp * ipw + k * 32 + lane;
-        key[k] = 0u;
-        val[k] = 0;
-        if (k < nk && p < cnt) {
-            key[k] = static_cast<unsigned int>(__ldg(idx + c0 + p));
-            val[k] = static_cast<int>(c0 + p);
-            bad |= static_cast<long long>(key[k]) >= M;
-        }
+    for (int i = tid; i < cnt; i += kCluThreads) {
+        const unsigned int k = static_cast<unsigned int>(__ldg(idx + c0 + i));
+        bad |= static_cast<long long>(k) >= M;
+        S.kv[i] = make_uint2(k, static_cast<unsigned int>(c0 + i));
     }
     const int cta_bad = __syncthreads_or(bad);
     if (tid == 0) S.bad = cta_bad;
 
-    // 2. stable radix passes over the destination digits
+    // 2. stable radix passes over the destination digits.  The slice stays
+    //    intact in kv until this CTA arrives at the pass's first cluster
+    //    barrier (other CTAs write into it only after that barrier).
+    unsigned int key[kCluItems];
+    int rank[kCluItems];
     for (int pass = 0; pass < np32; ++pass) {
         const int shift = 8 * pass;
-        if (pass > 0) {
 #pragma unroll
-            for (int k = 0; k < kCluItems; ++k) {
-                const int p = warp * ipw + k * 32 + lane;
-                if (k < nk && p < cnt) {
-                    const uint2 e = S.kv[p];
-                    key[k] = e.x;
-                    val[k] = static_cast<int>(e.y);
-                }
-            }
+        for (int k = 0; k < kCluItems; ++k) {
+            const int p = warp * ipw + k * 32 + lane;
+            key[k] = k < nk && p < cnt ? S.kv[p].x : 0u;
         }
         for (int i = tid; i < kCluWarps * kCluRadix; i += kCluThreads) S.whist[i] = 0;
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < kCluItems; ++k) {
-            const bool valid = k < nk && warp * ipw + k * 32 + lane < cnt;
+            if (k >= nk) break;  // uniform over the block
+            const int nlive = cnt - (warp * ipw + k * 32);  // lanes below this hold elements
+            const unsigned int live = nlive >= 32 ? 0xffffffffu : (nlive <= 0 ? 0u : (1u << nlive) - 1u);
+            const bool valid = (live >> lane) & 1u;
             const int d = static_cast<int>((key[k] >> shift) & 255u);
-            const unsigned int peers = digit_peers(d, valid);
-            const int leader = __ffs(peers) - 1;
-            int old = 0;
-            if (valid && lane == leader) {
-                old = S.whist[warp * kCluRadix + d];
-                S.whist[warp * kCluRadix + d] = old + __popc(peers);
-            }
-            old = __shfl_sync(0xffffffffu, old, leader);
+            const unsigned int peers = digit_peers(d, live);
+            // every lane reads its digit's running count (no branch, no
+            // shuffle); the lowest lane of each digit group writes it back
+            const int old = S.whist[warp * kCluRadix + d];
             rank[k] = old + __popc(peers & lt);
+            __syncwarp();
+            if (valid && (peers & lt) == 0u) S.whist[warp * kCluRadix + d] = old + __popc(peers);
             __syncwarp();
         }
         __syncthreads();
@@ -262,35 +253,55 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
             }
             S.chist[tid] = mine;
         }
-        cl.sync();  // every CTA's digit counts are visible
-        if (pass == 0 && tid == 0) {
-            int b = 0;
-            for (int r = 0; r < C; ++r) b |= *cl.map_shared_rank(&S.bad, r);
-            S.any_bad = b;
-        }
-        int excl = 0, tot = 0;
-        if (tid < kCluRadix) {
-            for (int r = 0; r < C; ++r) {
-                const int v = *cl.map_shared_rank(&S.chist[tid], r);
-                excl += r < c ? v : 0;
-                tot += v;
-            }
-        }
-        int sc[3] = {mine, tot, 0}, sums[3];
-        block_excl_scan3(sc, S.ws, sums);  // sc = {local digit start, global digit start, 0}
-        if (tid < kCluRadix) {
-            S.tstart[tid] = sc[0];
-            S.gbase[tid] = sc[1] + excl;
-        }
+        int sum_unused;
+        const int lstart = block_excl_scan<kCluThreads>(tid < kCluRadix ? mine : 0, S.ws, &sum_unused);
+        if (tid < kCluRadix) S.tstart[tid] = lstart;
         __syncthreads();
+        // stage the slice in (digit, position) order; needs only this CTA's counts
 #pragma unroll
         for (int k = 0; k < kCluItems; ++k) {
-            if (k < nk && warp * ipw + k * 32 + lane < cnt) {
+            const int p = warp * ipw + k * 32 + lane;
+            if (k < nk && p < cnt) {
                 const int d = static_cast<int>((key[k] >> shift) & 255u);
                 const int lpos = S.tstart[d] + S.whist[warp * kCluRadix + d] + rank[k];  // in [0, cnt)
-                S.stage[lpos] = make_uint2(key[k], static_cast<unsigned int>(val[k]));
+                S.stage[lpos] = S.kv[p];
             }
         }
+        cl.sync();  // every CTA's digit counts are visible; the stage is complete
+        if (pass == 0 && warp == kCluWarps - 1) {
+            const int b = lane < C ? *cl.map_shared_rank(&S.bad, lane) : 0;
+            const int any = __any_sync(0xffffffffu, b != 0);
+            if (lane == 0) S.any_bad = any;
+        }
+        // digit d's counts in every CTA: thread (j, d) reads CTAs j, j+4, ...,
+        // the four partial sums meet in the (now free) warp histogram
+        int* part = S.whist;
+        {
+            const int d = tid & (kCluRadix - 1), j = tid >> 8;
+            int pe = 0, pt = 0;
+#pragma unroll
+            for (int r4 = 0; r4 < kCluMaxCtas / 4; ++r4) {
+                const int r = j + 4 * r4;
+                if (r < C) {
+                    const int x = *cl.map_shared_rank(&S.chist[d], r);
+                    pt += x;
+                    pe += r < c ? x : 0;
+                }
+            }
+            part[tid] = pe;
+            part[kCluThreads + tid] = pt;
+        }
+        __syncthreads();
+        int excl = 0, tot = 0;
+        if (tid < kCluRadix) {
+#pragma unroll
+            for (int j = 0; j < kCluThreads / kCluRadix; ++j) {
+                excl += part[j * kCluRadix + tid];
+                tot += part[kCluThreads + j * kCluRadix + tid];
+            }
+        }
+        const int gstart = block_excl_scan<kCluThreads>(tid < kCluRadix ? tot : 0, S.ws, &sum_unused);
+        if (tid < kCluRadix) S.gbase[tid] = gstart + excl;
         __syncthreads();
         for (int i = tid; i < cnt; i += kCluThreads) {
             const uint2 e = S.stage[i];
@@ -312,8 +323,8 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
             if (i > 0) first = S.kv[i - 1].x != k;
             else first = c == 0 || cl.map_shared_rank(S.kv, c - 1)[E - 1].x != k;
             if (first) {
-                const int owner = static_cast<int>(k / static_cast<unsigned long long>(R));
-                *cl.map_shared_rank(&S.rstart[k - static_cast<long long>(owner) * R], owner) =
+                const unsigned int owner = k / static_cast<unsigned int>(R);  // k < M, R < 2^31
+                *cl.map_shared_rank(&S.rstart[k - owner * static_cast<unsigned int>(R)], owner) =
                     static_cast<int>(c0 + i);
             }
         }
@@ -329,11 +340,10 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
         }
     }
     cl.sync();  // row starts and counts are visible
-    if (tid == 0) {
-        int sum = 0;
-        if (!any_bad)
-            for (int r = 0; r < C; ++r) sum += *cl.map_shared_rank(&S.cnt_lt[c], r);
-        S.next_start = sum;
+    if (warp == 0) {
+        int v = !any_bad && lane < C ? *cl.map_shared_rank(&S.cnt_lt[c], lane) : 0;
+        v = __reduce_add_sync(0xffffffffu, v);
+        if (lane == 0) S.next_start = v;
     }
     __syncthreads();
 

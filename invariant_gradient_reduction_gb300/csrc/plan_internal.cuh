@@ -28,7 +28,7 @@ enum {
 // kCluRowsPerThread destinations per thread.
 constexpr int kCluMaxCtas = 16;
 constexpr int kCluMaxSlice = 8192;
-constexpr int kCluTargetSlice = 4096;
+constexpr int kCluTargetSlice = 2048;
 constexpr int kCluRowsPerThread = 8;
 
 // CTAs the single-cluster plan would use for (N, M); 0 where it does not apply.

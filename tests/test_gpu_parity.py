@@ -46,10 +46,10 @@ SCATTER_SMALL = ["tiny_moe", "moe_combine", "ep_invariance", "sparse_key_scatter
 # --------------------------------------------------------------------------
 
 def cluster_plan_applies(N, M, src):
-    """Mirror of the single-cluster plan's size rule (1024 threads, slices of ~4096, <= 16 CTAs)."""
+    """Mirror of the single-cluster plan's size rule (1024 threads, slices of ~2048, <= 16 CTAs)."""
     if src or N <= 0 or N > 16 * 8192:
         return False
-    C = min(16, max(1, -(-N // 4096)))
+    C = min(16, max(1, -(-N // 2048)))
     return -(-(-(-M // C)) // 1024) <= 8
 
 
