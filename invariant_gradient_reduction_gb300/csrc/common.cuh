@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "det_reduce.h"
 
 namespace detr {
@@ -39,6 +41,33 @@ void count_launch();
         if (detr_e_ != cudaSuccess) return detr::cuda_fail(detr_e_); \
         detr::count_launch();                             \
     } while (0)
+
+// Programmatic dependent launch.  A kernel launched by launch_after_previous()
+// may begin while the kernel before it on the stream is still running (its
+// launch and start-up overlap that kernel's tail); it calls pdl_wait() before
+// it reads anything earlier work wrote, and that wait returns once the
+// earlier kernel has finished and its writes are visible.  A kernel that
+// calls pdl_launch_dependents() lets the kernel after it start early.  Both
+// instructions do nothing for kernels launched the ordinary way.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_after_previous(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                         cudaStream_t st, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }

@@ -66,6 +66,8 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
     const long long seg_terms = static_cast<long long>(kChunk) << a.g;
 
     const long long nwarps = static_cast<long long>(gridDim.x) * kGatherWarps;
+    pdl_wait();                 // the plan (or whatever wrote x and w) has finished
+    pdl_launch_dependents();    // the hot-destination pass may be launched now
     long long n_tasks, n_seg;
     if (!task_counts(a, &n_tasks, &n_seg)) return;
     for (long long task = static_cast<long long>(blockIdx.x) * kGatherWarps + warp; task < n_tasks;
@@ -191,6 +193,7 @@ finish_kernel(const int4* finish, long long n_items, int H, const float* part, l
               long long ldo, const int* dev_counters)
 {
     extern __shared__ float fstk[];  // [levels][kFinishThreads]
+    pdl_wait();  // the gather pass has written every partial slot
     if (dev_counters) {
         if (dev_counters[kCtrErrIndex] | dev_counters[kCtrErrDup] | dev_counters[kCtrErrTimeout]) return;
         n_items = static_cast<long long>(dev_counters[kCtrHot]) * H;
@@ -243,7 +246,8 @@ static det_status launch_gather(const GatherArgs& a, const ShardTable& t, int gr
         grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(a.n_tasks, kGatherWarps),
                                                                         int64_t(std::max(per_sm, 1)) * sms)));
     }
-    gather_reduce_kernel<XT, OT, VECTOR><<<grid, kGatherThreads, smem, st>>>(a, t);
+    DETR_CUDA(launch_after_previous(gather_reduce_kernel<XT, OT, VECTOR>, dim3(grid), dim3(kGatherThreads), smem, st,
+                                    a, t));
     DETR_LAUNCHED();
     return DET_OK;
 }
@@ -434,12 +438,14 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
         const size_t fsmem = static_cast<size_t>(log2_floor(std::max<int64_t>(1, max_segs)) + 1) * kFinishThreads *
                              sizeof(float);
         const int* dc = dev_counts ? plan->counters : nullptr;
+        const int4* fin = plan->finish;
+        const float* part = a.part;
         if (out_dtype == DET_BF16)
-            finish_kernel<__nv_bfloat16><<<fgrid, kFinishThreads, fsmem, st>>>(plan->finish, items, a.H, a.part,
-                                                                               a.ldpart, out, ldo, dc);
+            DETR_CUDA(launch_after_previous(finish_kernel<__nv_bfloat16>, dim3(fgrid), dim3(kFinishThreads), fsmem, st,
+                                            fin, items, a.H, part, a.ldpart, out, ldo, dc));
         else
-            finish_kernel<float><<<fgrid, kFinishThreads, fsmem, st>>>(plan->finish, items, a.H, a.part, a.ldpart,
-                                                                       out, ldo, dc);
+            DETR_CUDA(launch_after_previous(finish_kernel<float>, dim3(fgrid), dim3(kFinishThreads), fsmem, st, fin,
+                                            items, a.H, part, a.ldpart, out, ldo, dc));
         DETR_LAUNCHED();
     }
     if (opts && opts->debug_checks) return debug_sync_status(plan, st);

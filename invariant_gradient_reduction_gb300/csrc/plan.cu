@@ -362,6 +362,7 @@ units_kernel(const int* skeys, long long N, long long M, int g, int* row_ptr, in
     __shared__ int ws[kUnitThreads / 32 + 1];
     __shared__ int s_tile;
     __shared__ int s_excl[4];
+    pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
     if (threadIdx.x == 0) s_tile = atomicAdd(uticket, 1);
     __syncthreads();
     const int tile = s_tile;

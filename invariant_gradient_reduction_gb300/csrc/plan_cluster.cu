@@ -199,6 +199,7 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
     const long long r_hi = min_ll(M, r_lo + R);
     unsigned int lt;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+    pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
     if (tid == 0) S.tot[3] = 0;
     for (int i = tid; i < r_hi - r_lo; i += kCluThreads) S.rstart[i] = INT_MAX;
 
