@@ -1,4 +1,4 @@
-// block_scan.cuh -- exclusive scan of one int per thread over a thread block.
+// block_scan.cuh -- block scan and warp ranking primitives of the plan kernels.
 #pragma once
 
 namespace detr {
@@ -33,6 +33,22 @@ __device__ __forceinline__ int block_excl_scan(int v, int* ws, int* total)
     *total = ws[NT / 32];
     __syncthreads();
     return r;
+}
+
+// Lanes among `live` holding the same 8-bit digit as this lane, from one
+// ballot per digit bit.  Warp votes are the ranking's main cost (measured on
+// GB300: a few cycles each per SM sub-partition, while one match.any costs
+// about 250), so there is no separate vote for
+// validity and callers skip items that no lane holds.
+__device__ __forceinline__ unsigned int digit_peers(int d, unsigned int live)
+{
+    unsigned int peers = live;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const unsigned int set = __ballot_sync(0xffffffffu, (d >> b) & 1);
+        peers &= ((d >> b) & 1) ? set : ~set;
+    }
+    return peers;
 }
 
 }  // namespace detr

@@ -39,7 +39,6 @@ constexpr int kSmallThreads = 256, kSmallItems = 4;
 constexpr int64_t kSmallSortMaxN = 1 << 20;
 constexpr int kRadix = 256;
 constexpr int kHistThreads = 256;
-constexpr int kMaxPasses = 12;  // 8 order-key passes + up to 4 destination passes
 constexpr int kUnitThreads = 256;  // one row per thread
 constexpr unsigned long long kLookbackLimit = 1ull << 22;
 constexpr unsigned long long kFlagAggregate = 1ull << 32;
@@ -67,10 +66,10 @@ __device__ __forceinline__ void st_release(unsigned long long* p, unsigned long 
 // words (flag << 32 | count), zero before the kernel.  Publishes this tile's
 // aggregate, adds the earlier tiles' values (stopping at the first inclusive
 // prefix), publishes this tile's inclusive prefix and returns the exclusive
-// one.  Predecessors are read eight at a time (nearest first), so the walk
+// one.  Predecessors are read kLookbackBatch at a time (nearest first), so the walk
 // back over tiles that are still running costs few round trips.  Waits only
 // on tiles with smaller tickets; bounded.
-constexpr int kLookbackBatch = 8;
+constexpr int kLookbackBatch = 16;
 
 __device__ __forceinline__ void publish_aggregate(unsigned long long* status, int tile, int stride, int k,
                                                   unsigned int aggregate)
@@ -164,53 +163,84 @@ __device__ __forceinline__ int digit_of(K key, int shift)
 }
 
 // ------------------------------------------------------------------------
-// 1. histograms
+// 1-2. stable radix passes: count, offsets, scatter
 // ------------------------------------------------------------------------
 
-// ghist is [passes][256] in execution order: the 8 order-key byte passes
-// first when src_id is given, then the np32 destination digit passes.
-__global__ void __launch_bounds__(kHistThreads)
-plan_hist_kernel(const int* idx, const long long* src_id, long long N, unsigned int M, int np32, int* ghist,
-                 int* counters)
+// One pass sorts by one 8-bit digit in three kernels; no CTA ever waits for
+// another:
+//   tile_count_kernel     the digit counts of every tile of the pass's input
+//                         order, digit-major (counts[d * ntiles + t]); the
+//                         first destination pass also checks idx against M;
+//   tile_offset_kernel    one CTA per digit: exclusive scan of the digit's
+//                         counts over the tiles (in place) and its total;
+//   radix_scatter_kernel  each tile ranks its keys (peers of a digit from
+//                         ballots, in element order, warps in order), stages
+//                         them in shared memory in (digit, position) order and
+//                         writes them to their places: the digit's start, plus
+//                         the digit's keys in earlier tiles, plus the rank.
+template <typename K, int MODE, int NT, int ITEMS>
+__global__ void __launch_bounds__(NT)
+tile_count_kernel(const void* kin, const int* vin, const int* gather, long long N, int shift, long long M_check,
+                  int* counts, int ntiles, int* counters)
 {
-    __shared__ int hist[kMaxPasses * kRadix];
-    const int npass = np32 + (src_id ? 8 : 0);
-    const int dbase = src_id ? 8 : 0;
-    for (int i = threadIdx.x; i < npass * kRadix; i += kHistThreads) hist[i] = 0;
+    __shared__ int h[kRadix];
+    for (int i = threadIdx.x; i < kRadix; i += NT) h[i] = 0;
     __syncthreads();
+    const long long base = static_cast<long long>(blockIdx.x) * NT * ITEMS;
     bool bad = false;
-    const long long stride = static_cast<long long>(gridDim.x) * kHistThreads;
-    for (long long p = static_cast<long long>(blockIdx.x) * kHistThreads + threadIdx.x; p < N; p += stride) {
-        const unsigned int key = static_cast<unsigned int>(idx[p]);
-        if (key >= M) {
-            bad = true;
-        } else {
-            for (int j = 0; j < np32; ++j) atomicAdd(&hist[(dbase + j) * kRadix + ((key >> (8 * j)) & 255u)], 1);
-        }
-        if (src_id) {
-            const unsigned long long k64 = static_cast<unsigned long long>(src_id[p]) ^ 0x8000000000000000ull;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) atomicAdd(&hist[j * kRadix + static_cast<int>((k64 >> (8 * j)) & 255u)], 1);
+#pragma unroll 4
+    for (int k = 0; k < ITEMS; ++k) {
+        const long long p = base + static_cast<long long>(k) * NT + threadIdx.x;
+        if (p < N) {
+            K key;
+            int val;
+            load_kv<K, MODE>(kin, vin, gather, p, key, val);
+            if (M_check > 0 && static_cast<long long>(key) >= M_check) bad = true;
+            atomicAdd(&h[digit_of<K>(key, shift)], 1);
         }
     }
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(&counters[kCtrErrIndex], 1);
-    for (int i = threadIdx.x; i < npass * kRadix; i += kHistThreads)
-        if (hist[i]) atomicAdd(&ghist[i], hist[i]);
+    if (M_check > 0 && __syncthreads_or(bad) && threadIdx.x == 0) atomicOr(&counters[kCtrErrIndex], 1);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kRadix; i += NT) counts[static_cast<long long>(i) * ntiles + blockIdx.x] = h[i];
 }
 
-// ------------------------------------------------------------------------
-// 2. one stable radix pass
-// ------------------------------------------------------------------------
+constexpr int kOffThreads = 256;
+constexpr int kOffItems = 4;
+
+__global__ void __launch_bounds__(kOffThreads)
+tile_offset_kernel(int* counts, int ntiles, int* totals)
+{
+    __shared__ int ws[kOffThreads / 32 + 1];
+    int* row = counts + static_cast<long long>(blockIdx.x) * ntiles;
+    int carry = 0;
+    for (int t0 = 0; t0 < ntiles; t0 += kOffThreads * kOffItems) {
+        int v[kOffItems];
+        int sum = 0;
+#pragma unroll
+        for (int j = 0; j < kOffItems; ++j) {
+            const int t = t0 + threadIdx.x * kOffItems + j;
+            v[j] = t < ntiles ? row[t] : 0;
+            sum += v[j];
+        }
+        int tot;
+        int run = carry + block_excl_scan<kOffThreads>(sum, ws, &tot);
+#pragma unroll
+        for (int j = 0; j < kOffItems; ++j) {
+            const int t = t0 + threadIdx.x * kOffItems + j;
+            if (t < ntiles) row[t] = run;
+            run += v[j];
+        }
+        carry += tot;
+    }
+    if (threadIdx.x == 0) totals[blockIdx.x] = carry;
+}
 
 // Warp w owns elements [w*32*ITEMS, (w+1)*32*ITEMS) of the tile, item k of
-// lane l being element w*32*ITEMS + k*32 + l.  Ranks inside a warp come from
-// match_any in element order, warps are offset per digit in warp order, tiles
-// per digit by look-back; the tile is staged in shared memory in sorted order
-// and written out coalesced.
+// lane l being element w*32*ITEMS + k*32 + l.
 template <typename K, int MODE, int NT, int ITEMS, bool WRITE_KEYS>
-__global__ void __launch_bounds__(NT)
-radix_pass_kernel(const void* kin, const int* vin, const int* gather, K* kout, int* vout, const int* ghist_p,
-                  unsigned long long* status_p, int* ticket_p, long long N, int shift, int* counters)
+__global__ void __launch_bounds__(NT, sizeof(K) == 4 ? 3 : 2)  // three 32-bit-key tiles per SM
+radix_scatter_kernel(const void* kin, const int* vin, const int* gather, K* kout, int* vout, const int* offsets,
+                     const int* totals, int ntiles, long long N, int shift)
 {
     constexpr int W = NT / 32;
     constexpr int TILE = NT * ITEMS;
@@ -221,85 +251,70 @@ radix_pass_kernel(const void* kin, const int* vin, const int* gather, K* kout, i
     int* tstart = whist + W * kRadix;
     int* gbase = tstart + kRadix;
     int* ws = gbase + kRadix;                 // scan scratch (NT/32 + 1)
-    int* s_tile = ws + NT / 32 + 1;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) *s_tile = atomicAdd(ticket_p, 1);
-    for (int i = threadIdx.x; i < W * kRadix; i += NT) whist[i] = 0;
-    for (int i = threadIdx.x; i < kRadix; i += NT) tstart[i] = 0;  // tile histogram first
-    __syncthreads();
-    const int tile = *s_tile;
+    const int tile = blockIdx.x;
     const long long base = static_cast<long long>(tile) * TILE;
+    for (int i = threadIdx.x; i < W * kRadix; i += NT) whist[i] = 0;
+    const int tot_d = threadIdx.x < kRadix ? totals[threadIdx.x] : 0;
+    const int off_d = threadIdx.x < kRadix ? offsets[static_cast<long long>(threadIdx.x) * ntiles + tile] : 0;
     unsigned int lt;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
 
     K key[ITEMS];
     int val[ITEMS];
     int rank[ITEMS];
-    int dig[ITEMS];
+    const long long wbase = base + static_cast<long long>(warp) * 32 * ITEMS;  // item k of lane l: wbase + k*32 + l
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {  // all loads first
-        const long long p = base + static_cast<long long>(warp) * 32 * ITEMS + k * 32 + lane;
-        dig[k] = -1;
-        if (p < N) {
-            load_kv<K, MODE>(kin, vin, gather, p, key[k], val[k]);
-            dig[k] = 0;
-        }
+        const long long p = wbase + k * 32 + lane;
+        key[k] = 0;
+        val[k] = 0;
+        if (p < N) load_kv<K, MODE>(kin, vin, gather, p, key[k], val[k]);
     }
-    // this tile's digit counts, published before the ranking so that later
-    // tiles rarely wait for them
-#pragma unroll
-    for (int k = 0; k < ITEMS; ++k)
-        if (dig[k] >= 0) atomicAdd(&tstart[digit_of<K>(key[k], shift)], 1);
-    __syncthreads();
-    if (threadIdx.x < kRadix)
-        publish_aggregate(status_p, tile, kRadix, threadIdx.x, static_cast<unsigned int>(tstart[threadIdx.x]));
+    int total_unused;
+    const int dstart = block_excl_scan<NT>(tot_d, ws, &total_unused);  // also orders the whist zeroing
+    if (threadIdx.x < kRadix) gbase[threadIdx.x] = dstart + off_d;
+
+    // rank inside the warp: every lane reads its digit's running count, the
+    // lowest lane of each digit group writes it back
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
-        const bool valid = dig[k] >= 0;
-        const int d = valid ? digit_of<K>(key[k], shift) : kRadix;  // invalid lanes only match each other
-        const unsigned int peers = __match_any_sync(0xffffffffu, d);
-        const int leader = __ffs(peers) - 1;
-        int old = 0;
-        if (valid && lane == leader) {
-            old = whist[warp * kRadix + d];
-            whist[warp * kRadix + d] = old + __popc(peers);
-        }
-        old = __shfl_sync(0xffffffffu, old, leader);
+        const long long nl = N - (wbase + k * 32);
+        const unsigned int live = nl >= 32 ? 0xffffffffu : (nl <= 0 ? 0u : (1u << nl) - 1u);
+        if (live == 0u) continue;  // uniform over the warp
+        const bool valid = (live >> lane) & 1u;
+        const int d = digit_of<K>(key[k], shift);
+        const unsigned int peers = digit_peers(d, live);
+        const int old = whist[warp * kRadix + d];
         rank[k] = old + __popc(peers & lt);
-        dig[k] = valid ? d : -1;
+        __syncwarp();
+        if (valid && (peers & lt) == 0u) whist[warp * kRadix + d] = old + __popc(peers);
         __syncwarp();
     }
     __syncthreads();
 
-    // per digit: offsets of the warps (warp order), tile totals
+    // per digit: offsets of the warps (warp order), tile counts, staged starts
     int tot = 0;
     if (threadIdx.x < kRadix) {
         const int d = threadIdx.x;
-        int run = 0;
         for (int w = 0; w < W; ++w) {
             const int c = whist[w * kRadix + d];
-            whist[w * kRadix + d] = run;
-            run += c;
+            whist[w * kRadix + d] = tot;
+            tot += c;
         }
-        tot = run;
     }
-    int total_unused;
     const int excl = block_excl_scan<NT>(tot, ws, &total_unused);
-    const int gh = threadIdx.x < kRadix ? ghist_p[threadIdx.x] : 0;
-    const int dstart = block_excl_scan<NT>(gh, ws, &total_unused);
     if (threadIdx.x < kRadix) {
-        const int d = threadIdx.x;
-        const unsigned int before = lookback_walk(status_p, tile, kRadix, d, static_cast<unsigned int>(tot), counters);
-        tstart[d] = excl;
-        gbase[d] = dstart + static_cast<int>(before) - excl;
+        tstart[threadIdx.x] = excl;
+        gbase[threadIdx.x] -= excl;  // staged position i of digit d goes to gbase[d] + i
     }
     __syncthreads();
-
 #pragma unroll
     for (int k = 0; k < ITEMS; ++k) {
-        if (dig[k] >= 0) {
-            const int pos = tstart[dig[k]] + whist[warp * kRadix + dig[k]] + rank[k];
+        if (wbase + k * 32 + lane < N) {
+            const int dk = digit_of<K>(key[k], shift);
+            const int pos = tstart[dk] + whist[warp * kRadix + dk] + rank[k];
             skeys[pos] = key[k];
             svals[pos] = val[k];
         }
@@ -310,11 +325,9 @@ radix_pass_kernel(const void* kin, const int* vin, const int* gather, K* kout, i
     const int nvalid = rem < TILE ? static_cast<int>(rem) : TILE;
     for (int i = threadIdx.x; i < nvalid; i += NT) {
         const K kk = skeys[i];
-        const long long g = static_cast<long long>(gbase[digit_of<K>(kk, shift)]) + i;
-        if (g >= 0 && g < N) {  // only false after an expired look-back
-            if (WRITE_KEYS) kout[g] = kk;
-            vout[g] = svals[i];
-        }
+        const long long g = static_cast<long long>(gbase[digit_of<K>(kk, shift)]) + i;  // in [0, N)
+        if (WRITE_KEYS) kout[g] = kk;
+        vout[g] = svals[i];
     }
 }
 
@@ -322,7 +335,7 @@ template <typename K, int NT, int ITEMS>
 static size_t pass_smem_bytes()
 {
     return static_cast<size_t>(NT * ITEMS) * (sizeof(K) + sizeof(int)) +
-           static_cast<size_t>((NT / 32) * kRadix + 2 * kRadix + NT / 32 + 2) * sizeof(int);
+           static_cast<size_t>((NT / 32) * kRadix + 2 * kRadix + NT / 32 + 1) * sizeof(int);
 }
 
 // Sources of one destination must carry distinct order keys.
@@ -422,10 +435,10 @@ units_kernel(const int* skeys, long long N, long long M, int g, int* row_ptr, in
 // ------------------------------------------------------------------------
 
 struct PlanLayout {
-    // zeroed at the start of every plan: counters, tickets, histograms,
-    // per-destination counts, row_ptr and the look-back status words
-    size_t counters, tickets, ghist, row_ptr, status, ustatus, zero_end;
-    size_t perm, skeys, k32_tmp, v_tmp, k64_a, k64_b, va, vb, seg_units, row_units, finish, total;
+    // zeroed at the start of every multi-kernel plan: counters, the work
+    // list's ticket, row_ptr and its look-back status words
+    size_t counters, uticket, row_ptr, ustatus, zero_end;
+    size_t counts, totals, perm, skeys, k32_tmp, v_tmp, k64_a, k64_b, va, vb, seg_units, row_units, finish, total;
     int ntiles, nut, npass;
     int64_t max_segs, max_rows, max_finish;
 };
@@ -461,12 +474,12 @@ static PlanLayout plan_layout(int64_t N, int64_t M, bool with_src, int g)
     L.max_segs = 2 * cdiv(N, seg_terms) + 1;
     L.max_rows = M + 1;
     L.counters = take(kCtrCount * sizeof(int));
-    L.tickets = take(static_cast<size_t>(kMaxPasses + 1) * sizeof(int));
-    L.ghist = take(static_cast<size_t>(L.npass) * kRadix * sizeof(int));
+    L.uticket = take(sizeof(int));
     L.row_ptr = take(static_cast<size_t>(M + 1) * sizeof(int));
-    L.status = take(static_cast<size_t>(L.npass) * L.ntiles * kRadix * sizeof(unsigned long long));
     L.ustatus = take(static_cast<size_t>(L.nut) * 4 * sizeof(unsigned long long));
     L.zero_end = off;
+    L.counts = take(static_cast<size_t>(kRadix) * L.ntiles * sizeof(int));
+    L.totals = take(static_cast<size_t>(kRadix) * sizeof(int));
     L.perm = take(static_cast<size_t>(N) * sizeof(int));
     L.skeys = take(static_cast<size_t>(N) * sizeof(int));
     L.k32_tmp = take(static_cast<size_t>(N) * sizeof(int));
@@ -511,29 +524,34 @@ static det_status resolve_seg_log2(const det_opts* o, int* g)
 }
 
 template <typename K, int MODE, int NT, int ITEMS, bool WRITE_KEYS>
-static det_status radix_pass_t(const void* kin, const int* vin, const int* gather, K* kout, int* vout,
-                               const int* ghist_p, unsigned long long* status_p, int* ticket_p, int64_t N, int ntiles,
-                               int shift, int* counters, cudaStream_t st)
+static det_status radix_pass_t(const void* kin, const int* vin, const int* gather, K* kout, int* vout, int* counts,
+                               int* totals, int64_t N, int ntiles, int shift, int64_t M_check, int* counters,
+                               cudaStream_t st)
 {
+    tile_count_kernel<K, MODE, NT, ITEMS><<<ntiles, NT, 0, st>>>(kin, vin, gather, N, shift, M_check, counts, ntiles,
+                                                                 counters);
+    DETR_LAUNCHED();
+    tile_offset_kernel<<<kRadix, kOffThreads, 0, st>>>(counts, ntiles, totals);
+    DETR_LAUNCHED();
     const size_t smem = pass_smem_bytes<K, NT, ITEMS>();
-    auto kern = radix_pass_kernel<K, MODE, NT, ITEMS, WRITE_KEYS>;
+    auto kern = radix_scatter_kernel<K, MODE, NT, ITEMS, WRITE_KEYS>;
     { const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(kern), smem); if (a_) return a_; }
-    kern<<<ntiles, NT, smem, st>>>(kin, vin, gather, kout, vout, ghist_p, status_p, ticket_p, N, shift, counters);
+    kern<<<ntiles, NT, smem, st>>>(kin, vin, gather, kout, vout, counts, totals, ntiles, N, shift);
     DETR_LAUNCHED();
     return DET_OK;
 }
 
 template <typename K, int MODE, bool WRITE_KEYS>
 static det_status radix_pass(bool small, const void* kin, const int* vin, const int* gather, K* kout, int* vout,
-                             const int* ghist_p, unsigned long long* status_p, int* ticket_p, int64_t N, int ntiles,
-                             int shift, int* counters, cudaStream_t st)
+                             int* counts, int* totals, int64_t N, int ntiles, int shift, int64_t M_check,
+                             int* counters, cudaStream_t st)
 {
     if (small)
-        return radix_pass_t<K, MODE, kSmallThreads, kSmallItems, WRITE_KEYS>(kin, vin, gather, kout, vout, ghist_p,
-                                                                             status_p, ticket_p, N, ntiles, shift,
+        return radix_pass_t<K, MODE, kSmallThreads, kSmallItems, WRITE_KEYS>(kin, vin, gather, kout, vout, counts,
+                                                                             totals, N, ntiles, shift, M_check,
                                                                              counters, st);
-    return radix_pass_t<K, MODE, kBigThreads, kBigItems, WRITE_KEYS>(kin, vin, gather, kout, vout, ghist_p, status_p,
-                                                                     ticket_p, N, ntiles, shift, counters, st);
+    return radix_pass_t<K, MODE, kBigThreads, kBigItems, WRITE_KEYS>(kin, vin, gather, kout, vout, counts, totals, N,
+                                                                     ntiles, shift, M_check, counters, st);
 }
 
 }  // namespace detr
@@ -578,10 +596,10 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     cudaStream_t st = as_stream(stream);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     int* counters = reinterpret_cast<int*>(ws + L.counters);
-    int* tickets = reinterpret_cast<int*>(ws + L.tickets);
-    int* ghist = reinterpret_cast<int*>(ws + L.ghist);
+    int* uticket = reinterpret_cast<int*>(ws + L.uticket);
     int* row_ptr = reinterpret_cast<int*>(ws + L.row_ptr);
-    unsigned long long* status = reinterpret_cast<unsigned long long*>(ws + L.status);
+    int* counts = reinterpret_cast<int*>(ws + L.counts);
+    int* totals = reinterpret_cast<int*>(ws + L.totals);
     unsigned long long* ustatus = reinterpret_cast<unsigned long long*>(ws + L.ustatus);
     int* perm = reinterpret_cast<int*>(ws + L.perm);
     int* skeys = reinterpret_cast<int*>(ws + L.skeys);
@@ -602,69 +620,47 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     if (plan_path == 2 && !one_cluster) return DET_ERR_UNSUPPORTED;
     if (!one_cluster) {
     DETR_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, st));
-    int sms = 0;
-    s = current_sm_count(&sms);
-    if (s) return s;
 
     if (N > 0) {
-        const int hgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(N, kHistThreads * 2),
-                                                                                  int64_t(sms) * 8)));
-        plan_hist_kernel<<<hgrid, kHistThreads, 0, st>>>(idx, with_src ? reinterpret_cast<const long long*>(src_id)
-                                                                       : nullptr,
-                                                         N, static_cast<unsigned int>(M), np32, ghist, counters);
-        DETR_LAUNCHED();
         const int ntiles = L.ntiles;
         const bool small = N <= kSmallSortMaxN;
-        const size_t sstride = static_cast<size_t>(ntiles) * kRadix;
-        int pass = 0;
+        const int64_t noM = 0;  // no range check in this pass
         const int* vals_in = nullptr;
         if (with_src) {
             unsigned long long* k64[2] = {reinterpret_cast<unsigned long long*>(ws + L.k64_a),
                                           reinterpret_cast<unsigned long long*>(ws + L.k64_b)};
             int* v64[2] = {reinterpret_cast<int*>(ws + L.va), reinterpret_cast<int*>(ws + L.vb)};
-            for (int j = 0; j < 8; ++j, ++pass) {
+            for (int j = 0; j < 8; ++j) {
                 const int o = j & 1;
                 if (j == 0)
                     s = radix_pass<unsigned long long, KM_DIRECT, true>(small, src_id, nullptr, nullptr, k64[o], v64[o],
-                                                                        ghist + pass * kRadix, status + pass * sstride,
-                                                                        tickets + pass, N, ntiles, 0, counters, st);
+                                                                        counts, totals, N, ntiles, 0, noM, counters,
+                                                                        st);
                 else
                     s = radix_pass<unsigned long long, KM_CARRY, true>(small, k64[o ^ 1], v64[o ^ 1], nullptr, k64[o],
-                                                                       v64[o], ghist + pass * kRadix,
-                                                                       status + pass * sstride, tickets + pass, N,
-                                                                       ntiles, 8 * j, counters, st);
+                                                                       v64[o], counts, totals, N, ntiles, 8 * j, noM,
+                                                                       counters, st);
                 if (s) return s;
             }
             vals_in = v64[1];
         }
-        for (int j = 0; j < np32; ++j, ++pass) {
-            const bool last = j == np32 - 1;
+        // destination passes; the first checks idx against M, the last writes
+        // the sorted destinations, where the work list finds row_ptr
+        for (int j = 0; j < np32; ++j) {
             const bool to_final = ((np32 - 1 - j) % 2) == 0;
             unsigned int* ko = reinterpret_cast<unsigned int*>(to_final ? skeys : k32_tmp);
             int* vo = to_final ? perm : v_tmp;
             const unsigned int* ki = reinterpret_cast<const unsigned int*>(to_final ? k32_tmp : skeys);
             const int* vi = to_final ? v_tmp : perm;
-            const int* gh = ghist + pass * kRadix;
-            unsigned long long* stp = status + pass * sstride;
-            // the last pass writes the sorted destinations too: the work list
-            // finds row_ptr in them
-            const bool wk = true;
-            (void)last;
             if (j == 0 && with_src)
-                s = wk ? radix_pass<unsigned int, KM_GATHER, true>(small, nullptr, vals_in, idx, ko, vo, gh, stp,
-                                                                   tickets + pass, N, ntiles, 0, counters, st)
-                       : radix_pass<unsigned int, KM_GATHER, false>(small, nullptr, vals_in, idx, ko, vo, gh, stp,
-                                                                    tickets + pass, N, ntiles, 0, counters, st);
+                s = radix_pass<unsigned int, KM_GATHER, true>(small, nullptr, vals_in, idx, ko, vo, counts, totals, N,
+                                                              ntiles, 0, M, counters, st);
             else if (j == 0)
-                s = wk ? radix_pass<unsigned int, KM_DIRECT, true>(small, idx, nullptr, nullptr, ko, vo, gh, stp,
-                                                                   tickets + pass, N, ntiles, 0, counters, st)
-                       : radix_pass<unsigned int, KM_DIRECT, false>(small, idx, nullptr, nullptr, ko, vo, gh, stp,
-                                                                    tickets + pass, N, ntiles, 0, counters, st);
+                s = radix_pass<unsigned int, KM_DIRECT, true>(small, idx, nullptr, nullptr, ko, vo, counts, totals, N,
+                                                              ntiles, 0, M, counters, st);
             else
-                s = wk ? radix_pass<unsigned int, KM_CARRY, true>(small, ki, vi, nullptr, ko, vo, gh, stp,
-                                                                  tickets + pass, N, ntiles, 8 * j, counters, st)
-                       : radix_pass<unsigned int, KM_CARRY, false>(small, ki, vi, nullptr, ko, vo, gh, stp,
-                                                                   tickets + pass, N, ntiles, 8 * j, counters, st);
+                s = radix_pass<unsigned int, KM_CARRY, true>(small, ki, vi, nullptr, ko, vo, counts, totals, N, ntiles,
+                                                             8 * j, noM, counters, st);
             if (s) return s;
         }
         if (with_src && N > 1) {
@@ -675,7 +671,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     }
     if (M > 0) {
         units_kernel<<<L.nut, kUnitThreads, 0, st>>>(skeys, N, M, g, row_ptr, seg_units, row_units, finish, ustatus,
-                                                     tickets + kMaxPasses, L.nut, counters);
+                                                     uticket, L.nut, counters);
         DETR_LAUNCHED();
     }
     }  // multi-kernel plan

@@ -143,21 +143,6 @@ __device__ __forceinline__ int block_suffix_min_excl(int v, int* ws)
     return min(next, after);
 }
 
-// Lanes among `live` holding the same 8-bit digit as this lane, from one
-// ballot per digit bit.  Warp votes are the ranking's main cost (measured: about
-// a dozen cycles each per SM sub-partition), so there is no separate vote for
-// validity and callers skip items that no lane holds.
-__device__ __forceinline__ unsigned int digit_peers(int d, unsigned int live)
-{
-    unsigned int peers = live;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-        const unsigned int set = __ballot_sync(0xffffffffu, (d >> b) & 1);
-        peers &= ((d >> b) & 1) ? set : ~set;
-    }
-    return peers;
-}
-
 // Cluster barrier whose arrival does not wait for this thread's earlier
 // memory operations: for a CTA that only has to stay resident while other
 // CTAs read its shared memory.
