@@ -453,13 +453,374 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
 }
 
 // ------------------------------------------------------------------------
+// single-pass variant: at most 4096 destinations
+// ------------------------------------------------------------------------
+// With M <= 4096 the destination itself is the digit, so one counting pass
+// sorts, and the destination counts it yields give row_ptr directly:
+//   1. each CTA loads its slice; 16 warps rank it (peers of the whole
+//      destination from one ballot per bit, in element order, warps in order)
+//      against 16-bit per-warp counts of every destination;
+//   2. each CTA owns R consecutive destinations: it reads their counts in
+//      every CTA, writes each CTA's exclusive prefix back into that CTA's
+//      shared memory, and takes the totals as row lengths, with their
+//      work-list classification;
+//   3. a scan over the CTAs' totals gives each range its first position, so
+//      row_ptr of every owned destination;
+//   4. source i goes to perm[row_ptr[key] + earlier CTAs + earlier warps +
+//      rank].
+constexpr int kOneMaxBins = 4096;
+constexpr int kOneMaxSlice = 4096;
+constexpr int kOneRankWarps = 16;
+constexpr int kOneRowsPerThread = kOneMaxBins / kCluThreads;
+static_assert(kOneMaxSlice / kOneRankWarps / 32 <= 8, "ranking items per lane");
+
+struct OneShared {
+    uint2 kv[kOneMaxSlice];                               // {key, source position}
+    unsigned short rank[kOneMaxSlice];                    // rank among equal keys inside the ranking warp
+    unsigned short whist[kOneRankWarps * kOneMaxBins];    // per ranking warp counts, then warp offsets
+    int chist[kOneMaxBins];    // this CTA's count of each destination (read by the owners)
+    int pref[kOneMaxBins];     // earlier CTAs' count of each destination (written by the owners)
+    int rp[kOneMaxBins];       // row_ptr of the destinations this CTA owns (read by every CTA)
+    int ws[4 * (kCluWarps + 1)];
+    int tot[5];                // rows, seg units, row units, finish tasks, longest row (read by every CTA)
+    int base[4];
+    int grand[5];
+    int bad;                   // this CTA saw an index outside [0, M) (read by every CTA)
+    int any_bad;
+};
+
+// Exclusive scans of NV ints per thread over 1024 threads at once; tot gets
+// the block sums.  Ends synchronised.
+template <int NV>
+__device__ __forceinline__ void block_excl_scan_n(int v[NV], int* ws, int tot[NV])
+{
+    constexpr int W = kCluWarps;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        incl[j] = v[j];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl[j], o);
+            if (lane >= o) incl[j] += t;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) ws[j * (W + 1) + warp] = incl[j];
+    }
+    __syncthreads();
+    if (warp < NV) {
+        const int s = ws[warp * (W + 1) + lane];
+        int si = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) si += t;
+        }
+        ws[warp * (W + 1) + lane] = si - s;
+        if (lane == 31) ws[warp * (W + 1) + W] = si;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        tot[j] = ws[j * (W + 1) + W];
+        v[j] = incl[j] - v[j] + ws[j * (W + 1) + warp];
+    }
+    __syncthreads();
+}
+
+// Lanes among `live` holding the same nbits-bit key as this lane.
+__device__ __forceinline__ unsigned int key_peers(int d, unsigned int live, int nbits)
+{
+    unsigned int peers = live;
+#pragma unroll
+    for (int b = 0; b < 12; ++b) {
+        if (b < nbits) {  // uniform
+            const unsigned int set = __ballot_sync(0xffffffffu, (d >> b) & 1);
+            peers &= ((d >> b) & 1) ? set : ~set;
+        }
+    }
+    return peers;
+}
+
+__global__ void __launch_bounds__(kCluThreads, 1)
+plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, int E, int nbits, int g,
+                        int* __restrict__ row_ptr, int* __restrict__ perm, int4* __restrict__ seg_units,
+                        int4* __restrict__ row_units, int4* __restrict__ finish, int* __restrict__ counters)
+{
+    cg::cluster_group cl = cg::this_cluster();
+    extern __shared__ __align__(16) unsigned char clu_smem[];
+    OneShared& S = *reinterpret_cast<OneShared*>(clu_smem);
+    const int C = static_cast<int>(cl.num_blocks());
+    const int c = static_cast<int>(cl.block_rank());
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cnt = slice_len(N, E, c);
+    const long long c0 = static_cast<long long>(c) * E;
+    const int B = 1 << nbits;  // >= M
+    const int R = static_cast<int>((M + C - 1) / C);  // destinations per owner, <= kOneMaxBins
+    const int r_lo = static_cast<int>(min_ll(M, static_cast<long long>(c) * R));
+    const int r_hi = static_cast<int>(min_ll(M, static_cast<long long>(r_lo) + R));
+    unsigned int lt;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+    pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
+    unsigned int* wz = reinterpret_cast<unsigned int*>(S.whist);
+    for (int i = tid; i < kOneRankWarps * B / 2 + 1; i += kCluThreads)
+        if (i < kOneRankWarps * kOneMaxBins / 2) wz[i] = 0u;
+    if (tid == 0) S.tot[4] = 0;
+
+    // 1. the slice, then the ranking: warp w < 16 owns [w*ipw, (w+1)*ipw)
+    bool bad = false;
+    for (int i = tid; i < cnt; i += kCluThreads) {
+        const unsigned int k = static_cast<unsigned int>(__ldg(idx + c0 + i));
+        bad |= static_cast<long long>(k) >= M;
+        S.kv[i] = make_uint2(k, static_cast<unsigned int>(c0 + i));
+    }
+    const int cta_bad = __syncthreads_or(bad);
+    if (tid == 0) S.bad = cta_bad;
+    const int ipw = (((cnt + kOneRankWarps - 1) / kOneRankWarps) + 31) & ~31;
+    const int nk = ipw >> 5;  // <= 8
+    if (warp < kOneRankWarps) {
+        unsigned short* wh = S.whist + warp * B;
+        for (int k = 0; k < nk; ++k) {
+            const int p0 = warp * ipw + k * 32;
+            const int nl = cnt - p0;
+            const unsigned int live = nl >= 32 ? 0xffffffffu : (nl <= 0 ? 0u : (1u << nl) - 1u);
+            if (live == 0u) break;  // uniform over the warp
+            const int p = p0 + lane;
+            const bool valid = (live >> lane) & 1u;
+            const int d = valid ? static_cast<int>(S.kv[p].x & static_cast<unsigned int>(B - 1)) : 0;
+            const unsigned int peers = key_peers(d, live, nbits);
+            const int old = wh[d];
+            if (valid) S.rank[p] = static_cast<unsigned short>(old + __popc(peers & lt));
+            __syncwarp();
+            if (valid && (peers & lt) == 0u) wh[d] = static_cast<unsigned short>(old + __popc(peers));
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // warp offsets and this CTA's count of every destination
+    for (int d = tid; d < B; d += kCluThreads) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < kOneRankWarps; ++w) {
+            const int x = S.whist[w * B + d];
+            S.whist[w * B + d] = static_cast<unsigned short>(run);
+            run += x;
+        }
+        S.chist[d] = run;
+    }
+    cl.sync();  // every CTA's counts are visible
+    if (warp == kCluWarps - 1) {
+        const int b = lane < C ? *cl.map_shared_rank(&S.bad, lane) : 0;
+        const int any = __any_sync(0xffffffffu, b != 0);
+        if (lane == 0) S.any_bad = any;
+    }
+    __syncthreads();
+    const bool any_bad = S.any_bad != 0;
+
+    // 2. owned destinations [r_lo, r_hi), q consecutive per thread: counts in
+    //    every CTA, each CTA's prefix written back, totals = row lengths
+    const int q = (R + kCluThreads - 1) / kCluThreads;  // <= kOneRowsPerThread
+    const int t_lo = min(r_hi, r_lo + tid * q);
+    const int nrows = any_bad ? 0 : min(r_hi, t_lo + q) - t_lo;
+    int len[kOneRowsPerThread];
+#pragma unroll
+    for (int j = 0; j < kOneRowsPerThread; ++j) {
+        len[j] = 0;
+        if (j < nrows) {
+            const int m = t_lo + j;
+            int x[kCluMaxCtas];
+#pragma unroll
+            for (int r = 0; r < kCluMaxCtas; ++r) x[r] = r < C ? *cl.map_shared_rank(&S.chist[m], r) : 0;
+            int run = 0;
+#pragma unroll
+            for (int r = 0; r < kCluMaxCtas; ++r) {
+                if (r < C) *cl.map_shared_rank(&S.pref[m], r) = run;
+                run += x[r];
+            }
+            len[j] = run;
+        }
+    }
+    const int G = 1 << g;
+    int v4[4] = {0, 0, 0, 0};  // rows' sources, seg units, row units, finish tasks
+    int mx = 0;
+#pragma unroll
+    for (int j = 0; j < kOneRowsPerThread; ++j) {
+        if (j < nrows) {
+            const int nch = (len[j] + 31) >> 5;
+            v4[0] += len[j];
+            if (nch > G) {
+                v4[1] += (nch + G - 1) >> g;
+                v4[3] += 1;
+            } else {
+                v4[2] += 1;
+            }
+            mx = max(mx, len[j]);
+        }
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0 && mx > 0) atomicMax(&S.tot[4], mx);
+    int t4[4];
+    block_excl_scan_n<4>(v4, S.ws, t4);
+    if (tid == 0) {
+        S.tot[0] = t4[0];
+        S.tot[1] = t4[1];
+        S.tot[2] = t4[2];
+        S.tot[3] = t4[3];
+    }
+    cl.sync();  // prefixes and every CTA's totals are visible
+
+    // 3. bases from the CTAs' totals; row_ptr of the owned destinations
+    if (warp == 0) {
+        int v[4] = {0, 0, 0, 0}, m = 0;
+        if (lane < C) {
+            const int* rt = cl.map_shared_rank(S.tot, lane);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = rt[j];
+            m = rt[4];
+        }
+        int in[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = __shfl_up_sync(0xffffffffu, in[j], o);
+                if (lane >= o) in[j] += t;
+            }
+        }
+        const int gm = __reduce_max_sync(0xffffffffu, m);
+        if (lane == c) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) S.base[j] = in[j] - v[j];
+        }
+        if (lane == 31) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) S.grand[j] = in[j];
+            S.grand[4] = gm;
+        }
+    }
+    __syncthreads();
+    int rstart = v4[0] + S.base[0];
+#pragma unroll
+    for (int j = 0; j < kOneRowsPerThread; ++j) {
+        if (j < nrows) {
+            S.rp[t_lo + j - r_lo] = rstart;
+            rstart += len[j];
+        }
+    }
+    cl.sync();  // row_ptr of every range is visible
+
+    // 4. perm
+    if (!any_bad) {
+        for (int i = tid; i < cnt; i += kCluThreads) {
+            const uint2 e = S.kv[i];
+            const int w = i / ipw;
+            const int o = static_cast<int>(e.x) / R;  // e.x < M
+            const int pos = cl.map_shared_rank(S.rp, o)[e.x - o * R] + S.pref[e.x] + S.whist[w * B + e.x] + S.rank[i];
+            perm[pos] = static_cast<int>(e.y);  // pos in [0, N)
+        }
+    }
+    // the last reads of other CTAs' shared memory are done: arrive now, write
+    // the lists, wait before leaving
+    cluster_arrive_relaxed();
+    if (!any_bad) {
+        int eA = v4[1] + S.base[1], eB = v4[2] + S.base[2], eC = v4[3] + S.base[3];
+#pragma unroll
+        for (int j = 0; j < kOneRowsPerThread; ++j) {
+            if (j < nrows) {
+                const int m = t_lo + j;
+                const int nch = (len[j] + 31) >> 5;
+                row_ptr[m] = S.rp[m - r_lo];
+                if (nch > G) {
+                    const int a = (nch + G - 1) >> g;
+                    finish[eC++] = make_int4(m, eA, a, 0);
+                    for (int s = 0; s < a; ++s) seg_units[eA + s] = make_int4(m, s, eA + s, 0);
+                    eA += a;
+                } else {
+                    row_units[eB++] = make_int4(m, -1, 0, 0);
+                }
+            }
+        }
+        if (c == 0 && tid == 0) row_ptr[M] = static_cast<int>(N);
+    }
+    if (c == 0 && tid < kCtrCount) {
+        int v = 0;
+        if (tid == kCtrErrIndex) v = any_bad ? 1 : 0;
+        else if (!any_bad && tid == kCtrSegs) v = S.grand[1];
+        else if (!any_bad && tid == kCtrNormal) v = S.grand[2];
+        else if (!any_bad && tid == kCtrHot) v = S.grand[3];
+        else if (!any_bad && tid == kCtrMaxLen) v = S.grand[4];
+        counters[tid] = v;
+    }
+    cluster_wait();  // no CTA leaves while another may still read its shared memory
+}
+
+// ------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------
 
 namespace {
 std::mutex g_clu_mu;
-signed char g_clu_ok[kMaxDevices][kCluMaxCtas + 1];  // 0 unknown, 1 schedulable, -1 not
-bool g_clu_attr[kMaxDevices];
+signed char g_clu_ok[2][kMaxDevices][kCluMaxCtas + 1];  // [variant][device][C]: 0 unknown, 1 schedulable, -1 not
+bool g_clu_attr[2][kMaxDevices];
+
+int bits_of(int64_t v)
+{
+    int b = 0;
+    while (v > 0) { ++b; v >>= 1; }
+    return b;
+}
+
+// Launches one of the two cluster kernels on a cluster of C CTAs; *launched
+// stays false if the device cannot schedule such a cluster.
+template <typename Kern, typename... Args>
+det_status launch_on_cluster(int variant, Kern kern, int C, size_t smem, cudaStream_t st, bool* launched,
+                             Args... args)
+{
+    int dev = 0;
+    DETR_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return DET_OK;
+    {
+        std::lock_guard<std::mutex> lock(g_clu_mu);
+        if (!g_clu_attr[variant][dev]) {
+            DETR_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+            DETR_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+            g_clu_attr[variant][dev] = true;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned int>(C), 1, 1);
+    cfg.blockDim = dim3(kCluThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned int>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    signed char ok;
+    {
+        std::lock_guard<std::mutex> lock(g_clu_mu);
+        ok = g_clu_ok[variant][dev][C];
+    }
+    if (ok == 0) {
+        int n = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) (void)cudaGetLastError();
+        ok = (e == cudaSuccess && n >= 1) ? 1 : -1;
+        std::lock_guard<std::mutex> lock(g_clu_mu);
+        g_clu_ok[variant][dev][C] = ok;
+    }
+    if (ok < 0) return DET_OK;
+    DETR_CUDA(cudaLaunchKernelEx(&cfg, kern, args...));
+    DETR_LAUNCHED();
+    *launched = true;
+    return DET_OK;
+}
 }  // namespace
 
 int plan_cluster_ctas(int64_t N, int64_t M)
@@ -478,51 +839,17 @@ det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, 
     *launched = false;
     const int C = plan_cluster_ctas(N, M);
     if (C == 0) return DET_OK;
-    int dev = 0;
-    DETR_CUDA(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= kMaxDevices) return DET_OK;
-    const size_t smem = sizeof(CluShared);
-    auto kern = plan_cluster_kernel;
-    {
-        std::lock_guard<std::mutex> lock(g_clu_mu);
-        if (!g_clu_attr[dev]) {
-            DETR_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
-            DETR_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-            g_clu_attr[dev] = true;
-        }
+    const int E = static_cast<int>(cdiv(N, C));
+    if (M <= kOneMaxBins && E <= kOneMaxSlice) {
+        const det_status s = launch_on_cluster(1, plan_cluster_one_kernel, C, sizeof(OneShared), st, launched, idx,
+                                               static_cast<long long>(N), static_cast<long long>(M), E,
+                                               bits_of(M - 1), g, row_ptr, perm, seg_units, row_units, finish,
+                                               counters);
+        if (s || *launched) return s;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned int>(C), 1, 1);
-    cfg.blockDim = dim3(kCluThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned int>(C);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    signed char ok;
-    {
-        std::lock_guard<std::mutex> lock(g_clu_mu);
-        ok = g_clu_ok[dev][C];
-    }
-    if (ok == 0) {
-        int n = 0;
-        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        if (e != cudaSuccess) (void)cudaGetLastError();
-        ok = (e == cudaSuccess && n >= 1) ? 1 : -1;
-        std::lock_guard<std::mutex> lock(g_clu_mu);
-        g_clu_ok[dev][C] = ok;
-    }
-    if (ok < 0) return DET_OK;
-    const long long E = static_cast<long long>(cdiv(N, C));
-    DETR_CUDA(cudaLaunchKernelEx(&cfg, kern, idx, static_cast<long long>(N), static_cast<long long>(M),
-                                 static_cast<int>(E), np32, g, row_ptr, perm, seg_units, row_units, finish, counters));
-    DETR_LAUNCHED();
-    *launched = true;
-    return DET_OK;
+    return launch_on_cluster(0, plan_cluster_kernel, C, sizeof(CluShared), st, launched, idx,
+                             static_cast<long long>(N), static_cast<long long>(M), E, np32, g, row_ptr, perm,
+                             seg_units, row_units, finish, counters);
 }
 
 }  // namespace detr
