@@ -466,7 +466,8 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
 //      work-list classification;
 //   3. a scan over the CTAs' totals gives each range its first position, so
 //      row_ptr of every owned destination;
-//   4. source i goes to perm[row_ptr[key] + earlier CTAs + earlier warps +
+//   4. every CTA copies all ranges' row_ptr (coalesced remote reads), and
+//      source i goes to perm[row_ptr[key] + earlier CTAs + earlier warps +
 //      rank].
 constexpr int kOneMaxBins = 4096;
 constexpr int kOneMaxSlice = 4096;
@@ -482,9 +483,8 @@ struct OneShared {
     int pref[kOneMaxBins];     // earlier CTAs' count of each destination (written by the owners)
     int rp[kOneMaxBins];       // row_ptr of the destinations this CTA owns (read by every CTA)
     int ws[4 * (kCluWarps + 1)];
-    int tot[5];                // rows, seg units, row units, finish tasks, longest row (read by every CTA)
-    int base[4];
-    int grand[5];
+    int tot[5];                // rows, seg units, row units, finish tasks, longest row
+    int all_tot[kCluMaxCtas][5];  // every CTA's tot (written by that CTA)
     int bad;                   // this CTA saw an index outside [0, M) (read by every CTA)
     int any_bad;
 };
@@ -663,23 +663,23 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     mx = __reduce_max_sync(0xffffffffu, mx);
     if (lane == 0 && mx > 0) atomicMax(&S.tot[4], mx);
     int t4[4];
-    block_excl_scan_n<4>(v4, S.ws, t4);
-    if (tid == 0) {
-        S.tot[0] = t4[0];
-        S.tot[1] = t4[1];
-        S.tot[2] = t4[2];
-        S.tot[3] = t4[3];
+    block_excl_scan_n<4>(v4, S.ws, t4);  // ends synchronised: S.tot[4] is final
+    if (tid < 5 * C) {  // push this CTA's totals into every CTA
+        const int r = tid / 5, f = tid - 5 * (tid / 5);
+        const int v = f == 0 ? t4[0] : f == 1 ? t4[1] : f == 2 ? t4[2] : f == 3 ? t4[3] : S.tot[4];
+        *cl.map_shared_rank(&S.all_tot[c][f], r) = v;
     }
     cl.sync();  // prefixes and every CTA's totals are visible
 
-    // 3. bases from the CTAs' totals; row_ptr of the owned destinations
-    if (warp == 0) {
+    // 3. bases from the CTAs' totals (every warp computes them itself); row_ptr
+    //    of the owned destinations
+    int base[4], grand[5];
+    {
         int v[4] = {0, 0, 0, 0}, m = 0;
         if (lane < C) {
-            const int* rt = cl.map_shared_rank(S.tot, lane);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = rt[j];
-            m = rt[4];
+            for (int j = 0; j < 4; ++j) v[j] = S.all_tot[lane][j];
+            m = S.all_tot[lane][4];
         }
         int in[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
@@ -690,19 +690,14 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
                 if (lane >= o) in[j] += t;
             }
         }
-        const int gm = __reduce_max_sync(0xffffffffu, m);
-        if (lane == c) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) S.base[j] = in[j] - v[j];
+        for (int j = 0; j < 4; ++j) {
+            base[j] = __shfl_sync(0xffffffffu, in[j] - v[j], c);
+            grand[j] = __shfl_sync(0xffffffffu, in[j], 31);
         }
-        if (lane == 31) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) S.grand[j] = in[j];
-            S.grand[4] = gm;
-        }
+        grand[4] = __reduce_max_sync(0xffffffffu, m);
     }
-    __syncthreads();
-    int rstart = v4[0] + S.base[0];
+    int rstart = v4[0] + base[0];
 #pragma unroll
     for (int j = 0; j < kOneRowsPerThread; ++j) {
         if (j < nrows) {
@@ -712,13 +707,23 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     }
     cl.sync();  // row_ptr of every range is visible
 
-    // 4. perm
+    // 4. perm.  First every range's row_ptr into this CTA, in place of the
+    //    counts (no longer read): a warp reads 32 consecutive rows of one
+    //    owner, where one remote read per source would cost a network request
+    //    each.
+    int* rp_all = S.chist;
+    if (!any_bad) {
+        for (int m = tid; m < M; m += kCluThreads) {
+            const int o = m / R;
+            rp_all[m] = cl.map_shared_rank(S.rp, o)[m - o * R];
+        }
+    }
+    __syncthreads();
     if (!any_bad) {
         for (int i = tid; i < cnt; i += kCluThreads) {
-            const uint2 e = S.kv[i];
+            const uint2 e = S.kv[i];  // e.x < M
             const int w = i / ipw;
-            const int o = static_cast<int>(e.x) / R;  // e.x < M
-            const int pos = cl.map_shared_rank(S.rp, o)[e.x - o * R] + S.pref[e.x] + S.whist[w * B + e.x] + S.rank[i];
+            const int pos = rp_all[e.x] + S.pref[e.x] + S.whist[w * B + e.x] + S.rank[i];
             perm[pos] = static_cast<int>(e.y);  // pos in [0, N)
         }
     }
@@ -726,7 +731,7 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     // the lists, wait before leaving
     cluster_arrive_relaxed();
     if (!any_bad) {
-        int eA = v4[1] + S.base[1], eB = v4[2] + S.base[2], eC = v4[3] + S.base[3];
+        int eA = v4[1] + base[1], eB = v4[2] + base[2], eC = v4[3] + base[3];
 #pragma unroll
         for (int j = 0; j < kOneRowsPerThread; ++j) {
             if (j < nrows) {
@@ -748,10 +753,10 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     if (c == 0 && tid < kCtrCount) {
         int v = 0;
         if (tid == kCtrErrIndex) v = any_bad ? 1 : 0;
-        else if (!any_bad && tid == kCtrSegs) v = S.grand[1];
-        else if (!any_bad && tid == kCtrNormal) v = S.grand[2];
-        else if (!any_bad && tid == kCtrHot) v = S.grand[3];
-        else if (!any_bad && tid == kCtrMaxLen) v = S.grand[4];
+        else if (!any_bad && tid == kCtrSegs) v = grand[1];
+        else if (!any_bad && tid == kCtrNormal) v = grand[2];
+        else if (!any_bad && tid == kCtrHot) v = grand[3];
+        else if (!any_bad && tid == kCtrMaxLen) v = grand[4];
         counters[tid] = v;
     }
     cluster_wait();  // no CTA leaves while another may still read its shared memory
