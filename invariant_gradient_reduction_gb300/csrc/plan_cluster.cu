@@ -457,9 +457,9 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
 // ------------------------------------------------------------------------
 // With M <= 4096 the destination itself is the digit, so one counting pass
 // sorts, and the destination counts it yields give row_ptr directly:
-//   1. each CTA loads its slice; 16 warps rank it (peers of the whole
+//   1. each CTA loads its slice; its warps rank it (peers of the whole
 //      destination from one ballot per bit, in element order, warps in order)
-//      against 16-bit per-warp counts of every destination;
+//      against 8-bit per-warp counts of every destination;
 //   2. each CTA owns R consecutive destinations: it reads their counts in
 //      every CTA, writes each CTA's exclusive prefix back into that CTA's
 //      shared memory, and takes the totals as row lengths, with their
@@ -471,14 +471,14 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
 //      rank].
 constexpr int kOneMaxBins = 4096;
 constexpr int kOneMaxSlice = 4096;
-constexpr int kOneRankWarps = 16;
 constexpr int kOneRowsPerThread = kOneMaxBins / kCluThreads;
-static_assert(kOneMaxSlice / kOneRankWarps / 32 <= 8, "ranking items per lane");
+static_assert(kOneMaxSlice / kCluWarps <= 255, "a warp's count of one destination fits a byte");
+static_assert(kOneMaxBins / 4 <= kCluThreads, "one word of four counts per thread");
 
 struct OneShared {
     uint2 kv[kOneMaxSlice];                               // {key, source position}
-    unsigned short rank[kOneMaxSlice];                    // rank among equal keys inside the ranking warp
-    unsigned short whist[kOneRankWarps * kOneMaxBins];    // per ranking warp counts, then warp offsets
+    unsigned short rank[kOneMaxSlice];                    // rank among equal keys inside the warp
+    unsigned char whist[kCluWarps * kOneMaxBins];         // per warp count of every destination (< 256)
     int chist[kOneMaxBins];    // this CTA's count of each destination (read by the owners)
     int pref[kOneMaxBins];     // earlier CTAs' count of each destination (written by the owners)
     int rp[kOneMaxBins];       // row_ptr of the destinations this CTA owns (read by every CTA)
@@ -565,9 +565,8 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     unsigned int lt;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
     pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
-    unsigned int* wz = reinterpret_cast<unsigned int*>(S.whist);
-    for (int i = tid; i < kOneRankWarps * B / 2 + 1; i += kCluThreads)
-        if (i < kOneRankWarps * kOneMaxBins / 2) wz[i] = 0u;
+    unsigned int* wz = reinterpret_cast<unsigned int*>(S.whist);  // B is a multiple of 4
+    for (int i = tid; i < kCluWarps * B / 4; i += kCluThreads) wz[i] = 0u;
     if (tid == 0) S.tot[4] = 0;
 
     // 1. the slice, then the ranking: warp w < 16 owns [w*ipw, (w+1)*ipw)
@@ -579,10 +578,10 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     }
     const int cta_bad = __syncthreads_or(bad);
     if (tid == 0) S.bad = cta_bad;
-    const int ipw = (((cnt + kOneRankWarps - 1) / kOneRankWarps) + 31) & ~31;
-    const int nk = ipw >> 5;  // <= 8
-    if (warp < kOneRankWarps) {
-        unsigned short* wh = S.whist + warp * B;
+    const int ipw = (((cnt + kCluWarps - 1) / kCluWarps) + 31) & ~31;  // warp w owns [w*ipw, (w+1)*ipw)
+    const int nk = ipw >> 5;  // <= 4
+    {
+        unsigned char* wh = S.whist + warp * B;
         for (int k = 0; k < nk; ++k) {
             const int p0 = warp * ipw + k * 32;
             const int nl = cnt - p0;
@@ -595,21 +594,26 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
             const int old = wh[d];
             if (valid) S.rank[p] = static_cast<unsigned short>(old + __popc(peers & lt));
             __syncwarp();
-            if (valid && (peers & lt) == 0u) wh[d] = static_cast<unsigned short>(old + __popc(peers));
+            if (valid && (peers & lt) == 0u) wh[d] = static_cast<unsigned char>(old + __popc(peers));
             __syncwarp();
         }
     }
     __syncthreads();
-    // warp offsets and this CTA's count of every destination
-    for (int d = tid; d < B; d += kCluThreads) {
-        int run = 0;
-#pragma unroll
-        for (int w = 0; w < kOneRankWarps; ++w) {
-            const int x = S.whist[w * B + d];
-            S.whist[w * B + d] = static_cast<unsigned short>(run);
-            run += x;
+    // this CTA's count of every destination: thread t sums four destinations
+    // (one word) over the 32 warps, bytes split into two 16-bit lanes
+    if (tid < B / 4) {
+        const unsigned int* wr = reinterpret_cast<const unsigned int*>(S.whist);
+        unsigned int even = 0u, odd = 0u;
+#pragma unroll 8
+        for (int w = 0; w < kCluWarps; ++w) {
+            const unsigned int x = wr[w * (B / 4) + tid];
+            even += x & 0x00ff00ffu;
+            odd += (x >> 8) & 0x00ff00ffu;
         }
-        S.chist[d] = run;
+        S.chist[4 * tid + 0] = static_cast<int>(even & 0xffffu);
+        S.chist[4 * tid + 1] = static_cast<int>(odd & 0xffffu);
+        S.chist[4 * tid + 2] = static_cast<int>(even >> 16);
+        S.chist[4 * tid + 3] = static_cast<int>(odd >> 16);
     }
     cl.sync();  // every CTA's counts are visible
     if (warp == kCluWarps - 1) {
@@ -723,7 +727,9 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
         for (int i = tid; i < cnt; i += kCluThreads) {
             const uint2 e = S.kv[i];  // e.x < M
             const int w = i / ipw;
-            const int pos = rp_all[e.x] + S.pref[e.x] + S.whist[w * B + e.x] + S.rank[i];
+            int before = 0;  // equal keys in earlier warps of this CTA
+            for (int v = 0; v < w; ++v) before += S.whist[v * B + e.x];
+            const int pos = rp_all[e.x] + S.pref[e.x] + before + S.rank[i];
             perm[pos] = static_cast<int>(e.y);  // pos in [0, N)
         }
     }
@@ -848,7 +854,7 @@ det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, 
     if (M <= kOneMaxBins && E <= kOneMaxSlice) {
         const det_status s = launch_on_cluster(1, plan_cluster_one_kernel, C, sizeof(OneShared), st, launched, idx,
                                                static_cast<long long>(N), static_cast<long long>(M), E,
-                                               bits_of(M - 1), g, row_ptr, perm, seg_units, row_units, finish,
+                                               std::max(2, bits_of(M - 1)), g, row_ptr, perm, seg_units, row_units, finish,
                                                counters);
         if (s || *launched) return s;
     }
