@@ -1,4 +1,6 @@
-// plan.cu -- destination lists (CSR) and the reduce work list.
+// plan.cu -- destination lists (CSR) and the reduce work list, multi-kernel
+// method (small problems without order keys use one cluster kernel instead,
+// plan_cluster.cu).
 //
 // The terms of destination m are the sources with idx[i] = m in ascending
 // order key (src_id[i], default i): the stable (expert id, original token id)
@@ -6,22 +8,21 @@
 // and determinism", section 3.2).  Everything here is integer work and exact,
 // so any correct method gives the same bytes.  This one:
 //
-//   1. plan_hist_kernel     one read of idx (and src_id): range check and the
-//                           256-bin digit histograms of every radix pass;
-//   2. radix_pass_kernel    one kernel per 8-bit digit (order keys first when
-//                           given, then the destination): a stable LSD radix
-//                           pass.  Each tile ranks its keys (match_any in
-//                           element order), finds the number of equal digits in
-//                           earlier tiles by decoupled look-back, and writes
-//                           its keys to their final places;
-//   3. units_kernel         row_ptr (binary search of each destination in the
-//                           sorted destinations) and the work list, with
-//                           decoupled look-back over row tiles.
+//   1-2. per 8-bit digit (the order key's first when given, then the
+//        destination's), a stable LSD radix pass in three kernels: digit
+//        counts of every tile, their scan over the tiles, and a scatter in
+//        which each tile ranks its keys and writes them to their places.  The
+//        first destination pass checks idx against M;
+//   3.   row_bounds_kernel: the first and one-past-last sorted position of
+//        every destination present, from the boundaries of the sorted
+//        destinations;
+//   4.   the work list, counted per tile of destinations, scanned over the
+//        tiles and written: row lengths give row_ptr, and each destination one
+//        whole-row unit or (more than 2^g chunks) its segment units and a
+//        finish task.
 //
-// Look-back: tiles take their index from an atomic ticket when they start, so a
-// tile only ever waits for tiles that started before it.  Every wait is bounded;
-// on expiry the kernel sets kCtrErrTimeout, writes nothing out of range and the
-// plan reports DET_ERR_TIMEOUT.
+// No kernel here waits for another CTA: every cross-tile quantity goes
+// through a separate counting kernel and a scan.
 #include <algorithm>
 #include <new>
 
@@ -31,96 +32,16 @@
 
 namespace detr {
 
-// Sort tiles: large problems use 4096-key tiles (256 threads x 16 keys, two
-// CTAs per SM), small ones 1024-key tiles (256 x 4) so that more CTAs share
-// the work.
+// Sort tiles: large problems use 4096-key tiles (256 threads x 16 keys, three
+// CTAs per SM for 32-bit keys), small ones 1024-key tiles (256 x 4) so that
+// more CTAs share the work.
 constexpr int kBigThreads = 256, kBigItems = 16;
 constexpr int kSmallThreads = 256, kSmallItems = 4;
 constexpr int64_t kSmallSortMaxN = 1 << 20;
 constexpr int kRadix = 256;
-constexpr int kHistThreads = 256;
 constexpr int kUnitThreads = 256;  // one row per thread
-constexpr unsigned long long kLookbackLimit = 1ull << 22;
-constexpr unsigned long long kFlagAggregate = 1ull << 32;
-constexpr unsigned long long kFlagPrefix = 2ull << 32;
 
 enum KeyMode { KM_DIRECT = 0, KM_CARRY = 1, KM_GATHER = 2 };
-
-// ------------------------------------------------------------------------
-// block scans and look-back
-// ------------------------------------------------------------------------
-
-__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p)
-{
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v)
-{
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Decoupled look-back for one value of a tile.  status is [tiles][stride]
-// words (flag << 32 | count), zero before the kernel.  Publishes this tile's
-// aggregate, adds the earlier tiles' values (stopping at the first inclusive
-// prefix), publishes this tile's inclusive prefix and returns the exclusive
-// one.  Predecessors are read kLookbackBatch at a time (nearest first), so the walk
-// back over tiles that are still running costs few round trips.  Waits only
-// on tiles with smaller tickets; bounded.
-constexpr int kLookbackBatch = 16;
-
-__device__ __forceinline__ void publish_aggregate(unsigned long long* status, int tile, int stride, int k,
-                                                  unsigned int aggregate)
-{
-    st_release(&status[static_cast<long long>(tile) * stride + k], kFlagAggregate | aggregate);
-}
-
-// The walk back, once this tile's aggregate is published.
-__device__ __forceinline__ unsigned int lookback_walk(unsigned long long* status, int tile, int stride, int k,
-                                                      unsigned int aggregate, int* counters)
-{
-    unsigned long long excl = 0;
-    unsigned long long spins = 0;
-    int t = tile - 1;
-    while (t >= 0) {
-        unsigned long long v[kLookbackBatch];
-#pragma unroll
-        for (int q = 0; q < kLookbackBatch; ++q)
-            v[q] = t - q >= 0 ? ld_acquire(&status[static_cast<long long>(t - q) * stride + k]) : 0ull;
-        int used = 0;
-        bool done = false, stalled = false;
-#pragma unroll
-        for (int q = 0; q < kLookbackBatch; ++q) {
-            if (done || stalled || t - q < 0) continue;
-            const unsigned long long flag = v[q] >> 32;
-            if (flag == 0) {
-                stalled = true;
-                continue;
-            }
-            excl += v[q] & 0xffffffffull;
-            ++used;
-            if (flag == (kFlagPrefix >> 32)) done = true;
-        }
-        if (done) break;
-        t -= used;
-        if (stalled && ++spins > kLookbackLimit) {
-            atomicOr(&counters[kCtrErrTimeout], 1);
-            break;
-        }
-    }
-    st_release(&status[static_cast<long long>(tile) * stride + k],
-               kFlagPrefix | ((excl + aggregate) & 0xffffffffull));
-    return static_cast<unsigned int>(excl);
-}
-
-__device__ __forceinline__ unsigned int lookback(unsigned long long* status, int tile, int stride, int k,
-                                                 unsigned int aggregate, int* counters)
-{
-    publish_aggregate(status, tile, stride, k, aggregate);
-    return lookback_walk(status, tile, stride, k, aggregate, counters);
-}
 
 // ------------------------------------------------------------------------
 // keys
@@ -188,15 +109,21 @@ tile_count_kernel(const void* kin, const int* vin, const int* gather, long long 
     __syncthreads();
     const long long base = static_cast<long long>(blockIdx.x) * NT * ITEMS;
     bool bad = false;
-#pragma unroll 4
-    for (int k = 0; k < ITEMS; ++k) {
+    K key[ITEMS];
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) {  // all loads in flight first
         const long long p = base + static_cast<long long>(k) * NT + threadIdx.x;
+        key[k] = 0;
         if (p < N) {
-            K key;
             int val;
-            load_kv<K, MODE>(kin, vin, gather, p, key, val);
-            if (M_check > 0 && static_cast<long long>(key) >= M_check) bad = true;
-            atomicAdd(&h[digit_of<K>(key, shift)], 1);
+            load_kv<K, MODE>(kin, vin, gather, p, key[k], val);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < ITEMS; ++k) {
+        if (base + static_cast<long long>(k) * NT + threadIdx.x < N) {
+            if (M_check > 0 && static_cast<long long>(key[k]) >= M_check) bad = true;
+            atomicAdd(&h[digit_of<K>(key[k], shift)], 1);
         }
     }
     if (M_check > 0 && __syncthreads_or(bad) && threadIdx.x == 0) atomicOr(&counters[kCtrErrIndex], 1);
@@ -350,84 +277,132 @@ __global__ void dup_key_kernel(const int* skeys, const int* perm, const long lon
 // 3. row_ptr and the work list
 // ------------------------------------------------------------------------
 
-// First position p in the sorted destinations with skeys[p] >= m.
-__device__ __forceinline__ int lower_bound(const int* skeys, int n, int m)
+// Marks the sorted run of every destination present: rstart[k] = its first
+// position, rend[k] = one past its last (both stay 0 for an absent one).
+// kBoundItems positions per thread, all loads in flight.
+constexpr int kBoundItems = 4;
+
+__global__ void __launch_bounds__(kUnitThreads)
+row_bounds_kernel(const int* skeys, long long N, long long M, int* rstart, int* rend, const int* counters)
 {
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(skeys + mid) < m) lo = mid + 1;
-        else hi = mid;
+    if (counters[kCtrErrIndex]) return;  // keys may be out of range
+    const long long base = static_cast<long long>(blockIdx.x) * kUnitThreads * kBoundItems + threadIdx.x;
+    int k[kBoundItems], prev[kBoundItems], next[kBoundItems];
+#pragma unroll
+    for (int j = 0; j < kBoundItems; ++j) {
+        const long long p = base + static_cast<long long>(j) * kUnitThreads;
+        k[j] = p < N ? skeys[p] : -1;
+        prev[j] = p > 0 && p < N ? skeys[p - 1] : -1;
+        next[j] = p + 1 < N ? skeys[p + 1] : -1;
     }
-    return lo;
+#pragma unroll
+    for (int j = 0; j < kBoundItems; ++j) {
+        const long long p = base + static_cast<long long>(j) * kUnitThreads;
+        if (p >= N || k[j] < 0 || k[j] >= M) continue;
+        if (prev[j] != k[j]) rstart[k[j]] = static_cast<int>(p);
+        if (next[j] != k[j]) rend[k[j]] = static_cast<int>(p + 1);
+    }
 }
 
-// One row per thread: hot rows (more than 2^g chunks) give `seg` segment
-// units and one finish task; the others one whole-row unit.  row_ptr[m] is a
-// binary search of the sorted destinations (the row's end comes from the
-// next lane).  Emits the segment units [A], the row units [B], the finish
-// tasks [C], and the totals A, B, C and the longest list into the counter
-// block.
+// The work list in three kernels (no CTA waits for another), over tiles of
+// kUnitThreads destinations, one per thread:
+//   units_count_kernel  each tile's totals: sources (row lengths), hot
+//                       segments, whole-row units, finish tasks; and the
+//                       longest list;
+//   units_scan_kernel   one CTA: exclusive scans of the four totals over the
+//                       tiles, and the grand totals into the counter block;
+//   units_write_kernel  row_ptr, and the units: hot rows (more than 2^g
+//                       chunks) give `seg` segment units and one finish task,
+//                       the others one whole-row unit.
+struct RowClass {
+    int len, seg, whole, fin;
+};
+
+__device__ __forceinline__ RowClass classify_row(const int* rstart, const int* rend, long long m, long long M, int g)
+{
+    RowClass r{0, 0, 0, 0};
+    if (m < M) {
+        r.len = rend[m] - rstart[m];
+        const int nch = (r.len + kChunk - 1) / kChunk;
+        if (nch > (1 << g)) {
+            r.seg = (nch + (1 << g) - 1) >> g;
+            r.fin = 1;
+        } else {
+            r.whole = 1;
+        }
+    }
+    return r;
+}
+
 __global__ void __launch_bounds__(kUnitThreads)
-units_kernel(const int* skeys, long long N, long long M, int g, int* row_ptr, int4* seg_units, int4* row_units,
-             int4* finish, unsigned long long* ustatus, int* uticket, int nut, int* counters)
+units_count_kernel(const int* rstart, const int* rend, long long M, int g, int4* tile_tot, int* counters)
 {
     __shared__ int ws[kUnitThreads / 32 + 1];
-    __shared__ int s_tile;
-    __shared__ int s_excl[4];
+    if (counters[kCtrErrIndex]) return;
+    const long long m = static_cast<long long>(blockIdx.x) * kUnitThreads + threadIdx.x;
+    const RowClass r = classify_row(rstart, rend, m, M, g);
+    const int mx = __reduce_max_sync(0xffffffffu, r.len);
+    if ((threadIdx.x & 31) == 0 && mx > 0) atomicMax(&counters[kCtrMaxLen], mx);
+    int t[4];
+    block_excl_scan<kUnitThreads>(r.len, ws, &t[0]);
+    block_excl_scan<kUnitThreads>(r.seg, ws, &t[1]);
+    block_excl_scan<kUnitThreads>(r.whole, ws, &t[2]);
+    block_excl_scan<kUnitThreads>(r.fin, ws, &t[3]);
+    if (threadIdx.x == 0) tile_tot[blockIdx.x] = make_int4(t[0], t[1], t[2], t[3]);
+}
+
+constexpr int kUnitScanThreads = 1024;
+
+__global__ void __launch_bounds__(kUnitScanThreads)
+units_scan_kernel(int4* tile_tot, int nut, int* counters)
+{
+    __shared__ int ws[kUnitScanThreads / 32 + 1];
+    if (counters[kCtrErrIndex]) return;
+    int carry[4] = {0, 0, 0, 0};
+    for (int t0 = 0; t0 < nut; t0 += kUnitScanThreads) {
+        const int t = t0 + threadIdx.x;
+        const int4 v = t < nut ? tile_tot[t] : make_int4(0, 0, 0, 0);
+        int tot[4];
+        const int e0 = block_excl_scan<kUnitScanThreads>(v.x, ws, &tot[0]);
+        const int e1 = block_excl_scan<kUnitScanThreads>(v.y, ws, &tot[1]);
+        const int e2 = block_excl_scan<kUnitScanThreads>(v.z, ws, &tot[2]);
+        const int e3 = block_excl_scan<kUnitScanThreads>(v.w, ws, &tot[3]);
+        if (t < nut) tile_tot[t] = make_int4(carry[0] + e0, carry[1] + e1, carry[2] + e2, carry[3] + e3);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) carry[j] += tot[j];
+    }
+    if (threadIdx.x == 0) {
+        counters[kCtrSegs] = carry[1];
+        counters[kCtrNormal] = carry[2];
+        counters[kCtrHot] = carry[3];
+    }
+}
+
+__global__ void __launch_bounds__(kUnitThreads)
+units_write_kernel(const int* rstart, const int* rend, long long N, long long M, int g, const int4* tile_off,
+                   int* row_ptr, int4* seg_units, int4* row_units, int4* finish, const int* counters)
+{
+    __shared__ int ws[kUnitThreads / 32 + 1];
     pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
-    if (threadIdx.x == 0) s_tile = atomicAdd(uticket, 1);
-    __syncthreads();
-    const int tile = s_tile;
-    if (counters[kCtrErrIndex] || counters[kCtrErrTimeout]) {
-        // keep the look-back chain alive for later tiles, emit nothing
-        if (threadIdx.x < 3) lookback(ustatus, tile, 4, threadIdx.x, 0u, counters);
-        return;
-    }
-    const int lane = threadIdx.x & 31;
-    const int G = 1 << g;
-    const long long m = static_cast<long long>(tile) * kUnitThreads + threadIdx.x;
-    const int n = static_cast<int>(N);
-    const int start = m < M ? lower_bound(skeys, n, static_cast<int>(m)) : n;
-    int next = __shfl_down_sync(0xffffffffu, start, 1);
-    if (lane == 31) next = m + 1 < M ? lower_bound(skeys, n, static_cast<int>(m + 1)) : n;
-    if (m + 1 >= M) next = n;
-    const int len = m < M ? next - start : 0;
-    const int nch = (len + kChunk - 1) / kChunk;
-    int a = 0, b = 0, c = 0;
+    if (counters[kCtrErrIndex]) return;
+    const long long m = static_cast<long long>(blockIdx.x) * kUnitThreads + threadIdx.x;
+    const RowClass r = classify_row(rstart, rend, m, M, g);
+    const int4 off = tile_off[blockIdx.x];
+    int unused;
+    const int eR = off.x + block_excl_scan<kUnitThreads>(r.len, ws, &unused);
+    const int eA = off.y + block_excl_scan<kUnitThreads>(r.seg, ws, &unused);
+    const int eB = off.z + block_excl_scan<kUnitThreads>(r.whole, ws, &unused);
+    const int eC = off.w + block_excl_scan<kUnitThreads>(r.fin, ws, &unused);
     if (m < M) {
-        if (nch > G) { a = (nch + G - 1) >> g; c = 1; }
-        else b = 1;
-    }
-    int tA, tB, tC;
-    int eA = block_excl_scan<kUnitThreads>(a, ws, &tA);
-    int eB = block_excl_scan<kUnitThreads>(b, ws, &tB);
-    int eC = block_excl_scan<kUnitThreads>(c, ws, &tC);
-    if (threadIdx.x < 3) {
-        const int tot = threadIdx.x == 0 ? tA : (threadIdx.x == 1 ? tB : tC);
-        s_excl[threadIdx.x] =
-            static_cast<int>(lookback(ustatus, tile, 4, threadIdx.x, static_cast<unsigned int>(tot), counters));
-    }
-    __syncthreads();
-    eA += s_excl[0];
-    eB += s_excl[1];
-    eC += s_excl[2];
-    if (m < M) {
-        row_ptr[m] = start;
-        if (nch > G) {
-            finish[eC] = make_int4(static_cast<int>(m), eA, a, 0);
-            for (int s = 0; s < a; ++s) seg_units[eA + s] = make_int4(static_cast<int>(m), s, eA + s, 0);
+        row_ptr[m] = eR;
+        if (r.fin) {
+            finish[eC] = make_int4(static_cast<int>(m), eA, r.seg, 0);
+            for (int s = 0; s < r.seg; ++s) seg_units[eA + s] = make_int4(static_cast<int>(m), s, eA + s, 0);
         } else {
             row_units[eB] = make_int4(static_cast<int>(m), -1, 0, 0);
         }
-        if (len > 0) atomicMax(&counters[kCtrMaxLen], len);
     }
-    if (tile == nut - 1 && threadIdx.x == 0) {
-        row_ptr[M] = n;
-        counters[kCtrSegs] = s_excl[0] + tA;
-        counters[kCtrNormal] = s_excl[1] + tB;
-        counters[kCtrHot] = s_excl[2] + tC;
-    }
+    if (m == M - 1) row_ptr[M] = static_cast<int>(N);
 }
 
 // ------------------------------------------------------------------------
@@ -437,7 +412,8 @@ units_kernel(const int* skeys, long long N, long long M, int g, int* row_ptr, in
 struct PlanLayout {
     // zeroed at the start of every multi-kernel plan: counters, the work
     // list's ticket, row_ptr and its look-back status words
-    size_t counters, uticket, row_ptr, ustatus, zero_end;
+    size_t counters, row_ptr, rstart, rend, zero_end;
+    size_t utot;
     size_t counts, totals, perm, skeys, k32_tmp, v_tmp, k64_a, k64_b, va, vb, seg_units, row_units, finish, total;
     int ntiles, nut, npass;
     int64_t max_segs, max_rows, max_finish;
@@ -474,10 +450,11 @@ static PlanLayout plan_layout(int64_t N, int64_t M, bool with_src, int g)
     L.max_segs = 2 * cdiv(N, seg_terms) + 1;
     L.max_rows = M + 1;
     L.counters = take(kCtrCount * sizeof(int));
-    L.uticket = take(sizeof(int));
     L.row_ptr = take(static_cast<size_t>(M + 1) * sizeof(int));
-    L.ustatus = take(static_cast<size_t>(L.nut) * 4 * sizeof(unsigned long long));
+    L.rstart = take(static_cast<size_t>(M) * sizeof(int));
+    L.rend = take(static_cast<size_t>(M) * sizeof(int));
     L.zero_end = off;
+    L.utot = take(static_cast<size_t>(L.nut) * sizeof(int4));
     L.counts = take(static_cast<size_t>(kRadix) * L.ntiles * sizeof(int));
     L.totals = take(static_cast<size_t>(kRadix) * sizeof(int));
     L.perm = take(static_cast<size_t>(N) * sizeof(int));
@@ -596,11 +573,9 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     cudaStream_t st = as_stream(stream);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     int* counters = reinterpret_cast<int*>(ws + L.counters);
-    int* uticket = reinterpret_cast<int*>(ws + L.uticket);
     int* row_ptr = reinterpret_cast<int*>(ws + L.row_ptr);
     int* counts = reinterpret_cast<int*>(ws + L.counts);
     int* totals = reinterpret_cast<int*>(ws + L.totals);
-    unsigned long long* ustatus = reinterpret_cast<unsigned long long*>(ws + L.ustatus);
     int* perm = reinterpret_cast<int*>(ws + L.perm);
     int* skeys = reinterpret_cast<int*>(ws + L.skeys);
     int* k32_tmp = reinterpret_cast<int*>(ws + L.k32_tmp);
@@ -670,8 +645,20 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
         }
     }
     if (M > 0) {
-        units_kernel<<<L.nut, kUnitThreads, 0, st>>>(skeys, N, M, g, row_ptr, seg_units, row_units, finish, ustatus,
-                                                     uticket, L.nut, counters);
+        int* rstart = reinterpret_cast<int*>(ws + L.rstart);
+        int* rend = reinterpret_cast<int*>(ws + L.rend);
+        if (N > 0) {
+            const unsigned int bgrid = static_cast<unsigned int>(cdiv(N, int64_t(kUnitThreads) * kBoundItems));
+            row_bounds_kernel<<<bgrid, kUnitThreads, 0, st>>>(skeys, N, M, rstart, rend, counters);
+            DETR_LAUNCHED();
+        }
+        int4* tile_tot = reinterpret_cast<int4*>(ws + L.utot);
+        units_count_kernel<<<L.nut, kUnitThreads, 0, st>>>(rstart, rend, M, g, tile_tot, counters);
+        DETR_LAUNCHED();
+        units_scan_kernel<<<1, kUnitScanThreads, 0, st>>>(tile_tot, L.nut, counters);
+        DETR_LAUNCHED();
+        units_write_kernel<<<L.nut, kUnitThreads, 0, st>>>(rstart, rend, N, M, g, tile_tot, row_ptr, seg_units,
+                                                           row_units, finish, counters);
         DETR_LAUNCHED();
     }
     }  // multi-kernel plan
