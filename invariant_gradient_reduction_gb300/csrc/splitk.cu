@@ -15,7 +15,12 @@
 namespace detr {
 
 constexpr int kSplitThreads = 256;
-constexpr int kSplitBatch = 8;
+constexpr int kSplitBatch = 4;
+// Six CTAs per SM (at most 40 registers a thread) when one round of chunk
+// slots covers all splits: the 56-split, 393216-output reduce then runs as one
+// wave of resident CTAs, where 64 registers left a quarter of the CTAs for a
+// second wave.  Deeper counters (more rounds) keep four.
+constexpr int kSplitMinBlocks = 6;
 constexpr int kMaxSplitSlotsLog2 = 3;
 constexpr int kMaxSplitRounds = 127;
 
@@ -52,7 +57,7 @@ __device__ __forceinline__ void sk_push(float (&stk)[DR][VEC], unsigned int cnt,
 }
 
 template <typename OT, bool VECTOR, int DR>
-__global__ void __launch_bounds__(kSplitThreads) splitk_kernel(const __grid_constant__ SplitArgs a)
+__global__ void __launch_bounds__(kSplitThreads, DR == 1 ? kSplitMinBlocks : 4) splitk_kernel(const __grid_constant__ SplitArgs a)
 {
     constexpr int VEC = VECTOR ? 4 : 1;
     const int lane = threadIdx.x & 31;
