@@ -58,7 +58,8 @@ def cluster_plan_applies(N, M, src):
                                      (70000, 300, False), (20000, 70000, False), (9000, 600, True),
                                      (100000, 65536, False), (40000, 5, True), (31, 3, False),
                                      (4097, 4096, False), (131072, 16384, False), (131072, 131072, False),
-                                     (65536 + 17, 2, False)])
+                                     (65536 + 17, 2, False), (65536, 4096, False), (65537, 4096, False),
+                                     (2, 2, False), (100, 4096, False), (131072, 4097, False)])
 def test_plan_lists_match_oracle(N, M, src, plan_path):
     g = torch.Generator().manual_seed(N * 31 + M)
     idx = torch.randint(0, M, (N,), generator=g, dtype=torch.int32)
