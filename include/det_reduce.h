@@ -183,12 +183,16 @@ det_status det_plan_workspace_size(int64_t N, int64_t M, int32_t with_src_id,
  *  workspace  dev, >= det_plan_workspace_size(N, M, src_id != NULL) bytes,
  *             256-byte aligned; holds the plan's device arrays afterwards.
  *  out_plan   host out-param; release with det_plan_destroy.
- * Steps on the device: destination histogram, exclusive scan, stable LSD
- * radix sort of source rows by destination (after a sort by src_id when
- * given), all integer and exact; then the work list (whole destinations and
- * hot segments).  The call waits once for the stream to read the error flags
- * and the work counts; it is therefore not capturable in a CUDA graph.  The
- * plan is reusable for any x, w, H, dtype and shard split over the same idx.
+ * Steps on the device: a stable sort of the source rows by destination
+ * (after a sort by src_id when given), the destination counts and their
+ * exclusive scan (row_ptr), all integer and exact; then the work list (whole
+ * destinations and hot segments).  Small problems without src_id run as one
+ * kernel on one thread-block cluster, others as counting / scan / scatter
+ * kernels per 8-bit radix digit (opts->plan_path); every method gives the
+ * same arrays.  By default the call waits once for the stream to read the
+ * error flags and the work counts; with opts->async_plan it only enqueues
+ * (see det_plan_status).  The plan is reusable for any x, w, H, dtype and
+ * shard split over the same idx.
  * Errors: DET_ERR_ARG, DET_ERR_WORKSPACE, DET_ERR_UNSUPPORTED,
  * DET_ERR_INDEX_RANGE (an idx outside [0, M)), DET_ERR_ORDER_KEY,
  * DET_ERR_CUDA.  On error *out_plan is NULL.
@@ -202,10 +206,11 @@ det_status det_plan_destroy(det_plan plan);
 
 /*
  * Wait for the plan's kernels on `stream` and report what they found:
- * DET_OK, DET_ERR_INDEX_RANGE, DET_ERR_ORDER_KEY or DET_ERR_TIMEOUT.  For a
- * plan built with async_plan this is where errors surface; afterwards the
- * work counts are known on the host (det_plan_describe).  For a synchronous
- * plan it returns DET_OK.
+ * DET_OK, DET_ERR_INDEX_RANGE or DET_ERR_ORDER_KEY (or DET_ERR_TIMEOUT if a
+ * bounded wait of an earlier reduce with this plan expired).  For a plan
+ * built with async_plan this is where errors surface; afterwards the work
+ * counts are known on the host (det_plan_describe).  For a synchronous plan
+ * it returns DET_OK.
  */
 det_status det_plan_status(det_plan plan, void* stream);
 

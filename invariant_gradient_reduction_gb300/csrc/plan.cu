@@ -410,8 +410,8 @@ units_write_kernel(const int* rstart, const int* rend, long long N, long long M,
 // ------------------------------------------------------------------------
 
 struct PlanLayout {
-    // zeroed at the start of every multi-kernel plan: counters, the work
-    // list's ticket, row_ptr and its look-back status words
+    // zeroed at the start of every multi-kernel plan: counters, row_ptr and
+    // the destinations' run bounds
     size_t counters, row_ptr, rstart, rend, zero_end;
     size_t utot;
     size_t counts, totals, perm, skeys, k32_tmp, v_tmp, k64_a, k64_b, va, vb, seg_units, row_units, finish, total;
