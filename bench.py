@@ -52,6 +52,7 @@ WORKLOADS = {
     "sparse_key_scatter": "sparse_key_scatter Q=16384 K=512 S=65536 zipf=1.1 H=128 bf16 x -> fp32 out",
     "ep_invariance": "ep_invariance T=16384 E=256 top-k=8 H=7168 bf16 x, fp32 w -> bf16 out",
     "splitk": "splitk S=56 R=16384 C=24 fp32 -> fp32",
+    "embedding_backward": "embedding_backward T=32768 tokens V=131072 zipf=1.0 H=4096 bf16 dY, index_add into fp32 grad",
 }
 
 
@@ -323,6 +324,46 @@ def measure_e2e(case, timer, steps, warmup, torch):
             "d2h_bytes_per_step": bo, "ms_per_step": ms, "steps": steps}
 
 
+def measure_index_add(case, timer, steps, warmup, torch):
+    """The embedding backward: det_index_add of dY rows into an fp32 gradient.
+    Compulsory bytes: dY read once, idx once, each touched gradient row read
+    and written once."""
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    dev = case.x.device
+    touched = int((torch.bincount(case.idx.long(), minlength=case.M) > 0).sum().item())
+    cb = case.N * case.H * case.x.element_size() + case.N * 4 + 2 * touched * case.H * 4
+    grad = torch.zeros(case.M, case.H, dtype=torch.float32, device=dev)
+    ws_plan = torch.empty(dr.det_plan_workspace_size(case.N, case.M) + 256, dtype=torch.uint8, device=dev)
+    plan0 = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan, opts=ASYNC)
+    need = dr.det_scatter_workspace_size(plan0, case.H)
+    ws_red = torch.empty(need + 256, dtype=torch.uint8, device=dev) if need else None
+    state = {"plan": plan0}
+
+    def full():
+        p = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan, opts=ASYNC)
+        dr.det_index_add(p, case.x, grad, workspace=ws_red, opts=ASYNC)
+        state["plan"] = p
+
+    ws_fixed = torch.empty_like(ws_plan)
+    plan_fixed = dr.det_reduce_plan(case.idx, case.M, workspace=ws_fixed)
+    ws_atomic = torch.empty(dr.det_atomic_workspace_size(case.M, case.H, torch.float32) + 256, dtype=torch.uint8,
+                            device=dev)
+    t_full, l_full = timer.run(full, steps, warmup)
+    dr.det_plan_status(state["plan"])
+    t_red, _ = timer.run(lambda: dr.det_index_add(plan_fixed, case.x, grad, workspace=ws_red), steps, warmup)
+    t_atom, _ = timer.run(lambda: dr.det_atomic_index_add(case.idx, case.M, case.x, grad, workspace=ws_atomic),
+                          steps, warmup)
+    ms_full, ms_red, ms_atom = statistics.mean(t_full), statistics.mean(t_red), statistics.mean(t_atom)
+    d = plan_fixed.describe()
+    return {"compulsory_bytes": cb, "touched_rows": touched,
+            "plan_index_add": {"ms": ms_full, "gbs": gbs(cb, ms_full)},
+            "index_add_only": {"ms": ms_red, "gbs": gbs(cb, ms_red)},
+            "atomic_index_add": {"ms": ms_atom, "gbs": gbs(cb, ms_atom)},
+            "overhead_vs_atomic": {"index_add_only": ms_red / ms_atom - 1.0, "plan_index_add": ms_full / ms_atom - 1.0},
+            "launches_per_step": l_full / max(1, steps),
+            "plan": {k: v for k, v in d.items() if k not in ("row_ptr", "perm")}}
+
+
 def measure_splitk(timer, steps, warmup, torch, device):
     from invariant_gradient_reduction_gb300 import detreduce as dr
     from invariant_gradient_reduction_gb300 import workloads as wl
@@ -469,6 +510,13 @@ def run_ours(args):
             torch.cuda.empty_cache()
         also["splitk"] = measure_splitk(timer, max(10, min(args.steps, 50)), args.warmup, torch, device)
         also["splitk"]["workload"] = WORKLOADS["splitk"]
+        c3 = make_case("embedding_backward", device)
+        r3 = measure_index_add(c3, timer, max(5, min(args.steps, 30)), args.warmup, torch)
+        r3["frac_index_add_only"] = r3["index_add_only"]["gbs"] / peaks["hbm_gbs"]
+        r3["workload"] = WORKLOADS["embedding_backward"]
+        also["embedding_backward"] = r3
+        del c3
+        torch.cuda.empty_cache()
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:

@@ -255,6 +255,27 @@ det_status det_scatter_reduce(det_plan plan,
                               const det_opts* opts, void* stream);
 
 /*
+ * index_add_ with a deterministic order: the pages name index_add_ as the
+ * deterministic replacement of the atomic scatter_add_ (Megatron-LM
+ * determinism developer reference, section 3.1 op catalog).  Same arguments
+ * as det_scatter_reduce, but `out` is read as well as written: every
+ * destination m with at least one term becomes out[m] + S[m], one binary32
+ * add (round to nearest even) of the canonical sum S[m] to the value already
+ * there (bf16 out is read exactly as binary32), then stored as out_dtype;
+ * destinations without terms are not touched.  Repeated calls accumulate
+ * (e.g. embedding-gradient accumulation over micro-batches) and every call
+ * gives the same bits for the same inputs and the same prior contents.
+ * Runs on the register-staged kernel: opts->gather_path 2 or 3 give
+ * DET_ERR_UNSUPPORTED.  Other errors as det_scatter_reduce.
+ */
+det_status det_index_add(det_plan plan,
+                         const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                         det_dtype x_dtype, int64_t ldx, int64_t H,
+                         const float* w, void* out, int64_t ldo, det_dtype out_dtype,
+                         void* workspace, size_t ws_bytes,
+                         const det_opts* opts, void* stream);
+
+/*
  * det_scatter_reduce without a caller workspace.  The pages describe no such
  * call; it exists for callers that cannot allocate device memory when they
  * call in: code inside a larger runtime whose allocator owns all device
@@ -331,6 +352,20 @@ det_status det_atomic_scatter_reduce(const int32_t* idx, int64_t N, int64_t M,
                                      const float* w, void* out, int64_t ldo, det_dtype out_dtype,
                                      void* workspace, size_t ws_bytes,
                                      const det_opts* opts, void* stream);
+
+/*
+ * NOT DETERMINISTIC -- benchmark baseline only.  The atomic twin of
+ * det_index_add: each term is atomically added to out[idx[i]][h] as it is
+ * (no zeroing), so destinations without terms are untouched.  fp32 out only
+ * (DET_ERR_UNSUPPORTED for bf16).  Arguments and workspace as
+ * det_atomic_scatter_reduce.
+ */
+det_status det_atomic_index_add(const int32_t* idx, int64_t N, int64_t M,
+                                const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                                det_dtype x_dtype, int64_t ldx, int64_t H,
+                                const float* w, void* out, int64_t ldo, det_dtype out_dtype,
+                                void* workspace, size_t ws_bytes,
+                                const det_opts* opts, void* stream);
 
 #ifdef __cplusplus
 }

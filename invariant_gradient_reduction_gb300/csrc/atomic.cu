@@ -117,11 +117,16 @@ det_status det_atomic_workspace_size(int64_t M, int64_t H, det_dtype out_dtype, 
     return DET_OK;
 }
 
-det_status det_atomic_scatter_reduce(const int32_t* idx, int64_t N, int64_t M, const void* const* x_shards,
-                                     const int64_t* shard_rows, int32_t P, det_dtype x_dtype, int64_t ldx, int64_t H,
-                                     const float* w, void* out, int64_t ldo, det_dtype out_dtype, void* workspace,
-                                     size_t ws_bytes, const det_opts* opts, void* stream)
+}  // extern "C"
+
+// det_atomic_scatter_reduce (accumulate = false: out zeroed first) and
+// det_atomic_index_add (true: fp32 out only, added to in place).
+static det_status atomic_impl(const int32_t* idx, int64_t N, int64_t M, const void* const* x_shards,
+                              const int64_t* shard_rows, int32_t P, det_dtype x_dtype, int64_t ldx, int64_t H,
+                              const float* w, void* out, int64_t ldo, det_dtype out_dtype, void* workspace,
+                              size_t ws_bytes, const det_opts* opts, void* stream, bool accumulate)
 {
+    if (accumulate && out_dtype != DET_F32) return DET_ERR_UNSUPPORTED;
     if (N < 0 || M < 0) return DET_ERR_ARG;
     if (N > kMaxRows || M > kMaxRows) return DET_ERR_UNSUPPORTED;
     if (!dtype_ok(x_dtype) || !dtype_ok(out_dtype)) return DET_ERR_DTYPE;
@@ -160,8 +165,9 @@ det_status det_atomic_scatter_reduce(const int32_t* idx, int64_t N, int64_t M, c
     if (out_dtype == DET_F32) {
         a.acc = static_cast<float*>(out);
         a.lda = ldo;
-        DETR_CUDA(cudaMemset2DAsync(out, static_cast<size_t>(ldo) * 4, 0, static_cast<size_t>(H) * 4,
-                                    static_cast<size_t>(M), st));
+        if (!accumulate)
+            DETR_CUDA(cudaMemset2DAsync(out, static_cast<size_t>(ldo) * 4, 0, static_cast<size_t>(H) * 4,
+                                        static_cast<size_t>(M), st));
     } else {
         a.acc = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + 256);
         a.lda = H;
@@ -199,6 +205,26 @@ det_status det_atomic_scatter_reduce(const int32_t* idx, int64_t N, int64_t M, c
         if (bad) return DET_ERR_INDEX_RANGE;
     }
     return DET_OK;
+}
+
+extern "C" {
+
+det_status det_atomic_scatter_reduce(const int32_t* idx, int64_t N, int64_t M, const void* const* x_shards,
+                                     const int64_t* shard_rows, int32_t P, det_dtype x_dtype, int64_t ldx, int64_t H,
+                                     const float* w, void* out, int64_t ldo, det_dtype out_dtype, void* workspace,
+                                     size_t ws_bytes, const det_opts* opts, void* stream)
+{
+    return atomic_impl(idx, N, M, x_shards, shard_rows, P, x_dtype, ldx, H, w, out, ldo, out_dtype, workspace,
+                       ws_bytes, opts, stream, false);
+}
+
+det_status det_atomic_index_add(const int32_t* idx, int64_t N, int64_t M, const void* const* x_shards,
+                                const int64_t* shard_rows, int32_t P, det_dtype x_dtype, int64_t ldx, int64_t H,
+                                const float* w, void* out, int64_t ldo, det_dtype out_dtype, void* workspace,
+                                size_t ws_bytes, const det_opts* opts, void* stream)
+{
+    return atomic_impl(idx, N, M, x_shards, shard_rows, P, x_dtype, ldx, H, w, out, ldo, out_dtype, workspace,
+                       ws_bytes, opts, stream, true);
 }
 
 }  // extern "C"

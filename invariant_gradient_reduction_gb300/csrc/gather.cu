@@ -72,8 +72,8 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
     if (!task_counts(a, &n_tasks, &n_seg)) return;
     for (long long task = static_cast<long long>(blockIdx.x) * kGatherWarps + warp; task < n_tasks;
          task += nwarps) {
-        const long long u = task / a.tile_groups;
-        const int tg = static_cast<int>(task - u * a.tile_groups);
+        int t0, t1;
+        const long long u = task_unit(a, task, n_seg, &t0, &t1);
         const int4 ud = unit_at(a, u, n_seg);
         const int m = ud.x, seg = ud.y;
         const int lo = a.row_ptr[m], hi = a.row_ptr[m + 1];
@@ -83,10 +83,10 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
             end = static_cast<int>(min(static_cast<long long>(beg) + seg_terms, static_cast<long long>(hi)));
         }
         const int n = end - beg;
+        if (a.accumulate && n == 0) continue;  // index_add_ leaves it untouched
         const int nch = (n + kChunk - 1) / kChunk;
         const int nrounds = (nch + S - 1) >> a.S_log2;
-        const int t0 = tg * a.tiles_per_group;
-        const int t1 = min(t0 + a.tiles_per_group, a.ntiles);
+
         bool staged = false;
 
         for (int tile = t0; tile < t1; ++tile) {
@@ -167,7 +167,9 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
             scounter_collapse<VEC>(stk, 32, lane, cnt, res);
             if (slot == 0 && active) {
                 if (seg < 0) {
-                    store_out<OT, VEC>(a.out, static_cast<long long>(m) * a.ldo + e0, res, a.out_vec != 0);
+                    const long long off = static_cast<long long>(m) * a.ldo + e0;
+                    if (!a.accumulate) store_out<OT, VEC>(a.out, off, res, a.out_vec != 0);
+                    else if (n > 0) add_store_out<OT, VEC>(a.out, off, res, a.out_vec != 0);
                 } else {
                     float* o = a.part + static_cast<long long>(ud.z) * a.ldpart + e0;
                     if (VEC % 4 == 0) {
@@ -190,7 +192,7 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
 template <typename OT>
 __global__ void __launch_bounds__(kFinishThreads)
 finish_kernel(const int4* finish, long long n_items, int H, const float* part, long long ldpart, void* out,
-              long long ldo, const int* dev_counters)
+              long long ldo, const int* dev_counters, int accumulate)
 {
     extern __shared__ float fstk[];  // [levels][kFinishThreads]
     pdl_wait();  // the gather pass has written every partial slot
@@ -221,7 +223,8 @@ finish_kernel(const int4* finish, long long n_items, int H, const float* part, l
     }
     float res[1] = {0.0f};
     scounter_collapse<1>(fstk, kFinishThreads, threadIdx.x, cnt, res);
-    store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
+    if (accumulate) add_store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
+    else store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
     }
 }
 
@@ -291,10 +294,13 @@ det_status det_scatter_workspace_size(det_plan plan, int64_t H, size_t* bytes)
     return DET_OK;
 }
 
-det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const int64_t* shard_rows, int32_t P,
-                              det_dtype x_dtype, int64_t ldx, int64_t H, const float* w, void* out, int64_t ldo,
-                              det_dtype out_dtype, void* workspace, size_t ws_bytes, const det_opts* opts,
-                              void* stream)
+}  // extern "C"
+
+// det_scatter_reduce (accumulate = false) and det_index_add (true).
+static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards, const int64_t* shard_rows,
+                                      int32_t P, det_dtype x_dtype, int64_t ldx, int64_t H, const float* w, void* out,
+                                      int64_t ldo, det_dtype out_dtype, void* workspace, size_t ws_bytes,
+                                      const det_opts* opts, void* stream, bool accumulate)
 {
     if (!plan) return DET_ERR_ARG;
     if (!dtype_ok(x_dtype) || !dtype_ok(out_dtype)) return DET_ERR_DTYPE;
@@ -336,6 +342,7 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     a.H = static_cast<int>(H);
     a.g = plan->g;
     const bool dev_counts = !plan->counts_on_host;  // async plan: counts stay on the device
+    a.accumulate = accumulate ? 1 : 0;
     a.seg_units = plan->seg_units;
     a.row_units = plan->row_units;
     a.n_seg = dev_counts ? 0 : plan->n_segments;
@@ -366,8 +373,16 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
     if (opts && opts->tiles_per_task > 0) tpg = std::min(opts->tiles_per_task, a.ntiles);
     a.tiles_per_group = tpg;
     a.tile_groups = static_cast<int>(cdiv(a.ntiles, tpg));
-    a.n_tasks = dev_counts ? (plan->M + 2 * cdiv(plan->N, int64_t(kChunk) << plan->g) + 1) * a.tile_groups
-                           : plan->n_units * a.tile_groups;  // an upper bound when the counts are on the device
+    // A hot segment has 32 * 2^g terms, whatever the average: its tasks get
+    // their own, narrower tile groups (about 16 KB of sources each too).
+    const int64_t seg_terms = int64_t(kChunk) << plan->g;
+    int tpgs = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, 16384 / (seg_terms * tile_bytes))));
+    if (opts && opts->tiles_per_task > 0) tpgs = std::min(opts->tiles_per_task, a.ntiles);
+    a.seg_tiles_per_group = tpgs;
+    a.seg_tile_groups = static_cast<int>(cdiv(a.ntiles, tpgs));
+    const int64_t max_segs_all = 2 * cdiv(plan->N, seg_terms) + 1;
+    a.n_tasks = dev_counts ? plan->M * a.tile_groups + max_segs_all * a.seg_tile_groups  // an upper bound
+                           : plan->n_segments * a.seg_tile_groups + (plan->n_units - plan->n_segments) * a.tile_groups;
 
     // Binary-counter depth: enough levels for the longest unit's rounds.
     const int64_t G = int64_t(1) << plan->g;
@@ -388,6 +403,7 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
                          bulk_plan_tiles(H, xsz, plan->max_row_len, &tile_elems, &tile_stride, &bulk_tiles);
     if (path == 3 && !bulk_ok) return DET_ERR_UNSUPPORTED;
     if (path == 2 && !vec) return DET_ERR_UNSUPPORTED;
+    if (accumulate && path >= 2) return DET_ERR_UNSUPPORTED;  // the register-staged kernel only
     // The register-staged kernel is the default (measured faster on every
     // workload shape); the bulk kernel runs on request.
     if (bulk_ok && path == 3) {
@@ -442,14 +458,33 @@ det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const 
         const float* part = a.part;
         if (out_dtype == DET_BF16)
             DETR_CUDA(launch_after_previous(finish_kernel<__nv_bfloat16>, dim3(fgrid), dim3(kFinishThreads), fsmem, st,
-                                            fin, items, a.H, part, a.ldpart, out, ldo, dc));
+                                            fin, items, a.H, part, a.ldpart, out, ldo, dc, a.accumulate));
         else
             DETR_CUDA(launch_after_previous(finish_kernel<float>, dim3(fgrid), dim3(kFinishThreads), fsmem, st, fin,
-                                            items, a.H, part, a.ldpart, out, ldo, dc));
+                                            items, a.H, part, a.ldpart, out, ldo, dc, a.accumulate));
         DETR_LAUNCHED();
     }
     if (opts && opts->debug_checks) return debug_sync_status(plan, st);
     return DET_OK;
+}
+
+extern "C" {
+
+det_status det_scatter_reduce(det_plan plan, const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                              det_dtype x_dtype, int64_t ldx, int64_t H, const float* w, void* out, int64_t ldo,
+                              det_dtype out_dtype, void* workspace, size_t ws_bytes, const det_opts* opts,
+                              void* stream)
+{
+    return scatter_reduce_impl(plan, x_shards, shard_rows, P, x_dtype, ldx, H, w, out, ldo, out_dtype, workspace,
+                               ws_bytes, opts, stream, false);
+}
+
+det_status det_index_add(det_plan plan, const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                         det_dtype x_dtype, int64_t ldx, int64_t H, const float* w, void* out, int64_t ldo,
+                         det_dtype out_dtype, void* workspace, size_t ws_bytes, const det_opts* opts, void* stream)
+{
+    return scatter_reduce_impl(plan, x_shards, shard_rows, P, x_dtype, ldx, H, w, out, ldo, out_dtype, workspace,
+                               ws_bytes, opts, stream, true);
 }
 
 }  // extern "C"

@@ -83,8 +83,8 @@ gather_async_kernel(const __grid_constant__ GatherArgs a, const __grid_constant_
     if (!task_counts(a, &n_tasks, &n_seg)) return;
     for (long long task = static_cast<long long>(blockIdx.x) * kAsyncWarps + warp; task < n_tasks;
          task += nwarps) {
-        const long long u = task / a.tile_groups;
-        const int tg = static_cast<int>(task - u * a.tile_groups);
+        int t0, t1;
+        const long long u = task_unit(a, task, n_seg, &t0, &t1);
         const int4 ud = unit_at(a, u, n_seg);
         const int m = ud.x, seg = ud.y;
         const int lo = a.row_ptr[m], hi = a.row_ptr[m + 1];
@@ -97,8 +97,7 @@ gather_async_kernel(const __grid_constant__ GatherArgs a, const __grid_constant_
         const int nch = (n + kChunk - 1) / kChunk;
         const int nrounds = (nch + S - 1) >> a.S_log2;
         const int nb = nrounds * kAsyncBatchesPerRound;
-        const int t0 = tg * a.tiles_per_group;
-        const int t1 = min(t0 + a.tiles_per_group, a.ntiles);
+
 
         // stage round r of the list into buffer r & 1: row pointers and weights
         auto stage_round = [&](int r) {

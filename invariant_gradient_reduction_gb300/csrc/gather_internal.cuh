@@ -15,8 +15,10 @@ struct GatherArgs {
     const int4* row_units;
     long long n_seg;      // units below n_seg are hot segments
     long long n_tasks;
-    int tile_groups;      // task groups per unit
+    int tile_groups;      // task groups per whole-row unit
     int tiles_per_group;
+    int seg_tile_groups;  // task groups per hot-segment unit (segments are the longest units)
+    int seg_tiles_per_group;
     int ntiles;           // H-tiles per row
     int H;
     int T_log2;           // lanes per H-tile (row vector count)
@@ -33,6 +35,7 @@ struct GatherArgs {
     float* part;
     long long ldpart;
     const int* dev_counters;  // non-null: read the work counts (and plan errors) from the device
+    int accumulate;           // add to out (index_add_); destinations without terms stay untouched
 };
 
 // Work counts of a launch: from the host, or from the plan's counter block
@@ -46,7 +49,8 @@ __device__ __forceinline__ bool task_counts(const GatherArgs& a, long long* n_ta
         const int* c = a.dev_counters;
         if (c[kCtrErrIndex] | c[kCtrErrDup] | c[kCtrErrTimeout]) return false;
         *n_seg = c[kCtrSegs];
-        *n_tasks = (static_cast<long long>(c[kCtrSegs]) + c[kCtrNormal]) * a.tile_groups;
+        *n_tasks = static_cast<long long>(c[kCtrSegs]) * a.seg_tile_groups +
+                   static_cast<long long>(c[kCtrNormal]) * a.tile_groups;
     }
     return true;
 }
@@ -73,6 +77,29 @@ struct BulkArgs {
     long long ldo;
     int* status;           // counter block; kCtrErrTimeout is set if a bounded wait expires
 };
+
+// Task -> (unit, first and one-past-last H-tile): hot-segment units first,
+// each in seg_tile_groups tasks, then whole-row units in tile_groups tasks.
+__device__ __forceinline__ long long task_unit(const GatherArgs& a, long long task, long long n_seg, int* t0, int* t1)
+{
+    const long long seg_tasks = n_seg * a.seg_tile_groups;
+    long long u;
+    int tg, tpg;
+    if (task < seg_tasks) {
+        u = task / a.seg_tile_groups;
+        tg = static_cast<int>(task - u * a.seg_tile_groups);
+        tpg = a.seg_tiles_per_group;
+    } else {
+        const long long r = task - seg_tasks;
+        const long long ur = r / a.tile_groups;
+        tg = static_cast<int>(r - ur * a.tile_groups);
+        tpg = a.tiles_per_group;
+        u = n_seg + ur;
+    }
+    *t0 = tg * tpg;
+    *t1 = min(*t0 + tpg, a.ntiles);
+    return u;
+}
 
 __device__ __forceinline__ int4 unit_at(const GatherArgs& a, long long u, long long n_seg)
 {

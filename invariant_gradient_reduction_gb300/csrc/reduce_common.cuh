@@ -97,6 +97,35 @@ __device__ __forceinline__ void store_out(void* base, long long off, const float
     }
 }
 
+// Add VEC fp32 values to the OT values already in out and store the sums
+// (index_add_ semantics): out = OT(fl32(out + v)); bf16 reads back exactly.
+template <typename OT, int VEC>
+__device__ __forceinline__ void add_store_out(void* base, long long off, const float* v, bool vec)
+{
+    float old[VEC];
+    if (sizeof(OT) == 4) {
+        const float* o = static_cast<const float*>(base) + off;
+        if (vec && VEC % 4 == 0) {
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4) {
+                const float4 t = *reinterpret_cast<const float4*>(o + e);
+                old[e] = t.x; old[e + 1] = t.y; old[e + 2] = t.z; old[e + 3] = t.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) old[e] = o[e];
+        }
+    } else {
+        const unsigned short* o = static_cast<const unsigned short*>(base) + off;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) old[e] = __uint_as_float(static_cast<uint32_t>(o[e]) << 16);
+    }
+    float sum[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) sum[e] = __fadd_rn(old[e], v[e]);
+    store_out<OT, VEC>(base, off, sum, vec);
+}
+
 // Packed FP32 add (sm_100 and later): one instruction performs two IEEE
 // binary32 adds, each rounded to nearest even on its own, so the bits equal
 // those of two __fadd_rn.  Measured on this GPU over 2^21 random pairs: equal

@@ -79,11 +79,14 @@ def _declare(lib):
         "det_scatter_workspace_size": ([vp, i64, P(sz)], i32),
         "det_scatter_reduce": ([vp, P(vp), P(i64), i32, i32, i64, i64, vp, vp, i64, i32, vp, sz,
                                 P(det_opts), vp], i32),
+        "det_index_add": ([vp, P(vp), P(i64), i32, i32, i64, i64, vp, vp, i64, i32, vp, sz, P(det_opts), vp], i32),
         "det_splitk_reduce": ([vp, i32, i64, i64, vp, i32, P(det_opts), vp], i32),
         "det_hash": ([vp, ctypes.c_uint64, vp, vp], i32),
         "det_atomic_workspace_size": ([i64, i64, i32, P(sz)], i32),
         "det_atomic_scatter_reduce": ([vp, i64, i64, P(vp), P(i64), i32, i32, i64, i64, vp, vp, i64, i32, vp,
                                        sz, P(det_opts), vp], i32),
+        "det_atomic_index_add": ([vp, i64, i64, P(vp), P(i64), i32, i32, i64, i64, vp, vp, i64, i32, vp,
+                                  sz, P(det_opts), vp], i32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -268,9 +271,19 @@ def _shards(x: Union[torch.Tensor, Sequence[torch.Tensor]]):
     return ptrs, rows, len(xs), _TORCH_TO_DET[dt], ldx, H
 
 
+def det_index_add(plan: Plan, x, out: torch.Tensor, w: Optional[torch.Tensor] = None,
+                  opts: Optional[dict] = None, stream=None, workspace: Optional[torch.Tensor] = None):
+    """out[m] += canonical sum of w[i] * x[i] over the sources of m (one fp32 add; rows without sources untouched)."""
+    return _reduce_call("det_index_add", plan, x, out, w, opts, stream, workspace)
+
+
 def det_scatter_reduce(plan: Plan, x, out: torch.Tensor, w: Optional[torch.Tensor] = None,
                        opts: Optional[dict] = None, stream=None, workspace: Optional[torch.Tensor] = None):
     """out[m] = canonical sum of w[i] * x[i] over the sources of m (x: tensor or list of shards)."""
+    return _reduce_call("det_scatter_reduce", plan, x, out, w, opts, stream, workspace)
+
+
+def _reduce_call(name, plan, x, out, w, opts, stream, workspace):
     ptrs, rows, P, xdt, ldx, H = _shards(x)
     ldo, Ho = _rows(out)
     if Ho != H or out.shape[0] != plan.M:
@@ -281,10 +294,9 @@ def det_scatter_reduce(plan: Plan, x, out: torch.Tensor, w: Optional[torch.Tenso
         raise ValueError("w must be a contiguous float32 tensor")
     need = det_scatter_workspace_size(plan, H)
     ws = _workspace(need, out.device, workspace) if need > 0 else None
-    _check(lib().det_scatter_reduce(plan.handle, ptrs, rows, P, xdt, ldx, H, _ptr(w), _ptr(out), ldo,
-                                    _TORCH_TO_DET[out.dtype], _aligned_ptr(ws) if ws is not None else None,
-                                    _aligned_bytes(ws) if ws is not None else 0, _opts(opts), _stream(stream)),
-           "det_scatter_reduce")
+    _check(getattr(lib(), name)(plan.handle, ptrs, rows, P, xdt, ldx, H, _ptr(w), _ptr(out), ldo,
+                                _TORCH_TO_DET[out.dtype], _aligned_ptr(ws) if ws is not None else None,
+                                _aligned_bytes(ws) if ws is not None else 0, _opts(opts), _stream(stream)), name)
     return out
 
 
@@ -323,15 +335,25 @@ def det_atomic_workspace_size(M: int, H: int, out_dtype: torch.dtype) -> int:
 def det_atomic_scatter_reduce(idx: torch.Tensor, M: int, x, out: torch.Tensor, w: Optional[torch.Tensor] = None,
                               opts: Optional[dict] = None, stream=None, workspace: Optional[torch.Tensor] = None):
     """NOT deterministic: the atomicAdd scatter-add baseline (same arguments as det_scatter_reduce)."""
+    return _atomic_call("det_atomic_scatter_reduce", idx, M, x, out, w, opts, stream, workspace)
+
+
+def det_atomic_index_add(idx: torch.Tensor, M: int, x, out: torch.Tensor, w: Optional[torch.Tensor] = None,
+                         opts: Optional[dict] = None, stream=None, workspace: Optional[torch.Tensor] = None):
+    """NOT deterministic: atomicAdd into out as it is (the twin of det_index_add); fp32 out only."""
+    return _atomic_call("det_atomic_index_add", idx, M, x, out, w, opts, stream, workspace)
+
+
+def _atomic_call(name, idx, M, x, out, w, opts, stream, workspace):
     ptrs, rows, P, xdt, ldx, H = _shards(x)
     ldo, Ho = _rows(out)
     if Ho != H or out.shape[0] != M:
         raise ValueError("out must be [M, H]")
     need = det_atomic_workspace_size(M, H, out.dtype)
     ws = _workspace(need, out.device, workspace)
-    _check(lib().det_atomic_scatter_reduce(_ptr(idx), idx.numel(), M, ptrs, rows, P, xdt, ldx, H, _ptr(w), _ptr(out),
-                                           ldo, _TORCH_TO_DET[out.dtype], _aligned_ptr(ws), _aligned_bytes(ws),
-                                           _opts(opts), _stream(stream)), "det_atomic_scatter_reduce")
+    _check(getattr(lib(), name)(_ptr(idx), idx.numel(), M, ptrs, rows, P, xdt, ldx, H, _ptr(w), _ptr(out), ldo,
+                                _TORCH_TO_DET[out.dtype], _aligned_ptr(ws), _aligned_bytes(ws), _opts(opts),
+                                _stream(stream)), name)
     return out
 
 

@@ -150,6 +150,25 @@ def sparse_key_scatter(Q: int, K: int, S: int, H: int, zipf_s: float = 1.1, sigm
                        meta={"Q": Q, "K": K, "S": S, "zipf_s": zipf_s})
 
 
+def embedding_backward(T: int, V: int, H: int, zipf_s: float = 1.0, sigma: float = 0.02, seed: int = 6,
+                       device="cpu", x_dtype=torch.bfloat16, name: Optional[str] = None) -> ScatterCase:
+    """Token-embedding backward: the output gradients dY [T, H] of T tokens are
+    added into the fp32 weight gradient [V, H] at each token's id (index_add_).
+
+    Token ids are drawn with replacement from Zipf(zipf_s) over the vocabulary
+    (rank r with probability proportional to r^-s, the usual shape of token
+    frequencies), ranks mapped to ids by a seeded random permutation.
+    """
+    g = _cpu_gen(seed)
+    p = torch.arange(1, V + 1, dtype=torch.float64) ** (-zipf_s)
+    ranks = torch.multinomial(p / p.sum(), T, replacement=True, generator=g)
+    ids = torch.randperm(V, generator=g)[ranks].to(torch.int32)
+    x = _fill_normal((T, H), x_dtype, sigma, seed * 7919 + 7, device)
+    return ScatterCase(name=name or f"embedding_backward T={T} V={V} H={H} zipf={zipf_s}",
+                       idx=ids.to(device), x=x, w=None, M=V, out_dtype=torch.float32,
+                       meta={"T": T, "V": V, "zipf_s": zipf_s, "accumulate": True})
+
+
 def splitk_partials(S: int, R: int, C: int, seed: int = 5, device="cpu") -> torch.Tensor:
     """float32 [S, R*C] with values z * 2^U, z ~ N(0,1), U ~ Uniform[-8, 8)."""
     g = _dev_gen(seed * 7919 + 11, device)
@@ -168,6 +187,8 @@ FULL = {
                           out_dtype=torch.bfloat16, seed=3),
     "sparse_key_scatter": dict(kind="sparse", Q=16384, K=512, S=65536, H=128, zipf_s=1.1, sigma=0.02, seed=4),
     "splitk": dict(kind="splitk", S=56, R=16384, C=24, seed=5),
+    # beyond the five: the embedding backward (index_add_ into a 128K-row gradient)
+    "embedding_backward": dict(kind="embedding", T=32768, V=131072, H=4096, zipf_s=1.0, sigma=0.02, seed=6),
 }
 
 SMALL = {
@@ -178,6 +199,7 @@ SMALL = {
                           out_dtype=torch.bfloat16, seed=13),
     "sparse_key_scatter": dict(kind="sparse", Q=640, K=128, S=4096, H=128, zipf_s=1.1, sigma=0.02, seed=14),
     "splitk": dict(kind="splitk", S=56, R=1000, C=24, seed=15),
+    "embedding_backward": dict(kind="embedding", T=3000, V=2048, H=200, zipf_s=1.0, sigma=0.02, seed=16),
 }
 
 
@@ -190,6 +212,7 @@ MEDIUM = {
                           out_dtype=torch.bfloat16, seed=23),
     "tiny_moe": FULL["tiny_moe"],
     "splitk": FULL["splitk"],
+    "embedding_backward": dict(kind="embedding", T=8192, V=131072, H=4096, zipf_s=1.0, sigma=0.02, seed=26),
 }
 
 
@@ -201,6 +224,8 @@ def make(name: str, size: str = "full", device="cpu"):
         return moe_combine(device=device, name=f"{name}[{size}]", **spec)
     if kind == "sparse":
         return sparse_key_scatter(device=device, name=f"{name}[{size}]", **spec)
+    if kind == "embedding":
+        return embedding_backward(device=device, name=f"{name}[{size}]", **spec)
     return splitk_partials(spec["S"], spec["R"], spec["C"], seed=spec["seed"], device=device)
 
 
@@ -232,4 +257,4 @@ def cdiv(a: int, b: int) -> int:
 
 
 __all__ = ["ScatterCase", "moe_routing", "moe_combine", "zipf_key_lists", "sparse_key_scatter",
-           "splitk_partials", "FULL", "MEDIUM", "SMALL", "make", "ep_shard_rows", "split_rows", "round_up", "cdiv"]
+           "embedding_backward", "splitk_partials", "FULL", "MEDIUM", "SMALL", "make", "ep_shard_rows", "split_rows", "round_up", "cdiv"]

@@ -61,6 +61,8 @@ def _load():
         lib.oracle_build_lists.restype = ctypes.c_int
         lib.oracle_scatter_reduce.argtypes = [vp, vp, i64, i64, vp, vp, i32, i32, i64, i64, vp, vp, i64, i32]
         lib.oracle_scatter_reduce.restype = ctypes.c_int
+        lib.oracle_index_add.argtypes = [vp, vp, i64, i64, vp, vp, i32, i32, i64, i64, vp, vp, i64, i32]
+        lib.oracle_index_add.restype = ctypes.c_int
         lib.oracle_splitk_reduce.argtypes = [vp, i32, i64, i64, vp, i32]
         lib.oracle_splitk_reduce.restype = ctypes.c_int
         lib.oracle_mix64.argtypes = [u64]
@@ -127,8 +129,13 @@ def build_lists(idx, M: int, src_id=None):
     return row_ptr, perm[:N]
 
 
-def scatter_reduce(idx, x_shards, M: int, w=None, out_dtype: int = F32, src_id=None, H: int | None = None):
+def scatter_reduce(idx, x_shards, M: int, w=None, out_dtype: int = F32, src_id=None, H: int | None = None,
+                   out_init=None):
     """out[m] = canonical sum over {i : idx[i] = m} of w[i] * x[i] (rows in order-key order).
+
+    With ``out_init`` (float32 or uint16 bf16 bits [M, H]) the call has
+    index_add_ semantics: every destination with terms becomes
+    out_init[m] + sum (one binary32 add), the others keep out_init[m].
 
     ``x_shards`` is one 2-D array or a list of 2-D arrays (rows of consecutive
     global source ranges), all float32 or all uint16 (bf16 bits), rows
@@ -151,10 +158,15 @@ def scatter_reduce(idx, x_shards, M: int, w=None, out_dtype: int = F32, src_id=N
     ptrs = (ctypes.c_void_p * len(shards))(*[s.ctypes.data for s in shards])
     wv = None if w is None else np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
     sid = None if src_id is None else np.ascontiguousarray(src_id, dtype=np.int64).reshape(-1)
-    out = np.empty((M, H), dtype=np.float32 if out_dtype == F32 else np.uint16)
-    rc = _load().oracle_scatter_reduce(_ptr(idx), _ptr(sid), N, M, ctypes.cast(ptrs, ctypes.c_void_p),
-                                       _ptr(rows), len(shards), code, ldx, H, _ptr(wv), _ptr(out), H,
-                                       out_dtype)
+    odt = np.float32 if out_dtype == F32 else np.uint16
+    if out_init is None:
+        out = np.empty((M, H), dtype=odt)
+        fn = _load().oracle_scatter_reduce
+    else:
+        out = np.array(out_init, dtype=odt, copy=True).reshape(M, H)
+        fn = _load().oracle_index_add
+    rc = fn(_ptr(idx), _ptr(sid), N, M, ctypes.cast(ptrs, ctypes.c_void_p), _ptr(rows), len(shards), code, ldx, H,
+            _ptr(wv), _ptr(out), H, out_dtype)
     if rc != 0:
         raise OracleError(rc, "scatter_reduce")
     return out

@@ -219,10 +219,10 @@ static void or_store(void* base, int32_t dtype, int64_t off, float v)
  * order key is global, so the result cannot depend on P (the EP-size
  * invariance of the interview notes' "why pay the overhead" section).
  */
-int oracle_scatter_reduce(const int32_t* idx, const int64_t* src_id, int64_t N, int64_t M,
-                          const void* const* x_shards, const int64_t* shard_rows, int32_t P,
-                          int32_t x_dtype, int64_t ldx, int64_t H, const float* w,
-                          void* out, int64_t ldo, int32_t out_dtype)
+static int or_scatter(const int32_t* idx, const int64_t* src_id, int64_t N, int64_t M,
+                      const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                      int32_t x_dtype, int64_t ldx, int64_t H, const float* w,
+                      void* out, int64_t ldo, int32_t out_dtype, int accumulate)
 {
     if (N < 0 || M < 0 || H < 0 || P < 1 || ldx < H || ldo < H || (M > 0 && H > 0 && !out))
         return OR_ERR_ARG;
@@ -261,12 +261,41 @@ int oracle_scatter_reduce(const int32_t* idx, const int64_t* src_id, int64_t N, 
                 float p = w ? w[i] * xv : xv;
                 terms[j] = p;
             }
-            or_store(out, out_dtype, m * ldo + h, or_canonical_sum_buf(terms, n, level));
+            float sum = or_canonical_sum_buf(terms, n, level);
+            if (accumulate) {
+                if (n == 0) continue;                       /* untouched */
+                sum = or_load(out, out_dtype, m * ldo + h) + sum;  /* one binary32 add */
+            }
+            or_store(out, out_dtype, m * ldo + h, sum);
         }
     }
     free(terms); free(level);
     free(row_ptr); free(perm); free(shard_of); free(local_of);
     return rc;
+}
+
+int oracle_scatter_reduce(const int32_t* idx, const int64_t* src_id, int64_t N, int64_t M,
+                          const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                          int32_t x_dtype, int64_t ldx, int64_t H, const float* w,
+                          void* out, int64_t ldo, int32_t out_dtype)
+{
+    return or_scatter(idx, src_id, N, M, x_shards, shard_rows, P, x_dtype, ldx, H, w, out, ldo, out_dtype, 0);
+}
+
+/*
+ * index_add_ semantics (Megatron-LM determinism developer reference, section
+ * 3.1 op catalog: index_add_ is the deterministic replacement of the atomic
+ * scatter_add_): each destination with at least one term becomes
+ * out[m] + S[m], one binary32 add of the canonical sum S[m] to the value
+ * already there, then stored as out_dtype; destinations without terms are
+ * left as they are.
+ */
+int oracle_index_add(const int32_t* idx, const int64_t* src_id, int64_t N, int64_t M,
+                     const void* const* x_shards, const int64_t* shard_rows, int32_t P,
+                     int32_t x_dtype, int64_t ldx, int64_t H, const float* w,
+                     void* out, int64_t ldo, int32_t out_dtype)
+{
+    return or_scatter(idx, src_id, N, M, x_shards, shard_rows, P, x_dtype, ldx, H, w, out, ldo, out_dtype, 1);
 }
 
 /*

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import assert_bytes_equal, gpu_scatter, np_bits, oracle_scatter
+from helpers import assert_bytes_equal, case_np, gpu_scatter, np_bits, oracle_dtype, oracle_scatter
 from invariant_gradient_reduction_gb300 import detreduce as dr
 from invariant_gradient_reduction_gb300 import workloads as wl
 from invariant_gradient_reduction_gb300.workloads import ScatterCase
@@ -571,3 +571,80 @@ def test_async_plan_errors_reported_and_nothing_written():
     # a waited plan reports OK from det_plan_status
     plan = dr.det_reduce_plan(torch.tensor([0, 1], dtype=torch.int32, device=DEV), 2)
     dr.det_plan_status(plan)
+
+
+# --------------------------------------------------------------------------
+# det_index_add: index_add_ semantics, out += canonical sum
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", SCATTER_SMALL + ["embedding_backward"])
+def test_index_add_matches_oracle(name):
+    case = small_case(name)
+    g = torch.Generator(device=DEV).manual_seed(99)
+    init = (torch.randn(case.M, case.H, generator=g, device=DEV) * 3).to(case.out_dtype)
+    init[case.M - 1] = -0.0  # an empty destination (if any) must keep its bits
+    out = init.clone()
+    plan = dr.det_reduce_plan(case.idx, case.M, src_id=case.src_id)
+    dr.det_index_add(plan, case.x, out, w=case.w)
+    idx, x, w, sid = case_np(case)
+    want = oracle.scatter_reduce(idx, x, case.M, w=w, src_id=sid, out_dtype=oracle_dtype(case.out_dtype),
+                                 out_init=np_bits(init))
+    assert_bytes_equal(np_bits(out), want, f"{name} index_add")
+    # a second call adds the same sums once more, on any grid and with an unwaited plan
+    plan2 = dr.det_reduce_plan(case.idx, case.M, src_id=case.src_id, opts={"async_plan": 1})
+    dr.det_index_add(plan2, case.x, out, w=case.w, opts={"async_plan": 1, "grid_ctas": 5})
+    dr.det_plan_status(plan2)
+    want2 = oracle.scatter_reduce(idx, x, case.M, w=w, src_id=sid, out_dtype=oracle_dtype(case.out_dtype),
+                                  out_init=want)
+    assert_bytes_equal(np_bits(out), want2, f"{name} index_add twice")
+
+
+def test_index_add_empty_rows_untouched_and_paths():
+    idx = torch.tensor([0, 2, 2, 5], dtype=torch.int32, device=DEV)
+    M, H = 8, 16
+    x = torch.randn(4, H, device=DEV)
+    init = torch.randn(M, H, device=DEV)
+    init[0] = -0.0
+    init[1] = float("nan")  # untouched rows keep any bit pattern
+    init[3] = -0.0
+    out = init.clone()
+    plan = dr.det_reduce_plan(idx, M)
+    dr.det_index_add(plan, x, out)
+    untouched = [1, 3, 4, 6, 7]
+    assert out[untouched].view(torch.int32).equal(init[untouched].view(torch.int32))
+    want = oracle.scatter_reduce(idx.cpu().numpy(), x.cpu().numpy(), M, out_init=init.cpu().numpy())
+    assert_bytes_equal(np_bits(out), want, "index_add small")
+    for path in (2, 3):
+        with pytest.raises(dr.DetError) as e:
+            dr.det_index_add(plan, x, out, opts={"gather_path": path})
+        assert e.value.code == dr.DET_ERR_UNSUPPORTED
+
+
+def test_embedding_backward_index_add():
+    """Token-embedding backward (Zipf token ids, hot rows): det_index_add into an
+    fp32 gradient, twice, against the oracle; the atomic twin stays within the
+    reordering bound."""
+    case = small_case("embedding_backward")
+    g = torch.Generator(device=DEV).manual_seed(5)
+    grad = torch.randn(case.M, case.H, generator=g, device=DEV) * 1e-3
+    init = grad.clone()
+    plan = dr.det_reduce_plan(case.idx, case.M)
+    assert plan.describe()["n_hot_rows"] >= 1
+    dr.det_index_add(plan, case.x, grad)
+    idx, x, w, sid = case_np(case)
+    want = oracle.scatter_reduce(idx, x, case.M, out_init=init.cpu().numpy())
+    assert_bytes_equal(np_bits(grad), want, "embedding index_add")
+    dr.det_index_add(plan, case.x, grad)
+    want2 = oracle.scatter_reduce(idx, x, case.M, out_init=want)
+    assert_bytes_equal(np_bits(grad), want2, "embedding index_add twice")
+    # the atomic twin adds in scheduler order: close, not bit-equal in general
+    ga = init.clone()
+    dr.det_atomic_index_add(case.idx, case.M, case.x, ga, opts={"debug_checks": 1})
+    counts = np.bincount(idx, minlength=case.M)[:, None]
+    absum = np.abs(init.cpu().numpy().astype(np.float64))
+    np.add.at(absum, idx, np.abs(np_bits(case.x.float()).astype(np.float64)))
+    bound = 2 * (counts + 2) * 2.0 ** -24 * absum + 1e-30
+    assert np.all(np.abs(np_bits(ga).astype(np.float64) - want.astype(np.float64)) <= bound)
+    with pytest.raises(dr.DetError) as e:
+        dr.det_atomic_index_add(case.idx, case.M, case.x, grad.to(torch.bfloat16))
+    assert e.value.code == dr.DET_ERR_UNSUPPORTED

@@ -522,3 +522,62 @@ def test_hash_structure(oracle_mod):
     # byte order inside a word: bytes b0..b7 form the word sum b_k 256^k
     one = np.array([1, 0, 0, 0, 0, 0, 0, 0], np.uint8)
     assert o.hash_bytes(one) == (o.mix64(8 ^ C0) + o.mix64(1)) % 2 ** 64
+
+
+# --------------------------------------------------------------------------
+# index_add_ semantics (Megatron-LM determinism developer reference, section
+# 3.1 op catalog: index_add_ replaces the atomic scatter_add_)
+# --------------------------------------------------------------------------
+
+def test_index_add_exact_integers(oracle_mod):
+    """Small integers: every add is exact, so the result is the integer sum
+    out_init + sum of terms, and destinations without terms keep their bits."""
+    rng = np.random.default_rng(11)
+    N, M, H = 500, 40, 6
+    idx = rng.integers(0, M - 5, size=N).astype(np.int32)  # the last 5 destinations get no term
+    x = rng.integers(-8, 9, size=(N, H)).astype(np.float32)
+    w = rng.integers(-3, 4, size=N).astype(np.float32)
+    init = rng.integers(-1000, 1001, size=(M, H)).astype(np.float32)
+    init[-1, 0] = -0.0
+    init[-2, 1] = np.float32(np.nan)
+    got = oracle_mod.scatter_reduce(idx, x, M, w=w, out_init=init)
+    want = init.astype(np.float64).copy()
+    for i in range(N):
+        want[idx[i]] += float(w[i]) * x[i]
+    touched = np.zeros(M, bool)
+    touched[idx] = True
+    assert np.array_equal(got[touched], want[touched].astype(np.float32))
+    assert got[~touched].tobytes() == init[~touched].tobytes()  # -0.0 and the NaN pattern kept
+
+
+def test_index_add_is_one_add_of_the_canonical_sum(oracle_mod):
+    """From +0.0 it equals the plain scatter-reduce on touched destinations; a
+    second call adds the same canonical sums once more (x + S, not a refold)."""
+    rng = np.random.default_rng(12)
+    N, M, H = 700, 9, 5
+    idx = rng.integers(0, M, size=N).astype(np.int32)
+    x = (rng.standard_normal((N, H)) * 2.0 ** rng.integers(-8, 8, size=(N, 1))).astype(np.float32)
+    S = oracle_mod.scatter_reduce(idx, x, M)
+    zero = np.zeros((M, H), np.float32)
+    first = oracle_mod.scatter_reduce(idx, x, M, out_init=zero)
+    assert first.tobytes() == S.tobytes()
+    second = oracle_mod.scatter_reduce(idx, x, M, out_init=first)
+    assert second.tobytes() == (S + S).astype(np.float32).tobytes()  # numpy float32 add: one rounding
+    refold = oracle_mod.scatter_reduce(np.concatenate([idx, idx]), np.concatenate([x, x]), M)
+    assert not np.array_equal(second, refold)  # folding 2N terms is a different order
+
+
+def test_index_add_bf16_out_rounds_once(oracle_mod):
+    """bf16 out: the old value widens exactly, the binary32 add rounds, then one
+    RNE cast to bf16; checked against torch's CPU bf16 conversion."""
+    rng = np.random.default_rng(13)
+    N, M, H = 300, 7, 4
+    idx = rng.integers(0, M, size=N).astype(np.int32)
+    x = rng.standard_normal((N, H)).astype(np.float32)
+    init_f = rng.standard_normal((M, H)).astype(np.float32) * 100
+    init_b = torch.from_numpy(init_f).to(torch.bfloat16)
+    init_bits = init_b.view(torch.int16).numpy().view(np.uint16)
+    got = oracle_mod.scatter_reduce(idx, x, M, out_dtype=oracle_mod.BF16, out_init=init_bits)
+    S = oracle_mod.scatter_reduce(idx, x, M)
+    want = (torch.from_numpy(init_b.float().numpy() + S)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert got.tobytes() == want.tobytes()
