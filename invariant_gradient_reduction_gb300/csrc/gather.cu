@@ -345,7 +345,7 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
     a.accumulate = accumulate ? 1 : 0;
     a.seg_units = plan->seg_units;
     a.row_units = plan->row_units;
-    a.n_seg = dev_counts ? 0 : plan->n_segments;
+    a.n_seg = dev_counts ? 0 : plan->n_segments + plan->n_long;
     a.dev_counters = dev_counts ? plan->counters : nullptr;
     const int64_t n_units = dev_counts ? std::max<int64_t>(1, M) : plan->n_units;  // estimate when unknown
     a.row_ptr = plan->row_ptr;
@@ -373,7 +373,8 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
     if (opts && opts->tiles_per_task > 0) tpg = std::min(opts->tiles_per_task, a.ntiles);
     a.tiles_per_group = tpg;
     a.tile_groups = static_cast<int>(cdiv(a.ntiles, tpg));
-    // A hot segment has 32 * 2^g terms, whatever the average: its tasks get
+    // A hot segment has 32 * 2^g terms, whatever the average: its tasks, and
+    // those of the long rows (2..2^g chunks) listed after the segments, get
     // their own, narrower tile groups (about 16 KB of sources each too).
     const int64_t seg_terms = int64_t(kChunk) << plan->g;
     int tpgs = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, 16384 / (seg_terms * tile_bytes))));
@@ -381,8 +382,9 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
     a.seg_tiles_per_group = tpgs;
     a.seg_tile_groups = static_cast<int>(cdiv(a.ntiles, tpgs));
     const int64_t max_segs_all = 2 * cdiv(plan->N, seg_terms) + 1;
-    a.n_tasks = dev_counts ? plan->M * a.tile_groups + max_segs_all * a.seg_tile_groups  // an upper bound
-                           : plan->n_segments * a.seg_tile_groups + (plan->n_units - plan->n_segments) * a.tile_groups;
+    const int64_t max_tg = std::max(a.tile_groups, a.seg_tile_groups);
+    a.n_tasks = dev_counts ? plan->M * max_tg + max_segs_all * a.seg_tile_groups  // an upper bound
+                           : a.n_seg * a.seg_tile_groups + (plan->n_units - a.n_seg) * a.tile_groups;
 
     // Binary-counter depth: enough levels for the longest unit's rounds.
     const int64_t G = int64_t(1) << plan->g;

@@ -13,7 +13,7 @@ namespace detr {
 struct GatherArgs {
     const int4* seg_units;
     const int4* row_units;
-    long long n_seg;      // units below n_seg are hot segments
+    long long n_seg;      // units below n_seg have more than one chunk (hot segments, then long rows)
     long long n_tasks;
     int tile_groups;      // task groups per whole-row unit
     int tiles_per_group;
@@ -48,9 +48,9 @@ __device__ __forceinline__ bool task_counts(const GatherArgs& a, long long* n_ta
     if (a.dev_counters) {
         const int* c = a.dev_counters;
         if (c[kCtrErrIndex] | c[kCtrErrDup] | c[kCtrErrTimeout]) return false;
-        *n_seg = c[kCtrSegs];
-        *n_tasks = static_cast<long long>(c[kCtrSegs]) * a.seg_tile_groups +
-                   static_cast<long long>(c[kCtrNormal]) * a.tile_groups;
+        *n_seg = c[kCtrBig];
+        *n_tasks = static_cast<long long>(c[kCtrBig]) * a.seg_tile_groups +
+                   static_cast<long long>(c[kCtrShort]) * a.tile_groups;
     }
     return true;
 }
@@ -78,8 +78,9 @@ struct BulkArgs {
     int* status;           // counter block; kCtrErrTimeout is set if a bounded wait expires
 };
 
-// Task -> (unit, first and one-past-last H-tile): hot-segment units first,
-// each in seg_tile_groups tasks, then whole-row units in tile_groups tasks.
+// Task -> (unit, first and one-past-last H-tile): the units of more than one
+// chunk first (hot segments, then long rows), each in seg_tile_groups tasks,
+// then the short whole-row units in tile_groups tasks.
 __device__ __forceinline__ long long task_unit(const GatherArgs& a, long long task, long long n_seg, int* t0, int* t1)
 {
     const long long seg_tasks = n_seg * a.seg_tile_groups;

@@ -307,79 +307,87 @@ row_bounds_kernel(const int* skeys, long long N, long long M, int* rstart, int* 
 // The work list in three kernels (no CTA waits for another), over tiles of
 // kUnitThreads destinations, one per thread:
 //   units_count_kernel  each tile's totals: sources (row lengths), hot
-//                       segments, whole-row units, finish tasks; and the
-//                       longest list;
-//   units_scan_kernel   one CTA: exclusive scans of the four totals over the
+//                       segments, long and short whole-row units, finish
+//                       tasks; and the longest list;
+//   units_scan_kernel   one CTA: exclusive scans of the five totals over the
 //                       tiles, and the grand totals into the counter block;
 //   units_write_kernel  row_ptr, and the units: hot rows (more than 2^g
 //                       chunks) give `seg` segment units and one finish task,
-//                       the others one whole-row unit.
+//                       rows of 2..2^g chunks a long whole-row unit (listed
+//                       after the segments), the others a short one.
+constexpr int kUnitVals = 5;  // sources, segments, long rows, short rows, finish tasks
+
 struct RowClass {
-    int len, seg, whole, fin;
+    int v[kUnitVals];
 };
 
 __device__ __forceinline__ RowClass classify_row(const int* rstart, const int* rend, long long m, long long M, int g)
 {
-    RowClass r{0, 0, 0, 0};
+    RowClass r{{0, 0, 0, 0, 0}};
     if (m < M) {
-        r.len = rend[m] - rstart[m];
-        const int nch = (r.len + kChunk - 1) / kChunk;
+        r.v[0] = rend[m] - rstart[m];
+        const int nch = (r.v[0] + kChunk - 1) / kChunk;
         if (nch > (1 << g)) {
-            r.seg = (nch + (1 << g) - 1) >> g;
-            r.fin = 1;
+            r.v[1] = (nch + (1 << g) - 1) >> g;
+            r.v[4] = 1;
+        } else if (nch > 1) {
+            r.v[2] = 1;
         } else {
-            r.whole = 1;
+            r.v[3] = 1;
         }
     }
     return r;
 }
 
 __global__ void __launch_bounds__(kUnitThreads)
-units_count_kernel(const int* rstart, const int* rend, long long M, int g, int4* tile_tot, int* counters)
+units_count_kernel(const int* rstart, const int* rend, long long M, int g, int* tile_tot, int* counters)
 {
     __shared__ int ws[kUnitThreads / 32 + 1];
     if (counters[kCtrErrIndex]) return;
     const long long m = static_cast<long long>(blockIdx.x) * kUnitThreads + threadIdx.x;
     const RowClass r = classify_row(rstart, rend, m, M, g);
-    const int mx = __reduce_max_sync(0xffffffffu, r.len);
+    const int mx = __reduce_max_sync(0xffffffffu, r.v[0]);
     if ((threadIdx.x & 31) == 0 && mx > 0) atomicMax(&counters[kCtrMaxLen], mx);
-    int t[4];
-    block_excl_scan<kUnitThreads>(r.len, ws, &t[0]);
-    block_excl_scan<kUnitThreads>(r.seg, ws, &t[1]);
-    block_excl_scan<kUnitThreads>(r.whole, ws, &t[2]);
-    block_excl_scan<kUnitThreads>(r.fin, ws, &t[3]);
-    if (threadIdx.x == 0) tile_tot[blockIdx.x] = make_int4(t[0], t[1], t[2], t[3]);
+#pragma unroll
+    for (int j = 0; j < kUnitVals; ++j) {
+        int t;
+        block_excl_scan<kUnitThreads>(r.v[j], ws, &t);
+        if (threadIdx.x == 0) tile_tot[static_cast<long long>(blockIdx.x) * kUnitVals + j] = t;
+    }
 }
 
 constexpr int kUnitScanThreads = 1024;
 
 __global__ void __launch_bounds__(kUnitScanThreads)
-units_scan_kernel(int4* tile_tot, int nut, int* counters)
+units_scan_kernel(int* tile_tot, int nut, int* counters)
 {
     __shared__ int ws[kUnitScanThreads / 32 + 1];
     if (counters[kCtrErrIndex]) return;
-    int carry[4] = {0, 0, 0, 0};
+    int carry[kUnitVals] = {0, 0, 0, 0, 0};
     for (int t0 = 0; t0 < nut; t0 += kUnitScanThreads) {
         const int t = t0 + threadIdx.x;
-        const int4 v = t < nut ? tile_tot[t] : make_int4(0, 0, 0, 0);
-        int tot[4];
-        const int e0 = block_excl_scan<kUnitScanThreads>(v.x, ws, &tot[0]);
-        const int e1 = block_excl_scan<kUnitScanThreads>(v.y, ws, &tot[1]);
-        const int e2 = block_excl_scan<kUnitScanThreads>(v.z, ws, &tot[2]);
-        const int e3 = block_excl_scan<kUnitScanThreads>(v.w, ws, &tot[3]);
-        if (t < nut) tile_tot[t] = make_int4(carry[0] + e0, carry[1] + e1, carry[2] + e2, carry[3] + e3);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) carry[j] += tot[j];
+        for (int j = 0; j < kUnitVals; ++j) {
+            int* slot = tile_tot + static_cast<long long>(t) * kUnitVals + j;
+            const int v = t < nut ? *slot : 0;
+            int tot;
+            const int e = block_excl_scan<kUnitScanThreads>(v, ws, &tot);
+            if (t < nut) *slot = carry[j] + e;
+            carry[j] += tot;
+        }
     }
     if (threadIdx.x == 0) {
         counters[kCtrSegs] = carry[1];
-        counters[kCtrNormal] = carry[2];
-        counters[kCtrHot] = carry[3];
+        counters[kCtrLong] = carry[2];
+        counters[kCtrNormal] = carry[2] + carry[3];
+        counters[kCtrHot] = carry[4];
+        counters[kCtrBig] = carry[1] + carry[2];
+        counters[kCtrShort] = carry[3];
     }
 }
 
 __global__ void __launch_bounds__(kUnitThreads)
-units_write_kernel(const int* rstart, const int* rend, long long N, long long M, int g, const int4* tile_off,
+units_write_kernel(const int* rstart, const int* rend, long long N, long long M, int g, const int* tile_off,
                    int* row_ptr, int4* seg_units, int4* row_units, int4* finish, const int* counters)
 {
     __shared__ int ws[kUnitThreads / 32 + 1];
@@ -387,19 +395,22 @@ units_write_kernel(const int* rstart, const int* rend, long long N, long long M,
     if (counters[kCtrErrIndex]) return;
     const long long m = static_cast<long long>(blockIdx.x) * kUnitThreads + threadIdx.x;
     const RowClass r = classify_row(rstart, rend, m, M, g);
-    const int4 off = tile_off[blockIdx.x];
-    int unused;
-    const int eR = off.x + block_excl_scan<kUnitThreads>(r.len, ws, &unused);
-    const int eA = off.y + block_excl_scan<kUnitThreads>(r.seg, ws, &unused);
-    const int eB = off.z + block_excl_scan<kUnitThreads>(r.whole, ws, &unused);
-    const int eC = off.w + block_excl_scan<kUnitThreads>(r.fin, ws, &unused);
+    int e[kUnitVals];
+#pragma unroll
+    for (int j = 0; j < kUnitVals; ++j) {
+        int unused;
+        e[j] = tile_off[static_cast<long long>(blockIdx.x) * kUnitVals + j] +
+               block_excl_scan<kUnitThreads>(r.v[j], ws, &unused);
+    }
     if (m < M) {
-        row_ptr[m] = eR;
-        if (r.fin) {
-            finish[eC] = make_int4(static_cast<int>(m), eA, r.seg, 0);
-            for (int s = 0; s < r.seg; ++s) seg_units[eA + s] = make_int4(static_cast<int>(m), s, eA + s, 0);
+        row_ptr[m] = e[0];
+        if (r.v[4]) {
+            finish[e[4]] = make_int4(static_cast<int>(m), e[1], r.v[1], 0);
+            for (int s = 0; s < r.v[1]; ++s) seg_units[e[1] + s] = make_int4(static_cast<int>(m), s, e[1] + s, 0);
+        } else if (r.v[2]) {
+            seg_units[counters[kCtrSegs] + e[2]] = make_int4(static_cast<int>(m), -1, 0, 0);
         } else {
-            row_units[eB] = make_int4(static_cast<int>(m), -1, 0, 0);
+            row_units[e[3]] = make_int4(static_cast<int>(m), -1, 0, 0);
         }
     }
     if (m == M - 1) row_ptr[M] = static_cast<int>(N);
@@ -447,14 +458,14 @@ static PlanLayout plan_layout(int64_t N, int64_t M, bool with_src, int g)
     L.npass = dest_passes(M) + (with_src ? 8 : 0);
     const int64_t seg_terms = static_cast<int64_t>(kChunk) << g;
     L.max_finish = cdiv(N, seg_terms) + 1;
-    L.max_segs = 2 * cdiv(N, seg_terms) + 1;
+    L.max_segs = 2 * cdiv(N, seg_terms) + 1 + std::min<int64_t>(M, N / (kChunk + 1) + 1);  // + long rows
     L.max_rows = M + 1;
     L.counters = take(kCtrCount * sizeof(int));
     L.row_ptr = take(static_cast<size_t>(M + 1) * sizeof(int));
     L.rstart = take(static_cast<size_t>(M) * sizeof(int));
     L.rend = take(static_cast<size_t>(M) * sizeof(int));
     L.zero_end = off;
-    L.utot = take(static_cast<size_t>(L.nut) * sizeof(int4));
+    L.utot = take(static_cast<size_t>(L.nut) * kUnitVals * sizeof(int));
     L.counts = take(static_cast<size_t>(kRadix) * L.ntiles * sizeof(int));
     L.totals = take(static_cast<size_t>(kRadix) * sizeof(int));
     L.perm = take(static_cast<size_t>(N) * sizeof(int));
@@ -488,6 +499,7 @@ static void set_counts(det_plan_s* p, const int* h)
     p->n_units = static_cast<int64_t>(h[kCtrSegs]) + h[kCtrNormal];
     p->n_hot_rows = h[kCtrHot];
     p->max_row_len = h[kCtrMaxLen];
+    p->n_long = h[kCtrLong];
 }
 
 static det_status resolve_seg_log2(const det_opts* o, int* g)
@@ -652,7 +664,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
             row_bounds_kernel<<<bgrid, kUnitThreads, 0, st>>>(skeys, N, M, rstart, rend, counters);
             DETR_LAUNCHED();
         }
-        int4* tile_tot = reinterpret_cast<int4*>(ws + L.utot);
+        int* tile_tot = reinterpret_cast<int*>(ws + L.utot);
         units_count_kernel<<<L.nut, kUnitThreads, 0, st>>>(rstart, rend, M, g, tile_tot, counters);
         DETR_LAUNCHED();
         units_scan_kernel<<<1, kUnitScanThreads, 0, st>>>(tile_tot, L.nut, counters);
@@ -686,7 +698,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     p->finish = finish;
     if (async) {
         p->counts_on_host = false;
-        p->n_segments = p->n_units = p->n_hot_rows = p->max_row_len = -1;
+        p->n_segments = p->n_units = p->n_hot_rows = p->max_row_len = p->n_long = -1;
     } else {
         set_counts(p, h);
     }

@@ -63,24 +63,25 @@ struct CluShared {
     int tstart[kCluRadix];           // first staged position of each digit
     int gbase[kCluRadix];            // first global position of this CTA's keys of each digit
     int cnt_lt[kCluMaxCtas];         // keys of this slice below the end of CTA r's rows (read by the cluster)
-    int ws[3 * (kCluWarps + 1)];     // scan scratch
-    int tot[4];                      // seg units, row units, finish tasks, longest row (read by the cluster)
-    int base[3];                     // this CTA's offsets into the three unit arrays
-    int grand[4];                    // cluster totals
+    int ws[4 * (kCluWarps + 1)];     // scan scratch
+    int tot[5];                      // seg units, long and short row units, finish tasks, longest row (read by the cluster)
+    int base[4];                     // this CTA's offsets into the unit arrays
+    int grand[5];                    // cluster totals
     int bad;                         // this CTA saw an index outside [0, M) (read by the cluster)
     int any_bad;
     int next_start;                  // first sorted position past this CTA's rows
 };
 
-// Exclusive scans of three ints per thread over 1024 threads at once; tot gets
-// the three block sums.  Ends synchronised.
-__device__ __forceinline__ void block_excl_scan3(int v[3], int* ws, int tot[3])
+// Exclusive scans of NV ints per thread over 1024 threads at once; tot gets
+// the block sums.  Ends synchronised.
+template <int NV>
+__device__ __forceinline__ void block_excl_scan_n(int v[NV], int* ws, int tot[NV])
 {
-    constexpr int W = kCluWarps;  // 32: one lane per warp in the second level
+    constexpr int W = kCluWarps;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl[3];
+    int incl[NV];
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
+    for (int j = 0; j < NV; ++j) {
         incl[j] = v[j];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -90,10 +91,10 @@ __device__ __forceinline__ void block_excl_scan3(int v[3], int* ws, int tot[3])
     }
     if (lane == 31) {
 #pragma unroll
-        for (int j = 0; j < 3; ++j) ws[j * (W + 1) + warp] = incl[j];
+        for (int j = 0; j < NV; ++j) ws[j * (W + 1) + warp] = incl[j];
     }
     __syncthreads();
-    if (warp < 3) {
+    if (warp < NV) {
         const int s = ws[warp * (W + 1) + lane];
         int si = s;
 #pragma unroll
@@ -106,7 +107,7 @@ __device__ __forceinline__ void block_excl_scan3(int v[3], int* ws, int tot[3])
     }
     __syncthreads();
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
+    for (int j = 0; j < NV; ++j) {
         tot[j] = ws[j * (W + 1) + W];
         v[j] = incl[j] - v[j] + ws[j * (W + 1) + warp];
     }
@@ -185,7 +186,7 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
     unsigned int lt;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
     pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
-    if (tid == 0) S.tot[3] = 0;
+    if (tid == 0) S.tot[4] = 0;
     for (int i = tid; i < r_hi - r_lo; i += kCluThreads) S.rstart[i] = INT_MAX;
 
     // 1. the slice, in position order, into kv; in the passes item k of lane
@@ -352,9 +353,11 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
 #pragma unroll
     for (int j = 0; j < kCluRowsPerThread; ++j) rp[j] = min(rp[j], after);
 
-    // 4. the work list
+    // 4. the work list: hot rows (more than 2^g chunks) give segment units and
+    //    a finish task, rows of 2..2^g chunks a long whole-row unit, the
+    //    others a short one (long ones listed first)
     const int G = 1 << g;
-    int v3[3] = {0, 0, 0};
+    int v4[4] = {0, 0, 0, 0};  // segments, long rows, short rows, finish tasks
     int mx = 0;
 #pragma unroll
     for (int j = 0; j < kCluRowsPerThread; ++j) {
@@ -362,56 +365,53 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
             const int len = (j + 1 < nrows ? rp[j + 1] : after) - rp[j];
             const int nch = (len + 31) >> 5;
             if (nch > G) {
-                v3[0] += (nch + G - 1) >> g;
-                v3[2] += 1;
+                v4[0] += (nch + G - 1) >> g;
+                v4[3] += 1;
+            } else if (nch > 1) {
+                v4[1] += 1;
             } else {
-                v3[1] += 1;
+                v4[2] += 1;
             }
             mx = max(mx, len);
         }
     }
     mx = __reduce_max_sync(0xffffffffu, mx);
-    if (lane == 0 && mx > 0) atomicMax(&S.tot[3], mx);
-    int t3[3];
-    block_excl_scan3(v3, S.ws, t3);
+    if (lane == 0 && mx > 0) atomicMax(&S.tot[4], mx);
+    int t4[4];
+    block_excl_scan_n<4>(v4, S.ws, t4);
     if (tid == 0) {
-        S.tot[0] = t3[0];
-        S.tot[1] = t3[1];
-        S.tot[2] = t3[2];
+        S.tot[0] = t4[0];
+        S.tot[1] = t4[1];
+        S.tot[2] = t4[2];
+        S.tot[3] = t4[3];
     }
     cl.sync();  // every CTA's totals are visible (no global store is pending here)
     if (warp == 0) {
-        int a = 0, b = 0, h = 0, m = 0;
+        int v[4] = {0, 0, 0, 0}, m = 0;
         if (lane < C) {
             const int* rt = cl.map_shared_rank(S.tot, lane);
-            a = rt[0];
-            b = rt[1];
-            h = rt[2];
-            m = rt[3];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = rt[j];
+            m = rt[4];
         }
-        int ia = a, ib = b, ih = h;
+        int in[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int ta = __shfl_up_sync(0xffffffffu, ia, o);
-            const int tb = __shfl_up_sync(0xffffffffu, ib, o);
-            const int th = __shfl_up_sync(0xffffffffu, ih, o);
-            if (lane >= o) {
-                ia += ta;
-                ib += tb;
-                ih += th;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = __shfl_up_sync(0xffffffffu, in[j], o);
+                if (lane >= o) in[j] += t;
             }
         }
         const int gm = __reduce_max_sync(0xffffffffu, m);
         if (lane == c) {
-            S.base[0] = ia - a;
-            S.base[1] = ib - b;
-            S.base[2] = ih - h;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) S.base[j] = in[j] - v[j];
         }
         if (lane == 31) {
-            S.grand[0] = ia;
-            S.grand[1] = ib;
-            S.grand[2] = ih;
-            S.grand[3] = gm;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) S.grand[j] = in[j];
+            S.grand[4] = gm;
         }
     }
     __syncthreads();
@@ -420,7 +420,8 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
     cluster_arrive_relaxed();
     for (int i = tid; i < cnt; i += kCluThreads) perm[c0 + i] = static_cast<int>(S.kv[i].y);
     if (!any_bad) {
-        int eA = v3[0] + S.base[0], eB = v3[1] + S.base[1], eC = v3[2] + S.base[2];
+        int eA = v4[0] + S.base[0], eL = S.grand[0] + v4[1] + S.base[1], eS = v4[2] + S.base[2];
+        int eC = v4[3] + S.base[3];
 #pragma unroll
         for (int j = 0; j < kCluRowsPerThread; ++j) {
             if (j < nrows) {
@@ -433,8 +434,10 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
                     finish[eC++] = make_int4(m, eA, a, 0);
                     for (int s = 0; s < a; ++s) seg_units[eA + s] = make_int4(m, s, eA + s, 0);
                     eA += a;
+                } else if (nch > 1) {
+                    seg_units[eL++] = make_int4(m, -1, 0, 0);
                 } else {
-                    row_units[eB++] = make_int4(m, -1, 0, 0);
+                    row_units[eS++] = make_int4(m, -1, 0, 0);
                 }
             }
         }
@@ -444,9 +447,12 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
         int v = 0;
         if (tid == kCtrErrIndex) v = any_bad ? 1 : 0;
         else if (!any_bad && tid == kCtrSegs) v = S.grand[0];
-        else if (!any_bad && tid == kCtrNormal) v = S.grand[1];
-        else if (!any_bad && tid == kCtrHot) v = S.grand[2];
-        else if (!any_bad && tid == kCtrMaxLen) v = S.grand[3];
+        else if (!any_bad && tid == kCtrLong) v = S.grand[1];
+        else if (!any_bad && tid == kCtrNormal) v = S.grand[1] + S.grand[2];
+        else if (!any_bad && tid == kCtrHot) v = S.grand[3];
+        else if (!any_bad && tid == kCtrMaxLen) v = S.grand[4];
+        else if (!any_bad && tid == kCtrBig) v = S.grand[0] + S.grand[1];
+        else if (!any_bad && tid == kCtrShort) v = S.grand[2];
         counters[tid] = v;
     }
     cluster_wait();  // no CTA leaves while another may still read its shared memory
@@ -482,54 +488,12 @@ struct OneShared {
     int chist[kOneMaxBins];    // this CTA's count of each destination (read by the owners)
     int pref[kOneMaxBins];     // earlier CTAs' count of each destination (written by the owners)
     int rp[kOneMaxBins];       // row_ptr of the destinations this CTA owns (read by every CTA)
-    int ws[4 * (kCluWarps + 1)];
-    int tot[5];                // rows, seg units, row units, finish tasks, longest row
-    int all_tot[kCluMaxCtas][5];  // every CTA's tot (written by that CTA)
+    int ws[5 * (kCluWarps + 1)];
+    int tot[6];                // rows, seg units, long and short row units, finish tasks, longest row
+    int all_tot[kCluMaxCtas][6];  // every CTA's tot (written by that CTA)
     int bad;                   // this CTA saw an index outside [0, M) (read by every CTA)
     int any_bad;
 };
-
-// Exclusive scans of NV ints per thread over 1024 threads at once; tot gets
-// the block sums.  Ends synchronised.
-template <int NV>
-__device__ __forceinline__ void block_excl_scan_n(int v[NV], int* ws, int tot[NV])
-{
-    constexpr int W = kCluWarps;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl[NV];
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        incl[j] = v[j];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl[j], o);
-            if (lane >= o) incl[j] += t;
-        }
-    }
-    if (lane == 31) {
-#pragma unroll
-        for (int j = 0; j < NV; ++j) ws[j * (W + 1) + warp] = incl[j];
-    }
-    __syncthreads();
-    if (warp < NV) {
-        const int s = ws[warp * (W + 1) + lane];
-        int si = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, si, o);
-            if (lane >= o) si += t;
-        }
-        ws[warp * (W + 1) + lane] = si - s;
-        if (lane == 31) ws[warp * (W + 1) + W] = si;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        tot[j] = ws[j * (W + 1) + W];
-        v[j] = incl[j] - v[j] + ws[j * (W + 1) + warp];
-    }
-    __syncthreads();
-}
 
 // Lanes among `live` holding the same nbits-bit key as this lane.
 __device__ __forceinline__ unsigned int key_peers(int d, unsigned int live, int nbits)
@@ -567,7 +531,7 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
     unsigned int* wz = reinterpret_cast<unsigned int*>(S.whist);  // B is a multiple of 4
     for (int i = tid; i < kCluWarps * B / 4; i += kCluThreads) wz[i] = 0u;
-    if (tid == 0) S.tot[4] = 0;
+    if (tid == 0) S.tot[5] = 0;
 
     // 1. the slice, then the ranking: warp w < 16 owns [w*ipw, (w+1)*ipw)
     bool bad = false;
@@ -648,60 +612,63 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
         }
     }
     const int G = 1 << g;
-    int v4[4] = {0, 0, 0, 0};  // rows' sources, seg units, row units, finish tasks
+    // rows' sources, segment units, long rows (2..2^g chunks), short rows, finish tasks
+    int v5[5] = {0, 0, 0, 0, 0};
     int mx = 0;
 #pragma unroll
     for (int j = 0; j < kOneRowsPerThread; ++j) {
         if (j < nrows) {
             const int nch = (len[j] + 31) >> 5;
-            v4[0] += len[j];
+            v5[0] += len[j];
             if (nch > G) {
-                v4[1] += (nch + G - 1) >> g;
-                v4[3] += 1;
+                v5[1] += (nch + G - 1) >> g;
+                v5[4] += 1;
+            } else if (nch > 1) {
+                v5[2] += 1;
             } else {
-                v4[2] += 1;
+                v5[3] += 1;
             }
             mx = max(mx, len[j]);
         }
     }
     mx = __reduce_max_sync(0xffffffffu, mx);
-    if (lane == 0 && mx > 0) atomicMax(&S.tot[4], mx);
-    int t4[4];
-    block_excl_scan_n<4>(v4, S.ws, t4);  // ends synchronised: S.tot[4] is final
-    if (tid < 5 * C) {  // push this CTA's totals into every CTA
-        const int r = tid / 5, f = tid - 5 * (tid / 5);
-        const int v = f == 0 ? t4[0] : f == 1 ? t4[1] : f == 2 ? t4[2] : f == 3 ? t4[3] : S.tot[4];
+    if (lane == 0 && mx > 0) atomicMax(&S.tot[5], mx);
+    int t5[5];
+    block_excl_scan_n<5>(v5, S.ws, t5);  // ends synchronised: S.tot[5] is final
+    if (tid < 6 * C) {  // push this CTA's totals into every CTA
+        const int r = tid / 6, f = tid - 6 * (tid / 6);
+        const int v = f == 0 ? t5[0] : f == 1 ? t5[1] : f == 2 ? t5[2] : f == 3 ? t5[3] : f == 4 ? t5[4] : S.tot[5];
         *cl.map_shared_rank(&S.all_tot[c][f], r) = v;
     }
     cl.sync();  // prefixes and every CTA's totals are visible
 
     // 3. bases from the CTAs' totals (every warp computes them itself); row_ptr
     //    of the owned destinations
-    int base[4], grand[5];
+    int base[5], grand[6];
     {
-        int v[4] = {0, 0, 0, 0}, m = 0;
+        int v[5] = {0, 0, 0, 0, 0}, m = 0;
         if (lane < C) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = S.all_tot[lane][j];
-            m = S.all_tot[lane][4];
+            for (int j = 0; j < 5; ++j) v[j] = S.all_tot[lane][j];
+            m = S.all_tot[lane][5];
         }
-        int in[4] = {v[0], v[1], v[2], v[3]};
+        int in[5] = {v[0], v[1], v[2], v[3], v[4]};
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 5; ++j) {
                 const int t = __shfl_up_sync(0xffffffffu, in[j], o);
                 if (lane >= o) in[j] += t;
             }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 5; ++j) {
             base[j] = __shfl_sync(0xffffffffu, in[j] - v[j], c);
             grand[j] = __shfl_sync(0xffffffffu, in[j], 31);
         }
-        grand[4] = __reduce_max_sync(0xffffffffu, m);
+        grand[5] = __reduce_max_sync(0xffffffffu, m);
     }
-    int rstart = v4[0] + base[0];
+    int rstart = v5[0] + base[0];
 #pragma unroll
     for (int j = 0; j < kOneRowsPerThread; ++j) {
         if (j < nrows) {
@@ -737,7 +704,7 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     // the lists, wait before leaving
     cluster_arrive_relaxed();
     if (!any_bad) {
-        int eA = v4[1] + base[1], eB = v4[2] + base[2], eC = v4[3] + base[3];
+        int eA = v5[1] + base[1], eL = grand[1] + v5[2] + base[2], eS = v5[3] + base[3], eC = v5[4] + base[4];
 #pragma unroll
         for (int j = 0; j < kOneRowsPerThread; ++j) {
             if (j < nrows) {
@@ -749,8 +716,10 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
                     finish[eC++] = make_int4(m, eA, a, 0);
                     for (int s = 0; s < a; ++s) seg_units[eA + s] = make_int4(m, s, eA + s, 0);
                     eA += a;
+                } else if (nch > 1) {
+                    seg_units[eL++] = make_int4(m, -1, 0, 0);
                 } else {
-                    row_units[eB++] = make_int4(m, -1, 0, 0);
+                    row_units[eS++] = make_int4(m, -1, 0, 0);
                 }
             }
         }
@@ -760,9 +729,12 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
         int v = 0;
         if (tid == kCtrErrIndex) v = any_bad ? 1 : 0;
         else if (!any_bad && tid == kCtrSegs) v = grand[1];
-        else if (!any_bad && tid == kCtrNormal) v = grand[2];
-        else if (!any_bad && tid == kCtrHot) v = grand[3];
-        else if (!any_bad && tid == kCtrMaxLen) v = grand[4];
+        else if (!any_bad && tid == kCtrLong) v = grand[2];
+        else if (!any_bad && tid == kCtrNormal) v = grand[2] + grand[3];
+        else if (!any_bad && tid == kCtrHot) v = grand[4];
+        else if (!any_bad && tid == kCtrMaxLen) v = grand[5];
+        else if (!any_bad && tid == kCtrBig) v = grand[1] + grand[2];
+        else if (!any_bad && tid == kCtrShort) v = grand[3];
         counters[tid] = v;
     }
     cluster_wait();  // no CTA leaves while another may still read its shared memory

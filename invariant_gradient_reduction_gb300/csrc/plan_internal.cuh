@@ -19,6 +19,9 @@ enum {
     kCtrHot = 4,       // destinations split into segments (finish tasks)
     kCtrMaxLen = 5,    // longest destination list
     kCtrErrTimeout = 6,  // a bounded wait inside a reduce kernel expired
+    kCtrLong = 7,      // whole-destination units of 2..2^g chunks (in seg_units, after the segments)
+    kCtrBig = 8,       // units of more than one chunk: hot segments + long whole rows
+    kCtrShort = 9,     // whole-destination units of one chunk or less (row_units)
     kCtrCount = 16
 };
 
@@ -44,11 +47,13 @@ det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, 
 }  // namespace detr
 
 // Host handle.  Device arrays live in the caller's plan workspace.
-//   seg_units[u] = {row m, segment s, partial slot, 0} for the hot segments;
-//   row_units[u] = {row m, -1, 0, 0} for the whole-row units, in row order;
+//   seg_units[u] = {row m, segment s, partial slot, 0} for the hot segments,
+//                  then {row m, -1, 0, 0} for the n_long whole-row units of
+//                  2..2^g chunks: the units with more than one chunk;
+//   row_units[u] = {row m, -1, 0, 0} for the other whole-row units;
 //   finish[k]    = {row m, first partial slot, number of segments, 0}.
-// Work unit u of the reduce is seg_units[u] for u < n_segments, else
-// row_units[u - n_segments] (hot segments first: they are the longest).
+// Work unit u of the reduce is seg_units[u] for u < n_segments + n_long,
+// else row_units[u - n_segments - n_long] (the longest units first).
 struct det_plan_s {
     int64_t N = 0, M = 0;
     int g = 3;                       // a hot segment covers 2^g chunks of 32 terms
@@ -60,6 +65,6 @@ struct det_plan_s {
     int4* seg_units = nullptr;
     int4* row_units = nullptr;
     int4* finish = nullptr;
-    int64_t n_units = 0, n_segments = 0, n_hot_rows = 0, max_row_len = 0;
+    int64_t n_units = 0, n_segments = 0, n_hot_rows = 0, max_row_len = 0, n_long = 0;
     bool counts_on_host = true;      // false for an async plan until det_plan_status
 };
