@@ -384,7 +384,8 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
     const int64_t max_segs_all = 2 * cdiv(plan->N, seg_terms) + 1;
     const int64_t max_tg = std::max(a.tile_groups, a.seg_tile_groups);
     a.n_tasks = dev_counts ? plan->M * max_tg + max_segs_all * a.seg_tile_groups  // an upper bound
-                           : a.n_seg * a.seg_tile_groups + (plan->n_units - a.n_seg) * a.tile_groups;
+                           : a.n_seg * a.seg_tile_groups +
+                                 (plan->n_units - a.n_seg - (accumulate ? plan->n_empty : 0)) * a.tile_groups;
 
     // Binary-counter depth: enough levels for the longest unit's rounds.
     const int64_t G = int64_t(1) << plan->g;

@@ -49,8 +49,9 @@ __device__ __forceinline__ bool task_counts(const GatherArgs& a, long long* n_ta
         const int* c = a.dev_counters;
         if (c[kCtrErrIndex] | c[kCtrErrDup] | c[kCtrErrTimeout]) return false;
         *n_seg = c[kCtrBig];
+        // index_add_ has nothing to do for the empty destinations (listed last)
         *n_tasks = static_cast<long long>(c[kCtrBig]) * a.seg_tile_groups +
-                   static_cast<long long>(c[kCtrShort]) * a.tile_groups;
+                   static_cast<long long>(c[kCtrShort] + (a.accumulate ? 0 : c[kCtrEmpty])) * a.tile_groups;
     }
     return true;
 }

@@ -307,15 +307,16 @@ row_bounds_kernel(const int* skeys, long long N, long long M, int* rstart, int* 
 // The work list in three kernels (no CTA waits for another), over tiles of
 // kUnitThreads destinations, one per thread:
 //   units_count_kernel  each tile's totals: sources (row lengths), hot
-//                       segments, long and short whole-row units, finish
-//                       tasks; and the longest list;
-//   units_scan_kernel   one CTA: exclusive scans of the five totals over the
+//                       segments, long, short and empty whole-row units,
+//                       finish tasks; and the longest list;
+//   units_scan_kernel   one CTA: exclusive scans of the six totals over the
 //                       tiles, and the grand totals into the counter block;
 //   units_write_kernel  row_ptr, and the units: hot rows (more than 2^g
 //                       chunks) give `seg` segment units and one finish task,
 //                       rows of 2..2^g chunks a long whole-row unit (listed
-//                       after the segments), the others a short one.
-constexpr int kUnitVals = 5;  // sources, segments, long rows, short rows, finish tasks
+//                       after the segments), the others a short one (empty
+//                       destinations after the ones with terms).
+constexpr int kUnitVals = 6;  // sources, segments, long rows, short rows, finish tasks, empty rows
 
 struct RowClass {
     int v[kUnitVals];
@@ -323,7 +324,7 @@ struct RowClass {
 
 __device__ __forceinline__ RowClass classify_row(const int* rstart, const int* rend, long long m, long long M, int g)
 {
-    RowClass r{{0, 0, 0, 0, 0}};
+    RowClass r{{0, 0, 0, 0, 0, 0}};
     if (m < M) {
         r.v[0] = rend[m] - rstart[m];
         const int nch = (r.v[0] + kChunk - 1) / kChunk;
@@ -332,8 +333,10 @@ __device__ __forceinline__ RowClass classify_row(const int* rstart, const int* r
             r.v[4] = 1;
         } else if (nch > 1) {
             r.v[2] = 1;
-        } else {
+        } else if (nch == 1) {
             r.v[3] = 1;
+        } else {
+            r.v[5] = 1;
         }
     }
     return r;
@@ -363,7 +366,7 @@ units_scan_kernel(int* tile_tot, int nut, int* counters)
 {
     __shared__ int ws[kUnitScanThreads / 32 + 1];
     if (counters[kCtrErrIndex]) return;
-    int carry[kUnitVals] = {0, 0, 0, 0, 0};
+    int carry[kUnitVals] = {0, 0, 0, 0, 0, 0};
     for (int t0 = 0; t0 < nut; t0 += kUnitScanThreads) {
         const int t = t0 + threadIdx.x;
 #pragma unroll
@@ -379,10 +382,11 @@ units_scan_kernel(int* tile_tot, int nut, int* counters)
     if (threadIdx.x == 0) {
         counters[kCtrSegs] = carry[1];
         counters[kCtrLong] = carry[2];
-        counters[kCtrNormal] = carry[2] + carry[3];
+        counters[kCtrNormal] = carry[2] + carry[3] + carry[5];
         counters[kCtrHot] = carry[4];
         counters[kCtrBig] = carry[1] + carry[2];
         counters[kCtrShort] = carry[3];
+        counters[kCtrEmpty] = carry[5];
     }
 }
 
@@ -409,8 +413,10 @@ units_write_kernel(const int* rstart, const int* rend, long long N, long long M,
             for (int s = 0; s < r.v[1]; ++s) seg_units[e[1] + s] = make_int4(static_cast<int>(m), s, e[1] + s, 0);
         } else if (r.v[2]) {
             seg_units[counters[kCtrSegs] + e[2]] = make_int4(static_cast<int>(m), -1, 0, 0);
-        } else {
+        } else if (r.v[3]) {
             row_units[e[3]] = make_int4(static_cast<int>(m), -1, 0, 0);
+        } else {
+            row_units[counters[kCtrShort] + e[5]] = make_int4(static_cast<int>(m), -1, 0, 0);
         }
     }
     if (m == M - 1) row_ptr[M] = static_cast<int>(N);
@@ -500,6 +506,7 @@ static void set_counts(det_plan_s* p, const int* h)
     p->n_hot_rows = h[kCtrHot];
     p->max_row_len = h[kCtrMaxLen];
     p->n_long = h[kCtrLong];
+    p->n_empty = h[kCtrEmpty];
 }
 
 static det_status resolve_seg_log2(const det_opts* o, int* g)
@@ -698,7 +705,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     p->finish = finish;
     if (async) {
         p->counts_on_host = false;
-        p->n_segments = p->n_units = p->n_hot_rows = p->max_row_len = p->n_long = -1;
+        p->n_segments = p->n_units = p->n_hot_rows = p->max_row_len = p->n_long = p->n_empty = -1;
     } else {
         set_counts(p, h);
     }

@@ -63,10 +63,10 @@ struct CluShared {
     int tstart[kCluRadix];           // first staged position of each digit
     int gbase[kCluRadix];            // first global position of this CTA's keys of each digit
     int cnt_lt[kCluMaxCtas];         // keys of this slice below the end of CTA r's rows (read by the cluster)
-    int ws[4 * (kCluWarps + 1)];     // scan scratch
-    int tot[5];                      // seg units, long and short row units, finish tasks, longest row (read by the cluster)
-    int base[4];                     // this CTA's offsets into the unit arrays
-    int grand[5];                    // cluster totals
+    int ws[5 * (kCluWarps + 1)];     // scan scratch
+    int tot[6];                      // seg units, long, short rows, finish tasks, empty rows, longest row (read by the cluster)
+    int base[5];                     // this CTA's offsets into the unit arrays
+    int grand[6];                    // cluster totals
     int bad;                         // this CTA saw an index outside [0, M) (read by the cluster)
     int any_bad;
     int next_start;                  // first sorted position past this CTA's rows
@@ -186,7 +186,7 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
     unsigned int lt;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
     pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
-    if (tid == 0) S.tot[4] = 0;
+    if (tid == 0) S.tot[5] = 0;
     for (int i = tid; i < r_hi - r_lo; i += kCluThreads) S.rstart[i] = INT_MAX;
 
     // 1. the slice, in position order, into kv; in the passes item k of lane
@@ -357,7 +357,7 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
     //    a finish task, rows of 2..2^g chunks a long whole-row unit, the
     //    others a short one (long ones listed first)
     const int G = 1 << g;
-    int v4[4] = {0, 0, 0, 0};  // segments, long rows, short rows, finish tasks
+    int v4[5] = {0, 0, 0, 0, 0};  // segments, long rows, short rows, finish tasks, empty rows
     int mx = 0;
 #pragma unroll
     for (int j = 0; j < kCluRowsPerThread; ++j) {
@@ -369,36 +369,39 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
                 v4[3] += 1;
             } else if (nch > 1) {
                 v4[1] += 1;
-            } else {
+            } else if (nch == 1) {
                 v4[2] += 1;
+            } else {
+                v4[4] += 1;
             }
             mx = max(mx, len);
         }
     }
     mx = __reduce_max_sync(0xffffffffu, mx);
-    if (lane == 0 && mx > 0) atomicMax(&S.tot[4], mx);
-    int t4[4];
-    block_excl_scan_n<4>(v4, S.ws, t4);
+    if (lane == 0 && mx > 0) atomicMax(&S.tot[5], mx);
+    int t4[5];
+    block_excl_scan_n<5>(v4, S.ws, t4);
     if (tid == 0) {
         S.tot[0] = t4[0];
         S.tot[1] = t4[1];
         S.tot[2] = t4[2];
         S.tot[3] = t4[3];
+        S.tot[4] = t4[4];
     }
     cl.sync();  // every CTA's totals are visible (no global store is pending here)
     if (warp == 0) {
-        int v[4] = {0, 0, 0, 0}, m = 0;
+        int v[5] = {0, 0, 0, 0, 0}, m = 0;
         if (lane < C) {
             const int* rt = cl.map_shared_rank(S.tot, lane);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = rt[j];
-            m = rt[4];
+            for (int j = 0; j < 5; ++j) v[j] = rt[j];
+            m = rt[5];
         }
-        int in[4] = {v[0], v[1], v[2], v[3]};
+        int in[5] = {v[0], v[1], v[2], v[3], v[4]};
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 5; ++j) {
                 const int t = __shfl_up_sync(0xffffffffu, in[j], o);
                 if (lane >= o) in[j] += t;
             }
@@ -406,12 +409,12 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
         const int gm = __reduce_max_sync(0xffffffffu, m);
         if (lane == c) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) S.base[j] = in[j] - v[j];
+            for (int j = 0; j < 5; ++j) S.base[j] = in[j] - v[j];
         }
         if (lane == 31) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) S.grand[j] = in[j];
-            S.grand[4] = gm;
+            for (int j = 0; j < 5; ++j) S.grand[j] = in[j];
+            S.grand[5] = gm;
         }
     }
     __syncthreads();
@@ -421,7 +424,7 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
     for (int i = tid; i < cnt; i += kCluThreads) perm[c0 + i] = static_cast<int>(S.kv[i].y);
     if (!any_bad) {
         int eA = v4[0] + S.base[0], eL = S.grand[0] + v4[1] + S.base[1], eS = v4[2] + S.base[2];
-        int eC = v4[3] + S.base[3];
+        int eC = v4[3] + S.base[3], eE = S.grand[2] + v4[4] + S.base[4];
 #pragma unroll
         for (int j = 0; j < kCluRowsPerThread; ++j) {
             if (j < nrows) {
@@ -436,8 +439,10 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
                     eA += a;
                 } else if (nch > 1) {
                     seg_units[eL++] = make_int4(m, -1, 0, 0);
-                } else {
+                } else if (nch == 1) {
                     row_units[eS++] = make_int4(m, -1, 0, 0);
+                } else {
+                    row_units[eE++] = make_int4(m, -1, 0, 0);
                 }
             }
         }
@@ -448,11 +453,12 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
         if (tid == kCtrErrIndex) v = any_bad ? 1 : 0;
         else if (!any_bad && tid == kCtrSegs) v = S.grand[0];
         else if (!any_bad && tid == kCtrLong) v = S.grand[1];
-        else if (!any_bad && tid == kCtrNormal) v = S.grand[1] + S.grand[2];
+        else if (!any_bad && tid == kCtrNormal) v = S.grand[1] + S.grand[2] + S.grand[4];
         else if (!any_bad && tid == kCtrHot) v = S.grand[3];
-        else if (!any_bad && tid == kCtrMaxLen) v = S.grand[4];
+        else if (!any_bad && tid == kCtrMaxLen) v = S.grand[5];
         else if (!any_bad && tid == kCtrBig) v = S.grand[0] + S.grand[1];
         else if (!any_bad && tid == kCtrShort) v = S.grand[2];
+        else if (!any_bad && tid == kCtrEmpty) v = S.grand[4];
         counters[tid] = v;
     }
     cluster_wait();  // no CTA leaves while another may still read its shared memory
@@ -488,9 +494,9 @@ struct OneShared {
     int chist[kOneMaxBins];    // this CTA's count of each destination (read by the owners)
     int pref[kOneMaxBins];     // earlier CTAs' count of each destination (written by the owners)
     int rp[kOneMaxBins];       // row_ptr of the destinations this CTA owns (read by every CTA)
-    int ws[5 * (kCluWarps + 1)];
-    int tot[6];                // rows, seg units, long and short row units, finish tasks, longest row
-    int all_tot[kCluMaxCtas][6];  // every CTA's tot (written by that CTA)
+    int ws[6 * (kCluWarps + 1)];
+    int tot[7];                // rows, seg units, long, short rows, finish tasks, empty rows, longest row
+    int all_tot[kCluMaxCtas][7];  // every CTA's tot (written by that CTA)
     int bad;                   // this CTA saw an index outside [0, M) (read by every CTA)
     int any_bad;
 };
@@ -531,7 +537,7 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
     unsigned int* wz = reinterpret_cast<unsigned int*>(S.whist);  // B is a multiple of 4
     for (int i = tid; i < kCluWarps * B / 4; i += kCluThreads) wz[i] = 0u;
-    if (tid == 0) S.tot[5] = 0;
+    if (tid == 0) S.tot[6] = 0;
 
     // 1. the slice, then the ranking: warp w < 16 owns [w*ipw, (w+1)*ipw)
     bool bad = false;
@@ -612,8 +618,10 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
         }
     }
     const int G = 1 << g;
-    // rows' sources, segment units, long rows (2..2^g chunks), short rows, finish tasks
-    int v5[5] = {0, 0, 0, 0, 0};
+    // rows' sources, segment units, long rows (2..2^g chunks), short rows,
+    // finish tasks, empty rows
+    constexpr int NV = 6;
+    int v5[NV] = {0, 0, 0, 0, 0, 0};
     int mx = 0;
 #pragma unroll
     for (int j = 0; j < kOneRowsPerThread; ++j) {
@@ -625,48 +633,55 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
                 v5[4] += 1;
             } else if (nch > 1) {
                 v5[2] += 1;
-            } else {
+            } else if (nch == 1) {
                 v5[3] += 1;
+            } else {
+                v5[5] += 1;
             }
             mx = max(mx, len[j]);
         }
     }
     mx = __reduce_max_sync(0xffffffffu, mx);
-    if (lane == 0 && mx > 0) atomicMax(&S.tot[5], mx);
-    int t5[5];
-    block_excl_scan_n<5>(v5, S.ws, t5);  // ends synchronised: S.tot[5] is final
-    if (tid < 6 * C) {  // push this CTA's totals into every CTA
-        const int r = tid / 6, f = tid - 6 * (tid / 6);
-        const int v = f == 0 ? t5[0] : f == 1 ? t5[1] : f == 2 ? t5[2] : f == 3 ? t5[3] : f == 4 ? t5[4] : S.tot[5];
+    if (lane == 0 && mx > 0) atomicMax(&S.tot[NV], mx);
+    int t5[NV];
+    block_excl_scan_n<NV>(v5, S.ws, t5);  // ends synchronised: S.tot[NV] is final
+    if (tid < (NV + 1) * C) {  // push this CTA's totals into every CTA
+        const int r = tid / (NV + 1), f = tid - (NV + 1) * (tid / (NV + 1));
+        int v = S.tot[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+            if (f == j) v = t5[j];
         *cl.map_shared_rank(&S.all_tot[c][f], r) = v;
     }
     cl.sync();  // prefixes and every CTA's totals are visible
 
     // 3. bases from the CTAs' totals (every warp computes them itself); row_ptr
     //    of the owned destinations
-    int base[5], grand[6];
+    int base[NV], grand[NV + 1];
     {
-        int v[5] = {0, 0, 0, 0, 0}, m = 0;
+        int v[NV] = {0, 0, 0, 0, 0, 0}, m = 0;
         if (lane < C) {
 #pragma unroll
-            for (int j = 0; j < 5; ++j) v[j] = S.all_tot[lane][j];
-            m = S.all_tot[lane][5];
+            for (int j = 0; j < NV; ++j) v[j] = S.all_tot[lane][j];
+            m = S.all_tot[lane][NV];
         }
-        int in[5] = {v[0], v[1], v[2], v[3], v[4]};
+        int in[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) in[j] = v[j];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
-            for (int j = 0; j < 5; ++j) {
+            for (int j = 0; j < NV; ++j) {
                 const int t = __shfl_up_sync(0xffffffffu, in[j], o);
                 if (lane >= o) in[j] += t;
             }
         }
 #pragma unroll
-        for (int j = 0; j < 5; ++j) {
+        for (int j = 0; j < NV; ++j) {
             base[j] = __shfl_sync(0xffffffffu, in[j] - v[j], c);
             grand[j] = __shfl_sync(0xffffffffu, in[j], 31);
         }
-        grand[5] = __reduce_max_sync(0xffffffffu, m);
+        grand[NV] = __reduce_max_sync(0xffffffffu, m);
     }
     int rstart = v5[0] + base[0];
 #pragma unroll
@@ -705,6 +720,7 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     cluster_arrive_relaxed();
     if (!any_bad) {
         int eA = v5[1] + base[1], eL = grand[1] + v5[2] + base[2], eS = v5[3] + base[3], eC = v5[4] + base[4];
+        int eE = grand[3] + v5[5] + base[5];
 #pragma unroll
         for (int j = 0; j < kOneRowsPerThread; ++j) {
             if (j < nrows) {
@@ -718,8 +734,10 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
                     eA += a;
                 } else if (nch > 1) {
                     seg_units[eL++] = make_int4(m, -1, 0, 0);
-                } else {
+                } else if (nch == 1) {
                     row_units[eS++] = make_int4(m, -1, 0, 0);
+                } else {
+                    row_units[eE++] = make_int4(m, -1, 0, 0);
                 }
             }
         }
@@ -730,11 +748,12 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
         if (tid == kCtrErrIndex) v = any_bad ? 1 : 0;
         else if (!any_bad && tid == kCtrSegs) v = grand[1];
         else if (!any_bad && tid == kCtrLong) v = grand[2];
-        else if (!any_bad && tid == kCtrNormal) v = grand[2] + grand[3];
+        else if (!any_bad && tid == kCtrNormal) v = grand[2] + grand[3] + grand[5];
         else if (!any_bad && tid == kCtrHot) v = grand[4];
-        else if (!any_bad && tid == kCtrMaxLen) v = grand[5];
+        else if (!any_bad && tid == kCtrMaxLen) v = grand[NV];
         else if (!any_bad && tid == kCtrBig) v = grand[1] + grand[2];
         else if (!any_bad && tid == kCtrShort) v = grand[3];
+        else if (!any_bad && tid == kCtrEmpty) v = grand[5];
         counters[tid] = v;
     }
     cluster_wait();  // no CTA leaves while another may still read its shared memory

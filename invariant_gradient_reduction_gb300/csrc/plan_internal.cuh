@@ -21,7 +21,8 @@ enum {
     kCtrErrTimeout = 6,  // a bounded wait inside a reduce kernel expired
     kCtrLong = 7,      // whole-destination units of 2..2^g chunks (in seg_units, after the segments)
     kCtrBig = 8,       // units of more than one chunk: hot segments + long whole rows
-    kCtrShort = 9,     // whole-destination units of one chunk or less (row_units)
+    kCtrShort = 9,     // whole-destination units of 1..32 terms (row_units)
+    kCtrEmpty = 10,    // destinations without terms (row_units, after the short ones)
     kCtrCount = 16
 };
 
@@ -50,7 +51,8 @@ det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, 
 //   seg_units[u] = {row m, segment s, partial slot, 0} for the hot segments,
 //                  then {row m, -1, 0, 0} for the n_long whole-row units of
 //                  2..2^g chunks: the units with more than one chunk;
-//   row_units[u] = {row m, -1, 0, 0} for the other whole-row units;
+//   row_units[u] = {row m, -1, 0, 0} for the other whole-row units: those
+//                  with terms, then the empty ones (which index_add skips);
 //   finish[k]    = {row m, first partial slot, number of segments, 0}.
 // Work unit u of the reduce is seg_units[u] for u < n_segments + n_long,
 // else row_units[u - n_segments - n_long] (the longest units first).
@@ -65,6 +67,6 @@ struct det_plan_s {
     int4* seg_units = nullptr;
     int4* row_units = nullptr;
     int4* finish = nullptr;
-    int64_t n_units = 0, n_segments = 0, n_hot_rows = 0, max_row_len = 0, n_long = 0;
+    int64_t n_units = 0, n_segments = 0, n_hot_rows = 0, max_row_len = 0, n_long = 0, n_empty = 0;
     bool counts_on_host = true;      // false for an async plan until det_plan_status
 };
