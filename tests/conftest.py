@@ -18,3 +18,13 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture
+def replay(request):
+    """The replay harness (tests/replay.py).  With DETR_REPLAY_LOG=<file> set,
+    the fingerprint of every replayed call is appended to that file."""
+    from replay import Replay
+    r = Replay()
+    yield r
+    r.write_log(os.environ.get("DETR_REPLAY_LOG"), request.node.nodeid)

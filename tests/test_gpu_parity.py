@@ -208,24 +208,26 @@ def test_gather_path_changes_no_bit(name):
         assert_bytes_equal(np_bits(out), want, f"{name} path={path}")
 
 
-def test_replays_identical_under_contention():
-    """R replays give identical bytes and identical fingerprints, also while a side
-    stream runs matmuls (the pages' contention replay)."""
+def test_replays_identical_under_contention(replay):
+    """R replays give identical bytes and identical fingerprints while a side
+    stream runs matmuls (the pages' contention replay), for the scatter-reduce,
+    index_add, split-K and an unwaited plan + reduce."""
     case = small_case("sparse_key_scatter")
     base, plan = gpu_scatter(case)
-    want = np_bits(base)
-    h0 = dr.det_hash(base).item()
-    side = torch.cuda.Stream()
-    a = torch.randn(2048, 2048, device=DEV)
-    for r in range(6):
-        with torch.cuda.stream(side):
-            for _ in range(4):
-                a = a @ a.T * 1e-3
-        out = torch.empty_like(base)
-        dr.det_scatter_reduce(plan, case.x, out, w=case.w)
-        torch.cuda.synchronize()
-        assert dr.det_hash(out).item() == h0
-        assert_bytes_equal(np_bits(out), want, f"replay {r}")
+    out = replay.identical(lambda: dr.det_scatter_reduce(plan, case.x, torch.empty_like(base), w=case.w),
+                           name="scatter_reduce")
+    assert_bytes_equal(np_bits(out), np_bits(base), "replay")
+    init = torch.randn_like(base)
+    replay.identical(lambda: dr.det_index_add(plan, case.x, init.clone(), w=case.w), name="index_add")
+
+    def unwaited():
+        p = dr.det_reduce_plan(case.idx, case.M, opts={"async_plan": 1})
+        o = dr.det_scatter_reduce(p, case.x, torch.empty_like(base), w=case.w, opts={"async_plan": 1})
+        dr.det_plan_status(p)
+        return o
+    assert_bytes_equal(np_bits(replay.identical(unwaited, name="plan+reduce")), np_bits(base), "unwaited")
+    P = wl.make("splitk", "small", device=DEV)
+    replay.identical(lambda: dr.det_splitk_reduce(P, torch.empty(P.shape[1], device=DEV)), name="splitk")
 
 
 @pytest.mark.parametrize("P", [1, 2, 4, 8])
@@ -499,22 +501,17 @@ def test_atomic_baseline_bf16_and_index_errors():
     assert e.value.code == dr.DET_ERR_INDEX_RANGE
 
 
-def test_atomic_negative_control_differs_across_replays():
+def test_atomic_negative_control_differs_across_replays(replay):
     """The pages' negative control: the atomic path on hot keys is not byte-repeatable,
-    which shows the replay check is sensitive.  The deterministic path on the same
-    input is (see the replay test)."""
+    which shows the replay check is sensitive; the deterministic path on the same
+    input is."""
     case = wl.sparse_key_scatter(2048, 512, 8192, 128, device=DEV, seed=77)
-    ref = None
-    differing = 0
-    for r in range(6):
-        out = torch.empty(case.M, case.H, device=DEV)
-        dr.det_atomic_scatter_reduce(case.idx, case.M, case.x, out)
-        b = out.view(torch.int32).clone()
-        if ref is None:
-            ref = b
-        elif not torch.equal(b, ref):
-            differing += 1
-    assert differing > 0
+    replay.runs = 6
+    assert replay.differing(lambda: dr.det_atomic_scatter_reduce(
+        case.idx, case.M, case.x, torch.empty(case.M, case.H, device=DEV)), name="atomic") > 0
+    plan = dr.det_reduce_plan(case.idx, case.M)
+    replay.identical(lambda: dr.det_scatter_reduce(plan, case.x, torch.empty(case.M, case.H, device=DEV)),
+                     name="deterministic")
 
 
 # --------------------------------------------------------------------------
