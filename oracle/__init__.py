@@ -69,6 +69,10 @@ def _load():
         lib.oracle_mix64.restype = u64
         lib.oracle_hash.argtypes = [vp, u64]
         lib.oracle_hash.restype = u64
+        lib.oracle_router_topk.argtypes = [vp, i64, i32, i64, i32, i32, vp, vp]
+        lib.oracle_router_topk.restype = ctypes.c_int
+        lib.oracle_moe_route.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp]
+        lib.oracle_moe_route.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -197,3 +201,43 @@ def hash_bytes(buf) -> int:
         a = np.zeros(1, dtype=np.uint8)
         return int(_load().oracle_hash(_ptr(a), 0))
     return int(_load().oracle_hash(_ptr(a), a.size))
+
+
+def router_topk(scores, k: int, renormalize: bool = False):
+    """(ids int32 [T, k], w float32 [T, k]): each token's k greatest scores, greatest first.
+
+    Order: IEEE 754 totalOrder of the binary32 scores, the lower expert id
+    first among equal bit patterns.  ``renormalize``: w[r] / (w[0] + ... +
+    w[k-1]), the sum taken left to right in binary32 (oracle.c states the
+    definition).
+    """
+    s = np.ascontiguousarray(scores, dtype=np.float32)
+    T, E = s.shape
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    rc = _load().oracle_router_topk(_ptr(s), T, E, E, k, 1 if renormalize else 0, _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise OracleError(rc, "router_topk")
+    return ids, w
+
+
+def moe_route(ids, E: int, w=None):
+    """Dispatch layout of top-k routing (stable counting sort of the slots by expert).
+
+    ``ids`` int32 [T, k], ``w`` float32 [T, k] or None.  Returns
+    (expert_offsets int64 [E+1], row_token int32 [T*k], row_w float32 [T*k] or
+    None, slot_row int32 [T*k]).
+    """
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, k = ids.shape
+    N = T * k
+    wv = None if w is None else np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+    off = np.empty(E + 1, dtype=np.int64)
+    row_token = np.empty(max(N, 1), dtype=np.int32)
+    slot_row = np.empty(max(N, 1), dtype=np.int32)
+    row_w = None if wv is None else np.empty(max(N, 1), dtype=np.float32)
+    rc = _load().oracle_moe_route(_ptr(ids), _ptr(wv), T, k, E, _ptr(off), _ptr(row_token), _ptr(row_w),
+                                  _ptr(slot_row))
+    if rc != 0:
+        raise OracleError(rc, "moe_route")
+    return off, row_token[:N], None if row_w is None else row_w[:N], slot_row[:N]

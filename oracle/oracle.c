@@ -362,3 +362,100 @@ uint64_t oracle_hash(const void* p, uint64_t nbytes)
     }
     return h;
 }
+
+/* ------------------------------------------------------------------ */
+/* sorted router top-k and the MoE dispatch layout                     */
+/* ------------------------------------------------------------------ */
+
+/*
+ * The sorted router top-k is one of the hot spots of the deterministic path
+ * ("Megatron-LM determinism developer reference", section 3.3); the pages
+ * give no tie rule, so this library fixes one:
+ *   - scores are ordered by IEEE 754 totalOrder (so -0.0 < +0.0, +inf below
+ *     every positive NaN, -inf above every negative NaN): the unsigned order
+ *     of the bit pattern with its sign bit set when it was clear, and all
+ *     bits inverted when it was set;
+ *   - among equal bit patterns the lower expert id ranks first.
+ * Position r of token t's list is the r-th greatest score under that order.
+ */
+static uint32_t or_total_order_key(float f)
+{
+    uint32_t u = or_bits(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+/*
+ * ids[t][r], w[t][r] for r < k: the selection by repeated maximum -- round r
+ * takes, among the experts not taken yet, the one of greatest key, scanning e
+ * upwards and replacing only on a strictly greater key (so the lowest id
+ * wins a tie).  renormalize != 0: sum = w[0] + w[1] + ... + w[k-1] added
+ * left to right in binary32 from w[0], then each w[r] = fl32(w[r] / sum).
+ * scores[t][e] sits at scores[t * lds + e].  1 <= k <= E.
+ */
+int oracle_router_topk(const float* scores, int64_t T, int32_t E, int64_t lds, int32_t k, int32_t renormalize,
+                       int32_t* ids, float* w)
+{
+    if (T < 0 || E < 1 || k < 1 || k > E || lds < E || (T > 0 && (!scores || !ids || !w))) return OR_ERR_ARG;
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    if (!taken) return OR_ERR_NOMEM;
+    for (int64_t t = 0; t < T; ++t) {
+        const float* s = scores + t * lds;
+        memset(taken, 0, (size_t)E);
+        for (int32_t r = 0; r < k; ++r) {
+            int32_t best = -1;
+            uint32_t best_key = 0;
+            for (int32_t e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                uint32_t key = or_total_order_key(s[e]);
+                if (best < 0 || key > best_key) { best = e; best_key = key; }
+            }
+            taken[best] = 1;
+            ids[t * k + r] = best;
+            w[t * k + r] = s[best];
+        }
+        if (renormalize) {
+            float sum = w[t * k];
+            for (int32_t r = 1; r < k; ++r) sum = sum + w[t * k + r];
+            for (int32_t r = 0; r < k; ++r) w[t * k + r] = w[t * k + r] / sum;
+        }
+    }
+    free(taken);
+    return OR_OK;
+}
+
+/*
+ * The dispatch layout of top-k routing: slot i = t * k + j (token t's j-th
+ * choice, expert ids[i]) goes to dispatch row slot_row[i], the rows grouped
+ * by expert in ascending expert id and, inside an expert, in ascending slot
+ * -- for distinct choices per token the stable (expert id, original token
+ * id) order of the MoE backward ("DeepSeek-V4 book, Ch 09", section 3.2).
+ * Written as the textbook stable counting sort:
+ *   expert_offsets[e] = number of slots whose expert is below e (E+1 values);
+ *   walking the slots upwards, each takes the next free row of its expert;
+ *   row_token[p] = token of the slot at row p, row_w[p] = its weight (w may
+ *   be NULL, then row_w is not written).
+ * An expert id outside [0, E) gives OR_ERR_INDEX.
+ */
+int oracle_moe_route(const int32_t* ids, const float* w, int64_t T, int32_t k, int32_t E,
+                     int64_t* expert_offsets, int32_t* row_token, float* row_w, int32_t* slot_row)
+{
+    if (T < 0 || k < 0 || E < 1 || !expert_offsets) return OR_ERR_ARG;
+    const int64_t N = T * (int64_t)k;
+    if (N > 0 && (!ids || !row_token || !slot_row || (w && !row_w))) return OR_ERR_ARG;
+    for (int64_t i = 0; i < N; ++i)
+        if (ids[i] < 0 || ids[i] >= E) return OR_ERR_INDEX;
+    for (int32_t e = 0; e <= E; ++e) expert_offsets[e] = 0;
+    for (int64_t i = 0; i < N; ++i) expert_offsets[ids[i] + 1] += 1;     /* counts */
+    for (int32_t e = 0; e < E; ++e) expert_offsets[e + 1] += expert_offsets[e];
+    int64_t* next = (int64_t*)malloc((size_t)E * sizeof(int64_t));
+    if (!next) return OR_ERR_NOMEM;
+    for (int32_t e = 0; e < E; ++e) next[e] = expert_offsets[e];
+    for (int64_t i = 0; i < N; ++i) {
+        int64_t p = next[ids[i]]++;
+        slot_row[i] = (int32_t)p;
+        row_token[p] = (int32_t)(i / k);
+        if (w) row_w[p] = w[i];
+    }
+    free(next);
+    return OR_OK;
+}

@@ -581,3 +581,148 @@ def test_index_add_bf16_out_rounds_once(oracle_mod):
     S = oracle_mod.scatter_reduce(idx, x, M)
     want = (torch.from_numpy(init_b.float().numpy() + S)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert got.tobytes() == want.tobytes()
+
+
+# --------------------------------------------------------------------------
+# sorted router top-k and the MoE dispatch layout
+# --------------------------------------------------------------------------
+
+def _golden_cases(name):
+    """Blocks of `key value...` lines; `case <name>` starts a new block."""
+    cases, cur = [], {}
+    with open(os.path.join(HERE, "golden", name)) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "case":
+                cur = {"name": vals[0]}
+                cases.append(cur)
+            else:
+                cur[key] = vals
+    return cases or [cur]
+
+
+def _hexf(vals):
+    return np.array([int(v, 16) for v in vals], dtype=np.uint32).view(np.float32)
+
+
+@pytest.mark.parametrize("case", _golden_cases("router_topk_hand.txt"), ids=lambda c: c["name"])
+def test_router_topk_hand_cases(oracle_mod, case):
+    """Hand-derived order, tie and renormalisation cases (totalOrder, lower id first, left-to-right sum)."""
+    s = _hexf(case["scores"]).reshape(1, -1)
+    k = int(case["k"][0])
+    ids, w = oracle_mod.router_topk(s, k, renormalize=case["renormalize"][0] == "1")
+    assert ids.reshape(-1).tolist() == [int(v) for v in case["ids"]]
+    assert w.reshape(-1).view(np.uint32).tolist() == _hexf(case["w"]).view(np.uint32).tolist()
+
+
+def test_router_topk_is_torch_stable_sort(oracle_mod):
+    """Without signed zeros and NaN, totalOrder is the numeric order: the selection is the head of
+    torch's stable descending sort (equal scores keep ascending expert order), also checked with
+    Python's sorted().  Scores come from a small set so that ties are everywhere."""
+    rng = np.random.default_rng(11)
+    for T, E, k in [(64, 8, 2), (200, 128, 8), (33, 256, 8), (5, 7, 7), (40, 96, 1)]:
+        s = (rng.integers(-12, 13, size=(T, E)).astype(np.float32) / f32(8))
+        s[rng.random((T, E)) < 0.05] = np.inf
+        s[rng.random((T, E)) < 0.05] = -np.inf
+        s[s == 0] = f32(0.0)  # +0.0 only
+        ids, w = oracle_mod.router_topk(s, k)
+        ref = torch.sort(torch.from_numpy(s), dim=1, descending=True, stable=True).indices[:, :k].numpy()
+        assert np.array_equal(ids, ref.astype(np.int32))
+        for t in range(0, T, 7):
+            order = sorted(range(E), key=lambda e: (-float(s[t, e]), e))[:k]
+            assert ids[t].tolist() == order
+        assert np.array_equal(w.view(np.uint32), np.take_along_axis(s, ids.astype(np.int64), 1).view(np.uint32))
+
+
+def test_router_topk_renormalise_exact_sums(oracle_mod):
+    """Dyadic scores with few bits: the binary32 sum is exact, so each weight is the correctly
+    rounded quotient, which a binary64 quotient rounded once to binary32 gives (double rounding is
+    innocuous for division when 53 >= 2*24 + 2)."""
+    rng = np.random.default_rng(12)
+    s = rng.integers(1, 256, size=(300, 64)).astype(np.float32) * f32(2.0 ** -10)
+    ids, w = oracle_mod.router_topk(s, 8, renormalize=True)
+    top = np.take_along_axis(s, ids.astype(np.int64), 1).astype(np.float64)
+    expect = (top / top.sum(axis=1, keepdims=True)).astype(np.float32)
+    assert np.array_equal(w.view(np.uint32), expect.view(np.uint32))
+    # general inputs: the weights sum to 1 within a few ulp
+    s = rng.random((300, 64), dtype=np.float32)
+    _, w = oracle_mod.router_topk(s, 8, renormalize=True)
+    assert np.all(np.abs(w.astype(np.float64).sum(axis=1) - 1.0) < 8 * 2.0 ** -24 * 8)
+
+
+def test_router_topk_special_values_dominate(oracle_mod):
+    """With NaN, infinities, signed zeros and subnormals mixed in: the list is strictly decreasing in
+    (totalOrder key, -expert), and every chosen key beats every unchosen one.  The key here is built
+    from the sign and magnitude bits by comparisons, not by the oracle's bit trick."""
+    rng = np.random.default_rng(13)
+    T, E, k = 64, 40, 6
+    pool = np.array([np.nan, -np.nan, np.inf, -np.inf, 0.0, -0.0, 1e-45, -1e-45, 1.0, -1.0, 0.5, 3.0],
+                    dtype=np.float32)
+    s = pool[rng.integers(0, pool.size, size=(T, E))]
+    ids, _ = oracle_mod.router_topk(s, k)
+    u = s.view(np.uint32).astype(np.int64)
+    neg = u >= 2 ** 31
+    mag = u & 0x7FFFFFFF
+    key = np.where(neg, -mag - 1, mag)  # negatives below positives, larger magnitude lower
+    for t in range(T):
+        chosen = [(key[t, e], -e) for e in ids[t]]
+        assert chosen == sorted(chosen, reverse=True) and len(set(ids[t])) == k
+        rest = [(key[t, e], -e) for e in range(E) if e not in set(ids[t].tolist())]
+        assert min(chosen) > max(rest)
+
+
+def test_moe_route_hand_example(oracle_mod):
+    """The hand-derived T=3, k=2, E=6 layout (two experts without tokens) and its combine lists."""
+    g = _golden_cases("moe_route_hand.txt")[0]
+    T, k, E = int(g["T"][0]), int(g["k"][0]), int(g["E"][0])
+    ids = np.array([int(v) for v in g["ids"]], np.int32).reshape(T, k)
+    w = np.array([float(v) for v in g["w"]], np.float32).reshape(T, k)
+    off, row_token, row_w, slot_row = oracle_mod.moe_route(ids, E, w)
+    assert off.tolist() == [int(v) for v in g["expert_offsets"]]
+    assert row_token.tolist() == [int(v) for v in g["row_token"]]
+    assert slot_row.tolist() == [int(v) for v in g["slot_row"]]
+    row_slot = [int(v) for v in g["row_slot"]]
+    assert np.array_equal(row_w.view(np.uint32), w.reshape(-1)[row_slot].view(np.uint32))
+    row_ptr, perm = oracle_mod.build_lists(row_token, T)
+    assert row_ptr.tolist() == [int(v) for v in g["combine_row_ptr"]]
+    assert perm.tolist() == [int(v) for v in g["combine_perm"]]
+
+
+def test_moe_route_rank_formula(oracle_mod):
+    """Row of slot i = (slots with a lower expert) + (earlier slots with the same expert), computed
+    all-pairs; for distinct choices per token it is also the rank of the key e*T + t, the (expert id,
+    token id) order the workload generator uses."""
+    rng = np.random.default_rng(14)
+    for T, k, E, distinct in [(64, 2, 8, True), (50, 8, 16, True), (40, 3, 5, False), (1, 4, 4, True),
+                              (7, 1, 300, True)]:
+        if distinct:
+            ids = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+        else:
+            ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+        w = rng.random((T, k), dtype=np.float32)
+        off, row_token, row_w, slot_row = oracle_mod.moe_route(ids, E, w)
+        f = ids.reshape(-1).astype(np.int64)
+        N = f.size
+        lower = (f[None, :] < f[:, None]).sum(axis=1)
+        same_before = np.tril(f[None, :] == f[:, None], k=-1).sum(axis=1)
+        assert np.array_equal(slot_row, (lower + same_before).astype(np.int32))
+        assert np.array_equal(off, np.array([(f < e).sum() for e in range(E + 1)]))
+        assert sorted(slot_row.tolist()) == list(range(N))
+        inv = np.empty(N, np.int64)
+        inv[slot_row] = np.arange(N)
+        assert np.array_equal(row_token, (inv // k).astype(np.int32))
+        assert np.array_equal(row_w.view(np.uint32), w.reshape(-1)[inv].view(np.uint32))
+        if distinct:
+            t = np.repeat(np.arange(T), k)
+            assert np.array_equal(inv, np.argsort(f * T + t, kind="stable"))
+
+
+def test_moe_route_rejects_bad_ids(oracle_mod):
+    for bad in (-1, 6):
+        ids = np.array([[0, 1], [2, bad]], np.int32)
+        with pytest.raises(oracle_mod.OracleError) as ei:
+            oracle_mod.moe_route(ids, 6)
+        assert ei.value.code == -2
