@@ -53,6 +53,8 @@ WORKLOADS = {
     "ep_invariance": "ep_invariance T=16384 E=256 top-k=8 H=7168 bf16 x, fp32 w -> bf16 out",
     "splitk": "splitk S=56 R=16384 C=24 fp32 -> fp32",
     "embedding_backward": "embedding_backward T=32768 tokens V=131072 zipf=1.0 H=4096 bf16 dY, index_add into fp32 grad",
+    "moe_route": "moe_route T=4096 E=128 top-k=8 H=4096: softmax scores -> sorted top-k -> route plan -> combine, "
+                 "bf16 x -> bf16 out",
 }
 
 
@@ -364,6 +366,68 @@ def measure_index_add(case, timer, steps, warmup, torch):
             "plan": {k: v for k, v in d.items() if k not in ("row_ptr", "perm")}}
 
 
+def measure_moe_route(timer, steps, warmup, torch, device):
+    """The MoE combine driven by the route plan: router scores (T=4096, E=128) ->
+    sorted top-8 (renormalised) -> dispatch layout + combine plan from the ids
+    -> the combine of bf16 expert outputs [32768, 4096] in dispatch order.
+    Compulsory bytes as for the MoE combine (x, out, ids, weights); the
+    top-k leg adds the scores."""
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    from invariant_gradient_reduction_gb300 import workloads as wl
+    T, E, k, H = 4096, 128, 8, 4096
+    N = T * k
+    scores = wl.router_scores(T, E, seed=2, device=device)
+    ids, tw = dr.det_router_topk(scores, k, renormalize=True)
+    x = wl._fill_normal((N, H), torch.bfloat16, 1.0, 2 * 7919 + 1, device)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    ws = torch.empty(dr.det_moe_route_workspace_size(T, k, E, ASYNC) + 256, dtype=torch.uint8, device=device)
+    arrays = {"expert_offsets": torch.empty(E + 1, dtype=torch.int32, device=device),
+              "row_token": torch.empty(N, dtype=torch.int32, device=device),
+              "row_w": torch.empty(N, dtype=torch.float32, device=device), "slot_row": None}
+    topk_out = (torch.empty_like(ids), torch.empty_like(tw))
+    state = {}
+
+    def route():
+        p, _ = dr.det_moe_route_plan(ids, E, tw, opts=ASYNC, workspace=ws, out=arrays)
+        state["plan"] = p
+        return p
+
+    def route_combine():
+        dr.det_scatter_reduce(route(), x, out, w=arrays["row_w"], opts=ASYNC)
+
+    def topk_route_combine():
+        dr.det_router_topk(scores, k, renormalize=True, out=topk_out)
+        p, _ = dr.det_moe_route_plan(topk_out[0], E, topk_out[1], opts=ASYNC, workspace=ws, out=arrays)
+        state["plan"] = p
+        dr.det_scatter_reduce(p, x, out, w=arrays["row_w"], opts=ASYNC)
+
+    ws_dest = torch.empty(dr.det_plan_workspace_size(N, T) + 256, dtype=torch.uint8, device=device)
+
+    def dest_combine():
+        p = dr.det_reduce_plan(arrays["row_token"], T, workspace=ws_dest, opts=ASYNC)
+        state["plan"] = p
+        dr.det_scatter_reduce(p, x, out, w=arrays["row_w"], opts=ASYNC)
+
+    res = {}
+    cb = N * H * 2 + T * H * 2 + N * 4 + N * 4
+    for name, fn, nbytes in (("route_plan_combine", route_combine, cb),
+                             ("topk_route_plan_combine", topk_route_combine, cb + T * E * 4),
+                             ("destination_plan_combine", dest_combine, cb),
+                             ("route_plan_only", route, None),
+                             ("router_topk_only", lambda: dr.det_router_topk(scores, k, renormalize=True,
+                                                                             out=topk_out), None)):
+        t, launches = timer.run(fn, steps, warmup)
+        if "plan" in state:
+            dr.det_plan_status(state.pop("plan"))
+        ms = statistics.mean(t)
+        r = {"ms": ms, "launches_per_step": launches / max(1, steps)}
+        if nbytes:
+            r["gbs"] = gbs(nbytes, ms)
+        res[name] = r
+    fp = dr.det_hash(out).item() & (2 ** 64 - 1)
+    return {"compulsory_bytes": cb, "fingerprint": f"{fp:016x}", **res}
+
+
 def measure_splitk(timer, steps, warmup, torch, device):
     from invariant_gradient_reduction_gb300 import detreduce as dr
     from invariant_gradient_reduction_gb300 import workloads as wl
@@ -508,6 +572,11 @@ def run_ours(args):
             also[name] = r2
             del c2
             torch.cuda.empty_cache()
+        r4 = measure_moe_route(timer, max(5, min(args.steps, 30)), args.warmup, torch, device)
+        r4["frac_route_plan_combine"] = r4["route_plan_combine"]["gbs"] / peaks["hbm_gbs"]
+        r4["workload"] = WORKLOADS["moe_route"]
+        also["moe_route"] = r4
+        torch.cuda.empty_cache()
         also["splitk"] = measure_splitk(timer, max(10, min(args.steps, 50)), args.warmup, torch, device)
         also["splitk"]["workload"] = WORKLOADS["splitk"]
         c3 = make_case("embedding_backward", device)

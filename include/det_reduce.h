@@ -330,6 +330,77 @@ det_status det_splitk_reduce(const float* partials, int32_t S, int64_t count, in
 det_status det_hash(const void* p, uint64_t nbytes, uint64_t* out, void* stream);
 
 /*
+ * Sorted router top-k: for each token t, the k experts of greatest score,
+ * greatest first.  The pages name the sorted router top-k among the hot
+ * spots of the deterministic path ("Megatron-LM determinism developer
+ * reference", section 3.3) but fix no tie rule; this library's:
+ *   order  IEEE 754 totalOrder of the binary32 scores (-0.0 below +0.0, +NaN
+ *          above +inf, -NaN below -inf), and among equal bit patterns the
+ *          lower expert id first;
+ *   w      the chosen scores, bit for bit; with renormalize != 0 each divided
+ *          (one binary32 division, nearest even) by their binary32 sum taken
+ *          left to right from the greatest.
+ * The score function (softmax, sigmoid, ...) is the caller's: scores may be
+ * probabilities or logits.
+ *  scores    dev float [T][lds], lds >= E.
+ *  topk_ids  dev int32 [T][k].
+ *  topk_w    dev float [T][k], or NULL for ids only (not with renormalize).
+ *  1 <= k <= E.  Outputs must not overlap scores or each other.
+ * Errors: DET_ERR_ARG, DET_ERR_UNSUPPORTED (E > 1024, k > 32, T*k >= 2^31-1),
+ * DET_ERR_CUDA.
+ */
+det_status det_router_topk(const float* scores, int64_t T, int32_t E, int64_t lds, int32_t k,
+                           int32_t renormalize, int32_t* topk_ids, float* topk_w, void* stream);
+
+/* Bytes of device workspace det_moe_route_plan needs for T tokens, top-k, E
+ * experts.  Errors: DET_ERR_ARG, DET_ERR_UNSUPPORTED. */
+det_status det_moe_route_workspace_size(int64_t T, int32_t k, int32_t E, const det_opts* opts,
+                                        size_t* bytes);
+
+/*
+ * The integer side of the MoE dispatch and combine, straight from top-k
+ * routing: the dispatch layout and the combine's plan in one call.  Slot
+ * i = t*k + j is token t's j-th choice topk_ids[i].  The dispatch rows are
+ * the slots sorted stably by expert: expert 0's slots in ascending slot
+ * order, then expert 1's, ... -- for distinct choices per token, the stable
+ * (expert id, original token id) order of the MoE backward ("DeepSeek-V4
+ * book, Ch 09: Batch invariance and determinism", section 3.2).  The combine
+ * adds every dispatch row back into its token (the index_add_ of the
+ * Megatron-LM reference's op catalog, section 3.1).
+ *  topk_ids        dev int32 [T*k], each in [0, E) (a token may repeat one).
+ *  topk_w          dev float [T*k] or NULL.
+ *  expert_offsets  dev int32 [E+1]: expert e's rows are
+ *                  [expert_offsets[e], expert_offsets[e+1]); the last is T*k.
+ *  row_token       dev int32 [T*k]: token of each dispatch row (the combine's
+ *                  idx).
+ *  row_w           dev float [T*k] or NULL: topk_w of each dispatch row's
+ *                  slot (needs topk_w).
+ *  slot_row        dev int32 [T*k] or NULL: dispatch row of each slot.
+ *  workspace       dev, >= det_moe_route_workspace_size(T, k, E) bytes,
+ *                  256-byte aligned; holds the plan's arrays afterwards.
+ *  out_plan        host out-param: the combine's plan over M = T
+ *                  destinations, with the same lists and work counts that
+ *                  det_reduce_plan(row_token, NULL, T*k, T) builds.  Use it
+ *                  with det_scatter_reduce / det_index_add on x in dispatch
+ *                  row order and w = row_w.  Release with det_plan_destroy.
+ * Every token has exactly k terms, so the combine lists follow from each
+ * slot's rank in (expert, j) order inside its token; the only sort is the
+ * one by expert.  Small problems (E <= 256, T*k <= 131072) run as one kernel
+ * on a thread-block cluster, others as the destination-list plan over the
+ * expert ids plus two kernels (opts->plan_path 0 = auto, 1 = the latter, 2 =
+ * the cluster kernel or DET_ERR_UNSUPPORTED); both give the same bytes.
+ * opts->async_plan and opts->seg_chunks_log2 as for det_reduce_plan.
+ * Outputs must not overlap the inputs, each other or the workspace.
+ * Errors: DET_ERR_ARG, DET_ERR_WORKSPACE, DET_ERR_UNSUPPORTED,
+ * DET_ERR_INDEX_RANGE (an id outside [0, E): no output is written),
+ * DET_ERR_CUDA.  On error *out_plan is NULL.
+ */
+det_status det_moe_route_plan(const int32_t* topk_ids, const float* topk_w, int64_t T, int32_t k,
+                              int32_t E, int32_t* expert_offsets, int32_t* row_token, float* row_w,
+                              int32_t* slot_row, void* workspace, size_t ws_bytes,
+                              const det_opts* opts, void* stream, det_plan* out_plan);
+
+/*
  * Bytes of workspace det_atomic_scatter_reduce needs: 256 bytes of flags, plus
  * an fp32 [M][H] accumulator when out_dtype is DET_BF16.
  */

@@ -43,7 +43,6 @@ namespace cg = cooperative_groups;
 
 namespace detr {
 
-constexpr int kCluThreads = 1024;
 constexpr int kCluWarps = kCluThreads / 32;
 constexpr int kCluItems = 8;
 constexpr int kCluRadix = 256;
@@ -765,8 +764,8 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
 
 namespace {
 std::mutex g_clu_mu;
-signed char g_clu_ok[2][kMaxDevices][kCluMaxCtas + 1];  // [variant][device][C]: 0 unknown, 1 schedulable, -1 not
-bool g_clu_attr[2][kMaxDevices];
+signed char g_clu_ok[kCluVariants][kMaxDevices][kCluMaxCtas + 1];  // [variant][device][C]: 0 unknown, 1 schedulable, -1 not
+bool g_clu_attr[kCluVariants][kMaxDevices];
 
 int bits_of(int64_t v)
 {
@@ -774,13 +773,12 @@ int bits_of(int64_t v)
     while (v > 0) { ++b; v >>= 1; }
     return b;
 }
+}  // namespace
 
-// Launches one of the two cluster kernels on a cluster of C CTAs; *launched
-// stays false if the device cannot schedule such a cluster.
-template <typename Kern, typename... Args>
-det_status launch_on_cluster(int variant, Kern kern, int C, size_t smem, cudaStream_t st, bool* launched,
-                             Args... args)
+det_status launch_on_cluster(int variant, const void* kern, int C, size_t smem, cudaStream_t st, void** args,
+                             bool* launched)
 {
+    if (variant < 0 || variant >= kCluVariants || C < 1 || C > kCluMaxCtas) return DET_ERR_ARG;
     int dev = 0;
     DETR_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return DET_OK;
@@ -818,12 +816,11 @@ det_status launch_on_cluster(int variant, Kern kern, int C, size_t smem, cudaStr
         g_clu_ok[variant][dev][C] = ok;
     }
     if (ok < 0) return DET_OK;
-    DETR_CUDA(cudaLaunchKernelEx(&cfg, kern, args...));
+    DETR_CUDA(cudaLaunchKernelExC(&cfg, kern, args));
     DETR_LAUNCHED();
     *launched = true;
     return DET_OK;
 }
-}  // namespace
 
 int plan_cluster_ctas(int64_t N, int64_t M)
 {
@@ -841,17 +838,19 @@ det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, 
     *launched = false;
     const int C = plan_cluster_ctas(N, M);
     if (C == 0) return DET_OK;
-    const int E = static_cast<int>(cdiv(N, C));
+    int E = static_cast<int>(cdiv(N, C));
     if (M <= kOneMaxBins && E <= kOneMaxSlice) {
-        const det_status s = launch_on_cluster(1, plan_cluster_one_kernel, C, sizeof(OneShared), st, launched, idx,
-                                               static_cast<long long>(N), static_cast<long long>(M), E,
-                                               std::max(2, bits_of(M - 1)), g, row_ptr, perm, seg_units, row_units, finish,
-                                               counters);
+        long long n = N, m = M;
+        int nbits = std::max(2, bits_of(M - 1));
+        void* args[] = {&idx, &n, &m, &E, &nbits, &g, &row_ptr, &perm, &seg_units, &row_units, &finish, &counters};
+        const det_status s = launch_on_cluster(kCluVariantOnePass, reinterpret_cast<const void*>(plan_cluster_one_kernel),
+                                               C, sizeof(OneShared), st, args, launched);
         if (s || *launched) return s;
     }
-    return launch_on_cluster(0, plan_cluster_kernel, C, sizeof(CluShared), st, launched, idx,
-                             static_cast<long long>(N), static_cast<long long>(M), E, np32, g, row_ptr, perm,
-                             seg_units, row_units, finish, counters);
+    long long n = N, m = M;
+    void* args[] = {&idx, &n, &m, &E, &np32, &g, &row_ptr, &perm, &seg_units, &row_units, &finish, &counters};
+    return launch_on_cluster(kCluVariantTwoPass, reinterpret_cast<const void*>(plan_cluster_kernel), C,
+                             sizeof(CluShared), st, args, launched);
 }
 
 }  // namespace detr

@@ -35,6 +35,24 @@ constexpr int kCluMaxSlice = 8192;
 constexpr int kCluTargetSlice = 2048;
 constexpr int kCluRowsPerThread = 8;
 
+constexpr int kCluThreads = 1024;  // threads of every CTA of a cluster kernel
+
+// Cluster kernels of the library, each with its own cache of whether the
+// device can schedule it.
+enum {
+    kCluVariantTwoPass = 0,    // plan_cluster_kernel
+    kCluVariantOnePass = 1,    // plan_cluster_one_kernel
+    kCluVariantRoute = 2,      // route_cluster_kernel, one variant per items-per-thread count (4 of them)
+    kCluVariants = 6
+};
+
+// Launches a kernel of kCluThreads-thread CTAs on one cluster of C CTAs with
+// `smem` bytes of dynamic shared memory (args as for cudaLaunchKernel).
+// *launched stays false if the device cannot schedule such a cluster; the
+// answer is cached per (variant, device, C).
+det_status launch_on_cluster(int variant, const void* kern, int C, size_t smem, cudaStream_t st, void** args,
+                             bool* launched);
+
 // CTAs the single-cluster plan would use for (N, M); 0 where it does not apply.
 int plan_cluster_ctas(int64_t N, int64_t M);
 

@@ -87,6 +87,9 @@ def _declare(lib):
                                        sz, P(det_opts), vp], i32),
         "det_atomic_index_add": ([vp, i64, i64, P(vp), P(i64), i32, i32, i64, i64, vp, vp, i64, i32, vp,
                                   sz, P(det_opts), vp], i32),
+        "det_router_topk": ([vp, i64, i32, i64, i32, i32, vp, vp, vp], i32),
+        "det_moe_route_workspace_size": ([i64, i32, i32, P(det_opts), P(sz)], i32),
+        "det_moe_route_plan": ([vp, vp, i64, i32, i32, vp, vp, vp, vp, vp, sz, P(det_opts), vp, P(vp)], i32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -245,6 +248,72 @@ def plan_lists(plan: Plan):
     row_ptr = ws[rp_off:rp_off + 4 * (plan.M + 1)].view(torch.int32)
     perm = ws[pm_off:pm_off + 4 * plan.N].view(torch.int32)
     return row_ptr, perm
+
+
+def det_router_topk(scores: torch.Tensor, k: int, renormalize: bool = False, with_weights: bool = True,
+                    stream=None, out: Optional[tuple] = None):
+    """(ids int32 [T, k], w float32 [T, k] or None): each token's k greatest scores, greatest first.
+
+    ``scores`` float32 [T, E] (rows may be padded).  Order and renormalisation
+    as in det_router_topk of det_reduce.h.  ``out`` = (ids, w) to write into.
+    """
+    if scores.dtype != torch.float32:
+        raise ValueError("scores must be float32")
+    lds, E = _rows(scores)
+    T = scores.shape[0]
+    if out is not None:
+        ids, w = out
+    else:
+        ids = torch.empty((T, k), dtype=torch.int32, device=scores.device)
+        w = torch.empty((T, k), dtype=torch.float32, device=scores.device) if (with_weights or renormalize) else None
+    _check(lib().det_router_topk(_ptr(scores), T, E, lds, k, int(bool(renormalize)), _ptr(ids), _ptr(w),
+                                 _stream(stream)), "det_router_topk")
+    return ids, w
+
+
+def det_moe_route_workspace_size(T: int, k: int, E: int, opts: Optional[dict] = None) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().det_moe_route_workspace_size(T, k, E, _opts(opts), ctypes.byref(out)),
+           "det_moe_route_workspace_size")
+    return out.value
+
+
+def det_moe_route_plan(topk_ids: torch.Tensor, E: int, topk_w: Optional[torch.Tensor] = None,
+                       opts: Optional[dict] = None, stream=None, workspace: Optional[torch.Tensor] = None,
+                       with_slot_row: bool = True, out: Optional[dict] = None):
+    """Dispatch layout + combine plan of top-k routing (``topk_ids`` int32 [T, k], device).
+
+    Returns (plan, arrays): ``plan`` is the combine's Plan over M = T tokens;
+    ``arrays`` holds the device tensors expert_offsets int32 [E+1], row_token
+    int32 [T*k], row_w float32 [T*k] (None without topk_w) and slot_row int32
+    [T*k] (None unless with_slot_row).  ``out`` may give these tensors to
+    write into (same keys).
+    """
+    if topk_ids.dtype != torch.int32 or not topk_ids.is_contiguous() or topk_ids.dim() != 2:
+        raise ValueError("topk_ids must be a contiguous int32 [T, k] tensor")
+    if topk_w is not None and (topk_w.dtype != torch.float32 or not topk_w.is_contiguous()
+                               or topk_w.shape != topk_ids.shape):
+        raise ValueError("topk_w must be a contiguous float32 tensor shaped like topk_ids")
+    T, k = topk_ids.shape
+    N = T * k
+    dev = topk_ids.device
+    o = dict(out or {})
+    if "expert_offsets" not in o:
+        o["expert_offsets"] = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if "row_token" not in o:
+        o["row_token"] = torch.empty(N, dtype=torch.int32, device=dev)
+    if "row_w" not in o:
+        o["row_w"] = torch.empty(N, dtype=torch.float32, device=dev) if topk_w is not None else None
+    if "slot_row" not in o:
+        o["slot_row"] = torch.empty(N, dtype=torch.int32, device=dev) if with_slot_row else None
+    need = det_moe_route_workspace_size(T, k, E, opts)
+    ws = _workspace(need, dev, workspace)
+    h = ctypes.c_void_p(None)
+    _check(lib().det_moe_route_plan(_ptr(topk_ids), _ptr(topk_w), T, k, E, _ptr(o["expert_offsets"]),
+                                    _ptr(o["row_token"]), _ptr(o["row_w"]), _ptr(o["slot_row"]), _aligned_ptr(ws),
+                                    _aligned_bytes(ws), _opts(opts), _stream(stream), ctypes.byref(h)),
+           "det_moe_route_plan")
+    return Plan(h, ws, N, T), o
 
 
 def det_scatter_workspace_size(plan: Plan, H: int) -> int:

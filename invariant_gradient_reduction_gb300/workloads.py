@@ -19,6 +19,9 @@ Workloads (shapes follow the cases the pages name):
     Gumbel-top-k; rank -> key id through a seeded permutation so hot keys are
     scattered; source order i = q*K + j with keys ascending in a query;
     contributions N(0, sigma^2) in bf16; no weight.
+  * Router scores for the sorted router top-k and the route plan: softmax
+    probabilities of N(0,1) logits [T, E] (the score function is the caller's,
+    so the inputs are the probabilities themselves).
   * Split-K partials (Ch 09, section 3.3): [S, R*C] float32, values
     z * 2^U with z ~ N(0,1), U ~ Uniform[-8, 8) (mixed magnitudes).
 """
@@ -92,6 +95,13 @@ def moe_routing(T: int, E: int, k: int, seed: int):
     top = probs.gather(1, order)
     top = top / top.sum(dim=1, keepdim=True)
     return order, top.float()
+
+
+def router_scores(T: int, E: int, seed: int, device="cpu") -> torch.Tensor:
+    """float32 [T, E] router probabilities: softmax of N(0,1) logits, taken in fp64 and rounded once."""
+    g = _cpu_gen(seed)
+    logits = torch.randn(T, E, generator=g, dtype=torch.float32)
+    return torch.softmax(logits.double(), dim=1).float().to(device)
 
 
 def moe_combine(T: int, E: int, k: int, H: int, x_dtype=torch.bfloat16, out_dtype=torch.bfloat16,

@@ -128,3 +128,46 @@ def test_product_path_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(dr, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         dr.lib()
+
+
+def test_route_host_logic(lib):
+    """Sizes and fail-closed argument checks of the router top-k and the route plan (no CUDA call)."""
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    a = dr.det_moe_route_workspace_size(64, 2, 8)
+    b = dr.det_moe_route_workspace_size(4096, 8, 128)
+    c = dr.det_moe_route_workspace_size(16384, 8, 256)
+    assert 0 < a < b < c
+    assert dr.det_moe_route_workspace_size(0, 8, 8) > 0
+    assert dr.det_moe_route_workspace_size(100, 0, 8) > 0
+    # a long list (k > 32 * 2^g) needs segment units
+    assert dr.det_moe_route_workspace_size(100, 300, 512) > dr.det_moe_route_workspace_size(100, 300, 512, {"seg_chunks_log2": 6})
+    for args, code in [((-1, 2, 8), dr.DET_ERR_ARG), ((4, -1, 8), dr.DET_ERR_ARG), ((4, 2, 0), dr.DET_ERR_ARG),
+                       ((1 << 30, 4, 8), dr.DET_ERR_UNSUPPORTED)]:
+        with pytest.raises(dr.DetError) as e:
+            dr.det_moe_route_workspace_size(*args)
+        assert e.value.code == code
+    L = dr.lib()
+    h = ctypes.c_void_p(None)
+    fake = 1 << 20  # never dereferenced: every call below fails before its first CUDA call
+    # no workspace
+    assert L.det_moe_route_plan(fake, None, 4, 2, 8, fake * 2, fake * 3, None, None, None, 0, None, None,
+                                ctypes.byref(h)) == dr.DET_ERR_WORKSPACE
+    # row_w without topk_w; no expert_offsets; out_plan NULL
+    assert L.det_moe_route_plan(fake, None, 4, 2, 8, fake * 2, fake * 3, fake * 4, None, fake * 8, 1 << 20, None,
+                                None, ctypes.byref(h)) == dr.DET_ERR_ARG
+    assert L.det_moe_route_plan(fake, None, 4, 2, 8, None, fake * 3, None, None, fake * 8, 1 << 20, None, None,
+                                ctypes.byref(h)) == dr.DET_ERR_ARG
+    assert L.det_moe_route_plan(fake, None, 4, 2, 8, fake * 2, fake * 3, None, None, fake * 8, 1 << 20, None, None,
+                                None) == dr.DET_ERR_ARG
+    # an output overlapping the ids
+    assert L.det_moe_route_plan(fake, None, 4, 2, 8, fake * 2, fake + 16, None, None, fake * 8, 1 << 20, None, None,
+                                ctypes.byref(h)) == dr.DET_ERR_ARG
+    assert h.value is None
+    # top-k: k outside [1, E], E or k beyond the kernel's limits, renormalise without weights, overlap
+    for T, E, lds, k, ren, w, code in [(4, 8, 8, 0, 0, fake * 4, dr.DET_ERR_ARG), (4, 8, 8, 9, 0, fake * 4, dr.DET_ERR_ARG),
+                                       (4, 8, 7, 2, 0, fake * 4, dr.DET_ERR_ARG),
+                                       (4, 2048, 2048, 2, 0, fake * 4, dr.DET_ERR_UNSUPPORTED),
+                                       (4, 64, 64, 33, 0, fake * 4, dr.DET_ERR_UNSUPPORTED),
+                                       (4, 8, 8, 2, 1, None, dr.DET_ERR_ARG), (4, 8, 8, 2, 0, fake + 8, dr.DET_ERR_ARG)]:
+        assert L.det_router_topk(fake, T, E, lds, k, ren, fake * 2, w, None) == code
+    assert L.det_router_topk(None, 0, 8, 8, 2, 0, None, None, None) == dr.DET_OK  # nothing to do
