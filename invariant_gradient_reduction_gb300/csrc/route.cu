@@ -11,11 +11,11 @@
 // grid.
 //
 // Top-k: one warp per token.  Lane l holds the keys of experts l, l+32, ...:
-// the score's IEEE totalOrder key in the high word and the complement of the
-// expert id in the low word, so that the greatest 64-bit key is the greatest
-// score with the lowest id.  Round r takes the warp maximum (two 32-bit
-// redux.sync votes: the high word, then the low word among the lanes that
-// hold that high word); the one lane that holds it drops the key.
+// the score's IEEE totalOrder key as the high word and the complement of the
+// expert id as the low word, so that the greatest pair is the greatest score
+// with the lowest id.  Round r takes the warp maximum of the lanes' heads
+// (two 32-bit redux.sync votes: the high word, then the low word among the
+// lanes that hold that high word); the one lane that holds it drops it.
 //
 // Route plan.  Slot i = t*k + j is token t's j-th choice.  The dispatch rows
 // are the slots sorted stably by expert, so the combine's terms of token t
@@ -69,6 +69,77 @@ __device__ __forceinline__ unsigned int total_order_bits(unsigned int key)
     return (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
 }
 
+// Lane state of the top-k selection: the keys of its experts as (hi, lo) =
+// (totalOrder key of the score, 2^32 - 1 - expert id); a larger pair is a
+// greater score, or an equal score with a lower id.  Padding (no expert) is
+// (0, 0), below every real pair, whose lo is at least 2^32 - 1024.
+// Up to 8 keys a lane sorts them once (descending) and the round's winner
+// shifts its list; with more it keeps them unsorted and the winner rescans.
+template <int ITEMS>
+struct TopkLane {
+    unsigned int hi[ITEMS], lo[ITEMS];
+    static constexpr bool kSorted = ITEMS <= 8;
+
+    __device__ __forceinline__ static bool greater(unsigned int ah, unsigned int al, unsigned int bh, unsigned int bl)
+    {
+        return ah > bh || (ah == bh && al > bl);
+    }
+
+    __device__ __forceinline__ void prepare()
+    {
+        if constexpr (kSorted) {
+#pragma unroll
+            for (int pass = 0; pass < ITEMS; ++pass) {  // odd-even transposition sort
+#pragma unroll
+                for (int i = pass & 1; i + 1 < ITEMS; i += 2) {
+                    if (greater(hi[i + 1], lo[i + 1], hi[i], lo[i])) {
+                        const unsigned int th = hi[i], tl = lo[i];
+                        hi[i] = hi[i + 1];
+                        lo[i] = lo[i + 1];
+                        hi[i + 1] = th;
+                        lo[i + 1] = tl;
+                    }
+                }
+            }
+        } else {
+            best_to_front();
+        }
+    }
+
+    // Unsorted lists keep their greatest pair at index 0.
+    __device__ __forceinline__ void best_to_front()
+    {
+#pragma unroll
+        for (int i = 1; i < ITEMS; ++i) {
+            if (greater(hi[i], lo[i], hi[0], lo[0])) {
+                const unsigned int th = hi[i], tl = lo[i];
+                hi[i] = hi[0];
+                lo[i] = lo[0];
+                hi[0] = th;
+                lo[0] = tl;
+            }
+        }
+    }
+
+    // Drops the head (this lane won the round).
+    __device__ __forceinline__ void pop()
+    {
+        if constexpr (kSorted) {
+#pragma unroll
+            for (int i = 0; i + 1 < ITEMS; ++i) {
+                hi[i] = hi[i + 1];
+                lo[i] = lo[i + 1];
+            }
+            hi[ITEMS - 1] = 0u;
+            lo[ITEMS - 1] = 0u;
+        } else {
+            hi[0] = 0u;
+            lo[0] = 0u;
+            best_to_front();
+        }
+    }
+};
+
 template <int ITEMS>
 __global__ void __launch_bounds__(kTopkThreads)
 router_topk_kernel(const unsigned int* __restrict__ scores, long long T, int E, long long lds, int k,
@@ -78,32 +149,20 @@ router_topk_kernel(const unsigned int* __restrict__ scores, long long T, int E, 
     const long long nwarps = static_cast<long long>(gridDim.x) * kTopkWarps;
     for (long long t = static_cast<long long>(blockIdx.x) * kTopkWarps + (threadIdx.x >> 5); t < T; t += nwarps) {
         const unsigned int* s = scores + t * lds;
-        unsigned long long key[ITEMS];
+        TopkLane<ITEMS> L;
 #pragma unroll
         for (int it = 0; it < ITEMS; ++it) {  // all loads first
             const int e = it * 32 + lane;
-            key[it] = e < E ? (static_cast<unsigned long long>(total_order_key(__ldg(s + e))) << 32) |
-                                  (0xFFFFFFFFu - static_cast<unsigned int>(e))
-                            : 0ull;  // below every real key, whose low word is >= 2^32 - 1024
+            L.hi[it] = e < E ? total_order_key(__ldg(s + e)) : 0u;
+            L.lo[it] = e < E ? 0xFFFFFFFFu - static_cast<unsigned int>(e) : 0u;
         }
-        unsigned long long best = key[0];
-#pragma unroll
-        for (int it = 1; it < ITEMS; ++it) best = key[it] > best ? key[it] : best;
+        L.prepare();
         int my_e = 0;
         unsigned int my_s = 0u;
         for (int r = 0; r < k; ++r) {
-            const unsigned int hi = static_cast<unsigned int>(best >> 32);
-            const unsigned int h = __reduce_max_sync(0xffffffffu, hi);
-            const unsigned int l = __reduce_max_sync(0xffffffffu, hi == h ? static_cast<unsigned int>(best) : 0u);
-            const unsigned long long win = (static_cast<unsigned long long>(h) << 32) | l;
-            if (best == win) {  // one lane: the expert ids differ
-                best = 0ull;
-#pragma unroll
-                for (int it = 0; it < ITEMS; ++it) {
-                    if (key[it] == win) key[it] = 0ull;
-                    best = key[it] > best ? key[it] : best;
-                }
-            }
+            const unsigned int h = __reduce_max_sync(0xffffffffu, L.hi[0]);
+            const unsigned int l = __reduce_max_sync(0xffffffffu, L.hi[0] == h ? L.lo[0] : 0u);
+            if (L.hi[0] == h && L.lo[0] == l) L.pop();  // one lane: the expert ids differ
             if (lane == r) {
                 my_e = static_cast<int>(0xFFFFFFFFu - l);
                 my_s = total_order_bits(h);
@@ -198,11 +257,20 @@ struct RouteShared {
 };
 
 // CTA c owns tokens [c*Tc, (c+1)*Tc) and their slots; item it of lane l of
-// warp w is slot w*32*ITEMS + it*32 + l of the slice.
+// warp w is slot w*32*ITEMS + it*32 + l of the slice.  kmagic = ceil(2^32 / k)
+// turns the division of a slice position s < 2^13 by k into a multiply:
+// (s * kmagic) >> 32 exceeds s / k by less than s / 2^32 < 1/k, so its floor
+// is exact.
+__device__ __forceinline__ int div_k(int s, unsigned long long kmagic)
+{
+    return static_cast<int>((static_cast<unsigned long long>(s) * kmagic) >> 32);
+}
+
 template <int ITEMS>
 __global__ void __launch_bounds__(kCluThreads, 1)
-route_cluster_kernel(const int* __restrict__ ids, const float* __restrict__ tw, long long T, int k, int E, int Tc,
-                     int g, int* __restrict__ expert_offsets, int* __restrict__ row_token, float* __restrict__ row_w,
+route_cluster_kernel(const int* __restrict__ ids, const float* __restrict__ tw, long long T, int k,
+                     unsigned long long kmagic, int E, int Tc, int g, int* __restrict__ expert_offsets,
+                     int* __restrict__ row_token, float* __restrict__ row_w,
                      int* __restrict__ slot_row, int* __restrict__ row_ptr, int* __restrict__ perm,
                      int4* __restrict__ seg_units, int4* __restrict__ row_units, int4* __restrict__ finish,
                      int* __restrict__ counters)
@@ -315,7 +383,7 @@ route_cluster_kernel(const int* __restrict__ ids, const float* __restrict__ tw, 
             const int q = S.cstart[e] + S.whist[warp * kRouteMaxE + e] + rank[it];
             const int p = q + S.delta[e];
             S.pos[s] = p;
-            S.stage_tok[q] = static_cast<int>(t0 + s / k);
+            S.stage_tok[q] = static_cast<int>(t0) + div_k(s, kmagic);
             S.stage_w[q] = wv[it];
             S.stage_e[q] = static_cast<unsigned char>(e);
             if (slot_row) slot_row[s0 + s] = p;
@@ -333,8 +401,8 @@ route_cluster_kernel(const int* __restrict__ ids, const float* __restrict__ tw, 
     // 6. the combine plan: token t's terms are its dispatch rows in ascending
     //    order, i.e. its slots in (expert, j) order
     for (int s = tid; s < cnt; s += kCluThreads) {
-        const int j = s % k;
-        const int first = s - j;
+        const int first = div_k(s, kmagic) * k;
+        const int j = s - first;
         const int e = S.ex[s];
         int r = 0;
         for (int j2 = 0; j2 < k; ++j2) {
@@ -588,10 +656,11 @@ det_status det_moe_route_plan(const int32_t* topk_ids, const float* topk_w, int6
     int C = 0, Tc = 0, items = 0;
     if (plan_path != 1 && route_cluster_shape(T, k, E, &C, &Tc, &items)) {
         long long t = T;
+        unsigned long long kmagic = ((1ull << 32) + static_cast<unsigned long long>(k) - 1) / static_cast<unsigned long long>(k);
         const int* ids_a = topk_ids;
         const float* tw_a = topk_w;
         int k_a = k, E_a = E;
-        void* args[] = {&ids_a, &tw_a, &t, &k_a, &E_a, &Tc, &g, &expert_offsets, &row_token, &row_w, &slot_row,
+        void* args[] = {&ids_a, &tw_a, &t, &k_a, &kmagic, &E_a, &Tc, &g, &expert_offsets, &row_token, &row_w, &slot_row,
                         &row_ptr, &perm, &seg_units, &row_units, &finish, &counters};
         const void* kern = items == 1   ? reinterpret_cast<const void*>(route_cluster_kernel<1>)
                            : items == 2 ? reinterpret_cast<const void*>(route_cluster_kernel<2>)
