@@ -69,6 +69,8 @@ def parse_args(argv=None):
     ap.add_argument("--size", choices=["full", "medium"], default="full",
                     help="medium: a quarter-size case of the same shape (for profiler captures only)")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--also", default="sparse_key_scatter,moe_route,splitk,embedding_backward",
+                    help="comma-separated secondary workloads to measure (default: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     a = ap.parse_args(argv)
@@ -414,6 +416,9 @@ def measure_moe_route(timer, steps, warmup, torch, device):
                              ("topk_route_plan_combine", topk_route_combine, cb + T * E * 4),
                              ("destination_plan_combine", dest_combine, cb),
                              ("route_plan_only", route, None),
+                             ("route_plan_only_multi_kernel",
+                              lambda: state.__setitem__("plan", dr.det_moe_route_plan(
+                                  ids, E, tw, opts={**ASYNC, "plan_path": 1}, workspace=ws, out=arrays)[0]), None),
                              ("router_topk_only", lambda: dr.det_router_topk(scores, k, renormalize=True,
                                                                              out=topk_out), None)):
         t, launches = timer.run(fn, steps, warmup)
@@ -560,32 +565,34 @@ def run_ours(args):
             e2e["value"] = world * gbs(cb, e2e["ms_per_step"])
 
     also = {}
+    wanted = set(a for a in args.also.split(",") if a)
     if not args.no_also and rank == 0:
-        for name in ("sparse_key_scatter",):
-            if name == args.workload:
-                continue
-            c2 = make_case(name, device)
+        if "sparse_key_scatter" in wanted and args.workload != "sparse_key_scatter":
+            c2 = make_case("sparse_key_scatter", device)
             r2 = measure_scatter(c2, timer, max(5, min(args.steps, 30)), args.warmup, torch, with_e2e=False)
             r2.pop("times_full", None)
             r2["frac_reduce_only"] = r2["reduce_only"]["gbs"] / peaks["hbm_gbs"]
-            r2["workload"] = WORKLOADS[name]
-            also[name] = r2
+            r2["workload"] = WORKLOADS["sparse_key_scatter"]
+            also["sparse_key_scatter"] = r2
             del c2
             torch.cuda.empty_cache()
-        r4 = measure_moe_route(timer, max(5, min(args.steps, 30)), args.warmup, torch, device)
-        r4["frac_route_plan_combine"] = r4["route_plan_combine"]["gbs"] / peaks["hbm_gbs"]
-        r4["workload"] = WORKLOADS["moe_route"]
-        also["moe_route"] = r4
-        torch.cuda.empty_cache()
-        also["splitk"] = measure_splitk(timer, max(10, min(args.steps, 50)), args.warmup, torch, device)
-        also["splitk"]["workload"] = WORKLOADS["splitk"]
-        c3 = make_case("embedding_backward", device)
-        r3 = measure_index_add(c3, timer, max(5, min(args.steps, 30)), args.warmup, torch)
-        r3["frac_index_add_only"] = r3["index_add_only"]["gbs"] / peaks["hbm_gbs"]
-        r3["workload"] = WORKLOADS["embedding_backward"]
-        also["embedding_backward"] = r3
-        del c3
-        torch.cuda.empty_cache()
+        if "moe_route" in wanted:
+            r4 = measure_moe_route(timer, max(5, min(args.steps, 30)), args.warmup, torch, device)
+            r4["frac_route_plan_combine"] = r4["route_plan_combine"]["gbs"] / peaks["hbm_gbs"]
+            r4["workload"] = WORKLOADS["moe_route"]
+            also["moe_route"] = r4
+            torch.cuda.empty_cache()
+        if "splitk" in wanted:
+            also["splitk"] = measure_splitk(timer, max(10, min(args.steps, 50)), args.warmup, torch, device)
+            also["splitk"]["workload"] = WORKLOADS["splitk"]
+        if "embedding_backward" in wanted:
+            c3 = make_case("embedding_backward", device)
+            r3 = measure_index_add(c3, timer, max(5, min(args.steps, 30)), args.warmup, torch)
+            r3["frac_index_add_only"] = r3["index_add_only"]["gbs"] / peaks["hbm_gbs"]
+            r3["workload"] = WORKLOADS["embedding_backward"]
+            also["embedding_backward"] = r3
+            del c3
+            torch.cuda.empty_cache()
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
