@@ -35,6 +35,50 @@ __device__ __forceinline__ int block_excl_scan(int v, int* ws, int* total)
     return r;
 }
 
+// Exclusive scans of NV ints per thread over a block of NT threads at once;
+// tot gets the block sums.  `ws` is shared scratch of NV * (NT/32 + 1) ints.
+// Ends synchronised.
+template <int NT, int NV>
+__device__ __forceinline__ void block_excl_scan_n(int v[NV], int* ws, int tot[NV])
+{
+    constexpr int W = NT / 32;
+    static_assert(NV <= W && W <= 32, "one warp per value scans the warp sums");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        incl[j] = v[j];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl[j], o);
+            if (lane >= o) incl[j] += t;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) ws[j * (W + 1) + warp] = incl[j];
+    }
+    __syncthreads();
+    if (warp < NV) {
+        const int s = lane < W ? ws[warp * (W + 1) + lane] : 0;
+        int si = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) si += t;
+        }
+        if (lane < W) ws[warp * (W + 1) + lane] = si - s;
+        if (lane == 31) ws[warp * (W + 1) + W] = si;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        tot[j] = ws[j * (W + 1) + W];
+        v[j] = incl[j] - v[j] + ws[j * (W + 1) + warp];
+    }
+    __syncthreads();
+}
+
 // Lanes among `live` holding the same 8-bit digit as this lane, from one
 // ballot per digit bit.  Warp votes are the ranking's main cost (measured on
 // GB300: a few cycles each per SM sub-partition, while one match.any costs

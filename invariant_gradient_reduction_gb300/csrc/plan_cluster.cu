@@ -71,48 +71,6 @@ struct CluShared {
     int next_start;                  // first sorted position past this CTA's rows
 };
 
-// Exclusive scans of NV ints per thread over 1024 threads at once; tot gets
-// the block sums.  Ends synchronised.
-template <int NV>
-__device__ __forceinline__ void block_excl_scan_n(int v[NV], int* ws, int tot[NV])
-{
-    constexpr int W = kCluWarps;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl[NV];
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        incl[j] = v[j];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl[j], o);
-            if (lane >= o) incl[j] += t;
-        }
-    }
-    if (lane == 31) {
-#pragma unroll
-        for (int j = 0; j < NV; ++j) ws[j * (W + 1) + warp] = incl[j];
-    }
-    __syncthreads();
-    if (warp < NV) {
-        const int s = ws[warp * (W + 1) + lane];
-        int si = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, si, o);
-            if (lane >= o) si += t;
-        }
-        ws[warp * (W + 1) + lane] = si - s;
-        if (lane == 31) ws[warp * (W + 1) + W] = si;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        tot[j] = ws[j * (W + 1) + W];
-        v[j] = incl[j] - v[j] + ws[j * (W + 1) + warp];
-    }
-    __syncthreads();
-}
-
 // Minimum of v over the threads with a larger index (INT_MAX for the last
 // thread), over 1024 threads.  Ends synchronised.
 __device__ __forceinline__ int block_suffix_min_excl(int v, int* ws)
@@ -379,7 +337,7 @@ plan_cluster_kernel(const int* __restrict__ idx, long long N, long long M, int E
     mx = __reduce_max_sync(0xffffffffu, mx);
     if (lane == 0 && mx > 0) atomicMax(&S.tot[5], mx);
     int t4[5];
-    block_excl_scan_n<5>(v4, S.ws, t4);
+    block_excl_scan_n<kCluThreads, 5>(v4, S.ws, t4);
     if (tid == 0) {
         S.tot[0] = t4[0];
         S.tot[1] = t4[1];
@@ -643,7 +601,7 @@ plan_cluster_one_kernel(const int* __restrict__ idx, long long N, long long M, i
     mx = __reduce_max_sync(0xffffffffu, mx);
     if (lane == 0 && mx > 0) atomicMax(&S.tot[NV], mx);
     int t5[NV];
-    block_excl_scan_n<NV>(v5, S.ws, t5);  // ends synchronised: S.tot[NV] is final
+    block_excl_scan_n<kCluThreads, NV>(v5, S.ws, t5);  // ends synchronised: S.tot[NV] is final
     if (tid < (NV + 1) * C) {  // push this CTA's totals into every CTA
         const int r = tid / (NV + 1), f = tid - (NV + 1) * (tid / (NV + 1));
         int v = S.tot[NV];

@@ -53,13 +53,19 @@ def cluster_plan_applies(N, M, src):
     return -(-(-(-M // C)) // 1024) <= 8
 
 
+def plan_path_applies(path, N, M, src):
+    return cluster_plan_applies(N, M, src) if path == 2 else True
+
+
 @pytest.mark.parametrize("plan_path", [0, 1, 2])
 @pytest.mark.parametrize("N,M,src", [(0, 7, False), (1, 1, False), (1000, 1, False), (5000, 37, False),
                                      (70000, 300, False), (20000, 70000, False), (9000, 600, True),
                                      (100000, 65536, False), (40000, 5, True), (31, 3, False),
                                      (4097, 4096, False), (131072, 16384, False), (131072, 131072, False),
                                      (65536 + 17, 2, False), (65536, 4096, False), (65537, 4096, False),
-                                     (2, 2, False), (100, 4096, False), (131072, 4097, False)])
+                                     (2, 2, False), (100, 4096, False), (131072, 4097, False),
+                                     (1 << 18, 1 << 15, False), ((1 << 18) + 1, 5, False), (3, 1 << 15, False),
+                                     (200000, 20000, False), (77777, 151, False), (32768, 4096, False)])
 def test_plan_lists_match_oracle(N, M, src, plan_path):
     g = torch.Generator().manual_seed(N * 31 + M)
     idx = torch.randint(0, M, (N,), generator=g, dtype=torch.int32)
@@ -67,7 +73,7 @@ def test_plan_lists_match_oracle(N, M, src, plan_path):
     if src:
         sid = (torch.randperm(N, generator=g) * 5 - 100).to(torch.int64)
     opts = {"plan_path": plan_path}
-    if plan_path == 2 and not cluster_plan_applies(N, M, src):
+    if not plan_path_applies(plan_path, N, M, src):
         with pytest.raises(dr.DetError) as e:
             dr.det_reduce_plan(idx.to(DEV), M, src_id=None if sid is None else sid.to(DEV), opts=opts)
         assert e.value.code == dr.DET_ERR_UNSUPPORTED
@@ -144,15 +150,19 @@ def test_scatter_small_matches_oracle(name):
 
 @pytest.mark.parametrize("name", SCATTER_SMALL)
 def test_plan_paths_give_same_bytes(name):
-    """The multi-kernel plan and the single-cluster plan feed the reduce the same lists."""
+    """The multi-kernel and single-cluster plans feed the reduce the same lists and work counts."""
     case = small_case(name)
     want = oracle_scatter(case)
+    counts = {}
     for path in (1, 2):
-        if path == 2 and not cluster_plan_applies(case.N, case.M, case.src_id is not None):
+        if not plan_path_applies(path, case.N, case.M, case.src_id is not None):
             continue
         for seg in (3, 5):
             out, plan = gpu_scatter(case, opts={"plan_path": path, "seg_chunks_log2": seg})
             assert_bytes_equal(np_bits(out), want, f"{name} plan_path={path} g={seg}")
+            d = plan.describe()
+            c = (d["n_units"], d["n_segments"], d["n_hot_rows"], d["max_row_len"])
+            assert counts.setdefault(seg, c) == c, (path, seg, c, counts[seg])
 
 
 def test_cluster_plan_hot_rows():
