@@ -245,3 +245,20 @@ def test_route_plan_replays_identical(replay):
                               arrays["slot_row"], arrays["expert_offsets"]])
         outs.append(replay.identical(run, name=f"route path {path}"))
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("T,k,E", [(3000, 8, 128), (100, 1, 1), (5000, 1, 16), (40000, 3, 512)])
+def test_route_plan_without_weights(T, k, E):
+    """No top-k weights: the dispatch arrays still match the oracle, row_w is not produced, and the
+    combine without a multiply gives the oracle's bits."""
+    ids, _ = route_inputs(T, k, E, "distinct" if k <= E else "repeated", seed=T + k)
+    plan, arrays = dr.det_moe_route_plan(ids.to(DEV), E)
+    assert arrays["row_w"] is None
+    want_off, want_tok, _, want_slot = oracle.moe_route(ids.numpy(), E)
+    assert_bytes_equal(arrays["expert_offsets"].cpu().numpy().astype(np.int64), want_off, "offsets")
+    assert_bytes_equal(arrays["row_token"].cpu().numpy(), want_tok, "row_token")
+    assert_bytes_equal(arrays["slot_row"].cpu().numpy(), want_slot, "slot_row")
+    H = 48
+    x = torch.randn(T * k, H, generator=torch.Generator().manual_seed(k)).to(DEV)
+    out = dr.det_scatter_reduce(plan, x, torch.empty(T, H, device=DEV))
+    assert_bytes_equal(out.cpu().numpy(), oracle.scatter_reduce(want_tok, x.cpu().numpy(), T), "combine")
