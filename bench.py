@@ -72,6 +72,8 @@ def parse_args(argv=None):
     ap.add_argument("--also", default="sparse_key_scatter,moe_route,splitk,embedding_backward",
                     help="comma-separated secondary workloads to measure (default: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-dir", default=os.path.join(ROOT, "bench_out"),
+                    help="where the nvidia-smi clock samples of the timed region are written")
     ap.add_argument("--no-e2e", action="store_true")
     a = ap.parse_args(argv)
     a.warmup = max(3, a.warmup)
@@ -122,10 +124,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, out_dir: str):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(out_dir, f"clocks_rank{gpu_index}.csv")
         self.windows = []
 
     def start(self):
@@ -510,7 +512,7 @@ def run_ours(args):
     case = make_case(args.workload, device, args.size)
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local_rank).start()
+    sampler = ClockSampler(local_rank, args.clocks_dir).start()
     time.sleep(0.1)
     # warm-up, then exactly K timed steps bracketed by barrier + synchronize
     full, red, atom, out, plan, check_last_plan = scatter_step_fns(case, torch)
