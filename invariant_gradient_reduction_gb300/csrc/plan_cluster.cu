@@ -790,8 +790,8 @@ int plan_cluster_ctas(int64_t N, int64_t M)
 }
 
 det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, int np32, int* row_ptr, int* perm,
-                               int4* seg_units, int4* row_units, int4* finish, int* counters, cudaStream_t st,
-                               bool* launched)
+                               int4* seg_units, int4* row_units, int4* finish, int* counters, bool two_pass,
+                               cudaStream_t st, bool* launched)
 {
     *launched = false;
     const int C = plan_cluster_ctas(N, M);
@@ -805,6 +805,7 @@ det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, 
                                                C, sizeof(OneShared), st, args, launched);
         if (s || *launched) return s;
     }
+    if (!two_pass) return DET_OK;
     long long n = N, m = M;
     void* args[] = {&idx, &n, &m, &E, &np32, &g, &row_ptr, &perm, &seg_units, &row_units, &finish, &counters};
     return launch_on_cluster(kCluVariantTwoPass, reinterpret_cast<const void*>(plan_cluster_kernel), C,

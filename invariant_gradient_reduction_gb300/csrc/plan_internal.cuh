@@ -57,11 +57,13 @@ det_status launch_on_cluster(int variant, const void* kern, int C, size_t smem, 
 int plan_cluster_ctas(int64_t N, int64_t M);
 
 // Enqueues the single-cluster plan when it applies and the device can
-// schedule the cluster (*launched = true); otherwise does nothing.  Writes
-// row_ptr, perm, the three unit arrays and the whole counter block.
+// schedule the cluster (*launched = true); otherwise does nothing.  The
+// single-pass kernel is taken where it applies; the two-pass kernel only when
+// two_pass is set.  Writes row_ptr, perm, the three unit arrays and the whole
+// counter block.
 det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, int np32, int* row_ptr, int* perm,
-                               int4* seg_units, int4* row_units, int4* finish, int* counters, cudaStream_t st,
-                               bool* launched);
+                               int4* seg_units, int4* row_units, int4* finish, int* counters, bool two_pass,
+                               cudaStream_t st, bool* launched);
 
 }  // namespace detr
 
