@@ -115,9 +115,8 @@ typedef int32_t det_dtype;
  *                   memory; only without src_id, for N <= 131072 and
  *                   M <= 8192 x (cluster CTAs), and only where the device can
  *                   schedule the cluster (else DET_ERR_UNSUPPORTED).  Auto
- *                   takes path 2's single-pass kernel where it applies (no
- *                   src_id, N <= 65536, M <= 4096) and path 1 otherwise.
- *                   Both build the same lists.
+ *                   takes path 2 where it applies and N <= 65536, path 1
+ *                   otherwise.  Both build the same lists.
  *  reserved         must be zero.
  */
 typedef struct det_opts {

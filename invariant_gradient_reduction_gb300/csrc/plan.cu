@@ -607,11 +607,13 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     const int plan_path = opts ? opts->plan_path : 0;
     bool one_cluster = false;
     if (plan_path != 1 && !with_src && N > 0) {
-        // Auto leaves the two-pass cluster kernel out: measured on a 131072-source,
-        // 16384-destination plan, the reduce after it ran ~70 us longer than
-        // after the multi-kernel plan, more than the 15 us the plan itself saves.
+        // Auto takes the two-pass cluster kernel only up to 65536 sources: after
+        // it, on a 131072-source, 16384-destination plan, the reduce ran ~70 us
+        // longer than after the multi-kernel plan, more than the 15 us the plan
+        // itself saves; on a 32768-source, 131072-destination plan it saved 35 us.
+        const bool two_pass = plan_path == 2 || N <= (int64_t(1) << 16);
         s = launch_plan_cluster(idx, N, M, g, np32, row_ptr, perm, seg_units, row_units, finish, counters,
-                                plan_path == 2, st, &one_cluster);
+                                two_pass, st, &one_cluster);
         if (s) return s;
     }
     if (plan_path == 2 && !one_cluster) return DET_ERR_UNSUPPORTED;
