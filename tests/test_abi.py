@@ -171,3 +171,18 @@ def test_route_host_logic(lib):
                                        (4, 8, 8, 2, 1, None, dr.DET_ERR_ARG), (4, 8, 8, 2, 0, fake + 8, dr.DET_ERR_ARG)]:
         assert L.det_router_topk(fake, T, E, lds, k, ren, fake * 2, w, None) == code
     assert L.det_router_topk(None, 0, 8, 8, 2, 0, None, None, None) == dr.DET_OK  # nothing to do
+
+
+def test_route_binding_checks_arguments(lib):
+    """The binding rejects wrong dtypes and shapes before it calls the library (no GPU needed)."""
+    import torch
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    with pytest.raises(ValueError):
+        dr.det_moe_route_plan(torch.zeros((4, 2), dtype=torch.int64), 8)   # ids must be int32
+    with pytest.raises(ValueError):
+        dr.det_moe_route_plan(torch.zeros(8, dtype=torch.int32), 8)        # ids must be [T, k]
+    with pytest.raises(ValueError):
+        dr.det_moe_route_plan(torch.zeros((4, 2), dtype=torch.int32), 8,
+                              topk_w=torch.zeros((4, 3)))                  # weights shaped like the ids
+    with pytest.raises(ValueError):
+        dr.det_router_topk(torch.zeros((4, 8), dtype=torch.float64), 2)    # scores must be float32
