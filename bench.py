@@ -33,6 +33,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -69,7 +70,7 @@ def parse_args(argv=None):
     ap.add_argument("--size", choices=["full", "medium"], default="full",
                     help="medium: a quarter-size case of the same shape (for profiler captures only)")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--also", default="sparse_key_scatter,moe_route,splitk,embedding_backward",
+    ap.add_argument("--also", default="sparse_key_scatter,ep_invariance,moe_route,splitk,embedding_backward",
                     help="comma-separated secondary workloads to measure (default: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-dir", default=os.path.join(ROOT, "bench_out"),
@@ -330,6 +331,50 @@ def measure_e2e(case, timer, steps, warmup, torch):
             "d2h_bytes_per_step": bo, "ms_per_step": ms, "steps": steps}
 
 
+def measure_ep_invariance(timer, steps, warmup, torch, device, shard_counts=(1, 8)):
+    """The EP-invariance MoE combine (T=16384, E=256, top-8, H=7168) with the
+    sources split into P simulated expert shards (separate allocations): the
+    step (unwaited plan + reduce) and the reduce alone per P, and each P's
+    output fingerprint, which must all be equal."""
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    from invariant_gradient_reduction_gb300 import workloads as wl
+    case = make_case("ep_invariance", device)
+    cb = case.compulsory_bytes()
+    out = torch.empty(case.M, case.H, dtype=case.out_dtype, device=device)
+    ws_plan = torch.empty(dr.det_plan_workspace_size(case.N, case.M) + 256, dtype=torch.uint8, device=device)
+    plan0 = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan, opts=ASYNC)
+    need = dr.det_scatter_workspace_size(plan0, case.H)
+    ws_red = torch.empty(need + 256, dtype=torch.uint8, device=device) if need else None
+    plan_fixed = dr.det_reduce_plan(case.idx, case.M, workspace=torch.empty_like(ws_plan))
+    res = {"compulsory_bytes": cb, "plan": {k: v for k, v in plan_fixed.describe().items()
+                                            if k not in ("row_ptr", "perm")}}
+    fps = {}
+    for P in shard_counts:
+        xs = case.x if P == 1 else wl.split_rows(case.x, wl.ep_shard_rows(case, P))
+        state = {"plan": plan0}
+
+        def step():
+            p = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan, opts=ASYNC)
+            dr.det_scatter_reduce(p, xs, out, w=case.w, workspace=ws_red, opts=ASYNC)
+            state["plan"] = p
+
+        t_full, l_full = timer.run(step, steps, warmup)
+        dr.det_plan_status(state["plan"])
+        t_red, _ = timer.run(lambda: dr.det_scatter_reduce(plan_fixed, xs, out, w=case.w, workspace=ws_red),
+                             steps, warmup)
+        torch.cuda.synchronize()
+        fps[P] = dr.det_hash(out).item() & (2 ** 64 - 1)
+        ms_full, ms_red = statistics.mean(t_full), statistics.mean(t_red)
+        res[f"P{P}"] = {"plan_reduce": {"ms": ms_full, "gbs": gbs(cb, ms_full)},
+                        "reduce_only": {"ms": ms_red, "gbs": gbs(cb, ms_red)},
+                        "launches_per_step": l_full / max(1, steps), "out_fingerprint": f"{fps[P]:016x}"}
+        del xs
+    res["fingerprints_equal"] = len(set(fps.values())) == 1
+    del case
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_index_add(case, timer, steps, warmup, torch):
     """The embedding backward: det_index_add of dY rows into an fp32 gradient.
     Compulsory bytes: dY read once, idx once, each touched gradient row read
@@ -473,9 +518,54 @@ def oracle_sample_seconds(case, max_rows: int):
     return dt, cb, f"first {rows} of {case.M} destinations and their {n} sources ({cb} compulsory bytes)"
 
 
+def host_cpu():
+    """The host CPU model and the number of CPUs this process may run on."""
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                k, _, v = line.partition(":")
+                if k.strip() in ("model name", "Model Name", "CPU part") and v.strip():
+                    model = v.strip()
+                    if k.strip() != "CPU part":
+                        break
+    except OSError:
+        pass
+    try:
+        ncpu = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        ncpu = os.cpu_count() or 1
+    return {"model": model, "machine": platform.machine(), "nproc": ncpu}
+
+
+def pinned_to_one_core():
+    """Pin this thread to the first CPU it may run on (the oracle is single-threaded);
+    returns (that CPU, the previous affinity) or (None, None) where pinning is not available."""
+    try:
+        prev = os.sched_getaffinity(0)
+        cpu = min(prev)
+        os.sched_setaffinity(0, {cpu})
+        return cpu, prev
+    except (AttributeError, OSError, ValueError):
+        return None, None
+
+
 def cpu_baseline(case, budget_s: float = 20.0):
     import oracle
     oracle.build()
+    host = host_cpu()
+    cpu, prev = pinned_to_one_core()
+    try:
+        res = _cpu_baseline_runs(case, budget_s)
+    finally:
+        if prev is not None:
+            os.sched_setaffinity(0, prev)
+    res["host"] = dict(host, pinned_cpu=cpu)
+    return res
+
+
+def _cpu_baseline_runs(case, budget_s):
+    import oracle
     rows = min(case.M, 256)
     dt, cb, desc = oracle_sample_seconds(case, rows)
     # grow the sample towards ~1/3 of the budget per run, then take the median of 3 runs
@@ -578,6 +668,13 @@ def run_ours(args):
             also["sparse_key_scatter"] = r2
             del c2
             torch.cuda.empty_cache()
+        if "ep_invariance" in wanted and args.workload != "ep_invariance":
+            r5 = measure_ep_invariance(timer, max(5, min(args.steps, 20)), args.warmup, torch, device)
+            for P in (1, 8):
+                r5[f"P{P}"]["frac_plan_reduce"] = r5[f"P{P}"]["plan_reduce"]["gbs"] / peaks["hbm_gbs"]
+                r5[f"P{P}"]["frac_reduce_only"] = r5[f"P{P}"]["reduce_only"]["gbs"] / peaks["hbm_gbs"]
+            r5["workload"] = WORKLOADS["ep_invariance"]
+            also["ep_invariance"] = r5
         if "moe_route" in wanted:
             r4 = measure_moe_route(timer, max(5, min(args.steps, 30)), args.warmup, torch, device)
             r4["frac_route_plan_combine"] = r4["route_plan_combine"]["gbs"] / peaks["hbm_gbs"]
@@ -665,6 +762,8 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
+    host = host_cpu()
+    cpu, _prev = pinned_to_one_core()
     from invariant_gradient_reduction_gb300 import workloads as wl
     case = wl.make(args.workload, "full", device="cpu")
     # each step: the oracle on a bounded sample (a prefix of the destinations and their sources)
@@ -686,7 +785,8 @@ def run_reference(args):
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "step": "CPU oracle (lists + canonical fold) on a sample",
                    "parallelism": "single thread"},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
+                         "host": dict(host, pinned_cpu=cpu)},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

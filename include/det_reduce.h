@@ -114,9 +114,15 @@ typedef int32_t det_dtype;
  *                   of up to 16 CTAs holding the sources in distributed shared
  *                   memory; only without src_id, for N <= 131072 and
  *                   M <= 8192 x (cluster CTAs), and only where the device can
- *                   schedule the cluster (else DET_ERR_UNSUPPORTED).  Auto
- *                   takes path 2 where it applies and N <= 65536, path 1
- *                   otherwise.  Both build the same lists.
+ *                   schedule the cluster (else DET_ERR_UNSUPPORTED).  3 =
+ *                   owner plan: one kernel on clusters of 8 CTAs, one CTA per
+ *                   SM, each cluster owning a range of at most 1024
+ *                   destinations and reading all of idx; only without src_id,
+ *                   for 1 <= N <= 262144 and M <= min(32768, 1024 x (SMs/8)),
+ *                   and where the device can schedule the clusters (else
+ *                   DET_ERR_UNSUPPORTED).  Auto takes path 3 where it applies
+ *                   and N <= 131072, else path 2 where it applies and
+ *                   N <= 65536, else path 1.  All build the same lists.
  *  reserved         must be zero.
  */
 typedef struct det_opts {

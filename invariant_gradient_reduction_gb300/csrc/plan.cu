@@ -40,6 +40,8 @@ constexpr int kSmallThreads = 256, kSmallItems = 4;
 constexpr int64_t kSmallSortMaxN = 1 << 20;
 constexpr int kRadix = 256;
 constexpr int kUnitThreads = 256;  // one row per thread
+// Auto takes the owner plan up to this many sources (where it applies).
+constexpr int64_t kOwnAutoMaxN = int64_t(1) << 17;
 
 enum KeyMode { KM_DIRECT = 0, KM_CARRY = 1, KM_GATHER = 2 };
 
@@ -580,7 +582,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     int g;
     det_status s = resolve_seg_log2(opts, &g);
     if (s) return s;
-    if (opts && (opts->plan_path < 0 || opts->plan_path > 2 || opts->reserved[0])) return DET_ERR_ARG;
+    if (opts && (opts->plan_path < 0 || opts->plan_path > 3 || opts->reserved[0])) return DET_ERR_ARG;
     const bool with_src = src_id != nullptr && N > 0;
     const PlanLayout L = plan_layout(N, M, with_src, g);
     if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return DET_ERR_WORKSPACE;
@@ -605,18 +607,27 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
 
     const int np32 = dest_passes(M);
     const int plan_path = opts ? opts->plan_path : 0;
-    bool one_cluster = false;
-    if (plan_path != 1 && !with_src && N > 0) {
+    bool one_kernel_set = false;  // a single-cluster or owner plan was enqueued
+    if ((plan_path == 0 || plan_path == 3) && !with_src && N > 0 && (plan_path == 3 || N <= kOwnAutoMaxN)) {
+        s = launch_plan_owner(idx, N, M, g, row_ptr, perm, seg_units, row_units, finish, counters, st,
+                              &one_kernel_set);
+        if (s) return s;
+        if (plan_path == 3 && !one_kernel_set) return DET_ERR_UNSUPPORTED;
+    }
+    if (plan_path == 3 && (with_src || N == 0)) return DET_ERR_UNSUPPORTED;
+    if (!one_kernel_set && (plan_path == 0 || plan_path == 2) && !with_src && N > 0) {
         // Auto takes the two-pass cluster kernel only up to 65536 sources: after
         // it, on a 131072-source, 16384-destination plan, the reduce ran ~70 us
         // longer than after the multi-kernel plan, more than the 15 us the plan
         // itself saves; on a 32768-source, 131072-destination plan it saved 35 us.
         const bool two_pass = plan_path == 2 || N <= (int64_t(1) << 16);
         s = launch_plan_cluster(idx, N, M, g, np32, row_ptr, perm, seg_units, row_units, finish, counters,
-                                two_pass, st, &one_cluster);
+                                two_pass, st, &one_kernel_set);
         if (s) return s;
+        if (plan_path == 2 && !one_kernel_set) return DET_ERR_UNSUPPORTED;
     }
-    if (plan_path == 2 && !one_cluster) return DET_ERR_UNSUPPORTED;
+    if (plan_path == 2 && !one_kernel_set) return DET_ERR_UNSUPPORTED;
+    const bool one_cluster = one_kernel_set;
     if (!one_cluster) {
     DETR_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, st));
 

@@ -65,6 +65,20 @@ det_status launch_plan_cluster(const int32_t* idx, int64_t N, int64_t M, int g, 
                                int4* seg_units, int4* row_units, int4* finish, int* counters, bool two_pass,
                                cudaStream_t st, bool* launched);
 
+// Owner plan (plan_owner.cu): clusters of 8, 4 or 2 CTAs (one per SM) each
+// own at most kOwnMaxRows consecutive destinations and together read all
+// N <= kOwnMaxN sources; M <= kOwnMaxM (a full histogram per CTA).
+constexpr int64_t kOwnMaxN = int64_t(1) << 18;
+constexpr int64_t kOwnMaxM = int64_t(1) << 15;
+constexpr int kOwnMaxRows = 1024;
+
+// Enqueues the owner plan (one kernel) when it applies and the device can
+// schedule its clusters (*launched = true); otherwise does nothing.  Writes
+// row_ptr, perm, the three unit arrays and the whole counter block.
+det_status launch_plan_owner(const int32_t* idx, int64_t N, int64_t M, int g, int* row_ptr, int* perm,
+                             int4* seg_units, int4* row_units, int4* finish, int* counters, cudaStream_t st,
+                             bool* launched);
+
 }  // namespace detr
 
 // Host handle.  Device arrays live in the caller's plan workspace.

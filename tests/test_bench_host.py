@@ -21,10 +21,24 @@ def test_args_defaults_and_minimum_warmup():
     assert a.gpus == 1 and a.warmup >= 3 and a.steps >= 1 and a.impl == "ours"
     assert bench.parse_args(["--warmup", "1"]).warmup == 3
     # every secondary workload runs by default and has a description; the clock samples stay in the repo
-    assert set(a.also.split(",")) == {"sparse_key_scatter", "moe_route", "splitk", "embedding_backward"}
+    assert set(a.also.split(",")) == {"sparse_key_scatter", "ep_invariance", "moe_route", "splitk",
+                                      "embedding_backward"}
     assert all(w in bench.WORKLOADS for w in a.also.split(","))
     assert a.clocks_dir.startswith(ROOT)
     assert bench.parse_args(["--also", "moe_route"]).also == "moe_route"
+
+
+def test_cpu_baseline_host_record_and_pinning():
+    """The CPU baseline records the host CPU and runs pinned to one core, then restores the affinity."""
+    h = bench.host_cpu()
+    assert h["model"] and h["nproc"] >= 1 and h["machine"]
+    before = os.sched_getaffinity(0)
+    cpu, prev = bench.pinned_to_one_core()
+    try:
+        assert cpu in before and os.sched_getaffinity(0) == {cpu}
+    finally:
+        os.sched_setaffinity(0, prev)
+    assert os.sched_getaffinity(0) == before
 
 
 def _rank(n, ms, fp=7):

@@ -53,11 +53,27 @@ def cluster_plan_applies(N, M, src):
     return -(-(-(-M // C)) // 1024) <= 8
 
 
+def owner_plan_possible(N, M, src):
+    """The owner plan's hard limits (clusters of 8, 4 or 2 CTAs, each owning <= 1024 destinations, a
+    full histogram of M counts per CTA): outside them it must refuse.  Inside, whether it runs
+    also depends on how many clusters the device runs at once."""
+    return not src and 0 < N <= (1 << 18) and 0 < M <= (1 << 15)
+
+
+def owner_plan_sure(N, M, src):
+    """Inside the limits with at most 1024 destinations: one cluster is enough, so it may not refuse."""
+    return owner_plan_possible(N, M, src) and M <= 1024
+
+
 def plan_path_applies(path, N, M, src):
-    return cluster_plan_applies(N, M, src) if path == 2 else True
+    if path == 2:
+        return cluster_plan_applies(N, M, src)
+    if path == 3:
+        return owner_plan_possible(N, M, src)
+    return True
 
 
-@pytest.mark.parametrize("plan_path", [0, 1, 2])
+@pytest.mark.parametrize("plan_path", [0, 1, 2, 3])
 @pytest.mark.parametrize("N,M,src", [(0, 7, False), (1, 1, False), (1000, 1, False), (5000, 37, False),
                                      (70000, 300, False), (20000, 70000, False), (9000, 600, True),
                                      (100000, 65536, False), (40000, 5, True), (31, 3, False),
@@ -78,7 +94,13 @@ def test_plan_lists_match_oracle(N, M, src, plan_path):
             dr.det_reduce_plan(idx.to(DEV), M, src_id=None if sid is None else sid.to(DEV), opts=opts)
         assert e.value.code == dr.DET_ERR_UNSUPPORTED
         return
-    plan = dr.det_reduce_plan(idx.to(DEV), M, src_id=None if sid is None else sid.to(DEV), opts=opts)
+    try:
+        plan = dr.det_reduce_plan(idx.to(DEV), M, src_id=None if sid is None else sid.to(DEV), opts=opts)
+    except dr.DetError as e:
+        # only the owner plan may refuse inside its limits, and only where the
+        # device runs too few clusters at once for this many destinations
+        assert plan_path == 3 and e.code == dr.DET_ERR_UNSUPPORTED and not owner_plan_sure(N, M, src), (N, M)
+        return
     rp, perm = dr.plan_lists(plan)
     want_rp, want_perm = oracle.build_lists(idx.numpy(), M, src_id=None if sid is None else sid.numpy())
     assert np.array_equal(rp.cpu().numpy().astype(np.int64), want_rp)
@@ -106,7 +128,7 @@ def test_plan_zipf_hot_rows_and_work_list():
     assert d["n_hot_rows"] > 0
 
 
-@pytest.mark.parametrize("plan_path", [0, 1])
+@pytest.mark.parametrize("plan_path", [0, 1, 3])
 def test_plan_errors(plan_path):
     o = {"plan_path": plan_path}
     idx = torch.tensor([0, 1, 5, 2], dtype=torch.int32, device=DEV)
@@ -150,11 +172,11 @@ def test_scatter_small_matches_oracle(name):
 
 @pytest.mark.parametrize("name", SCATTER_SMALL)
 def test_plan_paths_give_same_bytes(name):
-    """The multi-kernel and single-cluster plans feed the reduce the same lists and work counts."""
+    """The multi-kernel, single-cluster and owner plans feed the reduce the same lists and work counts."""
     case = small_case(name)
     want = oracle_scatter(case)
     counts = {}
-    for path in (1, 2):
+    for path in (1, 2, 3):
         if not plan_path_applies(path, case.N, case.M, case.src_id is not None):
             continue
         for seg in (3, 5):
@@ -175,7 +197,7 @@ def test_cluster_plan_hot_rows():
     w = torch.rand(N, generator=g)
     case = _case(idx, x, M, w=w)
     want = oracle_scatter(case)
-    for path in (1, 2):
+    for path in (1, 2, 3):
         out, plan = gpu_scatter(case, opts={"plan_path": path})
         d = plan.describe()
         assert d["n_hot_rows"] > 0 and d["n_segments"] > d["n_hot_rows"]

@@ -34,6 +34,9 @@ MANIFEST = {
                 ["test_plan_lists_match_oracle", "test_plan_errors", "test_physical_row_permutation_with_src_id"]),
     "plan_cluster.cu": (["plan_cluster_kernel", "plan_cluster_one_kernel"],
                         ["test_plan_lists_match_oracle", "test_plan_paths_give_same_bytes"]),
+    "plan_owner.cu": (["owner_rank_kernel", "owner_list_kernel"],
+                      ["test_plan_lists_match_oracle", "test_plan_paths_give_same_bytes", "test_plan_errors",
+                       "test_cluster_plan_hot_rows"]),
     "route.cu": (["router_topk_kernel", "route_cluster_kernel", "route_rows_kernel", "route_combine_kernel"],
                  ["test_router_topk_matches_oracle", "test_router_topk_ties_and_special_values",
                   "test_route_plan_matches_oracle", "test_route_combine_matches_oracle"]),
