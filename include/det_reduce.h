@@ -120,9 +120,14 @@ typedef int32_t det_dtype;
  *                   destinations and reading all of idx; only without src_id,
  *                   for 1 <= N <= 262144 and M <= min(32768, 1024 x (SMs/8)),
  *                   and where the device can schedule the clusters (else
- *                   DET_ERR_UNSUPPORTED).  Auto takes path 3 where it applies
- *                   and N <= 131072, else path 2 where it applies and
- *                   N <= 65536, else path 1.  All build the same lists.
+ *                   DET_ERR_UNSUPPORTED).  4 = radix plan: per 8-bit digit a
+ *                   count, an offset and a scatter kernel over packed words,
+ *                   the row lengths counted by the last pass, and one kernel
+ *                   for the work list; only without src_id, for
+ *                   1 <= N < 2^24 and M <= 65536 (else DET_ERR_UNSUPPORTED).
+ *                   Auto takes path 3 where it applies and N <= 131072, else
+ *                   path 2 where it applies and N <= 65536, else path 4 where
+ *                   it applies, else path 1.  All build the same lists.
  *  reserved         must be zero.
  */
 typedef struct det_opts {

@@ -433,7 +433,7 @@ struct PlanLayout {
     // the destinations' run bounds
     size_t counters, row_ptr, rstart, rend, zero_end;
     size_t utot;
-    size_t counts, totals, perm, skeys, k32_tmp, v_tmp, k64_a, k64_b, va, vb, seg_units, row_units, finish, total;
+    size_t counts, totals, perm, skeys, k32_tmp, v_tmp, k64_a, k64_b, va, vb, seg_units, row_units, finish, rx_tbad, rx_tot1, rx_ustat, total;
     int ntiles, nut, npass;
     int64_t max_segs, max_rows, max_finish;
 };
@@ -489,6 +489,9 @@ static PlanLayout plan_layout(int64_t N, int64_t M, bool with_src, int g)
     L.seg_units = take(static_cast<size_t>(L.max_segs) * sizeof(int4));
     L.row_units = take(static_cast<size_t>(L.max_rows) * sizeof(int4));
     L.finish = take(static_cast<size_t>(L.max_finish) * sizeof(int4));
+    L.rx_tbad = take(static_cast<size_t>(plan_radix_tiles(N)) * sizeof(int));
+    L.rx_tot1 = take(static_cast<size_t>(kRadix) * sizeof(int));
+    L.rx_ustat = take(static_cast<size_t>(plan_radix_ustat_ints(M)) * sizeof(int));
     L.total = off;
     return L;
 }
@@ -582,7 +585,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     int g;
     det_status s = resolve_seg_log2(opts, &g);
     if (s) return s;
-    if (opts && (opts->plan_path < 0 || opts->plan_path > 3 || opts->reserved[0])) return DET_ERR_ARG;
+    if (opts && (opts->plan_path < 0 || opts->plan_path > 4 || opts->reserved[0])) return DET_ERR_ARG;
     const bool with_src = src_id != nullptr && N > 0;
     const PlanLayout L = plan_layout(N, M, with_src, g);
     if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return DET_ERR_WORKSPACE;
@@ -627,6 +630,26 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
         if (plan_path == 2 && !one_kernel_set) return DET_ERR_UNSUPPORTED;
     }
     if (plan_path == 2 && !one_kernel_set) return DET_ERR_UNSUPPORTED;
+    if (!one_kernel_set && (plan_path == 0 || plan_path == 4) && !with_src && plan_radix_applies(N, M)) {
+        RadixBuffers rb{};
+        rb.counts = counts;
+        rb.tbad = reinterpret_cast<int*>(ws + L.rx_tbad);
+        rb.totals0 = totals;
+        rb.totals1 = reinterpret_cast<int*>(ws + L.rx_tot1);
+        rb.packed = reinterpret_cast<int*>(ws + L.k32_tmp);
+        rb.perm = perm;
+        rb.rowcnt = reinterpret_cast<int*>(ws + L.rstart);
+        rb.ustat = reinterpret_cast<int*>(ws + L.rx_ustat);
+        rb.row_ptr = row_ptr;
+        rb.seg_units = seg_units;
+        rb.row_units = row_units;
+        rb.finish = finish;
+        rb.counters = counters;
+        s = launch_plan_radix(idx, N, M, g, rb, st);
+        if (s) return s;
+        one_kernel_set = true;
+    }
+    if (plan_path == 4 && !one_kernel_set) return DET_ERR_UNSUPPORTED;
     const bool one_cluster = one_kernel_set;
     if (!one_cluster) {
     DETR_CUDA(cudaMemsetAsync(ws, 0, L.zero_end, st));

@@ -79,6 +79,30 @@ det_status launch_plan_owner(const int32_t* idx, int64_t N, int64_t M, int g, in
                              int4* seg_units, int4* row_units, int4* finish, int* counters, cudaStream_t st,
                              bool* launched);
 
+// Radix plan (plan_radix.cu): no order keys, 1 <= N < 2^24, M <= 65536.
+struct RadixBuffers {
+    int* counts;     // [256][tiles]
+    int* tbad;       // [tiles]
+    int* totals0;    // [256]
+    int* totals1;    // [256]
+    int* packed;     // [N]
+    int* perm;       // [N]
+    int* rowcnt;     // [M]
+    int* ustat;      // [plan_radix_ustat_ints(M)]
+    int* row_ptr;    // [M+1]
+    int4* seg_units;
+    int4* row_units;
+    int4* finish;
+    int* counters;
+};
+bool plan_radix_applies(int64_t N, int64_t M);
+int64_t plan_radix_tiles(int64_t N);
+int64_t plan_radix_ustat_ints(int64_t M);
+// Enqueues the radix plan (DET_ERR_UNSUPPORTED where it does not apply).
+// Writes row_ptr, perm, the three unit arrays and the whole counter block.
+det_status launch_plan_radix(const int32_t* idx, int64_t N, int64_t M, int g, const RadixBuffers& b,
+                             cudaStream_t st);
+
 }  // namespace detr
 
 // Host handle.  Device arrays live in the caller's plan workspace.

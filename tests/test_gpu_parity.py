@@ -65,15 +65,22 @@ def owner_plan_sure(N, M, src):
     return owner_plan_possible(N, M, src) and M <= 1024
 
 
+def radix_plan_applies(N, M, src):
+    """Mirror of the radix plan's size rule (packed 24-bit source positions, one or two 8-bit digits)."""
+    return not src and 0 < N < (1 << 24) and 0 < M <= 65536
+
+
 def plan_path_applies(path, N, M, src):
     if path == 2:
         return cluster_plan_applies(N, M, src)
     if path == 3:
         return owner_plan_possible(N, M, src)
+    if path == 4:
+        return radix_plan_applies(N, M, src)
     return True
 
 
-@pytest.mark.parametrize("plan_path", [0, 1, 2, 3])
+@pytest.mark.parametrize("plan_path", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("N,M,src", [(0, 7, False), (1, 1, False), (1000, 1, False), (5000, 37, False),
                                      (70000, 300, False), (20000, 70000, False), (9000, 600, True),
                                      (100000, 65536, False), (40000, 5, True), (31, 3, False),
@@ -128,7 +135,7 @@ def test_plan_zipf_hot_rows_and_work_list():
     assert d["n_hot_rows"] > 0
 
 
-@pytest.mark.parametrize("plan_path", [0, 1, 3])
+@pytest.mark.parametrize("plan_path", [0, 1, 3, 4])
 def test_plan_errors(plan_path):
     o = {"plan_path": plan_path}
     idx = torch.tensor([0, 1, 5, 2], dtype=torch.int32, device=DEV)
@@ -172,11 +179,11 @@ def test_scatter_small_matches_oracle(name):
 
 @pytest.mark.parametrize("name", SCATTER_SMALL)
 def test_plan_paths_give_same_bytes(name):
-    """The multi-kernel, single-cluster and owner plans feed the reduce the same lists and work counts."""
+    """The multi-kernel, single-cluster, owner and radix plans feed the reduce the same lists and work counts."""
     case = small_case(name)
     want = oracle_scatter(case)
     counts = {}
-    for path in (1, 2, 3):
+    for path in (1, 2, 3, 4):
         if not plan_path_applies(path, case.N, case.M, case.src_id is not None):
             continue
         for seg in (3, 5):
@@ -197,7 +204,7 @@ def test_cluster_plan_hot_rows():
     w = torch.rand(N, generator=g)
     case = _case(idx, x, M, w=w)
     want = oracle_scatter(case)
-    for path in (1, 2, 3):
+    for path in (1, 2, 3, 4):
         out, plan = gpu_scatter(case, opts={"plan_path": path})
         d = plan.describe()
         assert d["n_hot_rows"] > 0 and d["n_segments"] > d["n_hot_rows"]

@@ -34,7 +34,10 @@ MANIFEST = {
                 ["test_plan_lists_match_oracle", "test_plan_errors", "test_physical_row_permutation_with_src_id"]),
     "plan_cluster.cu": (["plan_cluster_kernel", "plan_cluster_one_kernel"],
                         ["test_plan_lists_match_oracle", "test_plan_paths_give_same_bytes"]),
-    "plan_owner.cu": (["owner_rank_kernel", "owner_list_kernel"],
+    "plan_radix.cu": (["rx_count_kernel", "rx_offset_kernel", "rx_scatter_kernel", "rx_units_kernel"],
+                      ["test_plan_lists_match_oracle", "test_plan_paths_give_same_bytes", "test_plan_errors",
+                       "test_cluster_plan_hot_rows", "test_plan_zipf_hot_rows_and_work_list"]),
+    "plan_owner.cu": (["plan_owner_kernel"],
                       ["test_plan_lists_match_oracle", "test_plan_paths_give_same_bytes", "test_plan_errors",
                        "test_cluster_plan_hot_rows"]),
     "route.cu": (["router_topk_kernel", "route_cluster_kernel", "route_rows_kernel", "route_combine_kernel"],
