@@ -450,10 +450,7 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
         const int64_t max_row = dev_counts ? plan->N : plan->max_row_len;
         const long long items = dev_counts ? (cdiv(plan->N, (int64_t(kChunk) << plan->g) + 1) + 1) * H
                                            : plan->n_hot_rows * H;
-        // With the counts on the device the grid covers an upper bound, so it is
-        // kept to a few CTAs per SM (grid-stride loop): where the plan found no
-        // hot destination they all exit at once.
-        const int64_t fgrid64 = dev_counts ? std::min<int64_t>(cdiv(items, kFinishThreads), int64_t(sms) * 4)
+        const int64_t fgrid64 = dev_counts ? std::min<int64_t>(cdiv(items, kFinishThreads), int64_t(sms) * 16)
                                            : cdiv(items, kFinishThreads);
         const unsigned int fgrid = static_cast<unsigned int>(std::max<int64_t>(1, fgrid64));
         const int64_t max_segs = cdiv(cdiv(max_row, kChunk), G);

@@ -433,7 +433,7 @@ struct PlanLayout {
     // the destinations' run bounds
     size_t counters, row_ptr, rstart, rend, zero_end;
     size_t utot;
-    size_t counts, totals, perm, skeys, k32_tmp, v_tmp, k64_a, k64_b, va, vb, seg_units, row_units, finish, rx_tbad, rx_tot1, rx_ustat, total;
+    size_t counts, totals, perm, skeys, k32_tmp, v_tmp, k64_a, k64_b, va, vb, seg_units, row_units, finish, rx_tbad, rx_tot1, rx_btot, total;
     int ntiles, nut, npass;
     int64_t max_segs, max_rows, max_finish;
 };
@@ -491,7 +491,7 @@ static PlanLayout plan_layout(int64_t N, int64_t M, bool with_src, int g)
     L.finish = take(static_cast<size_t>(L.max_finish) * sizeof(int4));
     L.rx_tbad = take(static_cast<size_t>(plan_radix_tiles(N)) * sizeof(int));
     L.rx_tot1 = take(static_cast<size_t>(kRadix) * sizeof(int));
-    L.rx_ustat = take(static_cast<size_t>(plan_radix_ustat_ints(M)) * sizeof(int));
+    L.rx_btot = take(static_cast<size_t>(plan_radix_blocks(M)) * 8 * sizeof(int));
     L.total = off;
     return L;
 }
@@ -639,7 +639,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
         rb.packed = reinterpret_cast<int*>(ws + L.k32_tmp);
         rb.perm = perm;
         rb.rowcnt = reinterpret_cast<int*>(ws + L.rstart);
-        rb.ustat = reinterpret_cast<int*>(ws + L.rx_ustat);
+        rb.btot = reinterpret_cast<int*>(ws + L.rx_btot);
         rb.row_ptr = row_ptr;
         rb.seg_units = seg_units;
         rb.row_units = row_units;

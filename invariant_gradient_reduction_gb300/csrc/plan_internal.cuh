@@ -88,7 +88,7 @@ struct RadixBuffers {
     int* packed;     // [N]
     int* perm;       // [N]
     int* rowcnt;     // [M]
-    int* ustat;      // [plan_radix_ustat_ints(M)]
+    int* btot;       // [plan_radix_blocks(M) * 8]
     int* row_ptr;    // [M+1]
     int4* seg_units;
     int4* row_units;
@@ -97,7 +97,7 @@ struct RadixBuffers {
 };
 bool plan_radix_applies(int64_t N, int64_t M);
 int64_t plan_radix_tiles(int64_t N);
-int64_t plan_radix_ustat_ints(int64_t M);
+int64_t plan_radix_blocks(int64_t M);
 // Enqueues the radix plan (DET_ERR_UNSUPPORTED where it does not apply).
 // Writes row_ptr, perm, the three unit arrays and the whole counter block.
 det_status launch_plan_radix(const int32_t* idx, int64_t N, int64_t M, int g, const RadixBuffers& b,

@@ -11,9 +11,10 @@
 //
 // For N < 2^24 sources and M <= 65536 destinations (one or two 8-bit digits):
 //   per digit pass, three kernels, none of which waits for another CTA:
-//     rx_count_kernel    digit counts of every tile of 4096 words (the first
-//                        pass also checks idx against M and zeroes the row
-//                        counters and the work-list kernel's state);
+//     rx_count_kernel    digit counts of every tile of 4096 words, by a
+//                        persistent grid that prefetches its next tile (the
+//                        first pass also checks idx against M and zeroes the
+//                        row counters);
 //     rx_offset_kernel   one CTA per digit: exclusive scan of the digit's
 //                        counts over the tiles (the first pass also gathers
 //                        the tiles' range errors into the counter block);
@@ -28,11 +29,10 @@
 //                        destination to that destination's row counter (the
 //                        low digit of a word follows from its position in the
 //                        first pass's output);
-//   rx_units_kernel      row_ptr and the work list from the row counters: CTA
-//                        b of <= 64 takes a ticket, publishes its classes'
-//                        totals, reads every CTA's totals (bounded waits on
-//                        flags zeroed by the first kernel) and writes its
-//                        rows' row_ptr, units and finish tasks.
+//   rx_units_count_kernel, rx_units_write_kernel
+//                        row_ptr and the work list from the row counters:
+//                        class totals per block of 1024 destinations, then
+//                        each block's offsets from the blocks before it.
 // Every kernel is a programmatic dependent of the one before it: it is
 // launched while that one runs and waits (griddepcontrol.wait) before reading
 // what it wrote.
@@ -49,11 +49,9 @@ constexpr int kRxWarps = kRxThreads / 32;
 constexpr int kRxItems = 16;
 constexpr int kRxTile = kRxThreads * kRxItems;  // 4096 words per tile
 constexpr int kRxRadix = 256;
-constexpr int kRxUnitThreads = 1024;            // destinations per CTA of the units kernel
-constexpr int kRxMaxUnitCtas = 64;
-constexpr int kRxUnitStride = 8;                // ints per published CTA record: 7 totals + flag
-constexpr long long kRxPollLimit = 1 << 22;     // polls of a flag before the wait gives up
-static_assert(kRxMaxUnitCtas <= 2 * 32, "warp 0 reads every CTA's record, two per lane");
+constexpr int kRxUnitThreads = 1024;            // destinations per CTA of the work-list kernels
+constexpr int kRxMaxUnitBlocks = 64;            // blocks of 1024 destinations (M <= 65536)
+static_assert(kRxMaxUnitBlocks * 8 <= kRxUnitThreads, "one block total per thread");
 
 // ------------------------------------------------------------------------
 // counts
@@ -61,49 +59,76 @@ static_assert(kRxMaxUnitCtas <= 2 * 32, "warp 0 reads every CTA's record, two pe
 
 // MODE 0: the words are idx (digit = low byte; ids checked against M).
 // MODE 1: packed words of the first pass (digit = top byte).
-template <int MODE>
+// Persistent: CTA c counts tiles c, c + grid, ...; the next tile's 16-byte
+// loads are in flight while the current one is counted (VEC: the words are
+// 16-byte aligned).
+constexpr int kRxCountVec = kRxTile / (4 * kRxThreads);  // 16-byte loads per thread per tile
+
+template <bool VEC>
+__device__ __forceinline__ void rx_load_tile(const int* in, int N, int t, int tid, uint4 (&v)[kRxCountVec])
+{
+#pragma unroll
+    for (int j = 0; j < kRxCountVec; ++j) {
+        const int p = t * kRxTile + 4 * (j * kRxThreads + tid);
+        if (VEC && p + 3 < N) {
+            v[j] = __ldg(reinterpret_cast<const uint4*>(in + p));
+        } else {
+            v[j].x = p < N ? static_cast<unsigned int>(__ldg(in + p)) : 0u;
+            v[j].y = p + 1 < N ? static_cast<unsigned int>(__ldg(in + p + 1)) : 0u;
+            v[j].z = p + 2 < N ? static_cast<unsigned int>(__ldg(in + p + 2)) : 0u;
+            v[j].w = p + 3 < N ? static_cast<unsigned int>(__ldg(in + p + 3)) : 0u;
+        }
+    }
+}
+
+template <int MODE, bool VEC>
 __global__ void __launch_bounds__(kRxThreads)
 rx_count_kernel(const int* __restrict__ in, int N, unsigned int M, int* __restrict__ counts, int ntiles,
-                int* __restrict__ tbad, int* __restrict__ zero_a, int zero_na, int* __restrict__ zero_b,
-                int zero_nb)
+                int* __restrict__ tbad, int* __restrict__ zero_a, int zero_na)
 {
     __shared__ int wh[kRxWarps * kRxRadix];
     const int tid = threadIdx.x, warp = tid >> 5;
     pdl_launch_dependents();  // the next kernel may be launched now; it waits for this grid to finish
     for (int i = tid; i < kRxWarps * kRxRadix; i += kRxThreads) wh[i] = 0;
     pdl_wait();  // whatever wrote idx (or the previous pass) has finished
-    if (MODE == 0) {  // read by later kernels of this plan only
+    if (MODE == 0) {  // read by a later kernel of this plan only
         const int stride = static_cast<int>(gridDim.x) * kRxThreads;
         for (int i = static_cast<int>(blockIdx.x) * kRxThreads + tid; i < zero_na; i += stride) zero_a[i] = 0;
-        for (int i = static_cast<int>(blockIdx.x) * kRxThreads + tid; i < zero_nb; i += stride) zero_b[i] = 0;
     }
     __syncthreads();
-    const int base = static_cast<int>(blockIdx.x) * kRxTile;
-    unsigned int w[kRxItems];
-#pragma unroll
-    for (int k = 0; k < kRxItems; ++k) {  // all loads in flight first
-        const int p = base + k * kRxThreads + tid;
-        w[k] = p < N ? static_cast<unsigned int>(__ldg(in + p)) : 0u;
-    }
-    bool bad = false;
+    int t = blockIdx.x;
+    uint4 cur[kRxCountVec], nxt[kRxCountVec];
+    if (t < ntiles) rx_load_tile<VEC>(in, N, t, tid, cur);
     int* mh = wh + warp * kRxRadix;
+    for (; t < ntiles; t += gridDim.x) {
+        const int tn = t + static_cast<int>(gridDim.x);
+        if (tn < ntiles) rx_load_tile<VEC>(in, N, tn, tid, nxt);
+        bool bad = false;
 #pragma unroll
-    for (int k = 0; k < kRxItems; ++k) {
-        if (base + k * kRxThreads + tid < N) {
-            if (MODE == 0) bad |= w[k] >= M;  // a negative id is huge as unsigned
-            atomicAdd(&mh[MODE == 0 ? (w[k] & 255u) : (w[k] >> 24)], 1);
+        for (int j = 0; j < kRxCountVec; ++j) {
+            const int p = t * kRxTile + 4 * (j * kRxThreads + tid);
+            const unsigned int e[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (p + c < N) {
+                    if (MODE == 0) bad |= e[c] >= M;  // a negative id is huge as unsigned
+                    atomicAdd(&mh[MODE == 0 ? (e[c] & 255u) : (e[c] >> 24)], 1);
+                }
+            }
         }
-    }
-    if (MODE == 0) {
         const int b = __syncthreads_or(bad);
-        if (tid == 0) tbad[blockIdx.x] = b;
-    } else {
-        __syncthreads();
-    }
-    int c = 0;
+        if (MODE == 0 && tid == 0) tbad[t] = b;
+        int c = 0;
 #pragma unroll
-    for (int q = 0; q < kRxWarps; ++q) c += wh[q * kRxRadix + tid];
-    counts[static_cast<long long>(tid) * ntiles + blockIdx.x] = c;
+        for (int q = 0; q < kRxWarps; ++q) {
+            c += wh[q * kRxRadix + tid];
+            wh[q * kRxRadix + tid] = 0;
+        }
+        counts[static_cast<long long>(tid) * ntiles + t] = c;
+        __syncthreads();  // the histogram is zero again before the next tile's adds
+#pragma unroll
+        for (int j = 0; j < kRxCountVec; ++j) cur[j] = nxt[j];
+    }
 }
 
 // One CTA per digit: exclusive scan of the digit's tile counts, in place, and
@@ -168,35 +193,25 @@ struct RxScatterShared {
     int ws[kRxThreads / 32 + 1];
 };
 
-template <int MODE, bool LAST>
-__global__ void __launch_bounds__(kRxThreads, 4)
-rx_scatter_kernel(const int* __restrict__ in, int N, unsigned int* __restrict__ out, const int* __restrict__ offsets,
-                  const int* __restrict__ totals, const int* __restrict__ totals0, int ntiles,
-                  int* __restrict__ rowcnt, const int* __restrict__ counters)
+// One tile; FULL: all kTile words exist (no bounds checks).
+template <int MODE, bool LAST, bool FULL>
+__device__ __forceinline__ void rx_scatter_tile(RxScatterShared& S, const int* __restrict__ in, int N,
+                                                unsigned int* __restrict__ out, const int* __restrict__ offsets,
+                                                const int* __restrict__ totals, const int* __restrict__ totals0,
+                                                int ntiles, int* __restrict__ rowcnt)
 {
-    extern __shared__ __align__(16) unsigned char rx_smem[];
-    RxScatterShared& S = *reinterpret_cast<RxScatterShared*>(rx_smem);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tile = blockIdx.x;
     const int base = tile * kRxTile;
     unsigned int lt_mask;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt_mask));
-    pdl_launch_dependents();
-    for (int i = tid; i < kRxWarps * kRxRadix; i += kRxThreads) S.whist[i] = 0;
-    if (MODE == 1) {
-        for (int i = tid; i < kRxTile / 16; i += kRxThreads) reinterpret_cast<uint4*>(S.lomap)[i] = make_uint4(0, 0, 0, 0);
-    }
-    pdl_wait();  // the previous kernels' counts, offsets and words are visible
-    // with an id out of range the row counters would be indexed out of range:
-    // the last pass writes nothing (the plan reports the error)
-    if (LAST && counters[kCtrErrIndex]) return;
 
     const int wbase = base + warp * 32 * kRxItems;
     unsigned int wv[kRxItems];
 #pragma unroll
     for (int k = 0; k < kRxItems; ++k) {  // all loads first
         const int p = wbase + k * 32 + lane;
-        wv[k] = p < N ? static_cast<unsigned int>(__ldg(in + p)) : 0u;
+        wv[k] = FULL || p < N ? static_cast<unsigned int>(__ldg(in + p)) : 0u;
     }
     const int tot_d = totals[tid];
     const int off_d = offsets[static_cast<long long>(tid) * ntiles + tile];
@@ -245,10 +260,10 @@ rx_scatter_kernel(const int* __restrict__ in, int N, unsigned int* __restrict__ 
 #pragma unroll
     for (int k = 0; k < kRxItems; ++k) {
         const int nl = N - (wbase + k * 32);
-        const unsigned int live = nl >= 32 ? 0xffffffffu : (nl <= 0 ? 0u : (1u << nl) - 1u);
+        const unsigned int live = FULL || nl >= 32 ? 0xffffffffu : (nl <= 0 ? 0u : (1u << nl) - 1u);
         rank[k] = 0;
-        if (live == 0u) continue;  // uniform over the warp
-        const bool valid = (live >> lane) & 1u;
+        if (!FULL && live == 0u) continue;  // uniform over the warp
+        const bool valid = FULL || ((live >> lane) & 1u);
         const int d = static_cast<int>(MODE == 0 ? (wv[k] & 255u) : (wv[k] >> 24));
         const unsigned int peers = digit_peers(d, live);
         const int leader = __ffs(peers) - 1;
@@ -279,7 +294,7 @@ rx_scatter_kernel(const int* __restrict__ in, int N, unsigned int* __restrict__ 
 #pragma unroll
     for (int k = 0; k < kRxItems; ++k) {
         const int p = wbase + k * 32 + lane;
-        if (p < N) {
+        if (FULL || p < N) {
             const unsigned int w = wv[k];
             const int d = static_cast<int>(MODE == 0 ? (w & 255u) : (w >> 24));
             const int pos = S.tstart[d] + S.whist[warp * kRxRadix + d] + rank[k];
@@ -298,7 +313,7 @@ rx_scatter_kernel(const int* __restrict__ in, int N, unsigned int* __restrict__ 
     __syncthreads();
 
     const int rem = N - base;
-    const int nvalid = rem < kRxTile ? rem : kRxTile;
+    const int nvalid = FULL || rem >= kRxTile ? kRxTile : rem;
     for (int i0 = 0; i0 < kRxTile; i0 += kRxThreads) {
         const int i = i0 + tid;
         unsigned int key = 0xffffffffu;
@@ -322,6 +337,30 @@ rx_scatter_kernel(const int* __restrict__ in, int N, unsigned int* __restrict__ 
             }
         }
     }
+}
+
+template <int MODE, bool LAST>
+__global__ void __launch_bounds__(kRxThreads, 4)
+rx_scatter_kernel(const int* __restrict__ in, int N, unsigned int* __restrict__ out, const int* __restrict__ offsets,
+                  const int* __restrict__ totals, const int* __restrict__ totals0, int ntiles,
+                  int* __restrict__ rowcnt, const int* __restrict__ counters)
+{
+    extern __shared__ __align__(16) unsigned char rx_smem[];
+    RxScatterShared& S = *reinterpret_cast<RxScatterShared*>(rx_smem);
+    const int tid = threadIdx.x;
+    pdl_launch_dependents();
+    for (int i = tid; i < kRxWarps * kRxRadix; i += kRxThreads) S.whist[i] = 0;
+    if (MODE == 1) {
+        for (int i = tid; i < kRxTile / 16; i += kRxThreads) reinterpret_cast<uint4*>(S.lomap)[i] = make_uint4(0, 0, 0, 0);
+    }
+    pdl_wait();  // the previous kernels' counts, offsets and words are visible
+    // with an id out of range the row counters would be indexed out of range:
+    // the last pass writes nothing (the plan reports the error)
+    if (LAST && counters[kCtrErrIndex]) return;
+    if ((static_cast<long long>(blockIdx.x) + 1) * kRxTile <= N)  // uniform over the CTA
+        rx_scatter_tile<MODE, LAST, true>(S, in, N, out, offsets, totals, totals0, ntiles, rowcnt);
+    else
+        rx_scatter_tile<MODE, LAST, false>(S, in, N, out, offsets, totals, totals0, ntiles, rowcnt);
 }
 
 // ------------------------------------------------------------------------
@@ -350,115 +389,77 @@ __device__ __forceinline__ void rx_row_classes(int len, int g, int v[6])
     }
 }
 
-__device__ __forceinline__ int ld_acquire(const int* p)
+// The work list in two kernels over blocks of 1024 destinations:
+//   rx_units_count_kernel  each block's class totals (6) and longest row;
+//   rx_units_write_kernel  each CTA sums the totals of the blocks before its
+//                          own (its offsets) and of all blocks (the region
+//                          starts), scans its rows and writes row_ptr, the
+//                          units and the finish tasks.
+__global__ void __launch_bounds__(kRxUnitThreads)
+rx_units_count_kernel(const int* __restrict__ rowcnt, int M, int g, int* __restrict__ btot,
+                      const int* __restrict__ counters)
 {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release(int* p, int v)
-{
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// ustat: [0] ticket, then nb records of kRxUnitStride ints (7 totals, flag),
-// all zeroed by the first count kernel.  CTAs take tickets in launch order, so
-// a CTA waits only for CTAs that are already running.
-__global__ void __launch_bounds__(kRxUnitThreads, 1)
-rx_units_kernel(const int* __restrict__ rowcnt, int N, int M, int g, int* __restrict__ ustat,
-                int* __restrict__ row_ptr, int4* __restrict__ seg_units, int4* __restrict__ row_units,
-                int4* __restrict__ finish, int* __restrict__ counters)
-{
-    __shared__ int ws[6 * (kRxUnitThreads / 32 + 1)];
-    __shared__ int stot[7];   // this CTA's totals
-    __shared__ int sbase[6];  // totals of the CTAs before it
-    __shared__ int sgrand[7]; // totals of all CTAs
-    __shared__ int sb;
-    __shared__ int sfail;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
-    pdl_wait();
-    if (counters[kCtrErrIndex]) return;
-    const int nb = static_cast<int>(gridDim.x);
-    if (tid == 0) {
-        sb = atomicAdd(ustat, 1);
-        sfail = 0;
-    }
+    __shared__ int stot[7];
+    const int tid = threadIdx.x, lane = tid & 31;
+    pdl_launch_dependents();
     if (tid < 7) stot[tid] = 0;
-    __syncthreads();
-    const int b = sb;  // < nb: one ticket per CTA
-    const int m = b * kRxUnitThreads + tid;
+    pdl_wait();
+    if (counters[kCtrErrIndex]) return;  // the same for every CTA
+    const int m = blockIdx.x * kRxUnitThreads + tid;
     const int len = m < M ? rowcnt[m] : 0;
     int v[6];
     rx_row_classes(len, g, v);
     if (m >= M) v[5] = 0;
-#pragma unroll
-    for (int j = 0; j < 6; ++j) {
-        const int t = __reduce_add_sync(0xffffffffu, v[j]);
-        if (lane == 0 && t) atomicAdd(&stot[j], t);
-    }
-    {
-        const int mx = __reduce_max_sync(0xffffffffu, len);
-        if (lane == 0 && mx) atomicMax(&stot[6], mx);
-    }
     __syncthreads();
-    int* rec = ustat + 1 + b * kRxUnitStride;
-    if (tid < 7) rec[tid] = stot[tid];
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        st_release(rec + 7, 1);
+#pragma unroll
+    for (int k = 0; k < 6; ++k) {
+        const int t = __reduce_add_sync(0xffffffffu, v[k]);
+        if (lane == 0 && t) atomicAdd(&stot[k], t);
     }
-    // every CTA's totals: warp 0, two records per lane, bounded waits
-    if (warp == 0) {
-        int pre[6] = {0, 0, 0, 0, 0, 0}, all[7] = {0, 0, 0, 0, 0, 0, 0};
-        bool fail = false;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = lane + 32 * h;
-            if (c < nb) {
-                const int* r = ustat + 1 + c * kRxUnitStride;
-                long long polls = 0;
-                while (ld_acquire(r + 7) == 0) {
-                    if (++polls > kRxPollLimit) {
-                        fail = true;
-                        break;
-                    }
-                }
-                if (!fail) {
-#pragma unroll
-                    for (int j = 0; j < 7; ++j) {
-                        const int x = r[j];
-                        if (j < 6) {
-                            all[j] += x;
-                            if (c < b) pre[j] += x;
-                        } else {
-                            all[6] = max(all[6], x);
-                        }
-                    }
-                }
+    const int mx = __reduce_max_sync(0xffffffffu, len);
+    if (lane == 0 && mx) atomicMax(&stot[6], mx);
+    __syncthreads();
+    if (tid < 7) btot[blockIdx.x * 8 + tid] = stot[tid];
+}
+
+__global__ void __launch_bounds__(kRxUnitThreads)
+rx_units_write_kernel(const int* __restrict__ rowcnt, int N, int M, int g, const int* __restrict__ btot,
+                      int* __restrict__ row_ptr, int4* __restrict__ seg_units, int4* __restrict__ row_units,
+                      int4* __restrict__ finish, int* __restrict__ counters)
+{
+    __shared__ int ws[6 * (kRxUnitThreads / 32 + 1)];
+    __shared__ int sbase[6], sgrand[7];
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x, nblk = static_cast<int>(gridDim.x);
+    pdl_launch_dependents();  // the reduce may be launched now; it waits for this grid to finish
+    pdl_wait();
+    if (counters[kCtrErrIndex]) return;  // the same for every CTA
+    const int m = b * kRxUnitThreads + tid;
+    const int len = m < M ? rowcnt[m] : 0;
+    // every block's totals into shared memory at once (one load per thread),
+    // then seven threads sum them
+    __shared__ int sb[kRxMaxUnitBlocks * 8];
+    if (tid < nblk * 8) sb[tid] = btot[tid];
+    __syncthreads();
+    if (tid < 7) {
+        int pre = 0, all = 0;
+        for (int q = 0; q < nblk; ++q) {
+            const int x = sb[q * 8 + tid];
+            if (tid == 6) {
+                all = max(all, x);
+            } else {
+                all += x;
+                if (q < b) pre += x;
             }
         }
-#pragma unroll
-        for (int j = 0; j < 6; ++j) {
-            pre[j] = __reduce_add_sync(0xffffffffu, pre[j]);
-            all[j] = __reduce_add_sync(0xffffffffu, all[j]);
-        }
-        all[6] = __reduce_max_sync(0xffffffffu, all[6]);
-        const bool anyfail = __any_sync(0xffffffffu, fail);
-        if (lane == 0) {
-#pragma unroll
-            for (int j = 0; j < 6; ++j) sbase[j] = pre[j];
-#pragma unroll
-            for (int j = 0; j < 7; ++j) sgrand[j] = all[j];
-            sfail = anyfail ? 1 : 0;
-            if (anyfail) atomicOr(&counters[kCtrErrTimeout], 1);
-        }
+        if (tid < 6) sbase[tid] = pre;
+        sgrand[tid] = all;
     }
+    int v[6];
+    rx_row_classes(len, g, v);
+    if (m >= M) v[5] = 0;
     int t6[6];
-    block_excl_scan_n<kRxUnitThreads, 6>(v, ws, t6);  // synchronises: sbase, sgrand, sfail are visible
-    if (sfail) return;
+    block_excl_scan_n<kRxUnitThreads, 6>(v, ws, t6);  // synchronises: sbase, sgrand are visible
     if (m < M) {
         const int G = 1 << g;
         row_ptr[m] = sbase[0] + v[0];
@@ -467,7 +468,7 @@ rx_units_kernel(const int* __restrict__ rowcnt, int N, int M, int g, int* __rest
             const int eA = sbase[1] + v[1];
             const int na = (nch + G - 1) >> g;
             finish[sbase[4] + v[4]] = make_int4(m, eA, na, 0);
-            for (int j = 0; j < na; ++j) seg_units[eA + j] = make_int4(m, j, eA + j, 0);
+            for (int q = 0; q < na; ++q) seg_units[eA + q] = make_int4(m, q, eA + q, 0);
         } else if (nch > 1) {
             seg_units[sgrand[1] + sbase[2] + v[2]] = make_int4(m, -1, 0, 0);
         } else if (nch == 1) {
@@ -477,7 +478,7 @@ rx_units_kernel(const int* __restrict__ rowcnt, int N, int M, int g, int* __rest
         }
         if (m == M - 1) row_ptr[M] = N;
     }
-    if (b == 0 && tid < kCtrCount && tid != kCtrErrIndex && tid != kCtrErrTimeout) {
+    if (b == 0 && tid < kCtrCount && tid != kCtrErrIndex) {
         const int* G7 = sgrand;
         int x = 0;
         if (tid == kCtrSegs) x = G7[1];
@@ -498,12 +499,12 @@ rx_units_kernel(const int* __restrict__ rowcnt, int N, int M, int g, int* __rest
 
 bool plan_radix_applies(int64_t N, int64_t M)
 {
-    return N >= 1 && N < (int64_t(1) << 24) && M >= 1 && M <= 65536 && cdiv(M, kRxUnitThreads) <= kRxMaxUnitCtas;
+    return N >= 1 && N < (int64_t(1) << 24) && M >= 1 && M <= 65536;
 }
 
 int64_t plan_radix_tiles(int64_t N) { return std::max<int64_t>(1, cdiv(N, kRxTile)); }
 
-int64_t plan_radix_ustat_ints(int64_t M) { return 1 + cdiv(M, kRxUnitThreads) * kRxUnitStride; }
+int64_t plan_radix_blocks(int64_t M) { return std::max<int64_t>(1, cdiv(M, kRxUnitThreads)); }
 
 det_status launch_plan_radix(const int32_t* idx, int64_t N, int64_t M, int g, const RadixBuffers& b,
                              cudaStream_t st)
@@ -513,14 +514,16 @@ det_status launch_plan_radix(const int32_t* idx, int64_t N, int64_t M, int g, co
     const unsigned int um = static_cast<unsigned int>(M);
     const bool two = M > kRxRadix;
     const size_t smem = sizeof(RxScatterShared);
-    const int nu = static_cast<int>(cdiv(M, kRxUnitThreads));
-    const int zero_a = static_cast<int>(M), zero_b = static_cast<int>(plan_radix_ustat_ints(M));
+    int sms = 1;
+    { const det_status a_ = current_sm_count(&sms); if (a_) return a_; }
+    const int cgrid = static_cast<int>(std::min<int64_t>(ntiles, int64_t(sms) * 4));
     const int* no_bad = nullptr;
     int* no_i = nullptr;
+    const bool vec_idx = aligned(idx, 16);
     // pass 0: the low byte of idx
-    DETR_CUDA(launch_after_previous(rx_count_kernel<0>, dim3(ntiles), dim3(kRxThreads), 0, st,
-                                    static_cast<const int*>(idx), n, um, b.counts, ntiles, b.tbad, b.rowcnt, zero_a,
-                                    b.ustat, zero_b));
+    DETR_CUDA(launch_after_previous(vec_idx ? rx_count_kernel<0, true> : rx_count_kernel<0, false>, dim3(cgrid),
+                                    dim3(kRxThreads), 0, st, static_cast<const int*>(idx), n, um, b.counts, ntiles,
+                                    b.tbad, b.rowcnt, static_cast<int>(M)));
     DETR_LAUNCHED();
     DETR_CUDA(launch_after_previous(rx_offset_kernel, dim3(kRxRadix), dim3(kRxThreads), 0, st, b.counts, ntiles,
                                     b.totals0, static_cast<const int*>(b.tbad), b.counters));
@@ -533,10 +536,9 @@ det_status launch_plan_radix(const int32_t* idx, int64_t N, int64_t M, int g, co
                                         static_cast<const int*>(b.totals0), no_bad, ntiles, no_i,
                                         static_cast<const int*>(b.counters)));
         DETR_LAUNCHED();
-        // pass 1: the high byte, from the packed words
-        DETR_CUDA(launch_after_previous(rx_count_kernel<1>, dim3(ntiles), dim3(kRxThreads), 0, st,
-                                        static_cast<const int*>(b.packed), n, um, b.counts, ntiles, no_i, no_i, 0,
-                                        no_i, 0));
+        // pass 1: the high byte, from the packed words (16-byte aligned in the workspace)
+        DETR_CUDA(launch_after_previous(rx_count_kernel<1, true>, dim3(cgrid), dim3(kRxThreads), 0, st,
+                                        static_cast<const int*>(b.packed), n, um, b.counts, ntiles, no_i, no_i, 0));
         DETR_LAUNCHED();
         DETR_CUDA(launch_after_previous(rx_offset_kernel, dim3(kRxRadix), dim3(kRxThreads), 0, st, b.counts, ntiles,
                                         b.totals1, no_bad, no_i));
@@ -558,9 +560,15 @@ det_status launch_plan_radix(const int32_t* idx, int64_t N, int64_t M, int g, co
                                         static_cast<const int*>(b.counters)));
         DETR_LAUNCHED();
     }
-    DETR_CUDA(launch_after_previous(rx_units_kernel, dim3(nu), dim3(kRxUnitThreads), 0, st,
-                                    static_cast<const int*>(b.rowcnt), n, static_cast<int>(M), g, b.ustat, b.row_ptr,
-                                    b.seg_units, b.row_units, b.finish, b.counters));
+    const unsigned int nblk = static_cast<unsigned int>(cdiv(M, kRxUnitThreads));
+    DETR_CUDA(launch_after_previous(rx_units_count_kernel, dim3(nblk), dim3(kRxUnitThreads), 0, st,
+                                    static_cast<const int*>(b.rowcnt), static_cast<int>(M), g, b.btot,
+                                    static_cast<const int*>(b.counters)));
+    DETR_LAUNCHED();
+    DETR_CUDA(launch_after_previous(rx_units_write_kernel, dim3(nblk), dim3(kRxUnitThreads), 0, st,
+                                    static_cast<const int*>(b.rowcnt), n, static_cast<int>(M), g,
+                                    static_cast<const int*>(b.btot), b.row_ptr, b.seg_units, b.row_units, b.finish,
+                                    b.counters));
     DETR_LAUNCHED();
     return DET_OK;
 }

@@ -34,7 +34,8 @@ MANIFEST = {
                 ["test_plan_lists_match_oracle", "test_plan_errors", "test_physical_row_permutation_with_src_id"]),
     "plan_cluster.cu": (["plan_cluster_kernel", "plan_cluster_one_kernel"],
                         ["test_plan_lists_match_oracle", "test_plan_paths_give_same_bytes"]),
-    "plan_radix.cu": (["rx_count_kernel", "rx_offset_kernel", "rx_scatter_kernel", "rx_units_kernel"],
+    "plan_radix.cu": (["rx_count_kernel", "rx_offset_kernel", "rx_scatter_kernel", "rx_units_count_kernel",
+                       "rx_units_write_kernel"],
                       ["test_plan_lists_match_oracle", "test_plan_paths_give_same_bytes", "test_plan_errors",
                        "test_cluster_plan_hot_rows", "test_plan_zipf_hot_rows_and_work_list"]),
     "plan_owner.cu": (["plan_owner_kernel"],
