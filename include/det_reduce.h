@@ -301,7 +301,10 @@ det_status det_index_add(det_plan plan,
  *    bytes), else DET_ERR_UNSUPPORTED and nothing is launched.
  *  - The first call on each device looks up the array's device address (once
  *    per device, with that device current) and keeps it; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept together with the id of
+ *    the context it belongs to: after a device reset the first call in the
+ *    new context looks it up again (so that call, too, should not be inside
+ *    a stream capture).
  *  - All calls share the one array and it keeps the last call's contents.
  *    Nothing in it needs clearing (each slot is written before it is read),
  *    but calls whose work overlaps on the GPU (other streams, other threads)

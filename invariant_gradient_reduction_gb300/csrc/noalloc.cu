@@ -24,11 +24,45 @@ constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on each device, looked up once per
-// device with that device current (the host-side symbol is only a stand-in and
-// must never be handed to a kernel).
-static void* g_scratch_addr[kNoAllocMaxDevices] = {};
+// Device address of g_noalloc_scratch on each device, looked up with that
+// device current (the host-side symbol is only a stand-in and must never be
+// handed to a kernel), together with the id of the context it was looked up
+// in: after a device reset the module is loaded again in a new context and
+// the array may have moved, so a changed context id means a new lookup.
+struct ScratchEntry {
+    void* addr;
+    unsigned long long ctx_id;
+};
+static ScratchEntry g_scratch[kNoAllocMaxDevices] = {};
 static std::mutex g_scratch_mu;
+
+// Id of the current context (0 if there is none yet or the driver cannot say),
+// through the driver's entry points, so that the library needs no link-time
+// dependency on the driver library.
+static unsigned long long current_context_id()
+{
+    using GetCurrent = int (*)(void**);
+    using GetId = int (*)(void*, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static bool resolved = false;
+    if (!resolved) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+        resolved = true;
+    }
+    void* ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == 0 && ctx && get_id(ctx, &id) == 0) return id;
+    return 0;
+}
 
 static det_status scratch_address(void** out)
 {
@@ -36,13 +70,15 @@ static det_status scratch_address(void** out)
     DETR_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kNoAllocMaxDevices) return DET_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchEntry& e = g_scratch[dev];
+    if (!e.addr || e.ctx_id == 0 || current_context_id() != e.ctx_id) {
         void* p = nullptr;
-        DETR_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+        DETR_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));  // also makes the context current
         if (!p) return DET_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        e.addr = p;
+        e.ctx_id = current_context_id();
     }
-    *out = g_scratch_addr[dev];
+    *out = e.addr;
     return DET_OK;
 }
 
@@ -64,7 +100,8 @@ extern "C" det_status det_scatter_reduce_noalloc(det_plan plan, const void* cons
     s = scratch_address(&scratch);
     if (s) return s;
     // The partial slots need no clearing: every slot is written by the first
-    // pass before the second pass reads it.
+    // pass before the second pass reads it.  The whole array is passed as the
+    // workspace, so the aliasing checks of det_scatter_reduce cover all of it.
     return det_scatter_reduce(plan, x_shards, shard_rows, P, x_dtype, ldx, H, w, out, ldo, out_dtype, scratch,
                               kNoAllocScratchBytes, opts, stream);
 }

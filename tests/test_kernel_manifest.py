@@ -22,7 +22,7 @@ MANIFEST = {
                   ["test_atomic_baseline_close_to_oracle", "test_atomic_baseline_bf16_and_index_errors",
                    "test_atomic_negative_control_differs_across_replays"]),
     "gather.cu": (["gather_reduce_kernel", "finish_kernel"],
-                  ["test_scatter_small_matches_oracle", "test_full_size_sampled_parity", "test_cluster_plan_hot_rows",
+                  ["test_scatter_small_matches_oracle", "test_full_size_parity", "test_cluster_plan_hot_rows",
                    "test_segment_size_changes_no_bit", "test_index_add_matches_oracle"]),
     "gather_async.cu": (["gather_async_kernel"], ["test_gather_path_changes_no_bit"]),
     "gather_bulk.cu": (["gather_bulk_kernel"], ["test_gather_path_changes_no_bit"]),

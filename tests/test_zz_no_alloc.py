@@ -4,14 +4,18 @@ path that must not allocate after start-up, an interface with no way to pass a
 workspace).  Its scratch is a fixed 16 MiB array in the library's device image.
 
 Called straight through the C ABI (ctypes), twice in a row, and compared byte
-for byte with det_scatter_reduce given a caller workspace (the same 0-ULP
-tolerance as every other parity test).  Collected last on purpose.
+for byte with the CPU oracle and with det_scatter_reduce given a caller
+workspace (the same 0-ULP tolerance as every other parity test).  Collected
+last on purpose.
 """
 import ctypes
 
 import numpy as np
 import pytest
 import torch
+
+import oracle
+from helpers import oracle_scatter
 
 pytestmark = pytest.mark.gpu
 
@@ -25,6 +29,7 @@ def lib():
         pytest.skip("needs a GPU")
     from invariant_gradient_reduction_gb300 import build
     build.build()
+    oracle.build()
     from invariant_gradient_reduction_gb300 import detreduce as dr
     L = dr.lib()
     f = L.det_scatter_reduce_noalloc
@@ -61,11 +66,49 @@ def test_noalloc_matches_workspace_entry_point_twice(lib, name):
         assert plan.describe()["n_segments"] > 0  # the scratch is really used
     want = torch.empty(case.M, case.H, dtype=case.out_dtype, device=DEV)
     dr.det_scatter_reduce(plan, case.x, want, w=case.w)
+    ref = oracle_scatter(case)
     for _ in range(2):
         got = torch.full_like(want, 7)
         assert _noalloc(lib, plan, case, got) == dr.DET_OK
         torch.cuda.synchronize()
         assert np.array_equal(_bits(got), _bits(want))
+        assert _bits(got).tobytes() == ref.tobytes()
+
+
+def test_noalloc_with_an_unwaited_plan(lib):
+    """A plan that does not wait: its counts stay on the device, the size check takes
+    the upper bound, and the hot destinations' finish pass reads its counts there."""
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    from invariant_gradient_reduction_gb300 import workloads as wl
+    oracle.build()
+    case = wl.make("sparse_key_scatter", "small", device=DEV)
+    plan = dr.det_reduce_plan(case.idx, case.M, opts={"async_plan": 1})
+    ref = oracle_scatter(case)
+    for _ in range(2):
+        got = torch.full((case.M, case.H), 7.0, dtype=case.out_dtype, device=DEV)
+        assert _noalloc(lib, plan, case, got) == dr.DET_OK
+        torch.cuda.synchronize()
+        assert _bits(got).tobytes() == ref.tobytes()
+    dr.det_plan_status(plan)
+    assert plan.describe()["n_segments"] > 0  # hot segments went through the shared array
+
+
+def test_noalloc_rejects_an_unwaited_plan_whose_bound_is_too_large(lib):
+    """An unwaited plan over 65536 sources bounds its partial slots by 513; at a
+    width of 8192 that is 513 x 32 KB > 16 MiB, so the call is refused before any
+    launch, whatever the data."""
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    from invariant_gradient_reduction_gb300.workloads import ScatterCase
+    N, H = 65536, 8192
+    x = torch.zeros(N, H, dtype=torch.bfloat16, device=DEV)
+    case = ScatterCase("bound", torch.arange(N, dtype=torch.int32, device=DEV) % 7, x, None, 7, torch.float32)
+    plan = dr.det_reduce_plan(case.idx, case.M, opts={"async_plan": 1})
+    assert dr.det_scatter_workspace_size(plan, H) > LIMIT
+    out = torch.empty(case.M, H, device=DEV)
+    assert _noalloc(lib, plan, case, out) == dr.DET_ERR_UNSUPPORTED
+    dr.det_plan_status(plan)
+    del x
+    torch.cuda.empty_cache()
 
 
 def test_noalloc_scratch_reuse_between_different_problems(lib):
@@ -83,6 +126,7 @@ def test_noalloc_scratch_reuse_between_different_problems(lib):
         assert _noalloc(lib, plan, case, got) == dr.DET_OK
         torch.cuda.synchronize()
         assert np.array_equal(_bits(got), _bits(want))
+        assert _bits(got).tobytes() == oracle_scatter(case).tobytes()
 
 
 def test_noalloc_rejects_scratch_beyond_limit(lib):
