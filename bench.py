@@ -53,6 +53,7 @@ WORKLOADS = {
     "sparse_key_scatter": "sparse_key_scatter Q=16384 K=512 S=65536 zipf=1.1 H=128 bf16 x -> fp32 out",
     "ep_invariance": "ep_invariance T=16384 E=256 top-k=8 H=7168 bf16 x, fp32 w -> bf16 out",
     "splitk": "splitk S=56 R=16384 C=24 fp32 -> fp32",
+    "splitk_gemm": "split-K GEMM with the split-ordered fold in its epilogue (16384 x 7168 x 24, 56 splits)",
     "embedding_backward": "embedding_backward T=32768 tokens V=131072 zipf=1.0 H=4096 bf16 dY, index_add into fp32 grad",
     "moe_route": "moe_route T=4096 E=128 top-k=8 H=4096: softmax scores -> sorted top-k -> route plan -> combine, "
                  "bf16 x -> bf16 out",
@@ -70,7 +71,7 @@ def parse_args(argv=None):
     ap.add_argument("--size", choices=["full", "medium"], default="full",
                     help="medium: a quarter-size case of the same shape (for profiler captures only)")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--also", default="sparse_key_scatter,ep_invariance,moe_route,splitk,embedding_backward",
+    ap.add_argument("--also", default="sparse_key_scatter,ep_invariance,moe_route,splitk,splitk_gemm,embedding_backward",
                     help="comma-separated secondary workloads to measure (default: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-dir", default=os.path.join(ROOT, "bench_out"),
@@ -494,6 +495,41 @@ def measure_splitk(timer, steps, warmup, torch, device):
     return res
 
 
+def measure_splitk_gemm(timer, steps, warmup, torch, device, peaks):
+    """The split-K producer with the fold in its epilogue (mHC-like shape: 16384
+    rows, K = 7168 in 56 splits of 128, 24 columns), against the same producer
+    writing its 56 partials to memory followed by det_splitk_reduce over them.
+    Compulsory bytes of the fused step: A and W read once, out written once."""
+    from invariant_gradient_reduction_gb300 import detreduce as dr
+    from invariant_gradient_reduction_gb300 import workloads as wl
+    R, K, C, S = 16384, 7168, 24, 56
+    A, W = wl.splitk_gemm_inputs(R, K, C, seed=5, device=device)
+    out = torch.empty(R, C, dtype=torch.float32, device=device)
+    out2 = torch.empty(R * C, dtype=torch.float32, device=device)
+    scratch = torch.empty(R, C, dtype=torch.float32, device=device)
+    P = torch.empty(S, R * C, dtype=torch.float32, device=device)
+    t_f, l_f = timer.run(lambda: dr.det_splitk_gemm_reduce(A, W, S, out), steps, warmup)
+
+    def unfused():
+        dr.det_splitk_gemm_reduce(A, W, S, scratch, partials=P)
+        dr.det_splitk_reduce(P, out2)
+
+    t_u, l_u = timer.run(unfused, steps, warmup)
+    torch.cuda.synchronize()
+    same = bool(torch.equal(out.view(-1).view(torch.int32), out2.view(torch.int32)))
+    cb = R * K * 2 + C * K * 2 + R * C * 4
+    ms_f, ms_u = statistics.mean(t_f), statistics.mean(t_u)
+    flops = 2.0 * R * K * C
+    return {"workload": f"split-K GEMM A bf16 [{R},{K}] x W bf16 [{C},{K}]^T, K in {S} splits of {K // S}, "
+                        f"fold over splits in the epilogue, fp32 out [{R},{C}]",
+            "compulsory_bytes": cb,
+            "fused": {"ms": ms_f, "gbs": gbs(cb, ms_f), "frac_hbm": gbs(cb, ms_f) / peaks["hbm_gbs"],
+                      "tflops": flops / (ms_f * 1e-3) / 1e12, "launches_per_step": l_f / max(1, steps)},
+            "partials_then_reduce": {"ms": ms_u, "gbs": gbs(cb, ms_u), "launches_per_step": l_u / max(1, steps),
+                                     "partial_bytes": S * R * C * 4},
+            "same_output_bits": same}
+
+
 def oracle_sample_seconds(case, max_rows: int):
     """Run the CPU oracle once on the first max_rows destinations and all their sources.
     Returns (seconds, compulsory bytes of the sample, description)."""
@@ -684,6 +720,10 @@ def run_ours(args):
         if "splitk" in wanted:
             also["splitk"] = measure_splitk(timer, max(10, min(args.steps, 50)), args.warmup, torch, device)
             also["splitk"]["workload"] = WORKLOADS["splitk"]
+        if "splitk_gemm" in wanted:
+            also["splitk_gemm"] = measure_splitk_gemm(timer, max(10, min(args.steps, 50)), args.warmup, torch, device,
+                                                      peaks)
+            torch.cuda.empty_cache()
         if "embedding_backward" in wanted:
             c3 = make_case("embedding_backward", device)
             r3 = measure_index_add(c3, timer, max(5, min(args.steps, 30)), args.warmup, torch)

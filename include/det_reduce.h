@@ -330,6 +330,44 @@ det_status det_splitk_reduce(const float* partials, int32_t S, int64_t count, in
                              void* out, det_dtype out_dtype, const det_opts* opts, void* stream);
 
 /*
+ * Split-K GEMM with the split-id-ordered reduce in its epilogue: the producer
+ * of the partials and their reduce in one kernel, so that the partials never
+ * go to memory (Ch 09, section 3.3: the mHC backward is forced into split-K,
+ * each split writes its own buffer and a reduce sums them in split-id order;
+ * "Bit-exact training interview notes", table "where nondeterminism comes
+ * from": several writers of one output get private slots merged in a fixed
+ * order, as in a grouped-GEMM epilogue).
+ *   P_s[r][c] = sum over the K/S values of k in split s (k in
+ *               [s*K/S, (s+1)*K/S)) of A[r][k] * W[c][k], accumulated in
+ *               binary32 by the tensor cores (bf16 products are exact; the
+ *               order of that accumulation inside one split is the hardware's,
+ *               the same for every call);
+ *   out[r][c] = canonical sum over s = 0 .. S-1 of P_s[r][c]: the same fold
+ *               as det_splitk_reduce (chunks of 32 splits left to right, then
+ *               the level-wise pairwise tree), stored as out_dtype.
+ *  A         dev bf16 [R][lda], K contiguous; lda >= K, lda*2 and A 16-byte
+ *            aligned.
+ *  W         dev bf16 [C][ldw] (the transposed right operand: row c holds
+ *            column c of B), same rules; 1 <= C <= 32.
+ *  K         a multiple of S, K/S a multiple of 64; 1 <= S <= 256.
+ *  ab_dtype  DET_BF16 (the only input type).
+ *  out       dev [R][ldo] of out_dtype, ldo >= C; overwritten.
+ *  partials  NULL, or dev float [S][ldp] (ldp >= R*C): each split's P_s is
+ *            also written there, row-major [R][C] (for checking the fold, or
+ *            for an unfused reduce by det_splitk_reduce, which then gives
+ *            the same out).
+ * One CTA per 128 rows on tensor cores (tcgen05) with TMA-fed shared memory;
+ * no workspace.  With opts->debug_checks the call waits and reports an
+ * expired bounded wait as DET_ERR_TIMEOUT.
+ * Errors: DET_ERR_ARG, DET_ERR_DTYPE, DET_ERR_UNSUPPORTED (C > 32, S > 256,
+ * K not S x a multiple of 64), DET_ERR_CUDA, DET_ERR_TIMEOUT.
+ */
+det_status det_splitk_gemm_reduce(const void* A, int64_t lda, const void* W, int64_t ldw, int64_t R, int32_t C,
+                                  int64_t K, int32_t S, det_dtype ab_dtype, void* out, int64_t ldo,
+                                  det_dtype out_dtype, float* partials, int64_t ldp, const det_opts* opts,
+                                  void* stream);
+
+/*
  * u64 fingerprint of nbytes bytes at dev pointer p, written to dev *out.
  * The repeatability gate compares per-tensor fingerprints byte for byte
  * instead of a printed loss ("Bit-exact training interview notes", "how to

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdetreduce.so")
-SOURCES = ["api.cu", "plan.cu", "plan_cluster.cu", "plan_owner.cu", "plan_radix.cu", "gather.cu", "gather_bulk.cu", "gather_async.cu", "splitk.cu", "hash.cu", "atomic.cu", "noalloc.cu", "route.cu"]
+SOURCES = ["api.cu", "plan.cu", "plan_cluster.cu", "plan_owner.cu", "plan_radix.cu", "gather.cu", "gather_bulk.cu", "gather_async.cu", "splitk.cu", "splitk_gemm.cu", "hash.cu", "atomic.cu", "noalloc.cu", "route.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no multiply-add contraction anywhere (the kernels also use
 # __fmul_rn/__fadd_rn explicitly); default IEEE division/sqrt/denormals.

@@ -81,6 +81,8 @@ def _declare(lib):
                                 P(det_opts), vp], i32),
         "det_index_add": ([vp, P(vp), P(i64), i32, i32, i64, i64, vp, vp, i64, i32, vp, sz, P(det_opts), vp], i32),
         "det_splitk_reduce": ([vp, i32, i64, i64, vp, i32, P(det_opts), vp], i32),
+        "det_splitk_gemm_reduce": ([vp, i64, vp, i64, i64, i32, i64, i32, i32, vp, i64, i32, vp, i64, P(det_opts),
+                                    vp], i32),
         "det_hash": ([vp, ctypes.c_uint64, vp, vp], i32),
         "det_atomic_workspace_size": ([i64, i64, i32, P(sz)], i32),
         "det_atomic_scatter_reduce": ([vp, i64, i64, P(vp), P(i64), i32, i32, i64, i64, vp, vp, i64, i32, vp,
@@ -379,6 +381,36 @@ def det_splitk_reduce(partials: torch.Tensor, out: torch.Tensor, opts: Optional[
         raise ValueError("out must be a contiguous float32/bfloat16 tensor of `count` elements")
     _check(lib().det_splitk_reduce(_ptr(partials), S, count, ldp, _ptr(out), _TORCH_TO_DET[out.dtype],
                                    _opts(opts), _stream(stream)), "det_splitk_reduce")
+    return out
+
+
+def det_splitk_gemm_reduce(A: torch.Tensor, W: torch.Tensor, S: int, out: torch.Tensor,
+                           partials: Optional[torch.Tensor] = None, opts: Optional[dict] = None, stream=None):
+    """out[r, c] = canonical sum over s of P_s[r, c], P_s = the split-s K-slice of A @ W.T.
+
+    ``A`` bf16 [R, K] and ``W`` bf16 [C, K] (rows may be padded: K contiguous),
+    K = S * (a multiple of 64), C <= 32; ``out`` float32/bfloat16 [R, C] (rows
+    may be padded).  ``partials``: None, or float32 [S, >= R*C] to receive each
+    split's partial as well (row-major [R, C] per split).
+    """
+    if A.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise ValueError("A and W must be bfloat16")
+    lda, K = _rows(A)
+    ldw, Kw = _rows(W)
+    if Kw != K:
+        raise ValueError("A and W need the same K")
+    R, C = A.shape[0], W.shape[0]
+    ldo, oc = _rows(out)
+    if out.shape[0] != R or oc != C or out.dtype not in _TORCH_TO_DET:
+        raise ValueError("out must be float32/bfloat16 [R, C]")
+    ldp = 0
+    if partials is not None:
+        if partials.dtype != torch.float32 or partials.dim() != 2 or partials.shape[0] != S:
+            raise ValueError("partials must be float32 [S, >= R*C]")
+        ldp = _rows(partials)[0]
+    _check(lib().det_splitk_gemm_reduce(_ptr(A), lda, _ptr(W), ldw, R, C, K, S, DET_BF16, _ptr(out), ldo,
+                                        _TORCH_TO_DET[out.dtype], _ptr(partials), ldp, _opts(opts), _stream(stream)),
+           "det_splitk_gemm_reduce")
     return out
 
 

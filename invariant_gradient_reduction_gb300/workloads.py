@@ -187,6 +187,14 @@ def splitk_partials(S: int, R: int, C: int, seed: int = 5, device="cpu") -> torc
     return (z * torch.exp2(u)).to(torch.float32)
 
 
+def splitk_gemm_inputs(R: int, K: int, C: int, seed: int = 5, device="cpu"):
+    """Inputs of a split-K GEMM out = A @ W.T: A bf16 [R, K] ~ N(0, 1) and W bf16
+    [C, K] ~ N(0, 1) * 2^-5 (the transposed right operand, K contiguous)."""
+    A = _fill_normal((R, K), torch.bfloat16, 1.0, seed * 7919 + 11, device)
+    W = _fill_normal((C, K), torch.bfloat16, 2.0 ** -5, seed * 7919 + 13, device)
+    return A, W
+
+
 # --- the five workloads at full size, and small versions for fast parity runs ---
 
 FULL = {
@@ -267,4 +275,4 @@ def cdiv(a: int, b: int) -> int:
 
 
 __all__ = ["ScatterCase", "moe_routing", "moe_combine", "zipf_key_lists", "sparse_key_scatter",
-           "embedding_backward", "splitk_partials", "FULL", "MEDIUM", "SMALL", "make", "ep_shard_rows", "split_rows", "round_up", "cdiv"]
+           "embedding_backward", "splitk_partials", "splitk_gemm_inputs", "FULL", "MEDIUM", "SMALL", "make", "ep_shard_rows", "split_rows", "round_up", "cdiv"]

@@ -187,6 +187,31 @@ def splitk_reduce(partials, out_dtype: int = F32):
     return out
 
 
+def splitk_gemm_partials(a_bits, w_bits, S: int) -> np.ndarray:
+    """Exact (binary64) per-split partial sums of a split-K GEMM: P[s][r][c] =
+    sum over the K/S values of k in split s of A[r][k] * W[c][k].
+
+    A is [R, K] and W is [C, K], both bf16 bit patterns (K contiguous); the K
+    dimension is cut into S equal consecutive splits, each producing its own
+    partial ("DeepSeek-V4 book, Ch 09", section 3.3: every K-split writes its
+    own buffer).  A bf16 times bf16 product is exact in binary64 and the sums
+    are taken in binary64, so this is the reference the GPU's binary32
+    tensor-core partials are compared with (within a rounding bound), not a
+    bit-exact one.  Returns float64 [S, R, C].
+    """
+    a = bf16_to_f32(a_bits).astype(np.float64)
+    w = bf16_to_f32(w_bits).astype(np.float64)
+    R, K = a.shape
+    C = w.shape[0]
+    if K % S:
+        raise ValueError("K must be a multiple of S")
+    ks = K // S
+    out = np.empty((S, R, C), dtype=np.float64)
+    for s in range(S):
+        out[s] = a[:, s * ks:(s + 1) * ks] @ w[:, s * ks:(s + 1) * ks].T
+    return out
+
+
 def mix64(z: int) -> int:
     return int(_load().oracle_mix64(z & 0xFFFFFFFFFFFFFFFF))
 

@@ -21,7 +21,7 @@ def test_args_defaults_and_minimum_warmup():
     assert a.gpus == 1 and a.warmup >= 3 and a.steps >= 1 and a.impl == "ours"
     assert bench.parse_args(["--warmup", "1"]).warmup == 3
     # every secondary workload runs by default and has a description; the clock samples stay in the repo
-    assert set(a.also.split(",")) == {"sparse_key_scatter", "ep_invariance", "moe_route", "splitk",
+    assert set(a.also.split(",")) == {"sparse_key_scatter", "ep_invariance", "moe_route", "splitk", "splitk_gemm",
                                       "embedding_backward"}
     assert all(w in bench.WORKLOADS for w in a.also.split(","))
     assert a.clocks_dir.startswith(ROOT)

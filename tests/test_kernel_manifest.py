@@ -45,6 +45,8 @@ MANIFEST = {
                  ["test_router_topk_matches_oracle", "test_router_topk_ties_and_special_values",
                   "test_route_plan_matches_oracle", "test_route_combine_matches_oracle"]),
     "splitk.cu": (["splitk_kernel"], ["test_splitk_matches_oracle", "test_splitk_split_counts"]),
+    "splitk_gemm.cu": (["splitk_gemm_kernel"], ["test_splitk_gemm_partials_exact_on_integers",
+                                                "test_splitk_gemm_fold_matches_oracle"]),
 }
 
 
