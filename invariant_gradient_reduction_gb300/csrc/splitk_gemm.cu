@@ -23,13 +23,15 @@
 // A (128 rows) and W (32 rows, zero past C) into a ring of shared-memory
 // stages with TMA (128-byte swizzle) on mbarriers; one thread of warp 1 issues
 // tcgen05.mma (bf16 in, fp32 accumulate, M = 128, N = 32, K = 16 each) into
-// one of two tensor-memory accumulators, alternating per split; warps 2..5
+// one of four tensor-memory accumulators, used in turn by the splits (so the
+// MMAs run up to four splits ahead of the epilogue); warps 2..5
 // read each finished accumulator (tcgen05.ld, one row per thread), release
 // it, and fold it into the row's running chunk in split order.  Every wait is
 // bounded; on expiry the CTA records the error, drains its own copies and
 // MMAs (bounded too), frees its tensor memory and returns.
 #include <cuda.h>  // CUtensorMap and the tensor-map enums (types only; entry points come from the runtime)
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -39,9 +41,10 @@ namespace detr {
 constexpr int kSgBM = 128;               // rows per CTA = tensor-memory lanes
 constexpr int kSgBN = 32;                // MMA N: columns of W (C <= 32, zero past C)
 constexpr int kSgBK = 64;                // K per stage: one 128-byte swizzle row of bf16
-constexpr int kSgStages = 8;
+constexpr int kSgStages = 9;            // at most; fewer when the fold stack needs the room
 constexpr int kSgThreads = 192;          // warp 0 TMA, warp 1 MMA (and tensor-memory owner), warps 2..5 epilogue
-constexpr int kSgTmemCols = 64;          // two accumulators of 32 columns
+constexpr int kSgAcc = 4;                // tensor-memory accumulators, used in turn by the splits
+constexpr int kSgTmemCols = kSgAcc * kSgBN;  // 128 columns
 constexpr int kSgMaxLevels = 4;          // fold counter levels: S <= 32 * 2^(levels - 1) = 256
 constexpr uint32_t kSgABytes = kSgBM * kSgBK * 2;  // 16 KB
 constexpr uint32_t kSgWBytes = kSgBN * kSgBK * 2;  // 4 KB
@@ -55,6 +58,7 @@ struct SgArgs {
     int R, C, S;
     int kbs;           // K blocks of 64 per split
     int levels;        // fold counter levels
+    int ns;            // shared-memory stages in use (<= kSgStages)
     void* out;
     long long ldo;
     int out_bf16;
@@ -172,7 +176,7 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                    const __grid_constant__ SgArgs a)
 {
     __shared__ __align__(8) unsigned long long bar_full[kSgStages], bar_empty[kSgStages];
-    __shared__ __align__(8) unsigned long long bar_tfull[2], bar_tempty[2], bar_drain;
+    __shared__ __align__(8) unsigned long long bar_tfull[kSgAcc], bar_tempty[kSgAcc], bar_drain;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
     extern __shared__ __align__(1024) unsigned char sg_dyn[];
@@ -180,18 +184,19 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t dyn = sg_smem(sg_dyn);
     const uint32_t base = (dyn + 1023u) & ~1023u;       // stages 1024-byte aligned for the swizzle
-    const uint32_t sA = base;                           // kSgStages x 16 KB
-    const uint32_t sW = base + kSgStages * kSgABytes;   // kSgStages x 4 KB
-    float* stack = reinterpret_cast<float*>(sg_dyn + (sW + kSgStages * kSgWBytes - dyn));  // [levels][32][128]
+    const uint32_t sA = base;                           // NS x 16 KB
+    const int NS = a.ns;
+    const uint32_t sW = base + NS * kSgABytes;          // NS x 4 KB
+    float* stack = reinterpret_cast<float*>(sg_dyn + (sW + NS * kSgWBytes - dyn));  // [levels][32][128]
     const int row0 = static_cast<int>(blockIdx.x) * kSgBM;
     const int nkb = a.S * a.kbs;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kSgStages; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(sg_smem(&bar_full[i]), 1);
             mbar_init(sg_smem(&bar_empty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kSgAcc; ++i) {
             mbar_init(sg_smem(&bar_tfull[i]), 1);
             mbar_init(sg_smem(&bar_tempty[i]), 4);  // one arrival per epilogue warp
         }
@@ -216,8 +221,8 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         if (lane == 0) {
             int issued = 0;
             for (int kb = 0; kb < nkb; ++kb) {
-                const int st = kb % kSgStages, use = kb / kSgStages;
-                if (kb >= kSgStages && !mbar_wait(sg_smem(&bar_empty[st]), (use - 1) & 1, &abort_flag)) {
+                const int st = kb % NS, use = kb / NS;
+                if (kb >= NS && !mbar_wait(sg_smem(&bar_empty[st]), (use - 1) & 1, &abort_flag)) {
                     abort_flag = 1;
                     atomicOr(&g_sg_status, 1);
                     break;
@@ -229,23 +234,23 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 ++issued;
             }
             // every copy this CTA issued has landed before it may leave
-            for (int kb = issued > kSgStages ? issued - kSgStages : 0; kb < issued; ++kb)
-                mbar_wait(sg_smem(&bar_full[kb % kSgStages]), (kb / kSgStages) & 1, &abort_flag);
+            for (int kb = issued > NS ? issued - NS : 0; kb < issued; ++kb)
+                mbar_wait(sg_smem(&bar_full[kb % NS]), (kb / NS) & 1, &abort_flag);
         }
     } else if (warp == 1) {
-        // MMA issuer: split s into accumulator s & 1
+        // MMA issuer: split s into accumulator s % kSgAcc
         if (lane == 0) {
             bool ok = true;
             for (int s = 0; s < a.S && ok; ++s) {
-                const int buf = s & 1;
-                if (s >= 2 && !mbar_wait(sg_smem(&bar_tempty[buf]), ((s >> 1) - 1) & 1, &abort_flag)) {
+                const int buf = s % kSgAcc;
+                if (s >= kSgAcc && !mbar_wait(sg_smem(&bar_tempty[buf]), ((s / kSgAcc) - 1) & 1, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(buf * kSgBN);
                 for (int j = 0; j < a.kbs; ++j) {
-                    const int kb = s * a.kbs + j, st = kb % kSgStages, use = kb / kSgStages;
+                    const int kb = s * a.kbs + j, st = kb % NS, use = kb / NS;
                     if (!mbar_wait(sg_smem(&bar_full[st]), use & 1, &abort_flag)) {
                         ok = false;
                         break;
@@ -278,9 +283,9 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         unsigned int cnt = 0;
         bool ok = true;
         for (int s = 0; s < a.S; ++s) {
-            const int buf = s & 1;
+            const int buf = s % kSgAcc;
             // the warp goes on only together (tcgen05.ld is warp-wide)
-            if (!__all_sync(0xffffffffu, mbar_wait(sg_smem(&bar_tfull[buf]), (s >> 1) & 1, &abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(sg_smem(&bar_tfull[buf]), (s / kSgAcc) & 1, &abort_flag))) {
                 ok = false;
                 break;
             }
@@ -442,8 +447,12 @@ extern "C" det_status det_splitk_gemm_reduce(const void* A, int64_t lda, const v
     a.out_bf16 = out_dtype == DET_BF16 ? 1 : 0;
     a.partials = partials;
     a.ldp = ldp;
-    const size_t smem = 1024 + static_cast<size_t>(kSgStages) * (kSgABytes + kSgWBytes) +
-                        static_cast<size_t>(a.levels) * 32 * kSgBM * sizeof(float);
+    // as many stages as fit beside the fold stack (227 KB per CTA at most)
+    const size_t stack = static_cast<size_t>(a.levels) * 32 * kSgBM * sizeof(float);
+    const size_t room = size_t(227) * 1024 - 2048 - 1024 - stack;
+    a.ns = static_cast<int>(std::min<size_t>(kSgStages, room / (kSgABytes + kSgWBytes)));
+    if (a.ns < 2) return DET_ERR_UNSUPPORTED;
+    const size_t smem = 1024 + static_cast<size_t>(a.ns) * (kSgABytes + kSgWBytes) + stack;
     s = allow_dynamic_smem(reinterpret_cast<const void*>(splitk_gemm_kernel), smem);
     if (s) return s;
     cudaStream_t st = as_stream(stream);
