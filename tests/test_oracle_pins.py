@@ -726,3 +726,64 @@ def test_moe_route_rejects_bad_ids(oracle_mod):
         with pytest.raises(oracle_mod.OracleError) as ei:
             oracle_mod.moe_route(ids, 6)
         assert ei.value.code == -2
+
+
+# --------------------------------------------------------------------------
+# split-K GEMM partials (the producer of the split-K reduce)
+# --------------------------------------------------------------------------
+
+def _bf16_ints(oracle, rng, shape, lo=-4, hi=5):
+    return oracle.f32_to_bf16(rng.integers(lo, hi, size=shape).astype(np.float32))
+
+
+def test_splitk_gemm_partials_brute_force(oracle_mod):
+    oracle = oracle_mod
+    """Each partial is the plain triple loop over its own K slice (rows of A
+    against rows of W), on tiny shapes with non-integer values."""
+    rng = np.random.default_rng(41)
+    for R, C, K, S in [(3, 2, 8, 2), (1, 1, 4, 4), (5, 3, 12, 3)]:
+        a = oracle.f32_to_bf16(rng.normal(size=(R, K)).astype(np.float32))
+        w = oracle.f32_to_bf16(rng.normal(size=(C, K)).astype(np.float32))
+        got = oracle.splitk_gemm_partials(a, w, S)
+        af = oracle.bf16_to_f32(a).astype(np.float64)
+        wf = oracle.bf16_to_f32(w).astype(np.float64)
+        ks = K // S
+        for s in range(S):
+            for r in range(R):
+                for c in range(C):
+                    v = 0.0
+                    for k in range(s * ks, (s + 1) * ks):
+                        v += af[r, k] * wf[c, k]
+                    assert got[s, r, c] == v
+
+
+def test_splitk_gemm_partials_sum_to_the_whole_product(oracle_mod):
+    oracle = oracle_mod
+    """Small integers: every partial and the whole product are exact, and the
+    partials add up to A @ W.T (a dropped or doubled K slice would not)."""
+    rng = np.random.default_rng(42)
+    a = _bf16_ints(oracle, rng, (7, 96))
+    w = _bf16_ints(oracle, rng, (5, 96))
+    p = oracle.splitk_gemm_partials(a, w, 6)
+    whole = oracle.bf16_to_f32(a).astype(np.float64) @ oracle.bf16_to_f32(w).astype(np.float64).T
+    assert p.shape == (6, 7, 5)
+    assert np.array_equal(p.sum(axis=0), whole)
+    # each split really is its own slice: zeroing one slice of A zeroes exactly that partial
+    a2 = a.copy()
+    a2[:, 16:32] = 0
+    p2 = oracle.splitk_gemm_partials(a2, w, 6)
+    assert np.all(p2[1] == 0) and np.array_equal(np.delete(p2, 1, 0), np.delete(p, 1, 0))
+
+
+def test_splitk_gemm_partials_orientation(oracle_mod):
+    oracle = oracle_mod
+    """W is [C, K] (the transposed right operand): a [K, C] array of the same
+    values gives other numbers or is rejected."""
+    rng = np.random.default_rng(43)
+    a = _bf16_ints(oracle, rng, (4, 6))
+    w = _bf16_ints(oracle, rng, (6, 6))  # square, so a transposed W is accepted but differs
+    p = oracle.splitk_gemm_partials(a, w, 2)
+    pt = oracle.splitk_gemm_partials(a, np.ascontiguousarray(w.T), 2)
+    assert not np.array_equal(p, pt)
+    with pytest.raises(ValueError):
+        oracle.splitk_gemm_partials(a, w, 4)  # K = 6 is not a multiple of 4
