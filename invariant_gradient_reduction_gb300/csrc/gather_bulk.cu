@@ -15,6 +15,7 @@
 // Every mbarrier wait is bounded; on expiry the CTA records kCtrErrTimeout in
 // the plan's counter block, drains the copies it issued (also bounded) and
 // returns.
+#include "bulk_copy.cuh"
 #include "common.cuh"
 #include "gather_internal.cuh"
 #include "plan_internal.cuh"
@@ -28,7 +29,6 @@ constexpr int kBulkStages = 3;
 constexpr int kBulkStageBytes = 64 * 1024;
 constexpr int kBulkMaxTerms = 32;
 constexpr int kBulkVecPerThread = 1;  // tile <= 8 KB = 512 16-byte vectors
-constexpr unsigned long long kWaitLimit = 1ull << 22;
 
 struct BulkStageMeta {
     int m;      // destination
@@ -36,57 +36,6 @@ struct BulkStageMeta {
     int col0;   // first element of the tile
     int bytes;  // bytes per term in this tile
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
-{
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: false if the barrier did not complete within the limit.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity)
-{
-    for (unsigned long long it = 0; it < kWaitLimit; ++it)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
 
 template <typename XT>
 struct BulkVec;

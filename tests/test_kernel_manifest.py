@@ -44,7 +44,7 @@ MANIFEST = {
     "route.cu": (["router_topk_kernel", "route_cluster_kernel", "route_rows_kernel", "route_combine_kernel"],
                  ["test_router_topk_matches_oracle", "test_router_topk_ties_and_special_values",
                   "test_route_plan_matches_oracle", "test_route_combine_matches_oracle"]),
-    "splitk.cu": (["splitk_kernel"], ["test_splitk_matches_oracle", "test_splitk_split_counts"]),
+    "splitk.cu": (["splitk_kernel", "splitk_two_chunk_kernel"], ["test_splitk_matches_oracle", "test_splitk_split_counts"]),
     "splitk_gemm.cu": (["splitk_gemm_kernel"], ["test_splitk_gemm_partials_exact_on_integers",
                                                 "test_splitk_gemm_fold_matches_oracle"]),
 }
