@@ -28,7 +28,9 @@
 //      before the owned range are its first row_ptr, the units before it are
 //      its offsets in the work list; the owned rows' lengths give their
 //      offsets; each CTA writes row_ptr and the units of 1/CS of the owned
-//      rows; the first CTA writes the counter block;
+//      rows; the first CTA writes the counter block (an id outside [0, M),
+//      flagged in step 1 and summed with the totals, stops every cluster
+//      here with only the error flag written);
 //   4. each warp reads its sub-range again in source order and places the
 //      owned matches (peers of a row in a round of 32 from one ballot per
 //      row-number bit): row start + earlier CTAs' and earlier warps' matches
@@ -53,7 +55,9 @@ constexpr int kCoWarps = kCoThreads / 32;
 constexpr int kCoClusters[3] = {8, 4, 2};  // cluster sizes tried, largest first (8 = the portable maximum)
 constexpr int kCoBatch = 8;          // 16-byte loads in flight per lane in the counting sweep
 constexpr int kCoScalarBatch = 8;    // 4-byte loads in flight per lane in the placing sweep
-constexpr int kCoAgg = 14;           // published totals: 7 before the owned range, 7 over all destinations
+constexpr int kCoAgg = 15;           // published totals: 7 before the owned range, 7 over all destinations, bad ids
+constexpr int kAggMax = 13;          // the longest row (a maximum, not a sum)
+constexpr int kAggBad = 14;          // CTAs that saw an id outside [0, M)
 constexpr size_t kCoMaxSmem = 200 * 1024;
 static_assert(kOwnMaxRows <= kCoThreads, "one owned row per thread");
 static_assert(kOwnMaxN / 32 < 65536, "a warp's count of one row fits 16 bits");
@@ -132,8 +136,11 @@ __device__ __forceinline__ void co_place(int rr, int pos, bool valid, unsigned i
 }
 
 // VEC: idx is 16-byte aligned (every sub-range starts at a multiple of 128
-// sources, so every full group of four is one 16-byte load).
-template <bool VEC, int CS>
+// sources, so every full group of four is one 16-byte load).  SHORT: a warp's
+// sub-range is shorter than one round of either sweep (fewer than 1024
+// sources), so both sweeps skip their batches past its end; with full rounds
+// the unguarded loops measured faster.
+template <bool VEC, int CS, bool SHORT>
 __global__ void __launch_bounds__(kCoThreads, 1)
 plan_owner_kernel(const __grid_constant__ CoArgs a)
 {
@@ -145,7 +152,6 @@ plan_owner_kernel(const __grid_constant__ CoArgs a)
     int* rstart = crow + a.Rk;                                             // [Rk]: first position of this CTA's matches
     __shared__ int agg[kCoAgg];   // this CTA's partial totals (read by the cluster)
     __shared__ int sagg[kCoAgg];  // the cluster's totals
-    __shared__ int sbad;          // this CTA saw an id outside [0, M) (read by the cluster)
     __shared__ int ws[6 * (kCoWarps + 1)];
 
     const int s = static_cast<int>(cl.block_rank());
@@ -173,9 +179,13 @@ plan_owner_kernel(const __grid_constant__ CoArgs a)
     // (0xffffffff: out of range, never a match)
     unsigned int nbad = 0u, npad = 0u;
     for (int p0 = wb + 4 * lane; p0 < we; p0 += 128 * kCoBatch) {
+        // batches that start past the sub-range hold no source of any lane
+        // (warp-uniform): skipped, so a short sub-range costs only its own work
+        const int nb = SHORT ? min(kCoBatch, (we - (p0 - 4 * lane) + 127) >> 7) : kCoBatch;
         int4 v[kCoBatch];
 #pragma unroll
         for (int b = 0; b < kCoBatch; ++b) {  // all loads in flight first
+            if (b >= nb) break;
             const int p = p0 + 128 * b;
             if (VEC && p + 3 < we) {
                 v[b] = __ldg(reinterpret_cast<const int4*>(a.idx + p));
@@ -189,6 +199,7 @@ plan_owner_kernel(const __grid_constant__ CoArgs a)
         }
 #pragma unroll
         for (int b = 0; b < kCoBatch; ++b) {
+            if (b >= nb) break;
             const unsigned int e[4] = {static_cast<unsigned int>(v[b].x), static_cast<unsigned int>(v[b].y),
                                        static_cast<unsigned int>(v[b].z), static_cast<unsigned int>(v[b].w)};
 #pragma unroll
@@ -200,16 +211,10 @@ plan_owner_kernel(const __grid_constant__ CoArgs a)
             }
         }
     }
-    const int my_bad = __syncthreads_or(nbad != npad);
-    if (tid == 0) sbad = my_bad;
+    // an id outside [0, M) is counted nowhere; the flag goes out with the
+    // totals and is acted on once they are read
+    if (__any_sync(0xffffffffu, nbad != npad) && lane == 0) atomicOr(&agg[kAggBad], 1);
     cl.sync();  // every CTA's counts are visible
-    // the cluster reads all of idx, so every cluster takes the same decision
-    const int any_bad = __syncthreads_or(tid < CS && *cl.map_shared_rank(&sbad, tid) != 0);
-    if (any_bad) {
-        if (k == 0 && s == 0 && tid < kCtrCount) a.counters[tid] = tid == kCtrErrIndex ? 1 : 0;
-        cl.sync();  // no CTA leaves while another may still read its flag
-        return;
-    }
 
     // 2. lengths of this CTA's 1/CS of the destinations, and their classes:
     //    totals over those before the owned range (vb) and over all (va)
@@ -239,11 +244,17 @@ plan_owner_kernel(const __grid_constant__ CoArgs a)
     if (tid < nr) {
         int run = 0;
         const int sh = (tid & 1) * 16;
-        for (int w = 0; w < kCoWarps; ++w) {
-            unsigned int* wr = whist + w * a.Rw + (tid >> 1);
-            const int x = static_cast<int>((*wr >> sh) & 0xffffu);
-            atomicAdd(wr, static_cast<unsigned int>(run - x) << sh);  // the half becomes run
-            run += x;
+        unsigned int* col = whist + (tid >> 1);
+        // eight warps' counts read at once, then their eight independent updates
+        for (int w0 = 0; w0 < kCoWarps; w0 += 8) {
+            int x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = static_cast<int>((col[(w0 + j) * a.Rw] >> sh) & 0xffffu);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                atomicAdd(col + (w0 + j) * a.Rw, static_cast<unsigned int>(run - x[j]) << sh);  // the half becomes run
+                run += x[j];
+            }
         }
         crow[tid] = run;
     }
@@ -254,7 +265,7 @@ plan_owner_kernel(const __grid_constant__ CoArgs a)
         if (lane == 0) {
             if (tb) atomicAdd(&agg[j], tb);
             if (ta) {
-                if (j == 6) atomicMax(&agg[7 + j], ta);
+                if (j == 6) atomicMax(&agg[kAggMax], ta);
                 else atomicAdd(&agg[7 + j], ta);
             }
         }
@@ -267,7 +278,7 @@ plan_owner_kernel(const __grid_constant__ CoArgs a)
 #pragma unroll
         for (int r = 0; r < CS; ++r) {
             const int x = cl.map_shared_rank(agg, r)[tid];
-            t = tid == kCoAgg - 1 ? max(t, x) : t + x;
+            t = tid == kAggMax ? max(t, x) : t + x;
         }
         sagg[tid] = t;
     }
@@ -283,6 +294,13 @@ plan_owner_kernel(const __grid_constant__ CoArgs a)
     cluster_arrive_release();
     int roff_tot;
     const int roff = block_excl_scan<kCoThreads>(rlen, ws, &roff_tot);  // synchronises: sagg is visible
+    if (sagg[kAggBad]) {
+        // every cluster read all of idx, so every CTA takes this branch: only
+        // the error flag is written
+        if (k == 0 && s == 0 && tid < kCtrCount) a.counters[tid] = tid == kCtrErrIndex ? 1 : 0;
+        cluster_wait_acquire();  // no CTA leaves while another may still read its shared memory
+        return;
+    }
     const int base = sagg[0];  // sources with idx < r_lo = row_ptr[r_lo]
     if (tid < nr) rstart[tid] = base + roff + before;
     // units of the owned rows, at offsets from the classes before each row
@@ -327,14 +345,17 @@ plan_owner_kernel(const __grid_constant__ CoArgs a)
     // 4. place the matches: the sub-range again in source order, 32 per round
     unsigned short* myc = reinterpret_cast<unsigned short*>(mywh);
     for (int p0 = wb; p0 < we; p0 += 32 * kCoScalarBatch) {
+        const int nb = SHORT ? min(kCoScalarBatch, (we - p0 + 31) >> 5) : kCoScalarBatch;  // rounds with a source (warp-uniform)
         unsigned int kk[kCoScalarBatch];
 #pragma unroll
         for (int b = 0; b < kCoScalarBatch; ++b) {
+            if (b >= nb) break;
             const int p = p0 + b * 32 + lane;
             kk[b] = p < we ? static_cast<unsigned int>(__ldg(a.idx + p)) : uM;
         }
 #pragma unroll
         for (int b = 0; b < kCoScalarBatch; ++b) {
+            if (b >= nb) break;
             const unsigned int rr = kk[b] - ulo;
             const bool valid = rr < unr;  // the padding M never matches: r_lo + nr <= M
             const unsigned int live = __ballot_sync(0xffffffffu, valid);
@@ -366,14 +387,18 @@ struct CoShape {
     size_t smem;
 };
 
-const void* co_kernel(int vec, int ci)
+const void* co_kernel(int vec, int ci, int shrt = 0)
 {
-    static const void* k[2][3] = {
-        {reinterpret_cast<const void*>(plan_owner_kernel<false, 8>), reinterpret_cast<const void*>(plan_owner_kernel<false, 4>),
-         reinterpret_cast<const void*>(plan_owner_kernel<false, 2>)},
-        {reinterpret_cast<const void*>(plan_owner_kernel<true, 8>), reinterpret_cast<const void*>(plan_owner_kernel<true, 4>),
-         reinterpret_cast<const void*>(plan_owner_kernel<true, 2>)}};
-    return k[vec][ci];
+    static const void* k[2][2][3] = {
+        {{reinterpret_cast<const void*>(plan_owner_kernel<false, 8, false>), reinterpret_cast<const void*>(plan_owner_kernel<false, 4, false>),
+          reinterpret_cast<const void*>(plan_owner_kernel<false, 2, false>)},
+         {reinterpret_cast<const void*>(plan_owner_kernel<true, 8, false>), reinterpret_cast<const void*>(plan_owner_kernel<true, 4, false>),
+          reinterpret_cast<const void*>(plan_owner_kernel<true, 2, false>)}},
+        {{reinterpret_cast<const void*>(plan_owner_kernel<false, 8, true>), reinterpret_cast<const void*>(plan_owner_kernel<false, 4, true>),
+          reinterpret_cast<const void*>(plan_owner_kernel<false, 2, true>)},
+         {reinterpret_cast<const void*>(plan_owner_kernel<true, 8, true>), reinterpret_cast<const void*>(plan_owner_kernel<true, 4, true>),
+          reinterpret_cast<const void*>(plan_owner_kernel<true, 2, true>)}}};
+    return k[shrt][vec][ci];
 }
 
 // Shape for clusters of CS CTAs, at most max_clusters of them (the number the
@@ -425,9 +450,13 @@ det_status co_max_clusters(int vec, int ci, int* out)
     std::lock_guard<std::mutex> lk(g_co_mu);
     int& n = g_co_clusters[vec][ci][dev];
     if (n == 0) {
+        // both sweep variants (full and short rounds) launch with the same
+        // block size, register limit and shared memory: one query serves both
+        for (int shrt = 0; shrt < 2; ++shrt) {
+            const det_status s = allow_dynamic_smem(co_kernel(vec, ci, shrt), kCoMaxSmem);
+            if (s) return s;
+        }
         const void* kern = co_kernel(vec, ci);
-        det_status s = allow_dynamic_smem(kern, kCoMaxSmem);
-        if (s) return s;
         CoShape sh{};
         sh.CS = kCoClusters[ci];
         sh.K = 1;
@@ -472,7 +501,7 @@ det_status launch_plan_owner(const int32_t* idx, int64_t N, int64_t M, int g, in
     bool ok = false;
     det_status s = co_pick(N, M, vec, &sh, &ci, &ok);
     if (s || !ok) return s;
-    const void* kern = co_kernel(vec, ci);
+    const void* kern = co_kernel(vec, ci, sh.sub < 128 * kCoBatch ? 1 : 0);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = co_config(sh, attr, st);
     CoArgs a{};
