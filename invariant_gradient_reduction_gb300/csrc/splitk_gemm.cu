@@ -43,7 +43,8 @@ constexpr int kSgBN = 32;                // MMA N: columns of W (C <= 32, zero p
 constexpr int kSgBK = 64;                // K per stage: one 128-byte swizzle row of bf16
 constexpr int kSgStages = 9;            // at most; fewer when the fold stack needs the room
 constexpr int kSgThreads = 192;          // warp 0 TMA, warp 1 MMA (and tensor-memory owner), warps 2..5 epilogue
-constexpr int kSgAcc = 4;                // tensor-memory accumulators, used in turn by the splits
+constexpr int kSgAcc = 4;                // tensor-memory accumulators, used in turn by the splits (a power of 2)
+static_assert((kSgAcc & (kSgAcc - 1)) == 0, "accumulator index by mask");
 constexpr int kSgTmemCols = kSgAcc * kSgBN;  // 128 columns
 constexpr int kSgMaxLevels = 4;          // fold counter levels: S <= 32 * 2^(levels - 1) = 256
 constexpr uint32_t kSgABytes = kSgBM * kSgBK * 2;  // 16 KB
@@ -171,6 +172,9 @@ __device__ __forceinline__ void sg_ld32(uint32_t taddr, float (&v)[32])
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// KPS: K blocks per stage fill (divides kbs), a constant so that the issuing
+// threads' index arithmetic stays as short as possible.
+template <int KPS>
 __global__ void __launch_bounds__(kSgThreads, 1)
 splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ SgArgs a)
@@ -184,10 +188,10 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t dyn = sg_smem(sg_dyn);
     const uint32_t base = (dyn + 1023u) & ~1023u;       // stages 1024-byte aligned for the swizzle
-    const uint32_t sA = base;                           // NS x 16 KB
     const int NS = a.ns;
-    const uint32_t sW = base + NS * kSgABytes;          // NS x 4 KB
-    float* stack = reinterpret_cast<float*>(sg_dyn + (sW + NS * kSgWBytes - dyn));  // [levels][32][128]
+    const uint32_t sA = base;                           // NS x KPS x 16 KB
+    const uint32_t sW = base + NS * KPS * kSgABytes;    // NS x KPS x 4 KB
+    float* stack = reinterpret_cast<float*>(sg_dyn + (sW + NS * KPS * kSgWBytes - dyn));  // [levels][32][128]
     const int row0 = static_cast<int>(blockIdx.x) * kSgBM;
     const int nkb = a.S * a.kbs;
 
@@ -217,32 +221,50 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0) {
-        // producer: K blocks in order, split after split
+        // producer: K blocks in order, split after split.  One thread issues
+        // every copy, so the loop carries the stage and its phase instead of
+        // dividing by the stage count.
         if (lane == 0) {
+            const int nfill = nkb / KPS;
             int issued = 0;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int st = kb % NS, use = kb / NS;
-                if (kb >= NS && !mbar_wait(sg_smem(&bar_empty[st]), (use - 1) & 1, &abort_flag)) {
+            int st = 0, kb = 0;
+            uint32_t ph = 0;  // parity of the stage's current use
+            for (int f = 0; f < nfill; ++f) {
+                if (f >= NS && !mbar_wait(sg_smem(&bar_empty[st]), ph ^ 1u, &abort_flag)) {
                     abort_flag = 1;
                     atomicOr(&g_sg_status, 1);
                     break;
                 }
                 const uint32_t bar = sg_smem(&bar_full[st]);
-                mbar_expect_tx(bar, kSgABytes + kSgWBytes);
-                sg_tma_2d(sA + st * kSgABytes, &tmA, kb * kSgBK, row0, bar);
-                sg_tma_2d(sW + st * kSgWBytes, &tmW, kb * kSgBK, 0, bar);
+                mbar_expect_tx(bar, KPS * (kSgABytes + kSgWBytes));
+                for (int j = 0; j < KPS; ++j, ++kb) {
+                    sg_tma_2d(sA + (st * KPS + j) * kSgABytes, &tmA, kb * kSgBK, row0, bar);
+                    sg_tma_2d(sW + (st * KPS + j) * kSgWBytes, &tmW, kb * kSgBK, 0, bar);
+                }
                 ++issued;
+                if (++st == NS) {
+                    st = 0;
+                    ph ^= 1u;
+                }
             }
             // every copy this CTA issued has landed before it may leave
-            for (int kb = issued > NS ? issued - NS : 0; kb < issued; ++kb)
-                mbar_wait(sg_smem(&bar_full[kb % NS]), (kb / NS) & 1, &abort_flag);
+            for (int f = issued > NS ? issued - NS : 0; f < issued; ++f)
+                mbar_wait(sg_smem(&bar_full[f % NS]), (f / NS) & 1, &abort_flag);
         }
     } else if (warp == 1) {
-        // MMA issuer: split s into accumulator s % kSgAcc
+        // MMA issuer: split s into accumulator s % kSgAcc.  This one thread's
+        // loop is the kernel's critical path (about 250 ns per K block when it
+        // divided by the stage count and rebuilt every descriptor), so it
+        // carries the stage, the phase and the descriptors: a stage's
+        // descriptors are the first stage's plus its offset >> 4, and each K
+        // step of 16 values adds 32 bytes (2 in the address field).
         if (lane == 0) {
             bool ok = true;
+            const uint64_t dA0 = sg_desc(sA), dW0 = sg_desc(sW);
+            int st = 0, sub = 0;  // stage and K block within its fill (KPS divides kbs)
+            uint32_t ph = 0;
             for (int s = 0; s < a.S && ok; ++s) {
-                const int buf = s % kSgAcc;
+                const int buf = s & (kSgAcc - 1);
                 if (s >= kSgAcc && !mbar_wait(sg_smem(&bar_tempty[buf]), ((s / kSgAcc) - 1) & 1, &abort_flag)) {
                     ok = false;
                     break;
@@ -250,17 +272,27 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(buf * kSgBN);
                 for (int j = 0; j < a.kbs; ++j) {
-                    const int kb = s * a.kbs + j, st = kb % NS, use = kb / NS;
-                    if (!mbar_wait(sg_smem(&bar_full[st]), use & 1, &abort_flag)) {
-                        ok = false;
-                        break;
+                    if (sub == 0) {
+                        if (!mbar_wait(sg_smem(&bar_full[st]), ph, &abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
                     }
-                    tc_fence_after();
+                    const int slot = st * KPS + sub;
+                    const uint64_t dA = dA0 + static_cast<uint64_t>(slot) * (kSgABytes >> 4);
+                    const uint64_t dW = dW0 + static_cast<uint64_t>(slot) * (kSgWBytes >> 4);
 #pragma unroll
                     for (int k = 0; k < kSgBK / 16; ++k)
-                        sg_mma(d, sg_desc(sA + st * kSgABytes + k * 32), sg_desc(sW + st * kSgWBytes + k * 32),
-                               (j > 0 || k > 0) ? 1u : 0u);
-                    sg_commit(sg_smem(&bar_empty[st]));  // the stage is free once these MMAs have read it
+                        sg_mma(d, dA + 2 * k, dW + 2 * k, (j > 0 || k > 0) ? 1u : 0u);
+                    if (++sub == KPS) {
+                        sg_commit(sg_smem(&bar_empty[st]));  // the stage is free once these MMAs have read it
+                        sub = 0;
+                        if (++st == NS) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
+                    }
                 }
                 if (ok) sg_commit(sg_smem(&bar_tfull[buf]));  // the accumulator is complete
             }
@@ -447,17 +479,24 @@ extern "C" det_status det_splitk_gemm_reduce(const void* A, int64_t lda, const v
     a.out_bf16 = out_dtype == DET_BF16 ? 1 : 0;
     a.partials = partials;
     a.ldp = ldp;
-    // as many stages as fit beside the fold stack (227 KB per CTA at most)
+    // two K blocks per stage fill where a split has an even number of them
+    // (half the barrier round trips of the issuing threads), and as many
+    // stages as fit beside the fold stack (227 KB per CTA at most)
+    const int kps = a.kbs % 2 == 0 ? 2 : 1;
     const size_t stack = static_cast<size_t>(a.levels) * 32 * kSgBM * sizeof(float);
     const size_t room = size_t(227) * 1024 - 2048 - 1024 - stack;
-    a.ns = static_cast<int>(std::min<size_t>(kSgStages, room / (kSgABytes + kSgWBytes)));
+    const size_t fill = static_cast<size_t>(kps) * (kSgABytes + kSgWBytes);
+    a.ns = static_cast<int>(std::min<size_t>(kSgStages, room / fill));
     if (a.ns < 2) return DET_ERR_UNSUPPORTED;
-    const size_t smem = 1024 + static_cast<size_t>(a.ns) * (kSgABytes + kSgWBytes) + stack;
-    s = allow_dynamic_smem(reinterpret_cast<const void*>(splitk_gemm_kernel), smem);
+    const size_t smem = 1024 + static_cast<size_t>(a.ns) * fill + stack;
+    const void* kern = kps == 2 ? reinterpret_cast<const void*>(splitk_gemm_kernel<2>)
+                                : reinterpret_cast<const void*>(splitk_gemm_kernel<1>);
+    s = allow_dynamic_smem(kern, smem);
     if (s) return s;
     cudaStream_t st = as_stream(stream);
     const unsigned int grid = static_cast<unsigned int>(cdiv(R, kSgBM));
-    splitk_gemm_kernel<<<grid, kSgThreads, smem, st>>>(mA, mW, a);
+    if (kps == 2) splitk_gemm_kernel<2><<<grid, kSgThreads, smem, st>>>(mA, mW, a);
+    else splitk_gemm_kernel<1><<<grid, kSgThreads, smem, st>>>(mA, mW, a);
     DETR_LAUNCHED();
     if (opts && opts->debug_checks) {
         DETR_CUDA(cudaStreamSynchronize(st));
