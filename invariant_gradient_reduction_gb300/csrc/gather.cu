@@ -39,7 +39,11 @@ constexpr int kFinishThreads = 256;
 #define DETR_GATHER_MIN_BLOCKS 3
 #endif
 
-template <typename XT, typename OT, bool VECTOR>
+// ACC: compiled for index_add_ (a.accumulate set: the canonical sum is added
+// to out, destinations without terms are left untouched), with the
+// destination tile requested early; the scatter-reduce instantiations keep
+// the code (and register allocation) without that request.
+template <typename XT, typename OT, bool VECTOR, bool ACC>
 __global__ void __launch_bounds__(kGatherThreads, DETR_GATHER_MIN_BLOCKS)
 gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant__ ShardTable tbl)
 {
@@ -93,6 +97,11 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
             const int v = tile * T + lane_t;
             const int e0 = v * VEC;
             const bool active = e0 < a.H;
+            // index_add_ reads the destination tile only after the fold: ask
+            // for it into L1 now, so that the read overlaps the source loads
+            if (ACC && slot == 0 && active && seg < 0)
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(static_cast<const char*>(a.out) +
+                                                            (static_cast<long long>(m) * a.ldo + e0) * sizeof(OT)));
             unsigned int cnt = 0;
             for (int r = 0; r < nrounds; ++r) {
                 if (nrounds > 1 || !staged) {
@@ -228,31 +237,38 @@ finish_kernel(const int4* finish, long long n_items, int H, const float* part, l
     }
 }
 
-template <typename XT, typename OT, bool VECTOR>
-static det_status launch_gather(const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
+template <typename XT, typename OT, bool VECTOR, bool ACC>
+static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
 {
     constexpr int VEC = Loader<XT, VECTOR>::VEC;
     const size_t smem = static_cast<size_t>(kGatherWarps) *
                         ((1 << a.S_log2) * kStagePad * (sizeof(void*) + sizeof(float)) +
                          static_cast<size_t>(a.levels) * VEC * 32 * sizeof(float));
     {
-        const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR>), smem);
+        const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR, ACC>), smem);
         if (a_) return a_;
     }
     if (grid <= 0) {
         // persistent: as many CTAs as fit at once; warps take tasks round-robin
         int per_sm = 1, sms = 1;
-        DETR_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_reduce_kernel<XT, OT, VECTOR>,
+        DETR_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_reduce_kernel<XT, OT, VECTOR, ACC>,
                                                                 kGatherThreads, smem));
         det_status s = current_sm_count(&sms);
         if (s) return s;
         grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(a.n_tasks, kGatherWarps),
                                                                         int64_t(std::max(per_sm, 1)) * sms)));
     }
-    DETR_CUDA(launch_after_previous(gather_reduce_kernel<XT, OT, VECTOR>, dim3(grid), dim3(kGatherThreads), smem, st,
+    DETR_CUDA(launch_after_previous(gather_reduce_kernel<XT, OT, VECTOR, ACC>, dim3(grid), dim3(kGatherThreads), smem, st,
                                     a, t));
     DETR_LAUNCHED();
     return DET_OK;
+}
+
+template <typename XT, typename OT, bool VECTOR>
+static det_status launch_gather(const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
+{
+    return a.accumulate ? launch_gather_t<XT, OT, VECTOR, true>(a, t, grid, st)
+                        : launch_gather_t<XT, OT, VECTOR, false>(a, t, grid, st);
 }
 
 template <typename XT, typename OT>

@@ -21,12 +21,14 @@
 //
 // One CTA owns 128 rows and all S splits.  Warp 0 streams 64-wide K blocks of
 // A (128 rows) and W (32 rows, zero past C) into a ring of shared-memory
-// stages with TMA (128-byte swizzle) on mbarriers; one thread of warp 1 issues
-// tcgen05.mma (bf16 in, fp32 accumulate, M = 128, N = 32, K = 16 each) into
-// one of four tensor-memory accumulators, used in turn by the splits (so the
-// MMAs run up to four splits ahead of the epilogue); warps 2..5
-// read each finished accumulator (tcgen05.ld, one row per thread), release
-// it, and fold it into the row's running chunk in split order.  Every wait is
+// stages with TMA (128-byte swizzle) on mbarriers, two blocks per stage fill
+// where they divide a split; one thread each of warps 1 and 2 issues
+// tcgen05.mma (bf16 in, fp32 accumulate, M = 128, N = 32, K = 16 each) for
+// the even and the odd splits into one of four tensor-memory accumulators,
+// used in turn by the splits (so the MMAs run up to four splits ahead of the
+// epilogue); warps 3..6 read each finished accumulator (tcgen05.ld, one row
+// per thread), release it, and fold it into the row's running chunk in split
+// order.  Every wait is
 // bounded; on expiry the CTA records the error, drains its own copies and
 // MMAs (bounded too), frees its tensor memory and returns.
 #include <cuda.h>  // CUtensorMap and the tensor-map enums (types only; entry points come from the runtime)
@@ -42,7 +44,8 @@ constexpr int kSgBM = 128;               // rows per CTA = tensor-memory lanes
 constexpr int kSgBN = 32;                // MMA N: columns of W (C <= 32, zero past C)
 constexpr int kSgBK = 64;                // K per stage: one 128-byte swizzle row of bf16
 constexpr int kSgStages = 9;            // at most; fewer when the fold stack needs the room
-constexpr int kSgThreads = 192;          // warp 0 TMA, warp 1 MMA (and tensor-memory owner), warps 2..5 epilogue
+constexpr int kSgIssuers = 2;            // MMA-issuing warps (one thread each), taking the splits in turn
+constexpr int kSgThreads = 32 * (1 + kSgIssuers + 4);  // warp 0 TMA, warps 1..2 MMA (1 owns the tensor memory), 3..6 epilogue
 constexpr int kSgAcc = 4;                // tensor-memory accumulators, used in turn by the splits (a power of 2)
 static_assert((kSgAcc & (kSgAcc - 1)) == 0, "accumulator index by mask");
 constexpr int kSgTmemCols = kSgAcc * kSgBN;  // 128 columns
@@ -180,7 +183,7 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                    const __grid_constant__ SgArgs a)
 {
     __shared__ __align__(8) unsigned long long bar_full[kSgStages], bar_empty[kSgStages];
-    __shared__ __align__(8) unsigned long long bar_tfull[kSgAcc], bar_tempty[kSgAcc], bar_drain;
+    __shared__ __align__(8) unsigned long long bar_tfull[kSgAcc], bar_tempty[kSgAcc], bar_drain[kSgIssuers];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
     extern __shared__ __align__(1024) unsigned char sg_dyn[];
@@ -204,7 +207,7 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             mbar_init(sg_smem(&bar_tfull[i]), 1);
             mbar_init(sg_smem(&bar_tempty[i]), 4);  // one arrival per epilogue warp
         }
-        mbar_init(sg_smem(&bar_drain), 1);
+        for (int i = 0; i < kSgIssuers; ++i) mbar_init(sg_smem(&bar_drain[i]), 1);
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -251,19 +254,25 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             for (int f = issued > NS ? issued - NS : 0; f < issued; ++f)
                 mbar_wait(sg_smem(&bar_full[f % NS]), (f / NS) & 1, &abort_flag);
         }
-    } else if (warp == 1) {
-        // MMA issuer: split s into accumulator s % kSgAcc.  This one thread's
-        // loop is the kernel's critical path (about 250 ns per K block when it
-        // divided by the stage count and rebuilt every descriptor), so it
-        // carries the stage, the phase and the descriptors: a stage's
-        // descriptors are the first stage's plus its offset >> 4, and each K
-        // step of 16 values adds 32 bytes (2 in the address field).
+    } else if (warp <= kSgIssuers) {
+        // MMA issuers: split s into accumulator s % kSgAcc, issued by thread
+        // 0 of warp 1 + s % kSgIssuers.  The issuing threads' loops are the
+        // kernel's critical path (one thread took about 250 ns per K block
+        // when it divided by the stage count and rebuilt every descriptor):
+        // two of them take the splits in turn, and each carries its stage,
+        // phase and descriptors (a stage's descriptors are the first stage's
+        // plus its offset >> 4; each K step of 16 values adds 32 bytes, 2 in
+        // the address field).  A split's fills are consecutive, and each
+        // issuer skips the other's; every wait points to an earlier split, so
+        // no cycle of waits can form.
         if (lane == 0) {
+            const int me = warp - 1;
             bool ok = true;
             const uint64_t dA0 = sg_desc(sA), dW0 = sg_desc(sW);
-            int st = 0, sub = 0;  // stage and K block within its fill (KPS divides kbs)
-            uint32_t ph = 0;
-            for (int s = 0; s < a.S && ok; ++s) {
+            const int nfps = a.kbs / KPS;  // stage fills per split
+            int st = (me * nfps) % NS, sub = 0;  // stage and K block within its fill (KPS divides kbs)
+            uint32_t ph = ((me * nfps) / NS) & 1u;
+            for (int s = me; s < a.S && ok; s += kSgIssuers) {
                 const int buf = s & (kSgAcc - 1);
                 if (s >= kSgAcc && !mbar_wait(sg_smem(&bar_tempty[buf]), ((s / kSgAcc) - 1) & 1, &abort_flag)) {
                     ok = false;
@@ -295,14 +304,20 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     }
                 }
                 if (ok) sg_commit(sg_smem(&bar_tfull[buf]));  // the accumulator is complete
+                for (int q = 0; q < (kSgIssuers - 1) * nfps; ++q) {  // the other issuers' fills
+                    if (++st == NS) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
             }
             if (!ok) {
                 abort_flag = 1;
                 atomicOr(&g_sg_status, 1);
             }
-            // every MMA this CTA issued has finished before its memory is freed
-            sg_commit(sg_smem(&bar_drain));
-            mbar_wait(sg_smem(&bar_drain), 0, &abort_flag);
+            // every MMA this thread issued has finished before the memory is freed
+            sg_commit(sg_smem(&bar_drain[me]));
+            mbar_wait(sg_smem(&bar_drain[me]), 0, &abort_flag);
         }
     } else {
         // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31

@@ -75,7 +75,8 @@ def test_splitk_gemm_partials_exact_on_integers(R, K, C, S):
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("R,C,S,ks", [(256, 24, 56, 128), (1000, 24, 56, 128), (384, 32, 100, 64), (130, 5, 7, 64),
-                                      (640, 16, 256, 64), (128, 24, 32, 128), (128, 24, 64, 64), (128, 24, 65, 64)])
+                                      (640, 16, 256, 64), (128, 24, 32, 128), (128, 24, 64, 64), (128, 24, 65, 64),
+                                      (256, 24, 8, 256), (200, 24, 9, 192), (128, 24, 3, 320)])
 def test_splitk_gemm_fold_matches_oracle(R, C, S, ks, out_dtype):
     """Normal inputs: the partials within the binary32 bound of the binary64
     GEMM; the output the oracle's canonical fold of those partials, byte for
