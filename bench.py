@@ -290,19 +290,9 @@ def measure_scatter(case, timer, steps, warmup, torch, with_e2e=True):
     }
     h = dr.det_hash(out).item() & (2 ** 64 - 1)
     res["out_fingerprint"] = f"{h:016x}"
-    res["plain_read_of_sources"] = plain_read(timer, case.x, steps, warmup)
     if with_e2e:
         res["e2e"] = measure_e2e(case, timer, max(3, min(steps, 20)), warmup, torch)
     return res
-
-
-def plain_read(timer, t, steps, warmup):
-    """A library read of the same bytes under the same flush and events
-    (torch.amax over t): the floor that launch, ramp and drain leave for a
-    kernel of this size, beside the copy peak measured on large buffers."""
-    ms = statistics.mean(timer.run(lambda: t.amax(), steps, warmup)[0])
-    nbytes = t.numel() * t.element_size()
-    return {"what": "torch.amax over the same input, same L2 flush", "bytes": nbytes, "ms": ms, "gbs": gbs(nbytes, ms)}
 
 
 def measure_e2e(case, timer, steps, warmup, torch):
@@ -502,7 +492,6 @@ def measure_splitk(timer, steps, warmup, torch, device):
         cb = P.numel() * 4 + out.numel() * out.element_size()
         ms = statistics.mean(t)
         res[name] = {"ms": ms, "gbs": gbs(cb, ms), "compulsory_bytes": cb, "launches_per_step": l / steps}
-    res["plain_read_of_partials"] = plain_read(timer, P, steps, warmup)
     return res
 
 
@@ -684,7 +673,6 @@ def run_ours(args):
     ms_red, ms_atom = statistics.mean(t_red), statistics.mean(t_atom)
     cb = case.compulsory_bytes()
     fingerprint = dr.det_hash(out).item() & (2 ** 64 - 1)
-    read_floor = plain_read(timer, case.x, args.steps, args.warmup)
 
     local = {"ms_step": ms_step, "ms_red": ms_red, "ms_atom": ms_atom, "launches": launches,
              "wall_ms_per_step": (t_wall1 - t_wall0) * 1e3 / args.steps, "fingerprint": fingerprint}
@@ -775,8 +763,7 @@ def run_ours(args):
                          "achieved": red_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": red_gbs / peaks["hbm_gbs"], "traffic": traffic,
                          "peak_source": peaks["source"] + " copy bandwidth (burst)",
-                         "algorithmic_bytes_per_launch": cb, "launch_ms": agg["ms_red"],
-                         "plain_read_of_sources": read_floor},
+                         "algorithmic_bytes_per_launch": cb, "launch_ms": agg["ms_red"]},
             "reduce_only": {"value": world * red_gbs, "ms": agg["ms_red"]},
             "atomic": {"ms": agg["ms_atom"], "value": world * gbs(cb, agg["ms_atom"]),
                        "overhead_reduce_only": agg["ms_red"] / agg["ms_atom"] - 1.0,
