@@ -247,6 +247,27 @@ static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int 
     {
         const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR, ACC>), smem);
         if (a_) return a_;
+        // An explicit shared-memory / L1 split: without one, the CTAs that a
+        // dependent launch places on SMs just left by a kernel with a large
+        // shared-memory footprint (the cluster plan: 222 KB per CTA) keep its
+        // split and run ~33% slower with a small L1 (measured: the 16 SMs of
+        // that plan's cluster held the reduce 74 us, 440 against 366 us per
+        // EP-invariance step).  Half the SM's shared memory, or what the
+        // resident CTAs need if that is more; preferring the largest L1
+        // instead halved the occupancy.
+        static int carve_set = -1;
+        int dev = 0, smem_sm = 0;
+        DETR_CUDA(cudaGetDevice(&dev));
+        DETR_CUDA(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
+        const size_t need = static_cast<size_t>(DETR_GATHER_MIN_BLOCKS) * (smem + 1024);
+        const int pct = smem_sm > 0 ? std::min<int>(100, std::max<int>(50, static_cast<int>(cdiv(
+                                                                              static_cast<int64_t>(need) * 100, smem_sm))))
+                                    : 50;
+        if (pct != carve_set) {
+            DETR_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR, ACC>),
+                                           cudaFuncAttributePreferredSharedMemoryCarveout, pct));
+            carve_set = pct;
+        }
     }
     if (grid <= 0) {
         // persistent: as many CTAs as fit at once; warps take tasks round-robin

@@ -151,6 +151,12 @@ def test_plan_errors(plan_path):
     with pytest.raises(dr.DetError) as e:
         dr.det_reduce_plan(big, 9, opts=o)
     assert e.value.code == dr.DET_ERR_INDEX_RANGE
+    # 2^18 sources: the owner plan's warps sweep full rounds (1024 sources each)
+    full = torch.zeros(1 << 18, dtype=torch.int32, device=DEV)
+    full[123457] = -5
+    with pytest.raises(dr.DetError) as e:
+        dr.det_reduce_plan(full, 9, opts=o)
+    assert e.value.code == dr.DET_ERR_INDEX_RANGE
     with pytest.raises(dr.DetError) as e:
         dr.det_reduce_plan(idx, 5, opts={"plan_path": 7})
     assert e.value.code == dr.DET_ERR_ARG
