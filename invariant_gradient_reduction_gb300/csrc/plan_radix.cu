@@ -254,8 +254,9 @@ __device__ __forceinline__ void rx_scatter_tile(RxScatterShared& S, const int* _
         __syncthreads();
     }
 
-    // rank inside the warp, item by item: the lowest lane of each digit group
-    // reads the warp's running count of the digit and writes it back advanced
+    // rank inside the warp, item by item: every lane reads the warp's running
+    // count of its digit, and the lowest lane of each digit group writes it
+    // back advanced
     unsigned short rank[kRxItems];
 #pragma unroll
     for (int k = 0; k < kRxItems; ++k) {
@@ -266,12 +267,11 @@ __device__ __forceinline__ void rx_scatter_tile(RxScatterShared& S, const int* _
         const bool valid = FULL || ((live >> lane) & 1u);
         const int d = static_cast<int>(MODE == 0 ? (wv[k] & 255u) : (wv[k] >> 24));
         const unsigned int peers = digit_peers(d, live);
-        const int leader = __ffs(peers) - 1;
-        int old = 0;
-        if (valid && lane == leader) old = S.whist[warp * kRxRadix + d];
-        old = __shfl_sync(0xffffffffu, old, valid ? leader : lane);
-        rank[k] = static_cast<unsigned short>(old + __popc(peers & lt_mask));
-        if (valid && lane == leader) S.whist[warp * kRxRadix + d] = old + __popc(peers);
+        const int old = valid ? S.whist[warp * kRxRadix + d] : 0;  // lanes of one digit read one word
+        const unsigned int below = peers & lt_mask;
+        rank[k] = static_cast<unsigned short>(old + __popc(below));
+        __syncwarp();  // every lane has read before the group's lowest lane writes
+        if (valid && below == 0u) S.whist[warp * kRxRadix + d] = old + __popc(peers);
         __syncwarp();
     }
     __syncthreads();
