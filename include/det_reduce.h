@@ -356,8 +356,9 @@ det_status det_splitk_reduce(const float* partials, int32_t S, int64_t count, in
  *            also written there, row-major [R][C] (for checking the fold, or
  *            for an unfused reduce by det_splitk_reduce, which then gives
  *            the same out).
- * One CTA per 128 rows on tensor cores (tcgen05) with TMA-fed shared memory;
- * no workspace.  With opts->debug_checks the call waits and reports an
+ * One CTA per 128 rows on tensor cores (tcgen05) with TMA-fed shared memory
+ * (two issuing threads take the even and the odd splits; each split's MMAs
+ * are issued by one thread, in K order); no workspace.  With opts->debug_checks the call waits and reports an
  * expired bounded wait as DET_ERR_TIMEOUT.
  * Errors: DET_ERR_ARG, DET_ERR_DTYPE, DET_ERR_UNSUPPORTED (C > 32, S > 256,
  * K not S x a multiple of 64), DET_ERR_CUDA, DET_ERR_TIMEOUT.
