@@ -94,10 +94,12 @@ typedef int32_t det_dtype;
  *                   DET_ERR_TIMEOUT (slower; for tests).
  *  gather_path      0 = auto.  1 = register-staged warp kernel, 2 = warp
  *                   kernel with cp.async copies into shared memory, 3 = TMA
- *                   bulk-staged kernel (only when every destination has at
- *                   most 32 terms and rows are at least 1 KB).  A path that
- *                   does not apply fails with DET_ERR_UNSUPPORTED.  For
- *                   comparing the kernels; every path gives the same bits.
+ *                   bulk-staged kernel (only with a waited plan, when every
+ *                   destination has at most 32 terms, rows are at least 1 KB
+ *                   and 16-byte aligned, and not for det_index_add).  Auto
+ *                   takes 3 where it applies, else 1.  A path that does not
+ *                   apply fails with DET_ERR_UNSUPPORTED.  Every path gives
+ *                   the same bits.
  *  tiles_per_task   0 = auto; > 0 = H-tiles one warp task of the warp kernels
  *                   covers (the work split changes no bit).
  *  async_plan       plan-time option.  0 (default): det_reduce_plan waits once

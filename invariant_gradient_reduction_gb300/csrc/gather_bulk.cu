@@ -28,6 +28,7 @@ constexpr int kBulkThreads = kBulkConsumers + 32;
 constexpr int kBulkStages = 3;
 constexpr int kBulkStageBytes = 64 * 1024;
 constexpr int kBulkMaxTerms = 32;
+constexpr int kBulkLook = 4;  // items whose source rows the producer reads ahead
 constexpr int kBulkVecPerThread = 1;  // tile <= 8 KB = 512 16-byte vectors
 
 struct BulkStageMeta {
@@ -119,9 +120,12 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
         // ---------------- producer warp ----------------
         // Item k of this CTA is blockIdx.x + k * gridDim.x.  The list lookups
         // run 32 items ahead (lane l holds item kb + l of the current and of
-        // the next batch), and the next item's source rows and weights are
-        // read while the producer waits for a free stage, so copies are issued
-        // as soon as a stage is released.
+        // the next batch).  The source rows of the next kBulkLook items are
+        // read ahead too (lane = term; an item's perm entries kBulkLook items
+        // before its copies, its weights two items before), so that after an
+        // L2 flush no item waits on its perm -> weight chain: the one
+        // producer warp issues every copy, and that chain was its critical
+        // path.
         const long long g = gridDim.x;
         int bm = 0, blo = 0, bn = -1, nm = 0, nlo = 0, nn = -1;
         auto fetch_meta = [&](long long kb, int& fm, int& flo, int& fn) {
@@ -133,25 +137,30 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
                 fn = a.row_ptr[fm + 1] - flo;
             }
         };
-        auto load_src = [&](long long k, int lo, int n, const unsigned char*& src, float& wv) {
-            src = nullptr;
-            wv = 1.0f;
-            if (lane < n) {
-                const long long it = blockIdx.x + k * g;
-                const int t = static_cast<int>(it % a.ntiles);
-                const int i = a.perm[lo + lane];
-                src = shard_row(tbl, i, a.ldx_bytes) + static_cast<long long>(t) * a.tile_elems * sizeof(XT);
-                if (a.w) wv = a.w[i];
-            }
-        };
         fetch_meta(0, bm, blo, bn);
         fetch_meta(32, nm, nlo, nn);
-        int cm = __shfl_sync(0xffffffffu, bm, 0);
-        int clo = __shfl_sync(0xffffffffu, blo, 0);
-        int cn = __shfl_sync(0xffffffffu, bn, 0);
-        const unsigned char* csrc = nullptr;
-        float cw = 1.0f;
-        if (blockIdx.x < n_items) load_src(0, clo, cn, csrc, cw);
+        long long batch = 0;  // bm/blo/bn hold items [32 batch, 32 batch + 32), nm/nlo/nn the next 32
+        // the ring: slot d holds item k + d
+        int rm[kBulkLook], rn[kBulkLook], rt[kBulkLook], ri[kBulkLook];
+        float rw[kBulkLook];
+        auto enter = [&](long long q, int d) {  // item q into slot d: its list entry and its perm loads
+            const int jq = static_cast<int>(q & 31);
+            const bool here = (q >> 5) == batch;
+            const int m = __shfl_sync(0xffffffffu, here ? bm : nm, jq);
+            const int lo = __shfl_sync(0xffffffffu, here ? blo : nlo, jq);
+            const int n = __shfl_sync(0xffffffffu, here ? bn : nn, jq);
+            rm[d] = m;
+            rn[d] = n;
+            rt[d] = static_cast<int>((blockIdx.x + q * g) % a.ntiles);
+            ri[d] = lane < n ? a.perm[lo + lane] : 0;
+            rw[d] = 1.0f;
+        };
+#pragma unroll
+        for (int d = 0; d < kBulkLook; ++d) enter(d, d);
+        if (a.w) {
+            if (lane < rn[0]) rw[0] = a.w[ri[0]];
+            if (lane < rn[1]) rw[1] = a.w[ri[1]];
+        }
         for (long long k = 0; blockIdx.x + k * g < n_items; ++k) {
             const int s = static_cast<int>(k % kBulkStages);
             const uint32_t ph = static_cast<uint32_t>((k / kBulkStages) & 1);
@@ -161,28 +170,31 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
                 if (lane == 0) { *abort_flag = 1; atomicOr(a.status + kCtrErrTimeout, 1); }
                 break;
             }
-            const long long it = blockIdx.x + k * g;
-            const int t = static_cast<int>(it % a.ntiles);
-            const int col0 = t * a.tile_elems;
+            const int cm = rm[0], cn = rn[0];
+            const int col0 = rt[0] * a.tile_elems;
             const int bytes = min(a.tile_elems, a.H - col0) * static_cast<int>(sizeof(XT));
-            if (lane < cn) swt[s * kBulkMaxTerms + lane] = cw;
+            if (lane < cn) swt[s * kBulkMaxTerms + lane] = rw[0];
             if (lane == 0) meta[s] = BulkStageMeta{cm, cn, col0, bytes};
             __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cn * bytes));
             __syncwarp();
             if (lane < cn)
                 bulk_g2s(stage_buf + static_cast<size_t>(s) * kBulkStageBytes + static_cast<size_t>(lane) * a.tile_stride,
-                         csrc, static_cast<uint32_t>(bytes), &full[s]);
-            // advance to item k+1
-            const int j = static_cast<int>((k + 1) & 31);
-            if (j == 0) {
+                         shard_row(tbl, ri[0], a.ldx_bytes) + static_cast<long long>(col0) * sizeof(XT),
+                         static_cast<uint32_t>(bytes), &full[s]);
+            // advance: the list batch, the ring, the weights two items ahead
+            const long long q = k + kBulkLook;
+            if ((q >> 5) > batch + 1) {
+                batch += 1;
                 bm = nm; blo = nlo; bn = nn;
-                fetch_meta(k + 1 + 32, nm, nlo, nn);
+                fetch_meta(32 * (batch + 1), nm, nlo, nn);
             }
-            cm = __shfl_sync(0xffffffffu, bm, j);
-            clo = __shfl_sync(0xffffffffu, blo, j);
-            cn = __shfl_sync(0xffffffffu, bn, j);
-            if (blockIdx.x + (k + 1) * g < n_items) load_src(k + 1, clo, cn, csrc, cw);
+#pragma unroll
+            for (int d = 0; d + 1 < kBulkLook; ++d) {
+                rm[d] = rm[d + 1]; rn[d] = rn[d + 1]; rt[d] = rt[d + 1]; ri[d] = ri[d + 1]; rw[d] = rw[d + 1];
+            }
+            enter(q, kBulkLook - 1);
+            if (a.w && lane < rn[1]) rw[1] = a.w[ri[1]];
         }
         return;
     }
