@@ -46,6 +46,7 @@ if ROOT not in sys.path:
 METRIC = "deterministic scatter-reduce HBM GB/s (% of peak) and overhead vs atomicAdd"
 UNIT = "GB/s"
 ASYNC = {"async_plan": 1}  # plans enqueue without a host wait
+STEP_KERNEL = {"gather_path": 1}  # the register-staged gather, which every unwaited-plan step runs
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 WORKLOADS = {
@@ -252,7 +253,14 @@ def scatter_step_fns(case, torch):
     ws_plan_fixed = torch.empty_like(ws_plan)
     plan_fixed = dr.det_reduce_plan(case.idx, case.M, workspace=ws_plan_fixed)
 
+    # the step's own gather kernel (the register-staged one: with an unwaited
+    # plan the row lengths are on the device only), for the roofline
     def reduce_only():
+        dr.det_scatter_reduce(plan_fixed, case.x, out, w=case.w, workspace=state.get("ws_red"), opts=STEP_KERNEL)
+
+    # what a caller with a waited plan gets: the library's choice (the TMA
+    # bulk kernel where every destination has at most 32 terms)
+    def reduce_only_auto():
         dr.det_scatter_reduce(plan_fixed, case.x, out, w=case.w, workspace=state.get("ws_red"))
 
     ws_atomic = torch.empty(dr.det_atomic_workspace_size(case.M, case.H, case.out_dtype) + 256, dtype=torch.uint8,
@@ -265,13 +273,14 @@ def scatter_step_fns(case, torch):
     def check_last_plan():
         dr.det_plan_status(state.get("plan", plan0))
 
-    return plan_and_reduce, reduce_only, atomic, out, plan_fixed, check_last_plan
+    state["reduce_only_auto"] = reduce_only_auto
+    return plan_and_reduce, reduce_only, atomic, out, plan_fixed, check_last_plan, state
 
 
 def measure_scatter(case, timer, steps, warmup, torch, with_e2e=True):
     from invariant_gradient_reduction_gb300 import detreduce as dr
     cb = case.compulsory_bytes()
-    full, red, atom, out, plan, check_last_plan = scatter_step_fns(case, torch)
+    full, red, atom, out, plan, check_last_plan, st = scatter_step_fns(case, torch)
     t_full, l_full = timer.run(full, steps, warmup)
     check_last_plan()
     t_red, _ = timer.run(red, steps, warmup)
@@ -641,7 +650,7 @@ def run_ours(args):
     sampler = ClockSampler(local_rank, args.clocks_dir).start()
     time.sleep(0.1)
     # warm-up, then exactly K timed steps bracketed by barrier + synchronize
-    full, red, atom, out, plan, check_last_plan = scatter_step_fns(case, torch)
+    full, red, atom, out, plan, check_last_plan, st = scatter_step_fns(case, torch)
     for _ in range(args.warmup):
         timer.flush()
         full()
@@ -669,12 +678,14 @@ def run_ours(args):
 
     # reduce-only (the dominant kernel, for the roofline) and the atomic baseline
     t_red, _ = timer.run(red, args.steps, args.warmup)
+    t_auto, _ = timer.run(st["reduce_only_auto"], args.steps, args.warmup)
     t_atom, _ = timer.run(atom, args.steps, args.warmup)
     ms_red, ms_atom = statistics.mean(t_red), statistics.mean(t_atom)
+    ms_auto = statistics.mean(t_auto)
     cb = case.compulsory_bytes()
     fingerprint = dr.det_hash(out).item() & (2 ** 64 - 1)
 
-    local = {"ms_step": ms_step, "ms_red": ms_red, "ms_atom": ms_atom, "launches": launches,
+    local = {"ms_step": ms_step, "ms_red": ms_red, "ms_auto": ms_auto, "ms_atom": ms_atom, "launches": launches,
              "wall_ms_per_step": (t_wall1 - t_wall0) * 1e3 / args.steps, "fingerprint": fingerprint}
     if world > 1:
         gathered = [None] * world
@@ -764,7 +775,10 @@ def run_ours(args):
                          "frac": red_gbs / peaks["hbm_gbs"], "traffic": traffic,
                          "peak_source": peaks["source"] + " copy bandwidth (burst)",
                          "algorithmic_bytes_per_launch": cb, "launch_ms": agg["ms_red"]},
-            "reduce_only": {"value": world * red_gbs, "ms": agg["ms_red"]},
+            "reduce_only": {"value": world * red_gbs, "ms": agg["ms_red"], "kernel": "gather_reduce_kernel"},
+            "reduce_only_auto": {"value": world * gbs(cb, agg["ms_auto"]), "ms": agg["ms_auto"],
+                                 "kernel": "the library's choice for a waited plan (TMA bulk kernel where every "
+                                           "destination has <= 32 terms)"},
             "atomic": {"ms": agg["ms_atom"], "value": world * gbs(cb, agg["ms_atom"]),
                        "overhead_reduce_only": agg["ms_red"] / agg["ms_atom"] - 1.0,
                        "overhead_plan_reduce": agg["ms_step"] / agg["ms_atom"] - 1.0},
@@ -788,6 +802,7 @@ def combine_ranks(per_rank):
     if len(fps) != 1:
         raise RuntimeError(f"replicas disagree on the output fingerprint: {sorted(fps)}")
     return {"ms_step": max(r["ms_step"] for r in per_rank), "ms_red": max(r["ms_red"] for r in per_rank),
+            "ms_auto": max(r["ms_auto"] for r in per_rank),
             "ms_atom": max(r["ms_atom"] for r in per_rank), "launches": sum(r["launches"] for r in per_rank),
             "wall_ms_per_step": max(r["wall_ms_per_step"] for r in per_rank), "fingerprint": fps.pop()}
 
