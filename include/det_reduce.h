@@ -97,7 +97,8 @@ typedef int32_t det_dtype;
  *                   bulk-staged kernel (only with a waited plan, when every
  *                   destination has at most 32 terms, rows are at least 1 KB
  *                   and 16-byte aligned, and not for det_index_add).  Auto
- *                   takes 3 where it applies, else 1.  A path that does not
+ *                   takes 3 where it applies and the sources are one shard,
+ *                   else 1.  A path that does not
  *                   apply fails with DET_ERR_UNSUPPORTED.  Every path gives
  *                   the same bits.
  *  tiles_per_task   0 = auto; > 0 = H-tiles one warp task of the warp kernels

@@ -442,15 +442,19 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
     const bool bulk_ok = vec && !dev_counts && !accumulate && plan->max_row_len <= 32 && H * xsz >= 1024 &&
                          plan->n_units > 0 &&
                          bulk_plan_tiles(H, xsz, plan->max_row_len, &tile_elems, &tile_stride, &bulk_tiles);
+    // with sources in several shards its one producer warp also looks up each
+    // term's shard, on its critical path (EP-invariance, 8 shards: 382 against
+    // 331 us for the register-staged kernel): auto takes it for one shard only
+    const bool bulk_auto = bulk_ok && P == 1;
     if (path == 3 && !bulk_ok) return DET_ERR_UNSUPPORTED;
     if (path == 2 && !vec) return DET_ERR_UNSUPPORTED;
     if (accumulate && path >= 2) return DET_ERR_UNSUPPORTED;  // the register-staged kernel only
     // Where it applies (the row counts are on the host, every destination has
-    // at most 32 terms, rows of 1 KB or more) the bulk kernel is the default:
+    // at most 32 terms, rows of 1 KB or more, one shard) the bulk kernel is the default:
     // with its producer reading source rows four items ahead it measured
     // 52.9 against 53.9 us (MoE combine) and 324 against 327 us
     // (EP-invariance).  Everything else takes the register-staged kernel.
-    if (bulk_ok && (path == 3 || path == 0)) {
+    if ((bulk_ok && path == 3) || (bulk_auto && path == 0)) {
         BulkArgs b{};
         b.units = plan->row_units;
         b.n_items = plan->n_units * bulk_tiles;
