@@ -271,8 +271,22 @@ def test_replays_identical_under_contention(replay):
         dr.det_plan_status(p)
         return o
     assert_bytes_equal(np_bits(replay.identical(unwaited, name="plan+reduce")), np_bits(base), "unwaited")
-    P = wl.make("splitk", "small", device=DEV)
+    P = wl.make("splitk", "small", device=DEV)  # 56 splits: the two-chunk kernel
     replay.identical(lambda: dr.det_splitk_reduce(P, torch.empty(P.shape[1], device=DEV)), name="splitk")
+    # a waited plan with <= 32 terms per destination and 2 KB rows: the TMA bulk kernel
+    mc = small_case("moe_combine")
+    mbase, mplan = gpu_scatter(mc)
+    mout = replay.identical(lambda: dr.det_scatter_reduce(mplan, mc.x, torch.empty_like(mbase), w=mc.w),
+                            name="moe_combine waited")
+    assert_bytes_equal(np_bits(mout), np_bits(mbase), "moe replay")
+    # the split-K GEMM: two MMA-issuing warps, the fold in the epilogue
+    A, W = wl.splitk_gemm_inputs(384, 56 * 128, 24, seed=3, device=DEV)
+
+    def gemm():
+        o = torch.empty(384, 24, device=DEV)
+        dr.det_splitk_gemm_reduce(A, W, 56, o)
+        return o
+    replay.identical(gemm, name="splitk_gemm")
 
 
 @pytest.mark.parametrize("P", [1, 2, 4, 8])
