@@ -96,7 +96,7 @@ typedef int32_t det_dtype;
  *                   kernel with cp.async copies into shared memory, 3 = TMA
  *                   bulk-staged kernel (only with a waited plan, when every
  *                   destination has at most 32 terms, rows are at least 1 KB
- *                   and 16-byte aligned, and not for det_index_add).  Auto
+ *                   and 16-byte aligned; det_index_add: see there).  Auto
  *                   takes 3 where it applies and the sources are one shard,
  *                   else 1.  A path that does not
  *                   apply fails with DET_ERR_UNSUPPORTED.  Every path gives
@@ -280,8 +280,15 @@ det_status det_scatter_reduce(det_plan plan,
  * destinations without terms are not touched.  Repeated calls accumulate
  * (e.g. embedding-gradient accumulation over micro-batches) and every call
  * gives the same bits for the same inputs and the same prior contents.
- * Runs on the register-staged kernel: opts->gather_path 2 or 3 give
- * DET_ERR_UNSUPPORTED.  Other errors as det_scatter_reduce.
+ * opts->gather_path 3 (16-byte aligned source rows, out rows 16-byte
+ * aligned and H a multiple of 16 bytes of both x and out) runs
+ * the destinations of 1..32 terms on a TMA-staged kernel that copies each
+ * one's source tiles and old out tile into shared memory, and the longer ones
+ * on the register-staged kernel; auto does so where it applies, the sources
+ * are one shard and rows are at least 1 KB, else it takes path 1.
+ * gather_path 2 gives DET_ERR_UNSUPPORTED, as does 3 where it does not
+ * apply.  Every path gives the same bits.  Other errors as
+ * det_scatter_reduce.
  */
 det_status det_index_add(det_plan plan,
                          const void* const* x_shards, const int64_t* shard_rows, int32_t P,

@@ -70,10 +70,13 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
     const long long seg_terms = static_cast<long long>(kChunk) << a.g;
 
     const long long nwarps = static_cast<long long>(gridDim.x) * kGatherWarps;
-    pdl_wait();                 // the plan (or whatever wrote x and w) has finished
+    if (!(ACC && a.beside_ring)) pdl_wait();  // the plan (or whatever wrote x and w) has finished
     pdl_launch_dependents();    // the hot-destination pass may be launched now
     long long n_tasks, n_seg;
-    if (!task_counts(a, &n_tasks, &n_seg)) return;
+    if (!task_counts(a, &n_tasks, &n_seg)) {
+        if (ACC && a.beside_ring) pdl_wait();
+        return;
+    }
     for (long long task = static_cast<long long>(blockIdx.x) * kGatherWarps + warp; task < n_tasks;
          task += nwarps) {
         int t0, t1;
@@ -193,6 +196,7 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
             }
         }
     }
+    if (ACC && a.beside_ring) pdl_wait();  // this grid ends after the ring kernel beside it
 }
 
 // Second pass for hot destinations: the level-wise tree over the row's
@@ -255,14 +259,16 @@ static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int 
         // EP-invariance step).  Half the SM's shared memory, or what the
         // resident CTAs need if that is more; preferring the largest L1
         // instead halved the occupancy.
+        // Beside the index_add_ ring kernel: all of it, for that kernel's ring.
         static int carve_set = -1;
         int dev = 0, smem_sm = 0;
         DETR_CUDA(cudaGetDevice(&dev));
         DETR_CUDA(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
         const size_t need = static_cast<size_t>(DETR_GATHER_MIN_BLOCKS) * (smem + 1024);
-        const int pct = smem_sm > 0 ? std::min<int>(100, std::max<int>(50, static_cast<int>(cdiv(
-                                                                              static_cast<int64_t>(need) * 100, smem_sm))))
-                                    : 50;
+        int pct = smem_sm > 0 ? std::min<int>(100, std::max<int>(50, static_cast<int>(cdiv(
+                                                                        static_cast<int64_t>(need) * 100, smem_sm))))
+                              : 50;
+                if (ACC && a.beside_ring) pct = 100;
         if (pct != carve_set) {
             DETR_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR, ACC>),
                                            cudaFuncAttributePreferredSharedMemoryCarveout, pct));
@@ -276,6 +282,9 @@ static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int 
                                                                 kGatherThreads, smem));
         det_status s = current_sm_count(&sms);
         if (s) return s;
+        // beside the ring kernel (544 threads of 64 registers and most of the
+        // shared memory on every SM) one CTA of this kernel fits per SM
+        if (ACC && a.beside_ring) per_sm = 1;
         grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(a.n_tasks, kGatherWarps),
                                                                         int64_t(std::max(per_sm, 1)) * sms)));
     }
@@ -446,9 +455,49 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
     // term's shard, on its critical path (EP-invariance, 8 shards: 382 against
     // 331 us for the register-staged kernel): auto takes it for one shard only
     const bool bulk_auto = bulk_ok && P == 1;
-    if (path == 3 && !bulk_ok) return DET_ERR_UNSUPPORTED;
+    // index_add_: the destinations of one chunk (1..32 terms) can take the
+    // TMA-staged ring kernel, the others stay on the register-staged kernel
+    // (and the finish pass).  Its copies need 16-byte x and out tiles: out
+    // rows 16-byte aligned and H a multiple of the quantum.  With an unwaited
+    // plan the ring kernel reads its unit count from the plan's counter block.
+    const int64_t n_short = dev_counts ? -1 : plan->n_units - plan->n_segments - plan->n_long - plan->n_empty;
+    const int acc_quantum = std::max(16 / xsz, 16 / osz);
+    const bool acc_bulk_ok = accumulate && vec && a.out_vec && H % acc_quantum == 0 && n_short != 0;
+    // auto: one shard (the producer's shard lookup is on its critical path)
+    // and rows of 1 KB or more (the embedding backward: 8 KB rows of mostly
+    // one to three terms)
+    const bool acc_bulk_auto = acc_bulk_ok && P == 1 && H * xsz >= 1024;
+    if (path == 3 && !(accumulate ? acc_bulk_ok : bulk_ok)) return DET_ERR_UNSUPPORTED;
     if (path == 2 && !vec) return DET_ERR_UNSUPPORTED;
-    if (accumulate && path >= 2) return DET_ERR_UNSUPPORTED;  // the register-staged kernel only
+    if (accumulate && path == 2) return DET_ERR_UNSUPPORTED;
+    if (accumulate && ((acc_bulk_ok && path == 3) || (acc_bulk_auto && path == 0))) {
+        BulkAccArgs b{};
+        b.units = plan->row_units;  // the short units come first in row_units
+        b.n_units = n_short;
+        b.H = a.H;
+        b.quantum = acc_quantum;
+        b.row_ptr = plan->row_ptr;
+        b.perm = plan->perm;
+        b.w = w;
+        b.ldx_bytes = a.ldx_bytes;
+        b.out = out;
+        b.ldo = ldo;
+        b.status = plan->counters;
+        b.dev_counters = dev_counts ? plan->counters : nullptr;
+        int64_t bgrid = opts && opts->grid_ctas > 0 ? opts->grid_ctas
+                                                    : (dev_counts ? sms : std::min<int64_t>(n_short, sms));
+        bgrid = std::max<int64_t>(1, std::min<int64_t>(bgrid, 2147483647));
+        s = launch_gather_bulk_acc(x_dtype, out_dtype, b, tbl, static_cast<int>(bgrid), st);
+        if (s) return s;
+        // The register-staged kernel takes the units of more than one chunk,
+        // beside the ring kernel: launched as its programmatic dependent, it
+        // starts at once on the shared memory the ring leaves free (one CTA
+        // per SM) and waits for the ring kernel only before it ends.  On the
+        // embedding backward: 128 us, against 150 us with the two kernels one
+        // after the other and 181 us with the register-staged kernel alone.
+        if (!dev_counts) a.n_tasks = a.n_seg * a.seg_tile_groups;
+        a.beside_ring = 1;
+    }
     // Where it applies (the row counts are on the host, every destination has
     // at most 32 terms, rows of 1 KB or more, one shard) the bulk kernel is the default:
     // with its producer reading source rows four items ahead it measured

@@ -36,6 +36,9 @@ struct GatherArgs {
     long long ldpart;
     const int* dev_counters;  // non-null: read the work counts (and plan errors) from the device
     int accumulate;           // add to out (index_add_); destinations without terms stay untouched
+    int beside_ring;          // index_add_ beside the ring kernel, which takes the one-chunk units: only the
+                              // units of more than one chunk, and the wait for the previous grid (the ring
+                              // kernel; everything before it had finished when it started) at the end
 };
 
 // Work counts of a launch: from the host, or from the plan's counter block
@@ -51,7 +54,9 @@ __device__ __forceinline__ bool task_counts(const GatherArgs& a, long long* n_ta
         *n_seg = c[kCtrBig];
         // index_add_ has nothing to do for the empty destinations (listed last)
         *n_tasks = static_cast<long long>(c[kCtrBig]) * a.seg_tile_groups +
-                   static_cast<long long>(c[kCtrShort] + (a.accumulate ? 0 : c[kCtrEmpty])) * a.tile_groups;
+                   (a.beside_ring ? 0LL
+                                  : static_cast<long long>(c[kCtrShort] + (a.accumulate ? 0 : c[kCtrEmpty])) *
+                                        a.tile_groups);
     }
     return true;
 }
@@ -113,5 +118,28 @@ size_t bulk_smem_bytes();
 bool bulk_plan_tiles(int64_t H, int xsz, int64_t max_terms, int* tile_elems, int* tile_stride, int* ntiles);
 det_status launch_gather_bulk(det_dtype x_dtype, det_dtype out_dtype, const BulkArgs& a, const ShardTable& t,
                               int grid, cudaStream_t st);
+
+// index_add_ on the destinations of one chunk (1..32 terms), TMA-staged: each
+// item is a destination's H-tile with its term tiles and the old destination
+// tile, packed into a byte ring of shared memory.
+struct BulkAccArgs {
+    const int4* units;     // the one-chunk whole-destination units (row_units[0 .. n_units))
+    long long n_units;
+    int H;
+    int quantum;           // tile widths are multiples of this many elements (16-byte x and out copies)
+    const int* row_ptr;
+    const int* perm;
+    const float* w;
+    long long ldx_bytes;
+    void* out;             // 16-byte aligned rows (ldo * sizeof(out) a multiple of 16)
+    long long ldo;
+    int* status;           // counter block; kCtrErrTimeout is set if a bounded wait expires
+    const int* dev_counters;  // non-null (plan that did not wait): n_units is the block's short-unit count,
+                              // or 0 if the plan recorded an error
+};
+
+size_t bulk_acc_smem_bytes();
+det_status launch_gather_bulk_acc(det_dtype x_dtype, det_dtype out_dtype, const BulkAccArgs& a, const ShardTable& t,
+                                  int grid, cudaStream_t st);
 
 }  // namespace detr

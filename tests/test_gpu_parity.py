@@ -611,6 +611,8 @@ def test_async_plan_errors_reported_and_nothing_written():
         plan = dr.det_reduce_plan(it, M, src_id=st, opts={"async_plan": 1})
         out = torch.full((M, H), 3.5, device=DEV)
         dr.det_scatter_reduce(plan, x, out, opts={"async_plan": 1})
+        # index_add through the ring kernel and the register-staged kernel beside it
+        dr.det_index_add(plan, x, out, opts={"async_plan": 1, "gather_path": 3})
         with pytest.raises(dr.DetError) as e:
             dr.det_plan_status(plan)
         assert e.value.code == code
@@ -661,10 +663,96 @@ def test_index_add_empty_rows_untouched_and_paths():
     assert out[untouched].view(torch.int32).equal(init[untouched].view(torch.int32))
     want = oracle.scatter_reduce(idx.cpu().numpy(), x.cpu().numpy(), M, out_init=init.cpu().numpy())
     assert_bytes_equal(np_bits(out), want, "index_add small")
-    for path in (2, 3):
-        with pytest.raises(dr.DetError) as e:
-            dr.det_index_add(plan, x, out, opts={"gather_path": path})
-        assert e.value.code == dr.DET_ERR_UNSUPPORTED
+    with pytest.raises(dr.DetError) as e:
+        dr.det_index_add(plan, x, out, opts={"gather_path": 2})
+    assert e.value.code == dr.DET_ERR_UNSUPPORTED
+    # the TMA-staged ring kernel takes 64-byte rows when asked for (auto keeps them on the register kernel)
+    out3 = init.clone()
+    dr.det_index_add(plan, x, out3, opts={"gather_path": 3, "debug_checks": 1})
+    assert_bytes_equal(np_bits(out3), want, "index_add small, ring kernel")
+
+
+def _mixed_lengths_idx(M, seed):
+    """Destination ids of a mix of row lengths in a shuffled source order: empty
+    rows, many of 1..3 terms, some of 4..32 (all one chunk), some of 33..300
+    (long rows) and one of 700 (a hot row cut into segments); row 0 is empty."""
+    rng = np.random.default_rng(seed)
+    u = rng.random(M)
+    lens = np.where(u < 0.3, 0, np.where(u < 0.7, 1, np.where(u < 0.85, rng.integers(2, 4, M),
+                    np.where(u < 0.97, rng.integers(4, 33, M), rng.integers(33, 301, M)))))
+    lens[M // 2] = 700
+    lens[0] = 0
+    idx = np.repeat(np.arange(M, dtype=np.int32), lens)
+    rng.shuffle(idx)
+    return idx
+
+
+@pytest.mark.parametrize("H,xdt,odt,weighted", [(4096, torch.bfloat16, torch.float32, False),
+                                                (1000, torch.bfloat16, torch.float32, True),
+                                                (520, torch.bfloat16, torch.bfloat16, False),
+                                                (300, torch.float32, torch.float32, True),
+                                                (264, torch.float32, torch.bfloat16, False)])
+def test_index_add_bulk_ring_matches_oracle(H, xdt, odt, weighted):
+    """det_index_add through the TMA-staged ring kernel for the one-chunk rows
+    (gather_path 3, and auto where it applies), with the long and hot rows on
+    the register-staged kernel and the finish pass: the same bytes as the
+    oracle and as the register-staged kernel alone (gather_path 1), for row
+    widths that give one tile or several per destination and ragged last
+    tiles, bf16 and fp32 outputs, weights and two shards."""
+    M = 700
+    idx_np = _mixed_lengths_idx(M, seed=H)
+    N = idx_np.size
+    g = torch.Generator(device=DEV).manual_seed(H)
+    x = (torch.randn(N, H, generator=g, device=DEV) * 2).to(xdt)
+    w = torch.rand(N, generator=g, device=DEV) if weighted else None
+    init = (torch.randn(M, H, generator=g, device=DEV) * 3).to(odt)
+    init[0] = float("nan")  # untouched rows keep any bits
+    idx = torch.from_numpy(idx_np).to(DEV)
+    plan = dr.det_reduce_plan(idx, M)
+    d = plan.describe()
+    assert d["n_hot_rows"] >= 1
+    want = oracle.scatter_reduce(idx_np, np_bits(x), M, w=None if w is None else w.cpu().numpy(),
+                                 out_dtype=oracle_dtype(odt), out_init=np_bits(init))
+    outs = {}
+    for path in (0, 1, 3):
+        out = init.clone()
+        dr.det_index_add(plan, x, out, w=w, opts={"gather_path": path, "debug_checks": 1})
+        assert_bytes_equal(np_bits(out), want, f"index_add H={H} path {path}")
+        outs[path] = out
+    # a plan that did not wait: the ring kernel reads its unit count on the device
+    plan2 = dr.det_reduce_plan(idx, M, opts={"async_plan": 1})
+    for path in (0, 3):
+        out = init.clone()
+        dr.det_index_add(plan2, x, out, w=w, opts={"async_plan": 1, "gather_path": path})
+        dr.det_plan_status(plan2)
+        assert_bytes_equal(np_bits(out), want, f"index_add H={H} unwaited plan, path {path}")
+    # two shards (the ring kernel when asked for it), and a small grid
+    cut = N // 3
+    out = init.clone()
+    dr.det_index_add(plan, [x[:cut], x[cut:]], out, w=w, opts={"gather_path": 3, "grid_ctas": 3, "debug_checks": 1})
+    assert_bytes_equal(np_bits(out), want, f"index_add H={H} two shards")
+    # the empty destination rows are untouched, bit for bit
+    empty = np.setdiff1d(np.arange(M), idx_np)
+    assert np_bits(outs[0])[empty].tobytes() == np_bits(init)[empty].tobytes()
+
+
+def test_index_add_bulk_ring_unsupported_layouts():
+    """The ring kernel's 16-byte copies need H a multiple of the quantum and
+    16-byte output rows: otherwise gather_path 3 is refused and auto takes the
+    register-staged kernel, with the oracle's bytes."""
+    M, H = 64, 1028  # bf16 x, fp32 out: the quantum is 8 elements
+    idx_np = _mixed_lengths_idx(M, seed=3)
+    g = torch.Generator(device=DEV).manual_seed(3)
+    x = torch.randn(idx_np.size, H, generator=g, device=DEV).to(torch.bfloat16)
+    init = torch.randn(M, H, generator=g, device=DEV)
+    plan = dr.det_reduce_plan(torch.from_numpy(idx_np).to(DEV), M)
+    out = init.clone()
+    with pytest.raises(dr.DetError) as e:
+        dr.det_index_add(plan, x, out, opts={"gather_path": 3})
+    assert e.value.code == dr.DET_ERR_UNSUPPORTED
+    dr.det_index_add(plan, x, out)
+    want = oracle.scatter_reduce(idx_np, np_bits(x), M, out_init=np_bits(init))
+    assert_bytes_equal(np_bits(out), want, "index_add H=1028")
 
 
 def test_embedding_backward_index_add():
