@@ -53,12 +53,13 @@ MANIFEST = {
 
 def _kernels_in(path):
     """Names of the `__global__` functions of a source: the first identifier after each
-    `__global__` that is followed by its parameter list (launch bounds may nest parentheses)."""
+    `__global__` that is followed by its parameter list (launch bounds and register caps may
+    nest parentheses)."""
     text = re.sub(r"//[^\n]*|/\*.*?\*/", " ", open(path).read(), flags=re.S)  # comments out
     names = set()
     for m in re.finditer(r"__global__\s+void\b", text):
         rest = text[m.end():]
-        if rest.lstrip().startswith("__launch_bounds__"):
+        while rest.lstrip().startswith(("__launch_bounds__", "__maxnreg__")):
             i = rest.index("(")
             depth = 0
             for j in range(i, len(rest)):
