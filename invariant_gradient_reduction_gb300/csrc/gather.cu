@@ -42,8 +42,11 @@ constexpr int kFinishThreads = 256;
 // ACC: compiled for index_add_ (a.accumulate set: the canonical sum is added
 // to out, destinations without terms are left untouched), with the
 // destination tile requested early; the scatter-reduce instantiations keep
-// the code (and register allocation) without that request.
-template <typename XT, typename OT, bool VECTOR, bool ACC>
+// the code (and register allocation) without that request.  BESIDE (with
+// ACC): the instantiation that runs beside the ring kernel (a.beside_ring),
+// with its wait for the previous grid at the end; a separate instantiation,
+// since the wait at the end cost the others 12 bytes more of spills.
+template <typename XT, typename OT, bool VECTOR, bool ACC, bool BESIDE>
 __global__ void __launch_bounds__(kGatherThreads, DETR_GATHER_MIN_BLOCKS)
 gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant__ ShardTable tbl)
 {
@@ -70,11 +73,11 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
     const long long seg_terms = static_cast<long long>(kChunk) << a.g;
 
     const long long nwarps = static_cast<long long>(gridDim.x) * kGatherWarps;
-    if (!(ACC && a.beside_ring)) pdl_wait();  // the plan (or whatever wrote x and w) has finished
+    if (!BESIDE) pdl_wait();    // the plan (or whatever wrote x and w) has finished
     pdl_launch_dependents();    // the hot-destination pass may be launched now
     long long n_tasks, n_seg;
     if (!task_counts(a, &n_tasks, &n_seg)) {
-        if (ACC && a.beside_ring) pdl_wait();
+        if (BESIDE) pdl_wait();
         return;
     }
     for (long long task = static_cast<long long>(blockIdx.x) * kGatherWarps + warp; task < n_tasks;
@@ -196,7 +199,7 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
             }
         }
     }
-    if (ACC && a.beside_ring) pdl_wait();  // this grid ends after the ring kernel beside it
+    if (BESIDE) pdl_wait();  // this grid ends after the ring kernel beside it
 }
 
 // Second pass for hot destinations: the level-wise tree over the row's
@@ -241,7 +244,7 @@ finish_kernel(const int4* finish, long long n_items, int H, const float* part, l
     }
 }
 
-template <typename XT, typename OT, bool VECTOR, bool ACC>
+template <typename XT, typename OT, bool VECTOR, bool ACC, bool BESIDE>
 static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
 {
     constexpr int VEC = Loader<XT, VECTOR>::VEC;
@@ -249,7 +252,7 @@ static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int 
                         ((1 << a.S_log2) * kStagePad * (sizeof(void*) + sizeof(float)) +
                          static_cast<size_t>(a.levels) * VEC * 32 * sizeof(float));
     {
-        const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR, ACC>), smem);
+        const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR, ACC, BESIDE>), smem);
         if (a_) return a_;
         // An explicit shared-memory / L1 split: without one, the CTAs that a
         // dependent launch places on SMs just left by a kernel with a large
@@ -268,9 +271,9 @@ static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int 
         int pct = smem_sm > 0 ? std::min<int>(100, std::max<int>(50, static_cast<int>(cdiv(
                                                                         static_cast<int64_t>(need) * 100, smem_sm))))
                               : 50;
-                if (ACC && a.beside_ring) pct = 100;
+                if (BESIDE) pct = 100;
         if (pct != carve_set) {
-            DETR_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR, ACC>),
+            DETR_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR, ACC, BESIDE>),
                                            cudaFuncAttributePreferredSharedMemoryCarveout, pct));
             carve_set = pct;
         }
@@ -278,17 +281,17 @@ static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int 
     if (grid <= 0) {
         // persistent: as many CTAs as fit at once; warps take tasks round-robin
         int per_sm = 1, sms = 1;
-        DETR_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_reduce_kernel<XT, OT, VECTOR, ACC>,
+        DETR_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_reduce_kernel<XT, OT, VECTOR, ACC, BESIDE>,
                                                                 kGatherThreads, smem));
         det_status s = current_sm_count(&sms);
         if (s) return s;
         // beside the ring kernel (544 threads of 64 registers and most of the
         // shared memory on every SM) one CTA of this kernel fits per SM
-        if (ACC && a.beside_ring) per_sm = 1;
+        if (BESIDE) per_sm = 1;
         grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(a.n_tasks, kGatherWarps),
                                                                         int64_t(std::max(per_sm, 1)) * sms)));
     }
-    DETR_CUDA(launch_after_previous(gather_reduce_kernel<XT, OT, VECTOR, ACC>, dim3(grid), dim3(kGatherThreads), smem, st,
+    DETR_CUDA(launch_after_previous(gather_reduce_kernel<XT, OT, VECTOR, ACC, BESIDE>, dim3(grid), dim3(kGatherThreads), smem, st,
                                     a, t));
     DETR_LAUNCHED();
     return DET_OK;
@@ -297,8 +300,10 @@ static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int 
 template <typename XT, typename OT, bool VECTOR>
 static det_status launch_gather(const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
 {
-    return a.accumulate ? launch_gather_t<XT, OT, VECTOR, true>(a, t, grid, st)
-                        : launch_gather_t<XT, OT, VECTOR, false>(a, t, grid, st);
+    if (!a.accumulate) return launch_gather_t<XT, OT, VECTOR, false, false>(a, t, grid, st);
+    // beside the ring kernel: 16-byte rows only
+    if (VECTOR && a.beside_ring) return launch_gather_t<XT, OT, VECTOR, true, VECTOR>(a, t, grid, st);
+    return launch_gather_t<XT, OT, VECTOR, true, false>(a, t, grid, st);
 }
 
 template <typename XT, typename OT>
