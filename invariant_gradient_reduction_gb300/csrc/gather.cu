@@ -500,8 +500,31 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
         // per SM) and waits for the ring kernel only before it ends.  On the
         // embedding backward: 128 us, against 150 us with the two kernels one
         // after the other and 181 us with the register-staged kernel alone.
-        if (!dev_counts) a.n_tasks = a.n_seg * a.seg_tile_groups;
         a.beside_ring = 1;
+        // With only the long units, at one CTA per SM, a warp folding a hot
+        // segment of 256 terms over 512-byte tiles waits for 32 dependent
+        // rounds of loads, and the warps that drew two such tasks ended last.
+        // Narrower tiles with two chunk slots per warp (2 chunks folded at
+        // once over 256-byte tiles) halve each chain and double the tasks
+        // (the split changes no bit).  Embedding backward: 126 us, against
+        // 131 us with 512-byte tiles, 130 us with 128-byte and 161 us with
+        // 64-byte ones.
+        constexpr int kBesideTlog2 = 4;
+        if (a.T_log2 > kBesideTlog2) {
+            a.T_log2 = kBesideTlog2;
+            a.S_log2 = 5 - a.T_log2;
+            a.ntiles = static_cast<int>(cdiv(V, int64_t(1) << a.T_log2));
+            const int64_t tb = (int64_t(1) << a.T_log2) * (vec ? 16 : xsz);
+            int tps = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, 16384 / (seg_terms * tb))));
+            if (opts && opts->tiles_per_task > 0) tps = std::min(opts->tiles_per_task, a.ntiles);
+            a.seg_tiles_per_group = tps;
+            a.seg_tile_groups = static_cast<int>(cdiv(a.ntiles, tps));
+            a.tiles_per_group = std::min(a.tiles_per_group, a.ntiles);
+            a.tile_groups = static_cast<int>(cdiv(a.ntiles, a.tiles_per_group));
+            a.levels = log2_floor(std::max<int64_t>(1, cdiv(max_chunks, int64_t(1) << a.S_log2))) + 1;
+            if (dev_counts) a.n_tasks = plan->M * a.tile_groups + max_segs_all * a.seg_tile_groups;
+        }
+        if (!dev_counts) a.n_tasks = a.n_seg * a.seg_tile_groups;
     }
     // Where it applies (the row counts are on the host, every destination has
     // at most 32 terms, rows of 1 KB or more, one shard) the bulk kernel is the default:

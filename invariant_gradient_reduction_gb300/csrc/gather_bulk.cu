@@ -28,7 +28,13 @@ constexpr int kBulkThreads = kBulkConsumers + 32;
 constexpr int kBulkStages = 3;
 constexpr int kBulkStageBytes = 64 * 1024;
 constexpr int kBulkMaxTerms = 32;
-constexpr int kBulkLook = 4;  // items whose source rows the producer reads ahead
+// The producers' unit pipeline: perm entries copied into shared memory
+// kPipePermAhead units (items) ahead, weights kPipeWAhead ahead, in
+// kPipeSlots slots.
+constexpr int kPipePermAhead = 12;
+constexpr int kPipeWAhead = 6;
+constexpr int kPipeSlots = 16;
+static_assert(kPipePermAhead == 2 * kPipeWAhead && kPipeSlots > kPipePermAhead, "unit pipeline distances");
 constexpr int kBulkVecPerThread = 1;  // tile <= 8 KB = 512 16-byte vectors
 
 struct BulkStageMeta {
@@ -102,7 +108,10 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
     uint64_t* empty = full + kBulkStages;
     float* swt = reinterpret_cast<float*>(empty + kBulkStages);            // [kBulkStages][32]
     BulkStageMeta* meta = reinterpret_cast<BulkStageMeta*>(swt + kBulkStages * kBulkMaxTerms);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + kBulkStages);
+    int* pu_perm = reinterpret_cast<int*>(meta + kBulkStages);              // producer's item pipeline [kPipeSlots][32]
+    float* pu_w = reinterpret_cast<float*>(pu_perm + kPipeSlots * 32);     // [kPipeSlots][32]
+    int* pu_mnt = reinterpret_cast<int*>(pu_w + kPipeSlots * 32);          // [kPipeSlots][3]: destination, terms, tile
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(pu_mnt + kPipeSlots * 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -118,50 +127,72 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
     const long long n_items = a.n_items;
     if (warp == kBulkConsumerWarps) {
         // ---------------- producer warp ----------------
-        // Item k of this CTA is blockIdx.x + k * gridDim.x.  The list lookups
-        // run 32 items ahead (lane l holds item kb + l of the current and of
-        // the next batch).  The source rows of the next kBulkLook items are
-        // read ahead too (lane = term; an item's perm entries kBulkLook items
-        // before its copies, its weights two items before), so that after an
-        // L2 flush no item waits on its perm -> weight chain: the one
-        // producer warp issues every copy, and that chain was its critical
-        // path.
+        // Item k of this CTA is blockIdx.x + k * gridDim.x.  Nothing the
+        // producer waits for per item is a load issued for that item: the
+        // list entries are read in batches of 32 items (lane l = item 32b +
+        // l), a batch's entries two batches ahead and their row_ptr bounds
+        // one batch ahead; each item's perm entries are copied into a
+        // shared-memory slot kPipePermAhead items ahead and its weights
+        // kPipeWAhead items ahead (cp.async, one commit group per item).  A
+        // ring of registers shifted one slot per item had made every item
+        // wait for the loads issued one item before: the producer issued an
+        // item every ~1.7 us and waited for a free stage 4% of the time.
         const long long g = gridDim.x;
-        int bm = 0, blo = 0, bn = -1, nm = 0, nlo = 0, nn = -1;
-        auto fetch_meta = [&](long long kb, int& fm, int& flo, int& fn) {
-            const long long it = blockIdx.x + (kb + lane) * g;
-            fn = -1;
-            if (it < n_items) {
-                fm = a.units[it / a.ntiles].x;
-                flo = a.row_ptr[fm];
-                fn = a.row_ptr[fm + 1] - flo;
+        auto item_of = [&](long long j) { return blockIdx.x + j * g; };
+        auto list_m = [&](long long b) -> int {  // lane l: the list entry of item 32 b + l, or -1
+            const long long it = item_of(32 * b + lane);
+            return it < n_items ? a.units[it / a.ntiles].x : -1;
+        };
+        // A: the batch being entered; X: the next (bounds issued one batch
+        // ago); Y: the one after (list entries)
+        int A_m = -1, A_lo = 0, A_hi = 0;
+        int X_m = list_m(0), X_lo = 0, X_hi = 0;
+        int Y_m = list_m(1);
+        if (X_m >= 0) { X_lo = a.row_ptr[X_m]; X_hi = a.row_ptr[X_m + 1]; }
+        long long batch = -1;  // the batch held in A
+        auto enter = [&](long long q) {  // item q into slot q % kPipeSlots, its perm copies issued
+            if ((q >> 5) != batch) {     // q grows by one per call: the next batch
+                A_m = X_m; A_lo = X_lo; A_hi = X_hi;
+                X_m = Y_m;
+                X_lo = X_hi = 0;
+                if (X_m >= 0) { X_lo = a.row_ptr[X_m]; X_hi = a.row_ptr[X_m + 1]; }
+                ++batch;
+                Y_m = list_m(batch + 2);
             }
+            const int l = static_cast<int>(q & 31);
+            const int m = __shfl_sync(0xffffffffu, A_m, l);
+            const int lo = __shfl_sync(0xffffffffu, A_lo, l);
+            const int n = m < 0 ? 0 : __shfl_sync(0xffffffffu, A_hi, l) - lo;
+            const int sl = static_cast<int>(q % kPipeSlots);
+            if (lane == 0) {
+                pu_mnt[3 * sl] = m;
+                pu_mnt[3 * sl + 1] = n;
+                pu_mnt[3 * sl + 2] = a.ntiles == 1 ? 0 : static_cast<int>(item_of(q) % a.ntiles);
+            }
+            if (lane < n) cp_async4(&pu_perm[sl * 32 + lane], a.perm + lo + lane);
         };
-        fetch_meta(0, bm, blo, bn);
-        fetch_meta(32, nm, nlo, nn);
-        long long batch = 0;  // bm/blo/bn hold items [32 batch, 32 batch + 32), nm/nlo/nn the next 32
-        // the ring: slot d holds item k + d
-        int rm[kBulkLook], rn[kBulkLook], rt[kBulkLook], ri[kBulkLook];
-        float rw[kBulkLook];
-        auto enter = [&](long long q, int d) {  // item q into slot d: its list entry and its perm loads
-            const int jq = static_cast<int>(q & 31);
-            const bool here = (q >> 5) == batch;
-            const int m = __shfl_sync(0xffffffffu, here ? bm : nm, jq);
-            const int lo = __shfl_sync(0xffffffffu, here ? blo : nlo, jq);
-            const int n = __shfl_sync(0xffffffffu, here ? bn : nn, jq);
-            rm[d] = m;
-            rn[d] = n;
-            rt[d] = static_cast<int>((blockIdx.x + q * g) % a.ntiles);
-            ri[d] = lane < n ? a.perm[lo + lane] : 0;
-            rw[d] = 1.0f;
+        auto fetch_w = [&](long long q) {  // item q's weights (its perm entries have landed)
+            const int sl = static_cast<int>(q % kPipeSlots);
+            if (a.w && lane < pu_mnt[3 * sl + 1]) cp_async4(&pu_w[sl * 32 + lane], a.w + pu_perm[sl * 32 + lane]);
         };
-#pragma unroll
-        for (int d = 0; d < kBulkLook; ++d) enter(d, d);
-        if (a.w) {
-            if (lane < rn[0]) rw[0] = a.w[ri[0]];
-            if (lane < rn[1]) rw[1] = a.w[ri[1]];
+        // commit group G_j holds perm(j + kPipePermAhead) and w(j + kPipeWAhead);
+        // item k needs G_{k - kPipeWAhead} and older
+        for (int j = -kPipePermAhead; j < 0; ++j) {
+            if (j >= -kPipeWAhead) {
+                cp_async_wait_pending<kPipeWAhead - 1>();
+                __syncwarp();
+                fetch_w(j + kPipeWAhead);
+            }
+            enter(j + kPipePermAhead);
+            cp_async_commit_group();
         }
-        for (long long k = 0; blockIdx.x + k * g < n_items; ++k) {
+        for (long long k = 0; item_of(k) < n_items; ++k) {
+            cp_async_wait_pending<kPipeWAhead - 1>();
+            __syncwarp();
+            const int sl = static_cast<int>(k % kPipeSlots);
+            const int cm = pu_mnt[3 * sl], cn = pu_mnt[3 * sl + 1], ct = pu_mnt[3 * sl + 2];
+            const int ri = lane < cn ? pu_perm[sl * 32 + lane] : 0;
+            const float rw = a.w && lane < cn ? pu_w[sl * 32 + lane] : 1.0f;
             const int s = static_cast<int>(k % kBulkStages);
             const uint32_t ph = static_cast<uint32_t>((k / kBulkStages) & 1);
             bool ok = true;
@@ -170,32 +201,22 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
                 if (lane == 0) { *abort_flag = 1; atomicOr(a.status + kCtrErrTimeout, 1); }
                 break;
             }
-            const int cm = rm[0], cn = rn[0];
-            const int col0 = rt[0] * a.tile_elems;
+            const int col0 = ct * a.tile_elems;
             const int bytes = min(a.tile_elems, a.H - col0) * static_cast<int>(sizeof(XT));
-            if (lane < cn) swt[s * kBulkMaxTerms + lane] = rw[0];
+            if (lane < cn) swt[s * kBulkMaxTerms + lane] = rw;
             if (lane == 0) meta[s] = BulkStageMeta{cm, cn, col0, bytes};
             __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cn * bytes));
             __syncwarp();
             if (lane < cn)
                 bulk_g2s(stage_buf + static_cast<size_t>(s) * kBulkStageBytes + static_cast<size_t>(lane) * a.tile_stride,
-                         shard_row(tbl, ri[0], a.ldx_bytes) + static_cast<long long>(col0) * sizeof(XT),
+                         shard_row(tbl, ri, a.ldx_bytes) + static_cast<long long>(col0) * sizeof(XT),
                          static_cast<uint32_t>(bytes), &full[s]);
-            // advance: the list batch, the ring, the weights two items ahead
-            const long long q = k + kBulkLook;
-            if ((q >> 5) > batch + 1) {
-                batch += 1;
-                bm = nm; blo = nlo; bn = nn;
-                fetch_meta(32 * (batch + 1), nm, nlo, nn);
-            }
-#pragma unroll
-            for (int d = 0; d + 1 < kBulkLook; ++d) {
-                rm[d] = rm[d + 1]; rn[d] = rn[d + 1]; rt[d] = rt[d + 1]; ri[d] = ri[d + 1]; rw[d] = rw[d + 1];
-            }
-            enter(q, kBulkLook - 1);
-            if (a.w && lane < rn[1]) rw[1] = a.w[ri[1]];
+            fetch_w(k + kPipeWAhead);
+            enter(k + kPipePermAhead);
+            cp_async_commit_group();
         }
+        cp_async_wait_pending<0>();  // no copy into shared memory outlives the kernel
         return;
     }
 
@@ -273,7 +294,8 @@ static det_status launch_bulk_t(const BulkArgs& a, const ShardTable& t, int grid
 size_t bulk_smem_bytes()
 {
     return static_cast<size_t>(kBulkStages) * kBulkStageBytes + 2 * kBulkStages * sizeof(uint64_t) +
-           kBulkStages * kBulkMaxTerms * sizeof(float) + kBulkStages * sizeof(BulkStageMeta) + 16;
+           kBulkStages * kBulkMaxTerms * sizeof(float) + kBulkStages * sizeof(BulkStageMeta) +
+           kPipeSlots * 32 * (sizeof(int) + sizeof(float)) + kPipeSlots * 3 * sizeof(int) + 16;
 }
 
 bool bulk_plan_tiles(int64_t H, int xsz, int64_t max_terms, int* tile_elems, int* tile_stride, int* ntiles)
@@ -312,7 +334,7 @@ det_status launch_gather_bulk(det_dtype x_dtype, det_dtype out_dtype, const Bulk
 // the stages would hold a few KB each.  Here an item is one H-tile of one
 // destination -- its n term tiles and the destination's old tile -- sized per
 // n (as wide as fits 64 KB, at most 8 KB of sources for the 512 consumer
-// threads), and the producer packs consecutive items into a 160 KB ring of
+// threads), and the producer packs consecutive items into a 128 KB ring of
 // shared memory, up to kAccSlots items in flight.  A consumer thread folds
 // its 16-byte column of the n terms left to right (the canonical fold of a
 // single chunk), adds the result to the old value once (__fadd_rn), rounds to
@@ -324,7 +346,9 @@ det_status launch_gather_bulk(det_dtype x_dtype, det_dtype out_dtype, const Bulk
 // which runs the longer destinations beside this kernel (128, 160 and 176 KB
 // rings measured the same on the embedding backward).
 constexpr int kAccSlots = 8;
-constexpr int kAccRingBytes = 160 * 1024;
+constexpr int kAccRingBytes = 128 * 1024;
+static_assert((kAccRingBytes & (kAccRingBytes - 1)) == 0 && (kAccSlots & (kAccSlots - 1)) == 0, "powers of two");
+constexpr int kAccChunk = 8;       // units per claim
 static_assert(kAccRingBytes >= 2 * (64 * 1024), "an item that does not fit the ring's tail must fit its head");
 constexpr int kAccItemMax = 64 * 1024;
 constexpr int kAccSpinCheck = 1024;  // consumer try_waits between looks at the abort flag
@@ -405,11 +429,14 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
     unsigned char* ring = smem;  // kAccRingBytes
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kAccRingBytes);
     uint64_t* empty = full + kAccSlots;
-    long long* slot_end = reinterpret_cast<long long*>(empty + kAccSlots);  // producer's: ring end of each slot's item
+    uint32_t* slot_end = reinterpret_cast<uint32_t*>(empty + kAccSlots);    // producer's: ring end of each slot's item
     float* swt = reinterpret_cast<float*>(slot_end + kAccSlots);           // [kAccSlots][32]
     AccMeta* meta = reinterpret_cast<AccMeta*>(swt + kAccSlots * kBulkMaxTerms);
     AccTile* tiles = reinterpret_cast<AccTile*>(meta + kAccSlots);         // [kBulkMaxTerms + 1], by n
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tiles + kBulkMaxTerms + 1);
+    int* pu_perm = reinterpret_cast<int*>(tiles + kBulkMaxTerms + 1);      // producer's unit pipeline [kPipeSlots][32]
+    float* pu_w = reinterpret_cast<float*>(pu_perm + kPipeSlots * 32);       // [kPipeSlots][32]
+    int* pu_mn = reinterpret_cast<int*>(pu_w + kPipeSlots * 32);             // [kPipeSlots][2]: destination, terms
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(pu_mn + kPipeSlots * 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -433,59 +460,92 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
     }
     if (warp == kBulkConsumerWarps) {
         // ---------------- producer warp ----------------
-        // Unit k of this CTA is blockIdx.x + k * gridDim.x; lane l holds the
-        // list entry of unit kb + l of the current and of the next batch of
-        // 32, and the source rows of the next kBulkLook units are read ahead
-        // (lane = term), as in the fixed-stage kernel above.
-        const long long g = gridDim.x;
-        int bm = 0, blo = 0, bn = -1, nm = 0, nlo = 0, nn = -1;
-        auto fetch_meta = [&](long long kb, int& fm, int& flo, int& fn) {
-            const long long u = blockIdx.x + (kb + lane) * g;
-            fn = -1;
-            if (u < n_units) {
-                fm = a.units[u].x;
-                flo = a.row_ptr[fm];
-                fn = a.row_ptr[fm + 1] - flo;
+        // Units come in chunks of kAccChunk list entries: this CTA's first
+        // two chunks are fixed (chunk c = list entries (c * grid + CTA) *
+        // kAccChunk ...), later ones are claimed from a counter in the plan's
+        // counter block, so that CTAs whose units were cheaper take more (the
+        // units differ in cost up to tenfold; with a fixed round-robin the
+        // last CTA ended ~30% after the first).  Nothing the producer waits
+        // for per unit is a load issued for that unit: a chunk's claim, its
+        // list entries and their row_ptr bounds are issued one chunk apart,
+        // its perm entries are copied into a shared-memory slot
+        // kPipePermAhead units ahead and its weights kPipeWAhead units ahead
+        // (cp.async, one commit group per unit).  (A ring of registers
+        // shifted one slot per unit had made every unit wait for the load
+        // issued one unit before.)
+        const long long G = gridDim.x;
+        int* ring_next = a.status + kCtrRingNext;
+        auto chunk_m = [&](long long base) -> int {  // lane l < kAccChunk: list entry base + l, or -1
+            return lane < kAccChunk && base + lane < n_units ? a.units[base + lane].x : -1;
+        };
+        const long long dyn0 = 2 * G * kAccChunk;  // claimed chunks start after the fixed ones
+        // A: the chunk being entered (lane l = its unit l); X: the next (bounds
+        // issued one chunk ago); Y: the one after (list entries); zclaim (lane
+        // 0): the claim of the one after that
+        int A_m = -1, A_lo = 0, A_hi = 0;
+        int X_m = chunk_m(static_cast<long long>(blockIdx.x) * kAccChunk), X_lo = 0, X_hi = 0;
+        int Y_m = chunk_m((G + blockIdx.x) * kAccChunk);
+        int zclaim = 0;  // lane 0: raw counter value of the claim (read one chunk later)
+        if (lane == 0) zclaim = atomicAdd(ring_next, kAccChunk);
+        if (X_m >= 0) { X_lo = a.row_ptr[X_m]; X_hi = a.row_ptr[X_m + 1]; }
+        long long chunk = -1;  // the chunk held in A
+        auto advance = [&]() {
+            A_m = X_m; A_lo = X_lo; A_hi = X_hi;
+            X_m = Y_m;
+            X_lo = X_hi = 0;
+            if (X_m >= 0) { X_lo = a.row_ptr[X_m]; X_hi = a.row_ptr[X_m + 1]; }
+            const long long zb = dyn0 + __shfl_sync(0xffffffffu, zclaim, 0);
+            Y_m = chunk_m(zb);
+            if (lane == 0 && zb < n_units) zclaim = atomicAdd(ring_next, kAccChunk);
+            ++chunk;
+        };
+        // unit q of this CTA enters the pipeline: its list entry into slot
+        // q % kPipeSlots (destination -1: no more units), its perm copies issued
+        auto enter = [&](long long q) {
+            if (q / kAccChunk != chunk) advance();  // q grows by one per call
+            const int l = static_cast<int>(q % kAccChunk);
+            const int m = __shfl_sync(0xffffffffu, A_m, l);
+            const int lo = __shfl_sync(0xffffffffu, A_lo, l);
+            const int n = m < 0 ? 0 : __shfl_sync(0xffffffffu, A_hi, l) - lo;
+            const int sl = static_cast<int>(q % kPipeSlots);
+            if (lane == 0) { pu_mn[2 * sl] = m; pu_mn[2 * sl + 1] = n; }
+            if (lane < n) cp_async4(&pu_perm[sl * 32 + lane], a.perm + lo + lane);
+        };
+        // weights of unit q (its perm entries have landed)
+        auto fetch_w = [&](long long q) {
+            const int sl = static_cast<int>(q % kPipeSlots);
+            if (a.w && lane < pu_mn[2 * sl + 1]) cp_async4(&pu_w[sl * 32 + lane], a.w + pu_perm[sl * 32 + lane]);
+        };
+        // Commit group G_j (j >= -kPipePermAhead) holds perm(j + kPipePermAhead)
+        // and w(j + kPipeWAhead): unit j needs G_{j - kPipeWAhead} and older,
+        // which leaves kPipeWAhead - 1 groups pending.  The prologue issues
+        // G_{-kPipePermAhead} .. G_{-1}.
+        for (int j = -kPipePermAhead; j < 0; ++j) {
+            if (j >= -kPipeWAhead) {
+                cp_async_wait_pending<kPipeWAhead - 1>();
+                __syncwarp();
+                fetch_w(j + kPipeWAhead);
             }
-        };
-        fetch_meta(0, bm, blo, bn);
-        fetch_meta(32, nm, nlo, nn);
-        long long batch = 0;
-        int rm[kBulkLook], rn[kBulkLook], ri[kBulkLook];
-        float rw[kBulkLook];
-        auto enter = [&](long long q, int d) {
-            const int jq = static_cast<int>(q & 31);
-            const bool here = (q >> 5) == batch;
-            const int m = __shfl_sync(0xffffffffu, here ? bm : nm, jq);
-            const int lo = __shfl_sync(0xffffffffu, here ? blo : nlo, jq);
-            const int n = __shfl_sync(0xffffffffu, here ? bn : nn, jq);
-            rm[d] = m;
-            rn[d] = n;
-            ri[d] = lane < n ? a.perm[lo + lane] : 0;
-            rw[d] = 1.0f;
-        };
-#pragma unroll
-        for (int d = 0; d < kBulkLook; ++d) enter(d, d);
-        if (a.w) {
-            if (lane < rn[0]) rw[0] = a.w[ri[0]];
-            if (lane < rn[1]) rw[1] = a.w[ri[1]];
+            enter(j + kPipePermAhead);
+            cp_async_commit_group();
         }
-        long long k = 0;      // items issued
-        long long tail = 0;   // items known to be consumed (all items below it)
-        long long pos = 0;    // unwrapped ring position of the next item
-        long long cend = 0;   // unwrapped ring end of item tail - 1 (0 before any)
+        // Ring positions are unwrapped 32-bit byte counts (differences stay
+        // below 2^31); items and slots are counted modulo 2^32 too.
+        uint32_t k = 0;     // items issued
+        uint32_t tail = 0;  // items known to be consumed (all items below it)
+        uint32_t pos = 0;   // unwrapped ring position of the next item
+        uint32_t cend = 0;  // unwrapped ring end of item tail - 1 (0 before any)
         bool ok = true;
         // Ring bytes [start, start + bytes) for item k, after the consumers
         // have freed them; false if a wait expired.
-        auto reserve = [&](long long bytes, long long* start) -> bool {
-            long long s0 = pos;
-            const long long r = s0 % kAccRingBytes;
+        auto reserve = [&](uint32_t bytes, uint32_t* start) -> bool {
+            uint32_t s0 = pos;
+            const uint32_t r = s0 & (kAccRingBytes - 1);
             if (r + bytes > kAccRingBytes) s0 += kAccRingBytes - r;  // items never wrap
-            const long long e = s0 + bytes;
-            while (tail + kAccSlots <= k || e > cend + kAccRingBytes) {
-                const int ts = static_cast<int>(tail % kAccSlots);
-                const uint32_t tph = static_cast<uint32_t>((tail / kAccSlots) & 1);
-                const bool w_ok = mbar_wait_bounded(&empty[ts], tph);
+            const uint32_t e = s0 + bytes;
+            while (static_cast<int>(k - tail) >= kAccSlots || static_cast<int>(e - cend) > kAccRingBytes) {
+                const uint32_t ts = tail & (kAccSlots - 1);
+                const bool w_ok = mbar_wait_bounded(&empty[ts], (tail / kAccSlots) & 1u);
                 if (!__all_sync(0xffffffffu, w_ok) || *abort_flag) return false;
                 cend = slot_end[ts];
                 ++tail;
@@ -494,28 +554,37 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
             *start = s0;
             return true;
         };
-        for (long long ku = 0; ok && blockIdx.x + ku * g < n_units; ++ku) {
-            const int cm = rm[0], cn = rn[0];
+        for (long long ku = 0; ok; ++ku) {
+            // perm(ku), w(ku) and perm(ku + kPipeWAhead) have landed: G_{ku - kPipeWAhead} and older
+            cp_async_wait_pending<kPipeWAhead - 1>();
+            __syncwarp();
+            const int sl = static_cast<int>(ku % kPipeSlots);
+            const int cm = pu_mn[2 * sl], cn = pu_mn[2 * sl + 1];
+            if (cm < 0) break;  // no more units (the claims come in order)
             const AccTile tl = tiles[cn];
-            const unsigned char* xrow = lane < cn ? shard_row(tbl, ri[0], a.ldx_bytes) : nullptr;
+            const int ri = lane < cn ? pu_perm[sl * 32 + lane] : 0;
+            const float rw = a.w && lane < cn ? pu_w[sl * 32 + lane] : 1.0f;
+            const unsigned char* xrow = lane < cn ? shard_row(tbl, ri, a.ldx_bytes) : nullptr;
             const unsigned char* orow = static_cast<const unsigned char*>(a.out) + static_cast<long long>(cm) * a.ldo * OSZ;
+            const uint32_t bytes = static_cast<uint32_t>(cn * tl.stride + tl.obytes);
             for (int t = 0; t < tl.nt; ++t) {
                 const int col0 = t * tl.te;
                 const int elems = min(tl.te, a.H - col0);
-                const long long bytes = static_cast<long long>(cn) * tl.stride + tl.obytes;
-                long long start = 0;
+                uint32_t start = 0;
                 if (!reserve(bytes, &start)) { ok = false; break; }
-                const int s = static_cast<int>(k % kAccSlots);
-                const int off = static_cast<int>(start % kAccRingBytes);
-                if (lane < cn) swt[s * kBulkMaxTerms + lane] = rw[0];
+                const uint32_t s = k & (kAccSlots - 1);
+                const int off = static_cast<int>(start & (kAccRingBytes - 1));
+                if (a.w && lane < cn) swt[s * kBulkMaxTerms + lane] = rw;
                 if (lane == 0) {
                     meta[s] = AccMeta{cm, cn, col0, elems, off, tl.stride};
                     slot_end[s] = start + bytes;
                 }
                 __syncwarp();
+                // the copies may complete before the expected byte count is
+                // set: the count goes below zero until then, and the phase
+                // cannot complete before this one arrival
                 const uint32_t xb = static_cast<uint32_t>(elems * XSZ), ob = static_cast<uint32_t>(elems * OSZ);
                 if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cn) * xb + ob);
-                __syncwarp();
                 if (lane < cn)
                     bulk_g2s(ring + off + lane * tl.stride, xrow + static_cast<long long>(col0) * XSZ, xb, &full[s]);
                 if (lane == 31)
@@ -523,26 +592,18 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
                 ++k;
             }
             if (!ok) break;
-            // advance: the list batch, the ring of units, the weights two units ahead
-            const long long q = ku + kBulkLook;
-            if ((q >> 5) > batch + 1) {
-                batch += 1;
-                bm = nm; blo = nlo; bn = nn;
-                fetch_meta(32 * (batch + 1), nm, nlo, nn);
-            }
-#pragma unroll
-            for (int d = 0; d + 1 < kBulkLook; ++d) {
-                rm[d] = rm[d + 1]; rn[d] = rn[d + 1]; ri[d] = ri[d + 1]; rw[d] = rw[d + 1];
-            }
-            enter(q, kBulkLook - 1);
-            if (a.w && lane < rn[1]) rw[1] = a.w[ri[1]];
+            // G_ku: w(ku + kPipeWAhead) (its perm entries are in G_{ku - kPipeWAhead}), perm(ku + kPipePermAhead)
+            fetch_w(ku + kPipeWAhead);
+            enter(ku + kPipePermAhead);
+            cp_async_commit_group();
         }
+        cp_async_wait_pending<0>();  // no copy into shared memory outlives the kernel
         if (ok) {
             // the end marker: an item of no terms in the next slot
-            long long start = 0;
+            uint32_t start = 0;
             ok = reserve(0, &start);
             if (ok) {
-                const int s = static_cast<int>(k % kAccSlots);
+                const uint32_t s = k & (kAccSlots - 1);
                 if (lane == 0) meta[s] = AccMeta{0, -1, 0, 0, 0, 0};
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
@@ -555,16 +616,26 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
         }
         // every copy this CTA issued lands before it exits: the items not
         // known to be consumed are the last of their slots (bounded waits)
-        for (long long j = max(tail, k - kAccSlots); j < k; ++j)
-            mbar_wait_bounded(&full[j % kAccSlots], static_cast<uint32_t>((j / kAccSlots) & 1));
+        for (uint32_t j = static_cast<int>(k - tail) > kAccSlots ? k - kAccSlots : tail; j != k; ++j)
+            mbar_wait_bounded(&full[j & (kAccSlots - 1)], (j / kAccSlots) & 1u);
+        // the last CTA to get here (after every claim of every CTA) sets the
+        // claim counter back to 0 for the next call with this plan
+        if (lane == 0) {
+            __threadfence();
+            if (atomicAdd(a.status + kCtrRingDone, 1) == static_cast<int>(gridDim.x) - 1) {
+                a.status[kCtrRingNext] = 0;
+                a.status[kCtrRingDone] = 0;
+                __threadfence();
+            }
+        }
         return;
     }
 
     // ---------------- consumer warps ----------------
     const int ctid = threadIdx.x;  // 0 .. kBulkConsumers-1
-    for (long long k = 0;; ++k) {
-        const int s = static_cast<int>(k % kAccSlots);
-        const uint32_t ph = static_cast<uint32_t>((k / kAccSlots) & 1);
+    for (uint32_t k = 0;; ++k) {
+        const uint32_t s = k & (kAccSlots - 1);
+        const uint32_t ph = (k / kAccSlots) & 1u;
         bool ok = false;
         for (unsigned long long it = 0; it < kBulkWaitLimit; ++it) {
             if (mbar_try_wait(&full[s], ph)) { ok = true; break; }
@@ -614,9 +685,10 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
 
 size_t bulk_acc_smem_bytes()
 {
-    return static_cast<size_t>(kAccRingBytes) + 2 * kAccSlots * sizeof(uint64_t) + kAccSlots * sizeof(long long) +
+    return static_cast<size_t>(kAccRingBytes) + 2 * kAccSlots * sizeof(uint64_t) + kAccSlots * sizeof(uint32_t) +
            kAccSlots * kBulkMaxTerms * sizeof(float) + kAccSlots * sizeof(AccMeta) +
-           (kBulkMaxTerms + 1) * sizeof(AccTile) + 16;
+           (kBulkMaxTerms + 1) * sizeof(AccTile) + kPipeSlots * 32 * (sizeof(int) + sizeof(float)) +
+           kPipeSlots * 2 * sizeof(int) + 16;
 }
 
 template <typename XT, typename OT>

@@ -23,6 +23,8 @@ enum {
     kCtrBig = 8,       // units of more than one chunk: hot segments + long whole rows
     kCtrShort = 9,     // whole-destination units of 1..32 terms (row_units)
     kCtrEmpty = 10,    // destinations without terms (row_units, after the short ones)
+    kCtrRingNext = 11, // index_add ring kernel: next unclaimed chunk of units (0 between calls)
+    kCtrRingDone = 12, // index_add ring kernel: CTAs finished (0 between calls)
     kCtrCount = 16
 };
 
