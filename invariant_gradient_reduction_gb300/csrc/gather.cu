@@ -300,10 +300,12 @@ static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int 
 template <typename XT, typename OT, bool VECTOR>
 static det_status launch_gather(const GatherArgs& a, const ShardTable& t, int grid, cudaStream_t st)
 {
-    if (!a.accumulate) return launch_gather_t<XT, OT, VECTOR, false, false>(a, t, grid, st);
     // beside the ring kernel: 16-byte rows only
-    if (VECTOR && a.beside_ring) return launch_gather_t<XT, OT, VECTOR, true, VECTOR>(a, t, grid, st);
-    return launch_gather_t<XT, OT, VECTOR, true, false>(a, t, grid, st);
+    if (!a.accumulate)
+        return VECTOR && a.beside_ring ? launch_gather_t<XT, OT, VECTOR, false, VECTOR>(a, t, grid, st)
+                                       : launch_gather_t<XT, OT, VECTOR, false, false>(a, t, grid, st);
+    return VECTOR && a.beside_ring ? launch_gather_t<XT, OT, VECTOR, true, VECTOR>(a, t, grid, st)
+                                   : launch_gather_t<XT, OT, VECTOR, true, false>(a, t, grid, st);
 }
 
 template <typename XT, typename OT>
@@ -457,30 +459,56 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
                          plan->n_units > 0 &&
                          bulk_plan_tiles(H, xsz, plan->max_row_len, &tile_elems, &tile_stride, &bulk_tiles);
     // with sources in several shards its one producer warp also looks up each
-    // term's shard, on its critical path (EP-invariance, 8 shards: 382 against
-    // 331 us for the register-staged kernel): auto takes it for one shard only
+    // term's shard, on its critical path (EP-invariance, 8 shards: 347 against
+    // 335 us for the register-staged kernel): auto takes it for one shard only
     const bool bulk_auto = bulk_ok && P == 1;
-    // index_add_: the destinations of one chunk (1..32 terms) can take the
-    // TMA-staged ring kernel, the others stay on the register-staged kernel
-    // (and the finish pass).  Its copies need 16-byte x and out tiles: out
-    // rows 16-byte aligned and H a multiple of the quantum.  With an unwaited
-    // plan the ring kernel reads its unit count from the plan's counter block.
-    const int64_t n_short = dev_counts ? -1 : plan->n_units - plan->n_segments - plan->n_long - plan->n_empty;
-    const int acc_quantum = std::max(16 / xsz, 16 / osz);
-    const bool acc_bulk_ok = accumulate && vec && a.out_vec && H % acc_quantum == 0 && n_short != 0;
-    // auto: one shard (the producer's shard lookup is on its critical path)
-    // and rows of 1 KB or more (the embedding backward: 8 KB rows of mostly
-    // one to three terms)
-    const bool acc_bulk_auto = acc_bulk_ok && P == 1 && H * xsz >= 1024;
-    if (path == 3 && !(accumulate ? acc_bulk_ok : bulk_ok)) return DET_ERR_UNSUPPORTED;
+    // The ring kernel: the destinations of at most one chunk (for index_add_
+    // the ones with terms: 1..32; for the scatter-reduce also the empty ones,
+    // which it writes as +0.0) are TMA-staged into a byte ring of shared
+    // memory, the longer ones stay on the register-staged kernel (and the
+    // finish pass).  Its copies need 16-byte x tiles (and, for index_add_,
+    // out tiles): out rows 16-byte aligned and H a multiple of the quantum.
+    // With an unwaited plan it reads its unit count from the plan's counter
+    // block.
+    const int64_t n_ring = dev_counts ? -1
+                                      : plan->n_units - plan->n_segments - plan->n_long -
+                                            (accumulate ? plan->n_empty : 0);
+    const int ring_quantum = accumulate ? std::max(16 / xsz, 16 / osz) : 16 / xsz;
+    const bool ring_ok = vec && a.out_vec && H % ring_quantum == 0 && n_ring != 0;
+    // Auto: the fixed-stage bulk kernel where it applies (a waited plan whose
+    // destinations all have at most 32 terms), else the ring for one shard
+    // (its producer's shard lookup is on its critical path) of rows of 1 KB
+    // or more: always for index_add_ (embedding backward: 128 against 181 us
+    // for the register-staged kernel alone), for the scatter-reduce when the
+    // sources are 1 GiB or more, where the ring's start (a claim, the list,
+    // the bounds and the perm entries before the first copy) is amortised
+    // (EP-invariance step with an unwaited plan: 332 against 354 us; the MoE
+    // combine's 268 MB: 70.5 against 68.7 us).
+    const bool ring_auto = ring_ok && P == 1 && H * xsz >= 1024 &&
+                           (accumulate || static_cast<double>(plan->N) * static_cast<double>(H * xsz) >= 1073741824.0);
+    bool use_bulk = false, use_ring = false;
+    if (path == 3) {
+        if (bulk_ok) use_bulk = true;
+        else if (ring_ok) use_ring = true;
+        else return DET_ERR_UNSUPPORTED;
+    } else if (path == 0) {
+        if (bulk_auto) use_bulk = true;
+        else if (ring_auto) use_ring = true;
+    }
     if (path == 2 && !vec) return DET_ERR_UNSUPPORTED;
     if (accumulate && path == 2) return DET_ERR_UNSUPPORTED;
-    if (accumulate && ((acc_bulk_ok && path == 3) || (acc_bulk_auto && path == 0))) {
-        BulkAccArgs b{};
-        b.units = plan->row_units;  // the short units come first in row_units
-        b.n_units = n_short;
+    if (use_ring) {
+        RingArgs b{};
+        b.units = plan->row_units;  // the one-chunk units come first in row_units, then the empty ones
+        b.n_units = n_ring;
         b.H = a.H;
-        b.quantum = acc_quantum;
+        b.quantum = ring_quantum;
+        // index_add_: 128 KB, which leaves room on the SM for the CTA of the
+        // register-staged kernel beside it (the embedding backward's long
+        // rows); the scatter-reduce: 192 KB, three of the MoE and EP shapes'
+        // 64 KB items in flight (EP-invariance step: 332 against 353 us with
+        // 128 KB)
+        b.ring_bytes = (accumulate ? 128 : 192) * 1024;
         b.row_ptr = plan->row_ptr;
         b.perm = plan->perm;
         b.w = w;
@@ -490,11 +518,11 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
         b.status = plan->counters;
         b.dev_counters = dev_counts ? plan->counters : nullptr;
         int64_t bgrid = opts && opts->grid_ctas > 0 ? opts->grid_ctas
-                                                    : (dev_counts ? sms : std::min<int64_t>(n_short, sms));
+                                                    : (dev_counts ? sms : std::min<int64_t>(n_ring, sms));
         bgrid = std::max<int64_t>(1, std::min<int64_t>(bgrid, 2147483647));
-        s = launch_gather_bulk_acc(x_dtype, out_dtype, b, tbl, static_cast<int>(bgrid), st);
+        s = launch_gather_ring(x_dtype, out_dtype, accumulate, b, tbl, static_cast<int>(bgrid), st);
         if (s) return s;
-        // The register-staged kernel takes the units of more than one chunk,
+    // The register-staged kernel takes the units of more than one chunk,
         // beside the ring kernel: launched as its programmatic dependent, it
         // starts at once on the shared memory the ring leaves free (one CTA
         // per SM) and waits for the ring kernel only before it ends.  On the
@@ -531,7 +559,7 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
     // with its producer reading source rows four items ahead it measured
     // 52.9 against 53.9 us (MoE combine) and 324 against 327 us
     // (EP-invariance).  Everything else takes the register-staged kernel.
-    if ((bulk_ok && path == 3) || (bulk_auto && path == 0)) {
+    if (use_bulk) {
         BulkArgs b{};
         b.units = plan->row_units;
         b.n_items = plan->n_units * bulk_tiles;

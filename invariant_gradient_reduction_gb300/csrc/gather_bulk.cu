@@ -326,70 +326,66 @@ det_status launch_gather_bulk(det_dtype x_dtype, det_dtype out_dtype, const Bulk
 }
 
 // ------------------------------------------------------------------------
-// index_add_ on one-chunk destinations: a byte ring of whole items
+// destinations of at most one chunk: a byte ring of whole items
 // ------------------------------------------------------------------------
 //
 // The embedding backward's rows have mostly one to three terms, and each
 // touched gradient row is read and written once: with a fixed stage per item
 // the stages would hold a few KB each.  Here an item is one H-tile of one
-// destination -- its n term tiles and the destination's old tile -- sized per
-// n (as wide as fits 64 KB, at most 8 KB of sources for the 512 consumer
-// threads), and the producer packs consecutive items into a 128 KB ring of
-// shared memory, up to kAccSlots items in flight.  A consumer thread folds
-// its 16-byte column of the n terms left to right (the canonical fold of a
-// single chunk), adds the result to the old value once (__fadd_rn), rounds to
-// the output type and stores.  The producer reuses ring bytes only after the
-// items that held them are consumed (their empty barriers, oldest first), and
-// ends with an item of no terms that tells the consumers to stop.
+// destination -- its n term tiles and, for index_add_ (ACC), the
+// destination's old tile -- sized per n (as wide as fits 64 KB, at most 8 KB
+// of sources for the 512 consumer threads), and the producer packs
+// consecutive items into a byte ring of shared memory (its size a launch
+// argument), up to kRingSlots items in flight.  A consumer thread folds its
+// 16-byte column of the n terms left to right (the canonical fold of a
+// single chunk; +0.0 for a destination without terms), adds the result to
+// the old value once (__fadd_rn) for index_add_, rounds to the output type
+// and stores.  The producer reuses ring bytes only after the items that held
+// them are consumed (their empty barriers, oldest first), and ends with an
+// item marked last that tells the consumers to stop.
+constexpr int kRingSlots = 8;
+static_assert((kRingSlots & (kRingSlots - 1)) == 0, "a power of two");
+constexpr int kRingChunk = 8;       // units per claim
+constexpr int kRingItemMax = 64 * 1024;
+constexpr int kRingSpinCheck = 1024;  // consumer try_waits between looks at the abort flag
 
-// The ring leaves room on the SM for one CTA of the register-staged kernel,
-// which runs the longer destinations beside this kernel (128, 160 and 176 KB
-// rings measured the same on the embedding backward).
-constexpr int kAccSlots = 8;
-constexpr int kAccRingBytes = 128 * 1024;
-static_assert((kAccRingBytes & (kAccRingBytes - 1)) == 0 && (kAccSlots & (kAccSlots - 1)) == 0, "powers of two");
-constexpr int kAccChunk = 8;       // units per claim
-static_assert(kAccRingBytes >= 2 * (64 * 1024), "an item that does not fit the ring's tail must fit its head");
-constexpr int kAccItemMax = 64 * 1024;
-constexpr int kAccSpinCheck = 1024;  // consumer try_waits between looks at the abort flag
-
-struct AccMeta {
+struct RingMeta {
     int m;       // destination (n < 0: no more items)
     int n;       // terms
     int col0;    // first element of the tile
     int elems;   // elements in the tile
-    int off;     // ring offset of the first term tile; the old tile follows the n term tiles
+    int off;     // ring offset of the first term tile; the old tile (ACC) follows the n term tiles
     int stride;  // bytes between term tiles (128-byte multiple)
 };
 
-struct AccTile {
+struct RingTile {
     int te;      // tile width in elements
     int stride;  // staged bytes per term tile
-    int obytes;  // staged bytes of the old destination tile
+    int obytes;  // staged bytes of the old destination tile (0 without ACC)
     int nt;      // tiles per row
 };
 
+__device__ __forceinline__ long long ring_cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
 // Tiling of a destination with n terms: the fewest tiles for which a tile of
 // x is at most 8 KB (one 16-byte column per consumer thread) and the item
-// (n term tiles + the old tile, each rounded to 128 bytes) fits kAccItemMax.
-__device__ __forceinline__ long long acc_cdiv(long long a, long long b) { return (a + b - 1) / b; }
-
-__device__ __forceinline__ AccTile acc_tile(int n, int H, int q, int xsz, int osz)
+// (n term tiles + the old tile, each rounded to 128 bytes) fits kRingItemMax.
+__device__ __forceinline__ RingTile ring_tile(int n, int H, int q, int xsz, int osz)
 {
-    AccTile t{};
+    RingTile t{};
     const long long per_elem = static_cast<long long>(n) * xsz + osz;
-    int nt = static_cast<int>(max(acc_cdiv(static_cast<long long>(H) * xsz, 16LL * kBulkConsumers),
-                                  acc_cdiv(static_cast<long long>(H) * per_elem, static_cast<long long>(kAccItemMax))));
+    int nt = static_cast<int>(max(ring_cdiv(static_cast<long long>(H) * xsz, 16LL * kBulkConsumers),
+                                  ring_cdiv(static_cast<long long>(H) * per_elem, static_cast<long long>(kRingItemMax))));
     nt = max(nt, 1);
     for (;; ++nt) {
-        const int te = static_cast<int>((acc_cdiv(H, nt) + q - 1) / q * q);
+        const int te = static_cast<int>((ring_cdiv(H, nt) + q - 1) / q * q);
         const int stride = (te * xsz + 127) / 128 * 128;
         const int ob = (te * osz + 127) / 128 * 128;
-        if (te * xsz <= 16 * kBulkConsumers && static_cast<long long>(n) * stride + ob <= kAccItemMax) {
+        if (te * xsz <= 16 * kBulkConsumers && static_cast<long long>(n) * stride + ob <= kRingItemMax) {
             t.te = te;
             t.stride = stride;
             t.obytes = ob;
-            t.nt = static_cast<int>(acc_cdiv(H, te));
+            t.nt = static_cast<int>(ring_cdiv(H, te));
             return t;
         }
     }
@@ -397,7 +393,7 @@ __device__ __forceinline__ AccTile acc_tile(int n, int H, int q, int xsz, int os
 
 // The old destination values of one 16-byte column of x (VEC elements).
 template <typename OT, int VEC>
-__device__ __forceinline__ void acc_load_old(const unsigned char* p, float* old)
+__device__ __forceinline__ void ring_load_old(const unsigned char* p, float* old)
 {
     if (sizeof(OT) == 4) {
 #pragma unroll
@@ -417,52 +413,58 @@ __device__ __forceinline__ void acc_load_old(const unsigned char* p, float* old)
 // kernel's 17 warps needs 5 x 2048 + 2 x 2560 <= 16384 registers; at 70
 // registers the second CTA did not fit and the two kernels ran one after
 // the other (201 against 128 us on the embedding backward).
-template <typename XT, typename OT>
+template <typename XT, typename OT, bool ACC>
 __global__ void __maxnreg__(64)
-gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_constant__ ShardTable tbl)
+gather_ring_kernel(const __grid_constant__ RingArgs a, const __grid_constant__ ShardTable tbl)
 {
     using BV = BulkVec<XT>;
     constexpr int VEC = BV::VEC;
     constexpr int XSZ = static_cast<int>(sizeof(XT));
     constexpr int OSZ = static_cast<int>(sizeof(OT));
     extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char* ring = smem;  // kAccRingBytes
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kAccRingBytes);
-    uint64_t* empty = full + kAccSlots;
-    uint32_t* slot_end = reinterpret_cast<uint32_t*>(empty + kAccSlots);    // producer's: ring end of each slot's item
-    float* swt = reinterpret_cast<float*>(slot_end + kAccSlots);           // [kAccSlots][32]
-    AccMeta* meta = reinterpret_cast<AccMeta*>(swt + kAccSlots * kBulkMaxTerms);
-    AccTile* tiles = reinterpret_cast<AccTile*>(meta + kAccSlots);         // [kBulkMaxTerms + 1], by n
-    int* pu_perm = reinterpret_cast<int*>(tiles + kBulkMaxTerms + 1);      // producer's unit pipeline [kPipeSlots][32]
-    float* pu_w = reinterpret_cast<float*>(pu_perm + kPipeSlots * 32);       // [kPipeSlots][32]
-    int* pu_mn = reinterpret_cast<int*>(pu_w + kPipeSlots * 32);             // [kPipeSlots][2]: destination, terms
+    const uint32_t R = static_cast<uint32_t>(a.ring_bytes);  // a multiple of 128, at least 2 * kRingItemMax
+    unsigned char* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + R);
+    uint64_t* empty = full + kRingSlots;
+    uint32_t* charge = reinterpret_cast<uint32_t*>(empty + kRingSlots);      // producer's: ring bytes each slot's item holds
+    float* swt = reinterpret_cast<float*>(charge + kRingSlots);              // [kRingSlots][32]
+    RingMeta* meta = reinterpret_cast<RingMeta*>(swt + kRingSlots * kBulkMaxTerms);
+    RingTile* tiles = reinterpret_cast<RingTile*>(meta + kRingSlots);       // [kBulkMaxTerms + 1], by n
+    int* pu_perm = reinterpret_cast<int*>(tiles + kBulkMaxTerms + 1);       // producer's unit pipeline [kPipeSlots][32]
+    float* pu_w = reinterpret_cast<float*>(pu_perm + kPipeSlots * 32);      // [kPipeSlots][32]
+    int* pu_mn = reinterpret_cast<int*>(pu_w + kPipeSlots * 32);            // [kPipeSlots][2]: destination, terms
     volatile int* abort_flag = reinterpret_cast<volatile int*>(pu_mn + kPipeSlots * 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kAccSlots; ++s) {
+        for (int s = 0; s < kRingSlots; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kBulkConsumerWarps);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (threadIdx.x <= kBulkMaxTerms) tiles[threadIdx.x] = acc_tile(threadIdx.x, a.H, a.quantum, XSZ, OSZ);
-    // the kernel for the other destinations may start now and run beside
-    // this one (it writes other rows; it waits for this grid before it ends)
+    if (threadIdx.x <= kBulkMaxTerms) tiles[threadIdx.x] = ring_tile(threadIdx.x, a.H, a.quantum, XSZ, ACC ? OSZ : 0);
+    // Launched the ordinary way, so everything before this grid has
+    // finished: the kernel for the other destinations may start now and run
+    // beside this one (it reads the plan without waiting, writes other rows,
+    // and waits for this grid before it ends).  (As a programmatic dependent
+    // of the plan, waiting here before letting it start, this kernel made the
+    // MoE step 3 us and the EP-invariance step 4 us slower.)
     pdl_launch_dependents();
     __syncthreads();
 
     long long n_units = a.n_units;
     if (a.dev_counters) {  // written by the plan's kernels, which finished before this grid started
         const int* c = a.dev_counters;
-        n_units = (c[kCtrErrIndex] | c[kCtrErrDup] | c[kCtrErrTimeout]) ? 0 : c[kCtrShort];
+        n_units = (c[kCtrErrIndex] | c[kCtrErrDup] | c[kCtrErrTimeout]) ? 0
+                                                                         : c[kCtrShort] + (ACC ? 0 : c[kCtrEmpty]);
     }
     if (warp == kBulkConsumerWarps) {
         // ---------------- producer warp ----------------
-        // Units come in chunks of kAccChunk list entries: this CTA's first
+        // Units come in chunks of kRingChunk list entries: this CTA's first
         // two chunks are fixed (chunk c = list entries (c * grid + CTA) *
-        // kAccChunk ...), later ones are claimed from a counter in the plan's
+        // kRingChunk ...), later ones are claimed from a counter in the plan's
         // counter block, so that CTAs whose units were cheaper take more (the
         // units differ in cost up to tenfold; with a fixed round-robin the
         // last CTA ended ~30% after the first).  Nothing the producer waits
@@ -475,18 +477,18 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
         // issued one unit before.)
         const long long G = gridDim.x;
         int* ring_next = a.status + kCtrRingNext;
-        auto chunk_m = [&](long long base) -> int {  // lane l < kAccChunk: list entry base + l, or -1
-            return lane < kAccChunk && base + lane < n_units ? a.units[base + lane].x : -1;
+        auto chunk_m = [&](long long base) -> int {  // lane l < kRingChunk: list entry base + l, or -1
+            return lane < kRingChunk && base + lane < n_units ? a.units[base + lane].x : -1;
         };
-        const long long dyn0 = 2 * G * kAccChunk;  // claimed chunks start after the fixed ones
+        const long long dyn0 = 2 * G * kRingChunk;  // claimed chunks start after the fixed ones
         // A: the chunk being entered (lane l = its unit l); X: the next (bounds
         // issued one chunk ago); Y: the one after (list entries); zclaim (lane
         // 0): the claim of the one after that
         int A_m = -1, A_lo = 0, A_hi = 0;
-        int X_m = chunk_m(static_cast<long long>(blockIdx.x) * kAccChunk), X_lo = 0, X_hi = 0;
-        int Y_m = chunk_m((G + blockIdx.x) * kAccChunk);
+        int X_m = chunk_m(static_cast<long long>(blockIdx.x) * kRingChunk), X_lo = 0, X_hi = 0;
+        int Y_m = chunk_m((G + blockIdx.x) * kRingChunk);
         int zclaim = 0;  // lane 0: raw counter value of the claim (read one chunk later)
-        if (lane == 0) zclaim = atomicAdd(ring_next, kAccChunk);
+        if (lane == 0) zclaim = atomicAdd(ring_next, kRingChunk);
         if (X_m >= 0) { X_lo = a.row_ptr[X_m]; X_hi = a.row_ptr[X_m + 1]; }
         long long chunk = -1;  // the chunk held in A
         auto advance = [&]() {
@@ -496,14 +498,14 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
             if (X_m >= 0) { X_lo = a.row_ptr[X_m]; X_hi = a.row_ptr[X_m + 1]; }
             const long long zb = dyn0 + __shfl_sync(0xffffffffu, zclaim, 0);
             Y_m = chunk_m(zb);
-            if (lane == 0 && zb < n_units) zclaim = atomicAdd(ring_next, kAccChunk);
+            if (lane == 0 && zb < n_units) zclaim = atomicAdd(ring_next, kRingChunk);
             ++chunk;
         };
         // unit q of this CTA enters the pipeline: its list entry into slot
         // q % kPipeSlots (destination -1: no more units), its perm copies issued
         auto enter = [&](long long q) {
-            if (q / kAccChunk != chunk) advance();  // q grows by one per call
-            const int l = static_cast<int>(q % kAccChunk);
+            if (q / kRingChunk != chunk) advance();  // q grows by one per call
+            const int l = static_cast<int>(q % kRingChunk);
             const int m = __shfl_sync(0xffffffffu, A_m, l);
             const int lo = __shfl_sync(0xffffffffu, A_lo, l);
             const int n = m < 0 ? 0 : __shfl_sync(0xffffffffu, A_hi, l) - lo;
@@ -529,29 +531,31 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
             enter(j + kPipePermAhead);
             cp_async_commit_group();
         }
-        // Ring positions are unwrapped 32-bit byte counts (differences stay
-        // below 2^31); items and slots are counted modulo 2^32 too.
-        uint32_t k = 0;     // items issued
+        // The ring: head is the offset where the next item may start, free
+        // the bytes not held by items in flight.  An item never wraps: when
+        // it does not fit before the end, it starts at 0 and also holds the
+        // bytes it skipped (its charge), which come free with it.
+        uint32_t k = 0;     // items issued (modulo 2^32)
         uint32_t tail = 0;  // items known to be consumed (all items below it)
-        uint32_t pos = 0;   // unwrapped ring position of the next item
-        uint32_t cend = 0;  // unwrapped ring end of item tail - 1 (0 before any)
+        uint32_t head = 0, free_bytes = R;
         bool ok = true;
         // Ring bytes [start, start + bytes) for item k, after the consumers
         // have freed them; false if a wait expired.
-        auto reserve = [&](uint32_t bytes, uint32_t* start) -> bool {
-            uint32_t s0 = pos;
-            const uint32_t r = s0 & (kAccRingBytes - 1);
-            if (r + bytes > kAccRingBytes) s0 += kAccRingBytes - r;  // items never wrap
-            const uint32_t e = s0 + bytes;
-            while (static_cast<int>(k - tail) >= kAccSlots || static_cast<int>(e - cend) > kAccRingBytes) {
-                const uint32_t ts = tail & (kAccSlots - 1);
-                const bool w_ok = mbar_wait_bounded(&empty[ts], (tail / kAccSlots) & 1u);
+        auto reserve = [&](uint32_t bytes, uint32_t* start, uint32_t* held) -> bool {
+            const uint32_t skip = head + bytes > R ? R - head : 0u;
+            const uint32_t need = skip + bytes;
+            while (static_cast<int>(k - tail) >= kRingSlots || free_bytes < need) {
+                const uint32_t ts = tail & (kRingSlots - 1);
+                const bool w_ok = mbar_wait_bounded(&empty[ts], (tail / kRingSlots) & 1u);
                 if (!__all_sync(0xffffffffu, w_ok) || *abort_flag) return false;
-                cend = slot_end[ts];
+                free_bytes += charge[ts];
                 ++tail;
             }
-            pos = e;
-            *start = s0;
+            *start = skip ? 0u : head;
+            head = *start + bytes;
+            if (head == R) head = 0;
+            free_bytes -= need;
+            *held = need;
             return true;
         };
         for (long long ku = 0; ok; ++ku) {
@@ -561,7 +565,7 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
             const int sl = static_cast<int>(ku % kPipeSlots);
             const int cm = pu_mn[2 * sl], cn = pu_mn[2 * sl + 1];
             if (cm < 0) break;  // no more units (the claims come in order)
-            const AccTile tl = tiles[cn];
+            const RingTile tl = tiles[cn];
             const int ri = lane < cn ? pu_perm[sl * 32 + lane] : 0;
             const float rw = a.w && lane < cn ? pu_w[sl * 32 + lane] : 1.0f;
             const unsigned char* xrow = lane < cn ? shard_row(tbl, ri, a.ldx_bytes) : nullptr;
@@ -570,25 +574,24 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
             for (int t = 0; t < tl.nt; ++t) {
                 const int col0 = t * tl.te;
                 const int elems = min(tl.te, a.H - col0);
-                uint32_t start = 0;
-                if (!reserve(bytes, &start)) { ok = false; break; }
-                const uint32_t s = k & (kAccSlots - 1);
-                const int off = static_cast<int>(start & (kAccRingBytes - 1));
+                uint32_t start = 0, held = 0;
+                if (!reserve(bytes, &start, &held)) { ok = false; break; }
+                const uint32_t s = k & (kRingSlots - 1);
                 if (a.w && lane < cn) swt[s * kBulkMaxTerms + lane] = rw;
                 if (lane == 0) {
-                    meta[s] = AccMeta{cm, cn, col0, elems, off, tl.stride};
-                    slot_end[s] = start + bytes;
+                    meta[s] = RingMeta{cm, cn, col0, elems, static_cast<int>(start), tl.stride};
+                    charge[s] = held;
                 }
                 __syncwarp();
                 // the copies may complete before the expected byte count is
                 // set: the count goes below zero until then, and the phase
                 // cannot complete before this one arrival
                 const uint32_t xb = static_cast<uint32_t>(elems * XSZ), ob = static_cast<uint32_t>(elems * OSZ);
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cn) * xb + ob);
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cn) * xb + (ACC ? ob : 0u));
                 if (lane < cn)
-                    bulk_g2s(ring + off + lane * tl.stride, xrow + static_cast<long long>(col0) * XSZ, xb, &full[s]);
-                if (lane == 31)
-                    bulk_g2s(ring + off + cn * tl.stride, orow + static_cast<long long>(col0) * OSZ, ob, &full[s]);
+                    bulk_g2s(ring + start + lane * tl.stride, xrow + static_cast<long long>(col0) * XSZ, xb, &full[s]);
+                if (ACC && lane == 31)
+                    bulk_g2s(ring + start + cn * tl.stride, orow + static_cast<long long>(col0) * OSZ, ob, &full[s]);
                 ++k;
             }
             if (!ok) break;
@@ -599,12 +602,15 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
         }
         cp_async_wait_pending<0>();  // no copy into shared memory outlives the kernel
         if (ok) {
-            // the end marker: an item of no terms in the next slot
-            uint32_t start = 0;
-            ok = reserve(0, &start);
+            // the end marker: an item of no bytes, marked last, in the next slot
+            uint32_t start = 0, held = 0;
+            ok = reserve(0, &start, &held);
             if (ok) {
-                const uint32_t s = k & (kAccSlots - 1);
-                if (lane == 0) meta[s] = AccMeta{0, -1, 0, 0, 0, 0};
+                const uint32_t s = k & (kRingSlots - 1);
+                if (lane == 0) {
+                    meta[s] = RingMeta{0, -1, 0, 0, 0, 0};
+                    charge[s] = 0;
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
                 ++k;
@@ -616,8 +622,8 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
         }
         // every copy this CTA issued lands before it exits: the items not
         // known to be consumed are the last of their slots (bounded waits)
-        for (uint32_t j = static_cast<int>(k - tail) > kAccSlots ? k - kAccSlots : tail; j != k; ++j)
-            mbar_wait_bounded(&full[j & (kAccSlots - 1)], (j / kAccSlots) & 1u);
+        for (uint32_t j = static_cast<int>(k - tail) > kRingSlots ? k - kRingSlots : tail; j != k; ++j)
+            mbar_wait_bounded(&full[j & (kRingSlots - 1)], (j / kRingSlots) & 1u);
         // the last CTA to get here (after every claim of every CTA) sets the
         // claim counter back to 0 for the next call with this plan
         if (lane == 0) {
@@ -634,19 +640,19 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
     // ---------------- consumer warps ----------------
     const int ctid = threadIdx.x;  // 0 .. kBulkConsumers-1
     for (uint32_t k = 0;; ++k) {
-        const uint32_t s = k & (kAccSlots - 1);
-        const uint32_t ph = (k / kAccSlots) & 1u;
+        const uint32_t s = k & (kRingSlots - 1);
+        const uint32_t ph = (k / kRingSlots) & 1u;
         bool ok = false;
         for (unsigned long long it = 0; it < kBulkWaitLimit; ++it) {
             if (mbar_try_wait(&full[s], ph)) { ok = true; break; }
-            if ((it & (kAccSpinCheck - 1)) == kAccSpinCheck - 1 && *abort_flag) break;
+            if ((it & (kRingSpinCheck - 1)) == kRingSpinCheck - 1 && *abort_flag) break;
         }
         if (!ok || *abort_flag) {
             *abort_flag = 1;
             atomicOr(a.status + kCtrErrTimeout, 1);
             break;
         }
-        const AccMeta md = meta[s];
+        const RingMeta md = meta[s];
         if (md.n < 0) break;  // no more items
         const unsigned char* buf = ring + md.off;
         const float* wts = swt + s * kBulkMaxTerms;
@@ -654,7 +660,7 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
         if (ctid < nvec) {
             float acc[VEC];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+            for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;  // a destination without terms: +0.0
             for (int j = 0; j < md.n; ++j) {
                 const uint4 raw = *reinterpret_cast<const uint4*>(buf + j * md.stride + ctid * 16);
                 float xf[VEC];
@@ -672,10 +678,12 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
                     for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(acc[e], xf[e]);
                 }
             }
-            float old[VEC];
-            acc_load_old<OT, VEC>(buf + md.n * md.stride + ctid * VEC * OSZ, old);
+            if (ACC) {
+                float old[VEC];
+                ring_load_old<OT, VEC>(buf + md.n * md.stride + ctid * VEC * OSZ, old);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(old[e], acc[e]);
+                for (int e = 0; e < VEC; ++e) acc[e] = __fadd_rn(old[e], acc[e]);
+            }
             bulk_store<OT, VEC>(a.out, static_cast<long long>(md.m) * a.ldo + md.col0 + ctid * VEC, acc, true);
         }
         __syncwarp();
@@ -683,43 +691,52 @@ gather_bulk_acc_kernel(const __grid_constant__ BulkAccArgs a, const __grid_const
     }
 }
 
-size_t bulk_acc_smem_bytes()
+size_t ring_smem_bytes(int ring_bytes)
 {
-    return static_cast<size_t>(kAccRingBytes) + 2 * kAccSlots * sizeof(uint64_t) + kAccSlots * sizeof(uint32_t) +
-           kAccSlots * kBulkMaxTerms * sizeof(float) + kAccSlots * sizeof(AccMeta) +
-           (kBulkMaxTerms + 1) * sizeof(AccTile) + kPipeSlots * 32 * (sizeof(int) + sizeof(float)) +
+    return static_cast<size_t>(ring_bytes) + 2 * kRingSlots * sizeof(uint64_t) + kRingSlots * sizeof(uint32_t) +
+           kRingSlots * kBulkMaxTerms * sizeof(float) + kRingSlots * sizeof(RingMeta) +
+           (kBulkMaxTerms + 1) * sizeof(RingTile) + kPipeSlots * 32 * (sizeof(int) + sizeof(float)) +
            kPipeSlots * 2 * sizeof(int) + 16;
 }
 
-template <typename XT, typename OT>
-static det_status launch_bulk_acc_t(const BulkAccArgs& a, const ShardTable& t, int grid, cudaStream_t st)
+template <typename XT, typename OT, bool ACC>
+static det_status launch_ring_t(const RingArgs& a, const ShardTable& t, int grid, cudaStream_t st)
 {
-    const size_t smem = bulk_acc_smem_bytes();
+    if (a.ring_bytes % 128 || a.ring_bytes < 2 * kRingItemMax) return DET_ERR_ARG;
+    const size_t smem = ring_smem_bytes(a.ring_bytes);
     {
         const det_status a_ =
-            allow_dynamic_smem(reinterpret_cast<const void*>(gather_bulk_acc_kernel<XT, OT>), smem);
+            allow_dynamic_smem(reinterpret_cast<const void*>(gather_ring_kernel<XT, OT, ACC>), smem);
         if (a_) return a_;
         // all of the SM's shared memory: the register-staged kernel that runs
         // beside it needs the rest of it on the same SM
         static bool carve_set = false;
         if (!carve_set) {
-            DETR_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(gather_bulk_acc_kernel<XT, OT>),
+            DETR_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(gather_ring_kernel<XT, OT, ACC>),
                                            cudaFuncAttributePreferredSharedMemoryCarveout, 100));
             carve_set = true;
         }
     }
-    gather_bulk_acc_kernel<XT, OT><<<grid, kBulkThreads, smem, st>>>(a, t);
+    gather_ring_kernel<XT, OT, ACC><<<grid, kBulkThreads, smem, st>>>(a, t);
     DETR_LAUNCHED();
     return DET_OK;
 }
 
-det_status launch_gather_bulk_acc(det_dtype x_dtype, det_dtype out_dtype, const BulkAccArgs& a, const ShardTable& t,
+template <bool ACC>
+static det_status launch_ring_acc(det_dtype x_dtype, det_dtype out_dtype, const RingArgs& a, const ShardTable& t,
                                   int grid, cudaStream_t st)
 {
-    if (x_dtype == DET_BF16 && out_dtype == DET_BF16) return launch_bulk_acc_t<uint16_t, __nv_bfloat16>(a, t, grid, st);
-    if (x_dtype == DET_BF16) return launch_bulk_acc_t<uint16_t, float>(a, t, grid, st);
-    if (out_dtype == DET_BF16) return launch_bulk_acc_t<float, __nv_bfloat16>(a, t, grid, st);
-    return launch_bulk_acc_t<float, float>(a, t, grid, st);
+    if (x_dtype == DET_BF16 && out_dtype == DET_BF16) return launch_ring_t<uint16_t, __nv_bfloat16, ACC>(a, t, grid, st);
+    if (x_dtype == DET_BF16) return launch_ring_t<uint16_t, float, ACC>(a, t, grid, st);
+    if (out_dtype == DET_BF16) return launch_ring_t<float, __nv_bfloat16, ACC>(a, t, grid, st);
+    return launch_ring_t<float, float, ACC>(a, t, grid, st);
+}
+
+det_status launch_gather_ring(det_dtype x_dtype, det_dtype out_dtype, bool accumulate, const RingArgs& a,
+                              const ShardTable& t, int grid, cudaStream_t st)
+{
+    return accumulate ? launch_ring_acc<true>(x_dtype, out_dtype, a, t, grid, st)
+                      : launch_ring_acc<false>(x_dtype, out_dtype, a, t, grid, st);
 }
 
 }  // namespace detr

@@ -36,9 +36,9 @@ struct GatherArgs {
     long long ldpart;
     const int* dev_counters;  // non-null: read the work counts (and plan errors) from the device
     int accumulate;           // add to out (index_add_); destinations without terms stay untouched
-    int beside_ring;          // index_add_ beside the ring kernel, which takes the one-chunk units: only the
-                              // units of more than one chunk, and the wait for the previous grid (the ring
-                              // kernel; everything before it had finished when it started) at the end
+    int beside_ring;          // beside the ring kernel, which takes the one-chunk units: only the units of
+                              // more than one chunk, and the wait for the previous grid (the ring kernel;
+                              // everything before it had finished when it started) at the end
 };
 
 // Work counts of a launch: from the host, or from the plan's counter block
@@ -119,14 +119,16 @@ bool bulk_plan_tiles(int64_t H, int xsz, int64_t max_terms, int* tile_elems, int
 det_status launch_gather_bulk(det_dtype x_dtype, det_dtype out_dtype, const BulkArgs& a, const ShardTable& t,
                               int grid, cudaStream_t st);
 
-// index_add_ on the destinations of one chunk (1..32 terms), TMA-staged: each
-// item is a destination's H-tile with its term tiles and the old destination
-// tile, packed into a byte ring of shared memory.
-struct BulkAccArgs {
+// The destinations of at most one chunk (1..32 terms; for the scatter-reduce
+// also those without terms), TMA-staged: each item is a destination's H-tile
+// with its term tiles (and, for index_add_, the old destination tile), packed
+// into a byte ring of shared memory.
+struct RingArgs {
     const int4* units;     // the one-chunk whole-destination units (row_units[0 .. n_units))
     long long n_units;
     int H;
-    int quantum;           // tile widths are multiples of this many elements (16-byte x and out copies)
+    int quantum;           // tile widths are multiples of this many elements (16-byte copies)
+    int ring_bytes;        // shared-memory ring: a multiple of 128, at least 128 KB
     const int* row_ptr;
     const int* perm;
     const float* w;
@@ -134,12 +136,12 @@ struct BulkAccArgs {
     void* out;             // 16-byte aligned rows (ldo * sizeof(out) a multiple of 16)
     long long ldo;
     int* status;           // counter block; kCtrErrTimeout is set if a bounded wait expires
-    const int* dev_counters;  // non-null (plan that did not wait): n_units is the block's short-unit count,
-                              // or 0 if the plan recorded an error
+    const int* dev_counters;  // non-null (plan that did not wait): n_units is the block's count of
+                              // such units, or 0 if the plan recorded an error
 };
 
-size_t bulk_acc_smem_bytes();
-det_status launch_gather_bulk_acc(det_dtype x_dtype, det_dtype out_dtype, const BulkAccArgs& a, const ShardTable& t,
-                                  int grid, cudaStream_t st);
+size_t ring_smem_bytes(int ring_bytes);
+det_status launch_gather_ring(det_dtype x_dtype, det_dtype out_dtype, bool accumulate, const RingArgs& a,
+                              const ShardTable& t, int grid, cudaStream_t st);
 
 }  // namespace detr

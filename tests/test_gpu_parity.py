@@ -687,18 +687,21 @@ def _mixed_lengths_idx(M, seed):
     return idx
 
 
+@pytest.mark.parametrize("accumulate", [True, False])
 @pytest.mark.parametrize("H,xdt,odt,weighted", [(4096, torch.bfloat16, torch.float32, False),
                                                 (1000, torch.bfloat16, torch.float32, True),
                                                 (520, torch.bfloat16, torch.bfloat16, False),
                                                 (300, torch.float32, torch.float32, True),
                                                 (264, torch.float32, torch.bfloat16, False)])
-def test_index_add_bulk_ring_matches_oracle(H, xdt, odt, weighted):
-    """det_index_add through the TMA-staged ring kernel for the one-chunk rows
+def test_index_add_bulk_ring_matches_oracle(H, xdt, odt, weighted, accumulate):
+    """The TMA-staged ring kernel for the destinations of at most one chunk
     (gather_path 3, and auto where it applies), with the long and hot rows on
-    the register-staged kernel and the finish pass: the same bytes as the
-    oracle and as the register-staged kernel alone (gather_path 1), for row
-    widths that give one tile or several per destination and ragged last
-    tiles, bf16 and fp32 outputs, weights and two shards."""
+    the register-staged kernel beside it and the finish pass: det_index_add
+    (accumulate) and det_scatter_reduce (empty rows written as +0.0) give the
+    same bytes as the oracle and as the register-staged kernel alone
+    (gather_path 1), for row widths that give one tile or several per
+    destination and ragged last tiles, bf16 and fp32 outputs, weights, plans
+    that did and did not wait, two shards and a small grid."""
     M = 700
     idx_np = _mixed_lengths_idx(M, seed=H)
     N = idx_np.size
@@ -706,34 +709,36 @@ def test_index_add_bulk_ring_matches_oracle(H, xdt, odt, weighted):
     x = (torch.randn(N, H, generator=g, device=DEV) * 2).to(xdt)
     w = torch.rand(N, generator=g, device=DEV) if weighted else None
     init = (torch.randn(M, H, generator=g, device=DEV) * 3).to(odt)
-    init[0] = float("nan")  # untouched rows keep any bits
+    init[0] = float("nan")  # untouched rows keep any bits (index_add); overwritten by the scatter-reduce
     idx = torch.from_numpy(idx_np).to(DEV)
     plan = dr.det_reduce_plan(idx, M)
     d = plan.describe()
     assert d["n_hot_rows"] >= 1
+    call = dr.det_index_add if accumulate else dr.det_scatter_reduce
     want = oracle.scatter_reduce(idx_np, np_bits(x), M, w=None if w is None else w.cpu().numpy(),
-                                 out_dtype=oracle_dtype(odt), out_init=np_bits(init))
+                                 out_dtype=oracle_dtype(odt), out_init=np_bits(init) if accumulate else None)
+    what = f"{'index_add' if accumulate else 'scatter'} H={H}"
     outs = {}
     for path in (0, 1, 3):
         out = init.clone()
-        dr.det_index_add(plan, x, out, w=w, opts={"gather_path": path, "debug_checks": 1})
-        assert_bytes_equal(np_bits(out), want, f"index_add H={H} path {path}")
+        call(plan, x, out, w=w, opts={"gather_path": path, "debug_checks": 1})
+        assert_bytes_equal(np_bits(out), want, f"{what} path {path}")
         outs[path] = out
     # a plan that did not wait: the ring kernel reads its unit count on the device
     plan2 = dr.det_reduce_plan(idx, M, opts={"async_plan": 1})
     for path in (0, 3):
         out = init.clone()
-        dr.det_index_add(plan2, x, out, w=w, opts={"async_plan": 1, "gather_path": path})
+        call(plan2, x, out, w=w, opts={"async_plan": 1, "gather_path": path})
         dr.det_plan_status(plan2)
-        assert_bytes_equal(np_bits(out), want, f"index_add H={H} unwaited plan, path {path}")
+        assert_bytes_equal(np_bits(out), want, f"{what} unwaited plan, path {path}")
     # two shards (the ring kernel when asked for it), and a small grid
     cut = N // 3
     out = init.clone()
-    dr.det_index_add(plan, [x[:cut], x[cut:]], out, w=w, opts={"gather_path": 3, "grid_ctas": 3, "debug_checks": 1})
-    assert_bytes_equal(np_bits(out), want, f"index_add H={H} two shards")
-    # the empty destination rows are untouched, bit for bit
-    empty = np.setdiff1d(np.arange(M), idx_np)
-    assert np_bits(outs[0])[empty].tobytes() == np_bits(init)[empty].tobytes()
+    call(plan, [x[:cut], x[cut:]], out, w=w, opts={"gather_path": 3, "grid_ctas": 3, "debug_checks": 1})
+    assert_bytes_equal(np_bits(out), want, f"{what} two shards")
+    if accumulate:  # the empty destination rows are untouched, bit for bit
+        empty = np.setdiff1d(np.arange(M), idx_np)
+        assert np_bits(outs[0])[empty].tobytes() == np_bits(init)[empty].tobytes()
 
 
 def test_index_add_bulk_ring_unsupported_layouts():

@@ -25,7 +25,7 @@ MANIFEST = {
                   ["test_scatter_small_matches_oracle", "test_full_size_parity", "test_cluster_plan_hot_rows",
                    "test_segment_size_changes_no_bit", "test_index_add_matches_oracle"]),
     "gather_async.cu": (["gather_async_kernel"], ["test_gather_path_changes_no_bit"]),
-    "gather_bulk.cu": (["gather_bulk_kernel", "gather_bulk_acc_kernel"],
+    "gather_bulk.cu": (["gather_bulk_kernel", "gather_ring_kernel"],
                        ["test_gather_path_changes_no_bit", "test_index_add_bulk_ring_matches_oracle"]),
     "hash.cu": (["hash_kernel"], ["test_hash_matches_oracle"]),
     "noalloc.cu": (None, "launches the gather and finish kernels of gather.cu; "
