@@ -94,13 +94,18 @@ typedef int32_t det_dtype;
  *                   DET_ERR_TIMEOUT (slower; for tests).
  *  gather_path      0 = auto.  1 = register-staged warp kernel, 2 = warp
  *                   kernel with cp.async copies into shared memory, 3 = TMA
- *                   bulk-staged kernel (only with a waited plan, when every
- *                   destination has at most 32 terms, rows are at least 1 KB
- *                   and 16-byte aligned; det_index_add: see there).  Auto
- *                   takes 3 where it applies and the sources are one shard,
- *                   else 1.  A path that does not
- *                   apply fails with DET_ERR_UNSUPPORTED.  Every path gives
- *                   the same bits.
+ *                   bulk-staged kernels: with a waited plan whose
+ *                   destinations all have at most 32 terms and rows of at
+ *                   least 1 KB, one 64 KB stage per destination tile; else,
+ *                   with 16-byte aligned source and out rows and H a
+ *                   multiple of 16 bytes, a byte ring in shared memory for
+ *                   the destinations of at most one chunk (also behind a
+ *                   plan that did not wait), the longer ones on the
+ *                   register-staged kernel beside it.  Auto takes the first
+ *                   where it applies to one shard, the ring for one shard of
+ *                   rows of at least 1 KB when the sources are at least
+ *                   1 GiB, else 1.  A path that does not apply fails with
+ *                   DET_ERR_UNSUPPORTED.  Every path gives the same bits.
  *  tiles_per_task   0 = auto; > 0 = H-tiles one warp task of the warp kernels
  *                   covers (the work split changes no bit).
  *  async_plan       plan-time option.  0 (default): det_reduce_plan waits once
@@ -258,7 +263,9 @@ det_status det_scatter_workspace_size(det_plan plan, int64_t H, size_t* bytes);
  *              aligned (may be NULL when that size is 0).
  * Rows are read with 16-byte vector loads when every shard pointer is
  * 16-byte aligned and ldx, H are multiples of 16 bytes' worth of elements;
- * otherwise with scalar loads.  Both give the same bits.
+ * otherwise with scalar loads.  Both give the same bits.  Calls that take
+ * the ring kernel (opts->gather_path) with one plan must not overlap on the
+ * GPU: it claims work from a counter in the plan's workspace.
  * Errors: DET_ERR_ARG, DET_ERR_DTYPE, DET_ERR_WORKSPACE, DET_ERR_UNSUPPORTED,
  * DET_ERR_CUDA.
  */
@@ -282,10 +289,12 @@ det_status det_scatter_reduce(det_plan plan,
  * gives the same bits for the same inputs and the same prior contents.
  * opts->gather_path 3 (16-byte aligned source rows, out rows 16-byte
  * aligned and H a multiple of 16 bytes of both x and out) runs
- * the destinations of 1..32 terms on a TMA-staged kernel that copies each
- * one's source tiles and old out tile into shared memory, and the longer ones
+ * the destinations of 1..32 terms on the TMA-staged ring kernel, which also
+ * copies each one's old out tile into shared memory, and the longer ones
  * on the register-staged kernel; auto does so where it applies, the sources
- * are one shard and rows are at least 1 KB, else it takes path 1.
+ * are one shard and rows are at least 1 KB, else it takes path 1.  Calls that
+ * take the ring kernel with one plan must not overlap on the GPU: it claims
+ * work from a counter in the plan's workspace.
  * gather_path 2 gives DET_ERR_UNSUPPORTED, as does 3 where it does not
  * apply.  Every path gives the same bits.  Other errors as
  * det_scatter_reduce.
