@@ -287,6 +287,52 @@ def test_replays_identical_under_contention(replay):
         dr.det_splitk_gemm_reduce(A, W, 56, o)
         return o
     replay.identical(gemm, name="splitk_gemm")
+    # the ring kernel (dynamic claims from the plan's counter, reset by its
+    # last CTA) with the register-staged kernel beside it: index_add and the
+    # scatter-reduce behind an unwaited plan, the same plan reused each time
+    ec = small_case("embedding_backward")
+    eplan = dr.det_reduce_plan(ec.idx, ec.M)
+    einit = torch.randn(ec.M, ec.H, device=DEV)
+    ering = replay.identical(lambda: dr.det_index_add(eplan, ec.x, einit.clone(), opts={"gather_path": 3}),
+                             name="index_add ring")
+    eref = dr.det_index_add(eplan, ec.x, einit.clone(), opts={"gather_path": 1})
+    assert_bytes_equal(np_bits(ering), np_bits(eref), "ring replay")
+    aplan = dr.det_reduce_plan(ec.idx, ec.M, opts={"async_plan": 1})
+    dr.det_plan_status(aplan)
+
+    def ring_scatter():
+        return dr.det_scatter_reduce(aplan, ec.x, torch.empty(ec.M, ec.H, device=DEV),
+                                     opts={"async_plan": 1, "gather_path": 3})
+    sring = replay.identical(ring_scatter, name="scatter ring")
+    sref = dr.det_scatter_reduce(eplan, ec.x, torch.empty(ec.M, ec.H, device=DEV), opts={"gather_path": 1})
+    assert_bytes_equal(np_bits(sring), np_bits(sref), "ring scatter replay")
+
+
+def test_ring_kernel_edge_cases():
+    """The ring kernel at its limits: destinations of exactly 32 terms and of
+    1 term in one plan (the widest and the narrowest items), H that leaves a
+    ragged last tile, a grid larger than the units, and many calls on one plan
+    (the claim counter must be back at 0 after each call)."""
+    M, H = 300, 1048  # bf16 rows of 2096 bytes: 32-term items are split into tiles, the last one ragged
+    lens = np.where(np.arange(M) % 3 == 0, 32, np.where(np.arange(M) % 3 == 1, 1, 0))
+    idx_np = np.repeat(np.arange(M, dtype=np.int32), lens)
+    np.random.default_rng(7).shuffle(idx_np)
+    g = torch.Generator(device=DEV).manual_seed(8)
+    x = torch.randn(idx_np.size, H, generator=g, device=DEV).to(torch.bfloat16)
+    idx = torch.from_numpy(idx_np).to(DEV)
+    plan = dr.det_reduce_plan(idx, M)
+    want = oracle.scatter_reduce(idx_np, np_bits(x), M)
+    for grid in (0, 1, 7, 1000):
+        for rep in range(3):
+            out = torch.full((M, H), 5.0, device=DEV)
+            dr.det_scatter_reduce(plan, x, out, opts={"gather_path": 3, "grid_ctas": grid, "debug_checks": 1})
+            assert_bytes_equal(np_bits(out), want, f"ring grid={grid} rep={rep}")
+    init = torch.randn(M, H, generator=g, device=DEV)
+    want_a = oracle.scatter_reduce(idx_np, np_bits(x), M, out_init=np_bits(init))
+    for rep in range(3):
+        out = init.clone()
+        dr.det_index_add(plan, x, out, opts={"gather_path": 3, "debug_checks": 1})
+        assert_bytes_equal(np_bits(out), want_a, f"ring index_add rep={rep}")
 
 
 @pytest.mark.parametrize("P", [1, 2, 4, 8])

@@ -26,7 +26,8 @@ MANIFEST = {
                    "test_segment_size_changes_no_bit", "test_index_add_matches_oracle"]),
     "gather_async.cu": (["gather_async_kernel"], ["test_gather_path_changes_no_bit"]),
     "gather_bulk.cu": (["gather_bulk_kernel", "gather_ring_kernel"],
-                       ["test_gather_path_changes_no_bit", "test_index_add_bulk_ring_matches_oracle"]),
+                       ["test_gather_path_changes_no_bit", "test_index_add_bulk_ring_matches_oracle",
+                        "test_ring_kernel_edge_cases"]),
     "hash.cu": (["hash_kernel"], ["test_hash_matches_oracle"]),
     "noalloc.cu": (None, "launches the gather and finish kernels of gather.cu; "
                          "test_noalloc_matches_workspace_entry_point_twice"),
