@@ -637,6 +637,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
         rb.totals0 = totals;
         rb.totals1 = reinterpret_cast<int*>(ws + L.rx_tot1);
         rb.packed = reinterpret_cast<int*>(ws + L.k32_tmp);
+        rb.lowd = ws + L.skeys;  // 4N bytes, unused by this method
         rb.perm = perm;
         rb.rowcnt = reinterpret_cast<int*>(ws + L.rstart);
         rb.btot = reinterpret_cast<int*>(ws + L.rx_btot);

@@ -88,6 +88,7 @@ struct RadixBuffers {
     int* totals0;    // [256]
     int* totals1;    // [256]
     int* packed;     // [N]
+    unsigned char* lowd;  // [N], 16-byte aligned: the low digit of each packed word
     int* perm;       // [N]
     int* rowcnt;     // [M]
     int* btot;       // [plan_radix_blocks(M) * 8]

@@ -23,12 +23,11 @@
 //                        order), stages them in shared memory in (digit,
 //                        position) order and writes them in runs.  The first
 //                        of two passes writes packed words (high digit << 24 |
-//                        source), so the second reads 4 bytes per source; the
-//                        last pass writes perm, and since its staged words are
-//                        in destination order it also adds each run of one
-//                        destination to that destination's row counter (the
-//                        low digit of a word follows from its position in the
-//                        first pass's output);
+//                        source), so the second reads 4 bytes per source, and
+//                        beside each word its low digit (one byte); the last
+//                        pass writes perm, and since its staged words are in
+//                        destination order it also adds each run of one
+//                        destination to that destination's row counter;
 //   rx_units_count_kernel, rx_units_write_kernel
 //                        row_ptr and the work list from the row counters:
 //                        class totals per block of 1024 destinations, then
@@ -178,15 +177,17 @@ rx_offset_kernel(int* __restrict__ counts, int ntiles, int* __restrict__ totals,
 // ------------------------------------------------------------------------
 
 // MODE 0: words are idx; the digit is the low byte; the output (first of two
-// passes) is (high byte << 24 | source), or (single pass, M <= 256) perm.
-// MODE 1: words are packed; the digit is the top byte; the output is perm.
+// passes) is (high byte << 24 | source) with the low byte in lowd at the same
+// position, or (single pass, M <= 256) perm.
+// MODE 1: words are packed; the digit is the top byte; lowd holds each word's
+// low byte; the output is perm.
 // LAST: the output is perm and the staged runs of equal destinations are
 // added to rowcnt.  Warp w owns words [w*32*ITEMS, (w+1)*32*ITEMS) of the
 // tile, item k of lane l being word w*32*ITEMS + k*32 + l.
 struct RxScatterShared {
     unsigned int sval[kRxTile];      // staged output words, in (digit, position) order
     unsigned short skey[kRxTile];    // staged destinations (LAST), or staged digits (first of two passes)
-    unsigned char lomap[kRxTile];    // MODE 1: the low digit of each input word of the tile
+    unsigned char lomap[kRxTile];    // MODE 1: the low digit of each input word of the tile (from lowd)
     int whist[kRxWarps * kRxRadix];  // per warp running digit counts, then warp offsets
     int tstart[kRxRadix];            // first staged position of each digit
     int gbase[kRxRadix];             // global position of staged position 0 of each digit
@@ -197,7 +198,7 @@ struct RxScatterShared {
 template <int MODE, bool LAST, bool FULL>
 __device__ __forceinline__ void rx_scatter_tile(RxScatterShared& S, const int* __restrict__ in, int N,
                                                 unsigned int* __restrict__ out, const int* __restrict__ offsets,
-                                                const int* __restrict__ totals, const int* __restrict__ totals0,
+                                                const int* __restrict__ totals, unsigned char* __restrict__ lowd,
                                                 int ntiles, int* __restrict__ rowcnt)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -219,38 +220,16 @@ __device__ __forceinline__ void rx_scatter_tile(RxScatterShared& S, const int* _
     const int dstart = block_excl_scan<kRxThreads>(tot_d, S.ws, &total_unused);  // orders the whist zeroing
     S.gbase[tid] = dstart + off_d;
     if (MODE == 1) {
-        // low digit of input word p = the first pass's digit bucket holding p:
-        // mark where each bucket starts inside this tile, then a running max
-        const int t0 = totals0[tid];
-        const int s0 = block_excl_scan<kRxThreads>(t0, S.ws, &total_unused);
-        if (t0 > 0 && s0 + t0 > base && s0 < base + kRxTile) S.lomap[s0 > base ? s0 - base : 0] = static_cast<unsigned char>(tid);
-        __syncthreads();
-        // thread t owns entries [16t, 16t+16): inclusive max scan over the tile
-        uint4 q = reinterpret_cast<const uint4*>(S.lomap)[tid];
-        unsigned char e[16];
-        *reinterpret_cast<uint4*>(e) = q;
-        int run = 0;
+        // the low digit of each input word, written beside it by the first
+        // pass (16-byte loads from the 16-byte aligned array; the tail of
+        // the last tile byte by byte, none past N)
+        const int b0 = base + 16 * tid;
+        if (FULL || b0 + 15 < N) {
+            reinterpret_cast<uint4*>(S.lomap)[tid] = *reinterpret_cast<const uint4*>(lowd + b0);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            run = max(run, static_cast<int>(e[j]));
-            e[j] = static_cast<unsigned char>(run);
+            for (int j = 0; j < 16; ++j) S.lomap[16 * tid + j] = b0 + j < N ? lowd[b0 + j] : 0;
         }
-        // carry in: the max over the threads before this one (a block max scan)
-        int incl = run;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl = max(incl, t);
-        }
-        if (lane == 31) S.ws[warp] = incl;
-        __syncthreads();
-        int carry = 0;
-        for (int q2 = 0; q2 < warp; ++q2) carry = max(carry, S.ws[q2]);
-        const int prev = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane > 0) carry = max(carry, prev);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) e[j] = static_cast<unsigned char>(max(static_cast<int>(e[j]), carry));
-        reinterpret_cast<uint4*>(S.lomap)[tid] = *reinterpret_cast<uint4*>(e);
         __syncthreads();
     }
 
@@ -300,7 +279,7 @@ __device__ __forceinline__ void rx_scatter_tile(RxScatterShared& S, const int* _
             const int pos = S.tstart[d] + S.whist[warp * kRxRadix + d] + rank[k];
             if (MODE == 0 && !LAST) {
                 S.sval[pos] = ((w >> 8) << 24) | static_cast<unsigned int>(p);  // w < M <= 65536, p < 2^24
-                S.skey[pos] = static_cast<unsigned short>(d);
+                S.skey[pos] = static_cast<unsigned short>(d);  // the low digit, written beside the word
             } else if (MODE == 0) {
                 S.sval[pos] = static_cast<unsigned int>(p);
                 S.skey[pos] = static_cast<unsigned short>(d);  // the destination itself (M <= 256)
@@ -321,6 +300,7 @@ __device__ __forceinline__ void rx_scatter_tile(RxScatterShared& S, const int* _
             key = S.skey[i];
             const int d = LAST && MODE == 1 ? static_cast<int>(key >> 8) : static_cast<int>(key);
             out[S.gbase[d] + i] = S.sval[i];  // in [0, N)
+            if (MODE == 0 && !LAST) lowd[S.gbase[d] + i] = static_cast<unsigned char>(d);
         }
         if (LAST) {
             // runs of one destination inside this warp's 32 staged words: one
@@ -342,7 +322,7 @@ __device__ __forceinline__ void rx_scatter_tile(RxScatterShared& S, const int* _
 template <int MODE, bool LAST>
 __global__ void __launch_bounds__(kRxThreads, 4)
 rx_scatter_kernel(const int* __restrict__ in, int N, unsigned int* __restrict__ out, const int* __restrict__ offsets,
-                  const int* __restrict__ totals, const int* __restrict__ totals0, int ntiles,
+                  const int* __restrict__ totals, unsigned char* __restrict__ lowd, int ntiles,
                   int* __restrict__ rowcnt, const int* __restrict__ counters)
 {
     extern __shared__ __align__(16) unsigned char rx_smem[];
@@ -350,17 +330,14 @@ rx_scatter_kernel(const int* __restrict__ in, int N, unsigned int* __restrict__ 
     const int tid = threadIdx.x;
     pdl_launch_dependents();
     for (int i = tid; i < kRxWarps * kRxRadix; i += kRxThreads) S.whist[i] = 0;
-    if (MODE == 1) {
-        for (int i = tid; i < kRxTile / 16; i += kRxThreads) reinterpret_cast<uint4*>(S.lomap)[i] = make_uint4(0, 0, 0, 0);
-    }
     pdl_wait();  // the previous kernels' counts, offsets and words are visible
     // with an id out of range the row counters would be indexed out of range:
     // the last pass writes nothing (the plan reports the error)
     if (LAST && counters[kCtrErrIndex]) return;
     if ((static_cast<long long>(blockIdx.x) + 1) * kRxTile <= N)  // uniform over the CTA
-        rx_scatter_tile<MODE, LAST, true>(S, in, N, out, offsets, totals, totals0, ntiles, rowcnt);
+        rx_scatter_tile<MODE, LAST, true>(S, in, N, out, offsets, totals, lowd, ntiles, rowcnt);
     else
-        rx_scatter_tile<MODE, LAST, false>(S, in, N, out, offsets, totals, totals0, ntiles, rowcnt);
+        rx_scatter_tile<MODE, LAST, false>(S, in, N, out, offsets, totals, lowd, ntiles, rowcnt);
 }
 
 // ------------------------------------------------------------------------
@@ -533,7 +510,7 @@ det_status launch_plan_radix(const int32_t* idx, int64_t N, int64_t M, int g, co
         { const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(k0), smem); if (a_) return a_; }
         DETR_CUDA(launch_after_previous(k0, dim3(ntiles), dim3(kRxThreads), smem, st, static_cast<const int*>(idx), n,
                                         reinterpret_cast<unsigned int*>(b.packed), static_cast<const int*>(b.counts),
-                                        static_cast<const int*>(b.totals0), no_bad, ntiles, no_i,
+                                        static_cast<const int*>(b.totals0), b.lowd, ntiles, no_i,
                                         static_cast<const int*>(b.counters)));
         DETR_LAUNCHED();
         // pass 1: the high byte, from the packed words (16-byte aligned in the workspace)
@@ -548,16 +525,15 @@ det_status launch_plan_radix(const int32_t* idx, int64_t N, int64_t M, int g, co
         DETR_CUDA(launch_after_previous(k1, dim3(ntiles), dim3(kRxThreads), smem, st,
                                         static_cast<const int*>(b.packed), n, reinterpret_cast<unsigned int*>(b.perm),
                                         static_cast<const int*>(b.counts), static_cast<const int*>(b.totals1),
-                                        static_cast<const int*>(b.totals0), ntiles, b.rowcnt,
-                                        static_cast<const int*>(b.counters)));
+                                        b.lowd, ntiles, b.rowcnt, static_cast<const int*>(b.counters)));
         DETR_LAUNCHED();
     } else {
         auto k0 = rx_scatter_kernel<0, true>;
         { const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(k0), smem); if (a_) return a_; }
         DETR_CUDA(launch_after_previous(k0, dim3(ntiles), dim3(kRxThreads), smem, st, static_cast<const int*>(idx), n,
                                         reinterpret_cast<unsigned int*>(b.perm), static_cast<const int*>(b.counts),
-                                        static_cast<const int*>(b.totals0), no_bad, ntiles, b.rowcnt,
-                                        static_cast<const int*>(b.counters)));
+                                        static_cast<const int*>(b.totals0), static_cast<unsigned char*>(nullptr),
+                                        ntiles, b.rowcnt, static_cast<const int*>(b.counters)));
         DETR_LAUNCHED();
     }
     const unsigned int nblk = static_cast<unsigned int>(cdiv(M, kRxUnitThreads));
