@@ -96,6 +96,25 @@ __device__ __forceinline__ void bulk_store(void* base, long long off, const floa
     }
 }
 
+// Tiling of rows of H elements for destinations of at most `terms` terms:
+// the fewest H-tiles of at most 8 KB whose staged rows fit one stage (the
+// host's bulk_plan_tiles, for a plan whose counts are on the device).
+__device__ __forceinline__ bool bulk_tiles_dev(int H, int xsz, int terms, int* te, int* stride, int* nt)
+{
+    const long long row_bytes = static_cast<long long>(H) * xsz;
+    for (int k = 1; k <= 64; ++k) {
+        const long long tb = ((row_bytes + k - 1) / k + 15) / 16 * 16;
+        if (tb > 16LL * kBulkConsumers * kBulkVecPerThread) continue;
+        const long long st = (tb + 127) / 128 * 128;
+        if (st * terms > kBulkStageBytes) continue;
+        *te = static_cast<int>(tb / xsz);
+        *stride = static_cast<int>(st);
+        *nt = static_cast<int>((H + *te - 1) / *te);
+        return true;
+    }
+    return false;
+}
+
 template <typename XT, typename OT>
 __global__ void __launch_bounds__(kBulkThreads, 1)
 gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ ShardTable tbl)
@@ -114,6 +133,8 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
     volatile int* abort_flag = reinterpret_cast<volatile int*>(pu_mnt + kPipeSlots * 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ long long s_items;
+    __shared__ int s_tile[3];  // elements, staged stride, tiles per row
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBulkStages; ++s) {
             mbar_init(&full[s], 1);
@@ -121,10 +142,24 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        long long ni = a.n_items;
+        int te = a.tile_elems, st = a.tile_stride, nt = a.ntiles;
+        if (a.dev_counters) {  // written by the plan's kernels, which finished before this grid started
+            const int* c = a.dev_counters;
+            ni = 0;
+            if (!(c[kCtrErrIndex] | c[kCtrErrDup] | c[kCtrErrTimeout]) && c[kCtrMaxLen] <= kBulkMaxTerms &&
+                bulk_tiles_dev(a.H, static_cast<int>(sizeof(XT)), max(1, c[kCtrMaxLen]), &te, &st, &nt))
+                ni = static_cast<long long>(c[kCtrShort] + c[kCtrEmpty]) * nt;  // every unit: none is longer
+        }
+        s_items = ni;
+        s_tile[0] = te;
+        s_tile[1] = st;
+        s_tile[2] = nt;
     }
     __syncthreads();
 
-    const long long n_items = a.n_items;
+    const long long n_items = s_items;
+    const int tile_elems = s_tile[0], tile_stride = s_tile[1], ntiles = s_tile[2];
     if (warp == kBulkConsumerWarps) {
         // ---------------- producer warp ----------------
         // Item k of this CTA is blockIdx.x + k * gridDim.x.  Nothing the
@@ -141,7 +176,7 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
         auto item_of = [&](long long j) { return blockIdx.x + j * g; };
         auto list_m = [&](long long b) -> int {  // lane l: the list entry of item 32 b + l, or -1
             const long long it = item_of(32 * b + lane);
-            return it < n_items ? a.units[it / a.ntiles].x : -1;
+            return it < n_items ? a.units[it / ntiles].x : -1;
         };
         // A: the batch being entered; X: the next (bounds issued one batch
         // ago); Y: the one after (list entries)
@@ -167,7 +202,7 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
             if (lane == 0) {
                 pu_mnt[3 * sl] = m;
                 pu_mnt[3 * sl + 1] = n;
-                pu_mnt[3 * sl + 2] = a.ntiles == 1 ? 0 : static_cast<int>(item_of(q) % a.ntiles);
+                pu_mnt[3 * sl + 2] = ntiles == 1 ? 0 : static_cast<int>(item_of(q) % ntiles);
             }
             if (lane < n) cp_async4(&pu_perm[sl * 32 + lane], a.perm + lo + lane);
         };
@@ -201,15 +236,15 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
                 if (lane == 0) { *abort_flag = 1; atomicOr(a.status + kCtrErrTimeout, 1); }
                 break;
             }
-            const int col0 = ct * a.tile_elems;
-            const int bytes = min(a.tile_elems, a.H - col0) * static_cast<int>(sizeof(XT));
+            const int col0 = ct * tile_elems;
+            const int bytes = min(tile_elems, a.H - col0) * static_cast<int>(sizeof(XT));
             if (lane < cn) swt[s * kBulkMaxTerms + lane] = rw;
             if (lane == 0) meta[s] = BulkStageMeta{cm, cn, col0, bytes};
             __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cn * bytes));
             __syncwarp();
             if (lane < cn)
-                bulk_g2s(stage_buf + static_cast<size_t>(s) * kBulkStageBytes + static_cast<size_t>(lane) * a.tile_stride,
+                bulk_g2s(stage_buf + static_cast<size_t>(s) * kBulkStageBytes + static_cast<size_t>(lane) * tile_stride,
                          shard_row(tbl, ri, a.ldx_bytes) + static_cast<long long>(col0) * sizeof(XT),
                          static_cast<uint32_t>(bytes), &full[s]);
             fetch_w(k + kPipeWAhead);
@@ -245,7 +280,7 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;  // empty destination: +0.0
                 for (int j = 0; j < md.n; ++j) {
-                    const uint4 raw = *reinterpret_cast<const uint4*>(buf + static_cast<size_t>(j) * a.tile_stride + v * 16);
+                    const uint4 raw = *reinterpret_cast<const uint4*>(buf + static_cast<size_t>(j) * tile_stride + v * 16);
                     float xf[VEC];
                     BV::expand(raw, xf);
                     if (a.w) {

@@ -36,6 +36,8 @@ struct GatherArgs {
     long long ldpart;
     const int* dev_counters;  // non-null: read the work counts (and plan errors) from the device
     int accumulate;           // add to out (index_add_); destinations without terms stay untouched
+    int only_long;            // behind the fixed-stage bulk kernel of an unwaited plan: no work unless some
+                              // destination has more than 32 terms (the bulk kernel did nothing then)
     int beside_ring;          // beside the ring kernel, which takes the one-chunk units: only the units of
                               // more than one chunk, and the wait for the previous grid (the ring kernel;
                               // everything before it had finished when it started) at the end
@@ -53,6 +55,10 @@ __device__ __forceinline__ bool task_counts(const GatherArgs& a, long long* n_ta
         if (c[kCtrErrIndex] | c[kCtrErrDup] | c[kCtrErrTimeout]) return false;
         *n_seg = c[kCtrBig];
         // index_add_ has nothing to do for the empty destinations (listed last)
+        if (a.only_long && c[kCtrMaxLen] <= kChunk) {
+            *n_tasks = 0;
+            return true;
+        }
         *n_tasks = static_cast<long long>(c[kCtrBig]) * a.seg_tile_groups +
                    (a.beside_ring ? 0LL
                                   : static_cast<long long>(c[kCtrShort] + (a.accumulate ? 0 : c[kCtrEmpty])) *
@@ -82,6 +88,8 @@ struct BulkArgs {
     void* out;
     long long ldo;
     int* status;           // counter block; kCtrErrTimeout is set if a bounded wait expires
+    const int* dev_counters;  // non-null (plan that did not wait): the items and the tiling follow from the
+                              // counter block; none when some destination has more than 32 terms
 };
 
 // Task -> (unit, first and one-past-last H-tile): the units of more than one

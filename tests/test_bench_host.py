@@ -42,7 +42,7 @@ def test_cpu_baseline_host_record_and_pinning():
 
 
 def _rank(n, ms, fp=7):
-    return {"ms_step": ms, "ms_red": ms / 2, "ms_auto": ms / 2, "ms_atom": ms / 3, "launches": n, "wall_ms_per_step": ms * 1.1,
+    return {"ms_step": ms, "ms_red": ms / 2, "ms_reg": ms / 2, "ms_atom": ms / 3, "launches": n, "wall_ms_per_step": ms * 1.1,
             "fingerprint": fp}
 
 
