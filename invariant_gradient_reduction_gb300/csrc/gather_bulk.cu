@@ -25,9 +25,22 @@ namespace detr {
 constexpr int kBulkConsumerWarps = 16;
 constexpr int kBulkConsumers = kBulkConsumerWarps * 32;
 constexpr int kBulkThreads = kBulkConsumers + 32;
-constexpr int kBulkStages = 3;
-constexpr int kBulkStageBytes = 64 * 1024;
+#ifndef DETR_BULK_STAGES
+#define DETR_BULK_STAGES 3
+#endif
+#ifndef DETR_BULK_STAGE_KB
+#define DETR_BULK_STAGE_KB 64
+#endif
+constexpr int kBulkStages = DETR_BULK_STAGES;
+constexpr int kBulkStageBytes = DETR_BULK_STAGE_KB * 1024;
 constexpr int kBulkMaxTerms = 32;
+// Producer warps of the fixed-stage kernel: items alternate between them
+// when a CTA has at least kBulkTwoProducerItems items (EP-invariance, ~215
+// items per CTA: 303 against 306.5 us); with fewer one producer works alone
+// (MoE combine, 27 items per CTA: 52.2 us with two, 51.4 with one).
+constexpr int kBulkProducers = 2;
+constexpr int kBulkTwoProducerItems = 64;
+constexpr int kBulkStageThreads = kBulkConsumers + 32 * kBulkProducers;
 // The producers' unit pipeline: perm entries copied into shared memory
 // kPipePermAhead units (items) ahead, weights kPipeWAhead ahead, in
 // kPipeSlots slots.
@@ -116,7 +129,7 @@ __device__ __forceinline__ bool bulk_tiles_dev(int H, int xsz, int terms, int* t
 }
 
 template <typename XT, typename OT>
-__global__ void __launch_bounds__(kBulkThreads, 1)
+__global__ void __launch_bounds__(kBulkStageThreads, 1)
 gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ ShardTable tbl)
 {
     using BV = BulkVec<XT>;
@@ -127,14 +140,14 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
     uint64_t* empty = full + kBulkStages;
     float* swt = reinterpret_cast<float*>(empty + kBulkStages);            // [kBulkStages][32]
     BulkStageMeta* meta = reinterpret_cast<BulkStageMeta*>(swt + kBulkStages * kBulkMaxTerms);
-    int* pu_perm = reinterpret_cast<int*>(meta + kBulkStages);              // producer's item pipeline [kPipeSlots][32]
-    float* pu_w = reinterpret_cast<float*>(pu_perm + kPipeSlots * 32);     // [kPipeSlots][32]
-    int* pu_mnt = reinterpret_cast<int*>(pu_w + kPipeSlots * 32);          // [kPipeSlots][3]: destination, terms, tile
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(pu_mnt + kPipeSlots * 3);
+    // each producer's item pipeline: perm [kPipeSlots][32], weights [kPipeSlots][32], (destination, terms, tile) [kPipeSlots][3]
+    int* pu_base = reinterpret_cast<int*>(meta + kBulkStages);
+    constexpr int kPuInts = kPipeSlots * (32 + 32 + 3);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(pu_base + kBulkProducers * kPuInts);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ long long s_items;
-    __shared__ int s_tile[3];  // elements, staged stride, tiles per row
+    __shared__ int s_tile[4];  // elements, staged stride, tiles per row, producers
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBulkStages; ++s) {
             mbar_init(&full[s], 1);
@@ -155,15 +168,22 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
         s_tile[0] = te;
         s_tile[1] = st;
         s_tile[2] = nt;
+        s_tile[3] = ni >= static_cast<long long>(kBulkTwoProducerItems) * gridDim.x ? kBulkProducers : 1;
     }
     __syncthreads();
 
     const long long n_items = s_items;
-    const int tile_elems = s_tile[0], tile_stride = s_tile[1], ntiles = s_tile[2];
-    if (warp == kBulkConsumerWarps) {
-        // ---------------- producer warp ----------------
-        // Item k of this CTA is blockIdx.x + k * gridDim.x.  Nothing the
-        // producer waits for per item is a load issued for that item: the
+    const int tile_elems = s_tile[0], tile_stride = s_tile[1], ntiles = s_tile[2], nprod = s_tile[3];
+    if (warp >= kBulkConsumerWarps) {
+        // ---------------- producer warps ----------------
+        // Item k of this CTA is blockIdx.x + k * gridDim.x; producer pw of
+        // nprod issues the items k = pw, pw + nprod, ... (its item j is k =
+        // j * nprod + pw) into stage k % kBulkStages, so that the
+        // stages fill in item order, as the consumers take them.  One
+        // producer warp had spent ~1 us of its own instructions per 64 KB
+        // item (27 items per CTA on the MoE combine), waiting for a free
+        // stage only a third of its time.  Nothing a producer waits for per
+        // item is a load issued for that item: the
         // list entries are read in batches of 32 items (lane l = item 32b +
         // l), a batch's entries two batches ahead and their row_ptr bounds
         // one batch ahead; each item's perm entries are copied into a
@@ -172,9 +192,14 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
         // ring of registers shifted one slot per item had made every item
         // wait for the loads issued one item before: the producer issued an
         // item every ~1.7 us and waited for a free stage 4% of the time.
+        const int pw = warp - kBulkConsumerWarps;
+        if (pw >= nprod) return;
+        int* pu_perm = pu_base + pw * kPuInts;
+        float* pu_w = reinterpret_cast<float*>(pu_perm + kPipeSlots * 32);
+        int* pu_mnt = pu_perm + kPipeSlots * 64;
         const long long g = gridDim.x;
-        auto item_of = [&](long long j) { return blockIdx.x + j * g; };
-        auto list_m = [&](long long b) -> int {  // lane l: the list entry of item 32 b + l, or -1
+        auto item_of = [&](long long j) { return blockIdx.x + (j * nprod + pw) * g; };
+        auto list_m = [&](long long b) -> int {  // lane l: the list entry of this producer's item 32 b + l, or -1
             const long long it = item_of(32 * b + lane);
             return it < n_items ? a.units[it / ntiles].x : -1;
         };
@@ -221,10 +246,11 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
             enter(j + kPipePermAhead);
             cp_async_commit_group();
         }
-        for (long long k = 0; item_of(k) < n_items; ++k) {
+        for (long long j = 0; item_of(j) < n_items; ++j) {
             cp_async_wait_pending<kPipeWAhead - 1>();
             __syncwarp();
-            const int sl = static_cast<int>(k % kPipeSlots);
+            const int sl = static_cast<int>(j % kPipeSlots);
+            const long long k = j * nprod + pw;  // the CTA's item index: its stage and phase
             const int cm = pu_mnt[3 * sl], cn = pu_mnt[3 * sl + 1], ct = pu_mnt[3 * sl + 2];
             const int ri = lane < cn ? pu_perm[sl * 32 + lane] : 0;
             const float rw = a.w && lane < cn ? pu_w[sl * 32 + lane] : 1.0f;
@@ -247,8 +273,8 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
                 bulk_g2s(stage_buf + static_cast<size_t>(s) * kBulkStageBytes + static_cast<size_t>(lane) * tile_stride,
                          shard_row(tbl, ri, a.ldx_bytes) + static_cast<long long>(col0) * sizeof(XT),
                          static_cast<uint32_t>(bytes), &full[s]);
-            fetch_w(k + kPipeWAhead);
-            enter(k + kPipePermAhead);
+            fetch_w(j + kPipeWAhead);
+            enter(j + kPipePermAhead);
             cp_async_commit_group();
         }
         cp_async_wait_pending<0>();  // no copy into shared memory outlives the kernel
@@ -321,7 +347,7 @@ static det_status launch_bulk_t(const BulkArgs& a, const ShardTable& t, int grid
         const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(gather_bulk_kernel<XT, OT>), smem);
         if (a_) return a_;
     }
-    gather_bulk_kernel<XT, OT><<<grid, kBulkThreads, smem, st>>>(a, t);
+    gather_bulk_kernel<XT, OT><<<grid, kBulkStageThreads, smem, st>>>(a, t);
     DETR_LAUNCHED();
     return DET_OK;
 }
@@ -330,7 +356,7 @@ size_t bulk_smem_bytes()
 {
     return static_cast<size_t>(kBulkStages) * kBulkStageBytes + 2 * kBulkStages * sizeof(uint64_t) +
            kBulkStages * kBulkMaxTerms * sizeof(float) + kBulkStages * sizeof(BulkStageMeta) +
-           kPipeSlots * 32 * (sizeof(int) + sizeof(float)) + kPipeSlots * 3 * sizeof(int) + 16;
+           static_cast<size_t>(kBulkProducers) * kPipeSlots * (32 + 32 + 3) * sizeof(int) + 16;
 }
 
 bool bulk_plan_tiles(int64_t H, int xsz, int64_t max_terms, int* tile_elems, int* tile_stride, int* ntiles)
