@@ -616,7 +616,11 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
         const int64_t max_row = dev_counts ? plan->N : plan->max_row_len;
         const long long items = dev_counts ? (cdiv(plan->N, (int64_t(kChunk) << plan->g) + 1) + 1) * H
                                            : plan->n_hot_rows * H;
-        const int64_t fgrid64 = dev_counts ? std::min<int64_t>(cdiv(items, kFinishThreads), int64_t(sms) * 16)
+        // behind the fixed-stage kernel it has work only when some row is
+        // longer than 32 terms (then it loops over its grid): a small grid
+        // ends sooner when it has none
+        const int64_t fcap = int64_t(sms) * (use_bulk_dev ? 2 : 16);
+        const int64_t fgrid64 = dev_counts ? std::min<int64_t>(cdiv(items, kFinishThreads), fcap)
                                            : cdiv(items, kFinishThreads);
         const unsigned int fgrid = static_cast<unsigned int>(std::max<int64_t>(1, fgrid64));
         const int64_t max_segs = cdiv(cdiv(max_row, kChunk), G);

@@ -174,6 +174,10 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
 
     const long long n_items = s_items;
     const int tile_elems = s_tile[0], tile_stride = s_tile[1], ntiles = s_tile[2], nprod = s_tile[3];
+    // the next kernel may be launched now: behind an unwaited plan the
+    // register-staged kernel, which waits for this grid before it reads
+    // anything (its launch then overlaps this kernel, not its end)
+    pdl_launch_dependents();
     if (warp >= kBulkConsumerWarps) {
         // ---------------- producer warps ----------------
         // Item k of this CTA is blockIdx.x + k * gridDim.x; producer pw of
