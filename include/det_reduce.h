@@ -101,12 +101,14 @@ typedef int32_t det_dtype;
  *                   multiple of 16 bytes, a byte ring in shared memory for
  *                   the destinations of at most one chunk (also behind a
  *                   plan that did not wait), the longer ones on the
- *                   register-staged kernel beside it.  Auto, for one shard
- *                   of rows of at least 1 KB: the first where it applies;
+ *                   register-staged kernel beside it.  Auto, for rows of
+ *                   at least 1 KB in one shard (in several shards, from 64
+ *                   destination tiles per SM): the first where it applies;
  *                   behind a plan that did not wait, the first with its
  *                   tiling read from the device when every destination turns
  *                   out to have at most 32 terms, else path 1 after it; the
- *                   ring when the sources are at least 1 GiB; else path 1.
+ *                   ring (one shard) when the sources are at least 1 GiB;
+ *                   else path 1.
  *                   A path that does not apply fails with
  *                   DET_ERR_UNSUPPORTED.  Every path gives the same bits.
  *  tiles_per_task   0 = auto; > 0 = H-tiles one warp task of the warp kernels

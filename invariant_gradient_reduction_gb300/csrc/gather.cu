@@ -458,10 +458,12 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
     const bool bulk_ok = vec && !dev_counts && !accumulate && plan->max_row_len <= 32 && H * xsz >= 1024 &&
                          plan->n_units > 0 &&
                          bulk_plan_tiles(H, xsz, plan->max_row_len, &tile_elems, &tile_stride, &bulk_tiles);
-    // with sources in several shards its one producer warp also looks up each
-    // term's shard, on its critical path (EP-invariance, 8 shards: 347 against
-    // 335 us for the register-staged kernel): auto takes it for one shard only
-    const bool bulk_auto = bulk_ok && P == 1;
+    // with sources in several shards a producer warp also looks up each
+    // term's shard: one alone fell behind (EP-invariance, 8 shards: 347
+    // against 335 us for the register-staged kernel), two keep up (309
+    // against 335 us), so auto takes it for shards where the kernel runs two
+    const bool bulk_auto =
+        bulk_ok && (P == 1 || plan->n_units * bulk_tiles >= static_cast<int64_t>(kBulkTwoProducerItems) * sms);
     // The ring kernel: the destinations of at most one chunk (for index_add_
     // the ones with terms: 1..32; for the scatter-reduce also the empty ones,
     // which it writes as +0.0) are TMA-staged into a byte ring of shared
@@ -493,7 +495,8 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
     // 66.6 us, against 68.6 us on the register-staged kernel and 71 us on the
     // ring; EP-invariance step: 329 against 353 and 333 us.
     int te32 = 0, st32 = 0, nt32 = 0;
-    const bool bulk_dev_auto = !accumulate && dev_counts && vec && P == 1 && H * xsz >= 1024 && M > 0 &&
+    const bool bulk_dev_auto = !accumulate && dev_counts && vec && H * xsz >= 1024 && M > 0 &&
+                               (P == 1 || M >= static_cast<int64_t>(kBulkTwoProducerItems) * sms) &&
                                bulk_plan_tiles(H, xsz, kChunk, &te32, &st32, &nt32);
     bool use_bulk = false, use_ring = false, use_bulk_dev = false;
     if (path == 3) {

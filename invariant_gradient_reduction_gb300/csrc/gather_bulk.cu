@@ -39,7 +39,6 @@ constexpr int kBulkMaxTerms = 32;
 // items per CTA: 303 against 306.5 us); with fewer one producer works alone
 // (MoE combine, 27 items per CTA: 52.2 us with two, 51.4 with one).
 constexpr int kBulkProducers = 2;
-constexpr int kBulkTwoProducerItems = 64;
 constexpr int kBulkStageThreads = kBulkConsumers + 32 * kBulkProducers;
 // The producers' unit pipeline: perm entries copied into shared memory
 // kPipePermAhead units (items) ahead, weights kPipeWAhead ahead, in

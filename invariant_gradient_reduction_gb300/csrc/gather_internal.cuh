@@ -121,6 +121,11 @@ __device__ __forceinline__ int4 unit_at(const GatherArgs& a, long long u, long l
     return u < n_seg ? a.seg_units[u] : a.row_units[u - n_seg];
 }
 
+// The fixed-stage kernel runs two producer warps from this many items per CTA
+// (one below); with sources in several shards only two keep up with the
+// per-term shard lookups, so auto takes it for shards from there.
+constexpr int kBulkTwoProducerItems = 64;
+
 size_t bulk_smem_bytes();
 // Tile a row of H elements so that max_terms staged tiles fit one stage; false if not possible.
 bool bulk_plan_tiles(int64_t H, int xsz, int64_t max_terms, int* tile_elems, int* tile_stride, int* ntiles);
