@@ -73,10 +73,17 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
     const long long seg_terms = static_cast<long long>(kChunk) << a.g;
 
     const long long nwarps = static_cast<long long>(gridDim.x) * kGatherWarps;
-    if (!BESIDE) pdl_wait();    // the plan (or whatever wrote x and w) has finished
-    pdl_launch_dependents();    // the hot-destination pass may be launched now
+    // Behind the fixed-stage kernel (only_long) the counts are the plan's,
+    // which had finished before that kernel started: they are read before
+    // the wait for it, so that a launch with nothing to do ends as soon as
+    // that kernel does.  Every launch waits for the grid before it, at the
+    // latest before it ends.
+    if (!BESIDE && !a.only_long) pdl_wait();  // the plan (or whatever wrote x and w) has finished
+    pdl_launch_dependents();                  // the hot-destination pass may be launched now
     long long n_tasks, n_seg;
-    if (!task_counts(a, &n_tasks, &n_seg)) {
+    const bool counted = task_counts(a, &n_tasks, &n_seg);
+    if (!BESIDE && a.only_long) pdl_wait();
+    if (!counted) {
         if (BESIDE) pdl_wait();
         return;
     }
@@ -211,36 +218,40 @@ finish_kernel(const int4* finish, long long n_items, int H, const float* part, l
               long long ldo, const int* dev_counters, int accumulate)
 {
     extern __shared__ float fstk[];  // [levels][kFinishThreads]
+    // The plan's counts (it had finished before the gather pass started) are
+    // read before the wait, so that a launch without hot destinations ends as
+    // soon as the gather pass does
+    if (dev_counters)
+        n_items = dev_counters[kCtrErrIndex] | dev_counters[kCtrErrDup]
+                      ? 0
+                      : static_cast<long long>(dev_counters[kCtrHot]) * H;
     pdl_wait();  // the gather pass has written every partial slot
-    if (dev_counters) {
-        if (dev_counters[kCtrErrIndex] | dev_counters[kCtrErrDup] | dev_counters[kCtrErrTimeout]) return;
-        n_items = static_cast<long long>(dev_counters[kCtrHot]) * H;
-    }
+    if (dev_counters && n_items > 0 && dev_counters[kCtrErrTimeout]) return;  // a gather kernel gave up
     for (long long t = static_cast<long long>(blockIdx.x) * kFinishThreads + threadIdx.x; t < n_items;
          t += static_cast<long long>(gridDim.x) * kFinishThreads) {
-    const long long row_task = t / H;
-    const int h = static_cast<int>(t - row_task * H);
-    const int4 ft = finish[row_task];
-    const int m = ft.x, s0 = ft.y, ns = ft.z;
-    unsigned int cnt = 0;
-    for (int s = 0; s < ns; s += kBatch) {
-        float v[kBatch];
+        const long long row_task = t / H;
+        const int h = static_cast<int>(t - row_task * H);
+        const int4 ft = finish[row_task];
+        const int m = ft.x, s0 = ft.y, ns = ft.z;
+        unsigned int cnt = 0;
+        for (int s = 0; s < ns; s += kBatch) {
+            float v[kBatch];
 #pragma unroll
-        for (int q = 0; q < kBatch; ++q)
-            if (s + q < ns) v[q] = __ldcs(part + static_cast<long long>(s0 + s + q) * ldpart + h);
+            for (int q = 0; q < kBatch; ++q)
+                if (s + q < ns) v[q] = __ldcs(part + static_cast<long long>(s0 + s + q) * ldpart + h);
 #pragma unroll
-        for (int q = 0; q < kBatch; ++q) {
-            if (s + q < ns) {
-                float node[1] = {v[q]};
-                scounter_push<1>(fstk, kFinishThreads, threadIdx.x, cnt, node);
-                ++cnt;
+            for (int q = 0; q < kBatch; ++q) {
+                if (s + q < ns) {
+                    float node[1] = {v[q]};
+                    scounter_push<1>(fstk, kFinishThreads, threadIdx.x, cnt, node);
+                    ++cnt;
+                }
             }
         }
-    }
-    float res[1] = {0.0f};
-    scounter_collapse<1>(fstk, kFinishThreads, threadIdx.x, cnt, res);
-    if (accumulate) add_store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
-    else store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
+        float res[1] = {0.0f};
+        scounter_collapse<1>(fstk, kFinishThreads, threadIdx.x, cnt, res);
+        if (accumulate) add_store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
+        else store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
     }
 }
 
@@ -271,7 +282,7 @@ static det_status launch_gather_t(const GatherArgs& a, const ShardTable& t, int 
         int pct = smem_sm > 0 ? std::min<int>(100, std::max<int>(50, static_cast<int>(cdiv(
                                                                         static_cast<int64_t>(need) * 100, smem_sm))))
                               : 50;
-                if (BESIDE) pct = 100;
+        if (BESIDE) pct = 100;
         if (pct != carve_set) {
             DETR_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(gather_reduce_kernel<XT, OT, VECTOR, ACC, BESIDE>),
                                            cudaFuncAttributePreferredSharedMemoryCarveout, pct));
@@ -535,7 +546,7 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
         bgrid = std::max<int64_t>(1, std::min<int64_t>(bgrid, 2147483647));
         s = launch_gather_ring(x_dtype, out_dtype, accumulate, b, tbl, static_cast<int>(bgrid), st);
         if (s) return s;
-    // The register-staged kernel takes the units of more than one chunk,
+        // The register-staged kernel takes the units of more than one chunk,
         // beside the ring kernel: launched as its programmatic dependent, it
         // starts at once on the shared memory the ring leaves free (one CTA
         // per SM) and waits for the ring kernel only before it ends.  On the
@@ -592,7 +603,11 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
         int64_t bgrid = opts && opts->grid_ctas > 0 ? opts->grid_ctas
                                                     : (use_bulk_dev ? sms : std::min<int64_t>(b.n_items, sms));
         bgrid = std::max<int64_t>(1, std::min<int64_t>(bgrid, 2147483647));
-        s = launch_gather_bulk(x_dtype, out_dtype, b, tbl, static_cast<int>(bgrid), st);
+        // Behind an unwaited owner plan, which releases the kernel after it
+        // only for its last phase, as that kernel's programmatic dependent:
+        // MoE step 62.6 against 64.5 us launched the ordinary way.
+        s = launch_gather_bulk(x_dtype, out_dtype, b, tbl, static_cast<int>(bgrid), use_bulk_dev && plan->late_release,
+                               st);
         if (s) return s;
         if (use_bulk_dev) {
             a.only_long = 1;  // the register-staged kernel below: only if some destination is longer

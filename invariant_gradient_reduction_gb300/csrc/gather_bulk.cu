@@ -144,6 +144,7 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
     constexpr int kPuInts = kPipeSlots * (32 + 32 + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(pu_base + kBulkProducers * kPuInts);
 
+    pdl_wait();  // as a programmatic dependent (behind an unwaited owner plan): the plan has finished
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ long long s_items;
     __shared__ int s_tile[4];  // elements, staged stride, tiles per row, producers
@@ -174,8 +175,8 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
     const long long n_items = s_items;
     const int tile_elems = s_tile[0], tile_stride = s_tile[1], ntiles = s_tile[2], nprod = s_tile[3];
     // the next kernel may be launched now: behind an unwaited plan the
-    // register-staged kernel, which waits for this grid before it reads
-    // anything (its launch then overlaps this kernel, not its end)
+    // register-staged kernel, which reads only the plan's counts before it
+    // waits for this grid (its launch then overlaps this kernel, not its end)
     pdl_launch_dependents();
     if (warp >= kBulkConsumerWarps) {
         // ---------------- producer warps ----------------
@@ -343,14 +344,18 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
 }
 
 template <typename XT, typename OT>
-static det_status launch_bulk_t(const BulkArgs& a, const ShardTable& t, int grid, cudaStream_t st)
+static det_status launch_bulk_t(const BulkArgs& a, const ShardTable& t, int grid, bool dependent, cudaStream_t st)
 {
     const size_t smem = bulk_smem_bytes();
     {
         const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(gather_bulk_kernel<XT, OT>), smem);
         if (a_) return a_;
     }
-    gather_bulk_kernel<XT, OT><<<grid, kBulkStageThreads, smem, st>>>(a, t);
+    if (dependent) {
+        DETR_CUDA(launch_after_previous(gather_bulk_kernel<XT, OT>, dim3(grid), dim3(kBulkStageThreads), smem, st, a, t));
+    } else {
+        gather_bulk_kernel<XT, OT><<<grid, kBulkStageThreads, smem, st>>>(a, t);
+    }
     DETR_LAUNCHED();
     return DET_OK;
 }
@@ -381,12 +386,13 @@ bool bulk_plan_tiles(int64_t H, int xsz, int64_t max_terms, int* tile_elems, int
 }
 
 det_status launch_gather_bulk(det_dtype x_dtype, det_dtype out_dtype, const BulkArgs& a, const ShardTable& t, int grid,
-                              cudaStream_t st)
+                              bool dependent, cudaStream_t st)
 {
-    if (x_dtype == DET_BF16 && out_dtype == DET_BF16) return launch_bulk_t<uint16_t, __nv_bfloat16>(a, t, grid, st);
-    if (x_dtype == DET_BF16) return launch_bulk_t<uint16_t, float>(a, t, grid, st);
-    if (out_dtype == DET_BF16) return launch_bulk_t<float, __nv_bfloat16>(a, t, grid, st);
-    return launch_bulk_t<float, float>(a, t, grid, st);
+    if (x_dtype == DET_BF16 && out_dtype == DET_BF16)
+        return launch_bulk_t<uint16_t, __nv_bfloat16>(a, t, grid, dependent, st);
+    if (x_dtype == DET_BF16) return launch_bulk_t<uint16_t, float>(a, t, grid, dependent, st);
+    if (out_dtype == DET_BF16) return launch_bulk_t<float, __nv_bfloat16>(a, t, grid, dependent, st);
+    return launch_bulk_t<float, float>(a, t, grid, dependent, st);
 }
 
 // ------------------------------------------------------------------------

@@ -129,8 +129,10 @@ constexpr int kBulkTwoProducerItems = 64;
 size_t bulk_smem_bytes();
 // Tile a row of H elements so that max_terms staged tiles fit one stage; false if not possible.
 bool bulk_plan_tiles(int64_t H, int xsz, int64_t max_terms, int* tile_elems, int* tile_stride, int* ntiles);
+// dependent: launched as a programmatic dependent of the kernel before it
+// (the kernel waits for that one before it reads anything).
 det_status launch_gather_bulk(det_dtype x_dtype, det_dtype out_dtype, const BulkArgs& a, const ShardTable& t,
-                              int grid, cudaStream_t st);
+                              int grid, bool dependent, cudaStream_t st);
 
 // The destinations of at most one chunk (1..32 terms; for the scatter-reduce
 // also those without terms), TMA-staged: each item is a destination's H-tile
