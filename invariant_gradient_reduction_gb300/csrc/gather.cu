@@ -603,9 +603,11 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
         int64_t bgrid = opts && opts->grid_ctas > 0 ? opts->grid_ctas
                                                     : (use_bulk_dev ? sms : std::min<int64_t>(b.n_items, sms));
         bgrid = std::max<int64_t>(1, std::min<int64_t>(bgrid, 2147483647));
-        // Behind an unwaited owner plan, which releases the kernel after it
-        // only for its last phase, as that kernel's programmatic dependent:
-        // MoE step 62.6 against 64.5 us launched the ordinary way.
+        // Behind an unwaited plan whose kernel releases the kernel after it
+        // only for its last phase (the owner plan, the route cluster
+        // kernel), as that kernel's programmatic dependent: MoE step 62.6
+        // against 64.5 us launched the ordinary way, route plan + combine
+        // 62.4 against 64.5 us.
         s = launch_gather_bulk(x_dtype, out_dtype, b, tbl, static_cast<int>(bgrid), use_bulk_dev && plan->late_release,
                                st);
         if (s) return s;

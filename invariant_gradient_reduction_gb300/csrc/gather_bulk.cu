@@ -144,7 +144,7 @@ gather_bulk_kernel(const __grid_constant__ BulkArgs a, const __grid_constant__ S
     constexpr int kPuInts = kPipeSlots * (32 + 32 + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(pu_base + kBulkProducers * kPuInts);
 
-    pdl_wait();  // as a programmatic dependent (behind an unwaited owner plan): the plan has finished
+    pdl_wait();  // as a programmatic dependent (behind an unwaited plan): the plan has finished
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ long long s_items;
     __shared__ int s_tile[4];  // elements, staged stride, tiles per row, producers
