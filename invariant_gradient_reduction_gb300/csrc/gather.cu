@@ -33,6 +33,9 @@ constexpr int kGatherWarps = kGatherThreads / 32;
 constexpr int kBatch = 8;
 constexpr int kStagePad = 33;
 constexpr int kFinishThreads = 256;
+#ifndef DETR_FINISH_FV
+#define DETR_FINISH_FV 4
+#endif
 
 
 #ifndef DETR_GATHER_MIN_BLOCKS
@@ -211,47 +214,68 @@ gather_reduce_kernel(const __grid_constant__ GatherArgs a, const __grid_constant
 
 // Second pass for hot destinations: the level-wise tree over the row's
 // segment nodes (aligned nodes of 2^g chunks), in segment order, through the
-// binary counter (stack in shared memory, one column per thread).
-template <typename OT>
+// binary counter (stack in shared memory, FV columns per thread).  An item
+// is FV adjacent columns of one hot row (FV = 4: 16-byte loads of the
+// partials, when H and the partial rows allow them).
+template <typename OT, int FV>
 __global__ void __launch_bounds__(kFinishThreads)
 finish_kernel(const int4* finish, long long n_items, int H, const float* part, long long ldpart, void* out,
               long long ldo, const int* dev_counters, int accumulate)
 {
-    extern __shared__ float fstk[];  // [levels][kFinishThreads]
+    extern __shared__ float fstk[];  // [levels][FV][kFinishThreads]
+    const int HV = H / FV;           // H % FV == 0
     // The plan's counts (it had finished before the gather pass started) are
     // read before the wait, so that a launch without hot destinations ends as
     // soon as the gather pass does
     if (dev_counters)
         n_items = dev_counters[kCtrErrIndex] | dev_counters[kCtrErrDup]
                       ? 0
-                      : static_cast<long long>(dev_counters[kCtrHot]) * H;
+                      : static_cast<long long>(dev_counters[kCtrHot]) * HV;
     pdl_wait();  // the gather pass has written every partial slot
     if (dev_counters && n_items > 0 && dev_counters[kCtrErrTimeout]) return;  // a gather kernel gave up
     for (long long t = static_cast<long long>(blockIdx.x) * kFinishThreads + threadIdx.x; t < n_items;
          t += static_cast<long long>(gridDim.x) * kFinishThreads) {
-        const long long row_task = t / H;
-        const int h = static_cast<int>(t - row_task * H);
+        const long long row_task = t / HV;
+        const int h = static_cast<int>(t - row_task * HV) * FV;
         const int4 ft = finish[row_task];
         const int m = ft.x, s0 = ft.y, ns = ft.z;
         unsigned int cnt = 0;
         for (int s = 0; s < ns; s += kBatch) {
-            float v[kBatch];
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q)
-                if (s + q < ns) v[q] = __ldcs(part + static_cast<long long>(s0 + s + q) * ldpart + h);
+            float v[kBatch][FV];
 #pragma unroll
             for (int q = 0; q < kBatch; ++q) {
                 if (s + q < ns) {
-                    float node[1] = {v[q]};
-                    scounter_push<1>(fstk, kFinishThreads, threadIdx.x, cnt, node);
+                    const float* src = part + static_cast<long long>(s0 + s + q) * ldpart + h;
+                    if constexpr (FV == 4) {
+                        const float4 f = __ldcs(reinterpret_cast<const float4*>(src));
+                        v[q][0] = f.x;
+                        v[q][1] = f.y;
+                        v[q][2] = f.z;
+                        v[q][3] = f.w;
+                    } else if constexpr (FV == 2) {
+                        const float2 f = __ldcs(reinterpret_cast<const float2*>(src));
+                        v[q][0] = f.x;
+                        v[q][1] = f.y;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < FV; ++e) v[q][e] = __ldcs(src + e);
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                if (s + q < ns) {
+                    scounter_push<FV>(fstk, kFinishThreads, threadIdx.x, cnt, v[q]);
                     ++cnt;
                 }
             }
         }
-        float res[1] = {0.0f};
-        scounter_collapse<1>(fstk, kFinishThreads, threadIdx.x, cnt, res);
-        if (accumulate) add_store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
-        else store_out<OT, 1>(out, static_cast<long long>(m) * ldo + h, res, false);
+        float res[FV];
+#pragma unroll
+        for (int e = 0; e < FV; ++e) res[e] = 0.0f;
+        scounter_collapse<FV>(fstk, kFinishThreads, threadIdx.x, cnt, res);
+        if (accumulate) add_store_out<OT, FV>(out, static_cast<long long>(m) * ldo + h, res, false);
+        else store_out<OT, FV>(out, static_cast<long long>(m) * ldo + h, res, false);
     }
 }
 
@@ -634,8 +658,14 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
     const bool maybe_hot = dev_counts ? plan->N > (int64_t(kChunk) << plan->g) : plan->n_hot_rows > 0;
     if (maybe_hot) {
         const int64_t max_row = dev_counts ? plan->N : plan->max_row_len;
-        const long long items = dev_counts ? (cdiv(plan->N, (int64_t(kChunk) << plan->g) + 1) + 1) * H
-                                           : plan->n_hot_rows * H;
+        // four adjacent columns per thread where the partial rows allow
+        // 16-byte loads (a quarter of the threads, each with four times the
+        // bytes in flight): sparse key scatter reduce 404.3 -> 401.4 us (two
+        // columns: 401.5 us)
+        int fv = DETR_FINISH_FV;
+        while (fv > 1 && !(H % fv == 0 && a.ldpart % fv == 0 && aligned(a.part, 4 * fv))) fv /= 2;
+        const long long items = (dev_counts ? (cdiv(plan->N, (int64_t(kChunk) << plan->g) + 1) + 1) * H
+                                            : plan->n_hot_rows * H) / fv;
         // behind the fixed-stage kernel it has work only when some row is
         // longer than 32 terms (then it loops over its grid): a small grid
         // ends sooner when it has none
@@ -645,16 +675,20 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
         const unsigned int fgrid = static_cast<unsigned int>(std::max<int64_t>(1, fgrid64));
         const int64_t max_segs = cdiv(cdiv(max_row, kChunk), G);
         const size_t fsmem = static_cast<size_t>(log2_floor(std::max<int64_t>(1, max_segs)) + 1) * kFinishThreads *
-                             sizeof(float);
+                             fv * sizeof(float);
         const int* dc = dev_counts ? plan->counters : nullptr;
         const int4* fin = plan->finish;
         const float* part = a.part;
-        if (out_dtype == DET_BF16)
-            DETR_CUDA(launch_after_previous(finish_kernel<__nv_bfloat16>, dim3(fgrid), dim3(kFinishThreads), fsmem, st,
-                                            fin, items, a.H, part, a.ldpart, out, ldo, dc, a.accumulate));
-        else
-            DETR_CUDA(launch_after_previous(finish_kernel<float>, dim3(fgrid), dim3(kFinishThreads), fsmem, st, fin,
-                                            items, a.H, part, a.ldpart, out, ldo, dc, a.accumulate));
+        auto kern = out_dtype == DET_BF16
+                        ? (fv == 4 ? finish_kernel<__nv_bfloat16, 4>
+                                   : fv == 2 ? finish_kernel<__nv_bfloat16, 2> : finish_kernel<__nv_bfloat16, 1>)
+                        : (fv == 4 ? finish_kernel<float, 4> : fv == 2 ? finish_kernel<float, 2> : finish_kernel<float, 1>);
+        {
+            const det_status a_ = allow_dynamic_smem(reinterpret_cast<const void*>(kern), fsmem);
+            if (a_) return a_;
+        }
+        DETR_CUDA(launch_after_previous(kern, dim3(fgrid), dim3(kFinishThreads), fsmem, st, fin, items, a.H, part,
+                                        a.ldpart, out, ldo, dc, a.accumulate));
         DETR_LAUNCHED();
     }
     if (opts && opts->debug_checks) return debug_sync_status(plan, st);
