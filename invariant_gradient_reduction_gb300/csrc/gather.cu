@@ -568,6 +568,9 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
         int64_t bgrid = opts && opts->grid_ctas > 0 ? opts->grid_ctas
                                                     : (dev_counts ? sms : std::min<int64_t>(n_ring, sms));
         bgrid = std::max<int64_t>(1, std::min<int64_t>(bgrid, 2147483647));
+        // as for the fixed-stage kernel below: embedding backward step 161.7
+        // against 166.4 us launched the ordinary way
+        b.dependent = dev_counts && plan->late_release;
         s = launch_gather_ring(x_dtype, out_dtype, accumulate, b, tbl, static_cast<int>(bgrid), st);
         if (s) return s;
         // The register-staged kernel takes the units of more than one chunk,
@@ -628,10 +631,10 @@ static det_status scatter_reduce_impl(det_plan plan, const void* const* x_shards
                                                     : (use_bulk_dev ? sms : std::min<int64_t>(b.n_items, sms));
         bgrid = std::max<int64_t>(1, std::min<int64_t>(bgrid, 2147483647));
         // Behind an unwaited plan whose kernel releases the kernel after it
-        // only for its last phase (the owner plan, the route cluster
-        // kernel), as that kernel's programmatic dependent: MoE step 62.6
-        // against 64.5 us launched the ordinary way, route plan + combine
-        // 62.4 against 64.5 us.
+        // only for its last phase (the owner plan, the two-pass cluster plan,
+        // the route cluster kernel), as that kernel's programmatic
+        // dependent: MoE step 62.6 against 64.5 us launched the ordinary
+        // way, route plan + combine 62.4 against 64.5 us.
         s = launch_gather_bulk(x_dtype, out_dtype, b, tbl, static_cast<int>(bgrid), use_bulk_dev && plan->late_release,
                                st);
         if (s) return s;

@@ -515,12 +515,15 @@ gather_ring_kernel(const __grid_constant__ RingArgs a, const __grid_constant__ S
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (threadIdx.x <= kBulkMaxTerms) tiles[threadIdx.x] = ring_tile(threadIdx.x, a.H, a.quantum, XSZ, ACC ? OSZ : 0);
-    // Launched the ordinary way, so everything before this grid has
-    // finished: the kernel for the other destinations may start now and run
-    // beside this one (it reads the plan without waiting, writes other rows,
-    // and waits for this grid before it ends).  (As a programmatic dependent
-    // of the plan, waiting here before letting it start, this kernel made the
-    // MoE step 3 us and the EP-invariance step 4 us slower.)
+    // Launched the ordinary way, or as the plan's programmatic dependent and
+    // past this wait, so everything before this grid has finished: the
+    // kernel for the other destinations may start now and run beside this
+    // one (it reads the plan without waiting, writes other rows, and waits
+    // for this grid before it ends).  (Behind a plan that released it at
+    // the plan's start, this kernel made the MoE step 3 us and the
+    // EP-invariance step 4 us slower: its CTAs sat on the SMs through the
+    // whole plan.)
+    pdl_wait();
     pdl_launch_dependents();
     __syncthreads();
 
@@ -787,7 +790,11 @@ static det_status launch_ring_t(const RingArgs& a, const ShardTable& t, int grid
             carve_set = true;
         }
     }
-    gather_ring_kernel<XT, OT, ACC><<<grid, kBulkThreads, smem, st>>>(a, t);
+    if (a.dependent) {
+        DETR_CUDA(launch_after_previous(gather_ring_kernel<XT, OT, ACC>, dim3(grid), dim3(kBulkThreads), smem, st, a, t));
+    } else {
+        gather_ring_kernel<XT, OT, ACC><<<grid, kBulkThreads, smem, st>>>(a, t);
+    }
     DETR_LAUNCHED();
     return DET_OK;
 }

@@ -153,6 +153,7 @@ struct RingArgs {
     int* status;           // counter block; kCtrErrTimeout is set if a bounded wait expires
     const int* dev_counters;  // non-null (plan that did not wait): n_units is the block's count of
                               // such units, or 0 if the plan recorded an error
+    int dependent;            // launched as a programmatic dependent of the kernel before it (the plan)
 };
 
 size_t ring_smem_bytes(int ring_bytes);

@@ -618,6 +618,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
         if (plan_path == 3 && !one_kernel_set) return DET_ERR_UNSUPPORTED;
     }
     const bool owner_plan = one_kernel_set;
+    bool cluster_late = false;  // the two-pass cluster kernel, which releases the reduce for its last phase
     if (plan_path == 3 && (with_src || N == 0)) return DET_ERR_UNSUPPORTED;
     if (!one_kernel_set && (plan_path == 0 || plan_path == 2) && !with_src && N > 0) {
         // Auto takes the two-pass cluster kernel only up to 65536 sources: after
@@ -628,6 +629,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
         s = launch_plan_cluster(idx, N, M, g, np32, row_ptr, perm, seg_units, row_units, finish, counters,
                                 two_pass, st, &one_kernel_set);
         if (s) return s;
+        cluster_late = two_pass && one_kernel_set;
         if (plan_path == 2 && !one_kernel_set) return DET_ERR_UNSUPPORTED;
     }
     if (plan_path == 2 && !one_kernel_set) return DET_ERR_UNSUPPORTED;
@@ -744,7 +746,7 @@ det_status det_reduce_plan(const int32_t* idx, const int64_t* src_id, int64_t N,
     p->seg_units = seg_units;
     p->row_units = row_units;
     p->finish = finish;
-    p->late_release = owner_plan;
+    p->late_release = owner_plan || cluster_late;
     if (async) {
         p->counts_on_host = false;
         p->n_segments = p->n_units = p->n_hot_rows = p->max_row_len = p->n_long = p->n_empty = -1;

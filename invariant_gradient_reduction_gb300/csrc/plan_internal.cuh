@@ -131,5 +131,6 @@ struct det_plan_s {
     int64_t n_units = 0, n_segments = 0, n_hot_rows = 0, max_row_len = 0, n_long = 0, n_empty = 0;
     bool counts_on_host = true;      // false for an async plan until det_plan_status
     bool late_release = false;       // built by a kernel that lets the kernel after it start only for its
-                                     // last phase (the owner plan, the route cluster kernel)
+                                     // last phase (the owner plan, the two-pass cluster plan, the route
+                                     // cluster kernel)
 };
